@@ -1,0 +1,468 @@
+"""Benchmark of the sparse self-speculative decoding attention hot path on GB300.
+
+One step = one speculative round of every layer of a synthetic multi-layer cache in the
+Qwen3-8B attention shape (32 requests, lengths U[2048, 8192], 32/8 heads, d = 128, bf16, pages of
+16 tokens, k = 4, top-K = 5%): for each layer verify (+ fused criticality) and Top-K select, then the
+k drafts of every layer (draft j of all layers, then draft j+1).  The step is captured once in a
+CUDA graph and replayed; each layer's KV (671 MB) is larger than L2 and the layers are cycled, so
+no timed kernel finds its inputs in L2 from a previous use.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU oracle instead, on a
+bounded sample of the same workload.  Multi-GPU (torchrun): every rank runs its own independent
+batch (weak scaling, no collective on the data path); timings are the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from sparse_self_speculative_verify_gb300 import metrics as M  # noqa: E402
+from sparse_self_speculative_verify_gb300 import workloads as W  # noqa: E402
+
+METRIC = "spec-decode attention HBM GB/s (% of ~8 TB/s peak); verify+draft rounds/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "verify_qwen3_8b_traffic.json")
+
+
+# --------------------------------------------------------------------------------------------
+# Distributed helpers (host side; tested with gloo on CPU).
+# --------------------------------------------------------------------------------------------
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws an independent batch of the same shape."""
+    return base + 7919 * rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, device=None) -> float:
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# --------------------------------------------------------------------------------------------
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+                "clocks_event_reasons.sw_power_cap"]
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--id={self.gpu_id}", "--query-gpu=" + ",".join(CLOCK_FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "200"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(CLOCK_FIELDS):
+                self.rows.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        sm = []
+        smax = None
+        reasons = set()
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                smax = float(r[1])
+            except ValueError:
+                continue
+            for name, v in zip(REASON_NAMES, r[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(device) -> str:
+    try:
+        u = torch.cuda.get_device_properties(device).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return str(torch.cuda.current_device())
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_self_speculative_verify_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(launch_units: int):
+    """DRAM bytes per verify launch from the committed ncu summary, scaled to this launch's units;
+    None when the kernels changed since the capture."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        d = json.load(f)
+    if d.get("kernel_src_sha") != kernel_source_sha():
+        return None
+    return d["dram_bytes_per_unit"] * launch_units
+
+
+# --------------------------------------------------------------------------------------------
+# Workload.
+# --------------------------------------------------------------------------------------------
+
+
+def make_layers(spec, n_layers: int, seed: int, device):
+    """n_layers independent caches of the same requests (shared lengths, own pages and values)."""
+    first = W.make_workload(spec, seed=seed, device=device)
+    lens = first.seq_lens.cpu().tolist()
+    layers = [first]
+    for l in range(1, n_layers):
+        layers.append(W.make_workload(spec, seed=seed + 101 * l, device=device, lengths=lens))
+    return layers
+
+
+# --------------------------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm).
+# --------------------------------------------------------------------------------------------
+
+
+def oracle_round_time(layer, reqs, threads: int):
+    """Time one round (verify + select + k drafts) of requests ``reqs`` of one layer with the
+    float64 oracle.  Returns (seconds, KV bytes of the round)."""
+    import numpy as np
+
+    import oracle
+    spec = layer.spec
+    ps = spec.page_size
+    lens = layer.seq_lens.cpu()[reqs]
+    pt = layer.page_table.cpu()[reqs]
+    npg = [(int(L) + ps - 1) // ps for L in lens.tolist()]
+    pages = torch.cat([pt[i, :n] for i, n in enumerate(npg)]).to(torch.int64)
+    pool = layer.pool[pages.to(layer.pool.device)].cpu()
+    new_pt = torch.full((len(reqs), max(npg)), -1, dtype=torch.int32)
+    off = 0
+    for i, n in enumerate(npg):
+        new_pt[i, :n] = torch.arange(off, off + n, dtype=torch.int32)
+        off += n
+    kv = oracle.PagedKV(pool, new_pt, lens)
+    qv = layer.q_verify.cpu()[reqs]
+    qd = layer.q_draft.cpu()[:, reqs]
+    kpr = layer.k_per_req.cpu()[reqs].numpy()
+    k_max = int(kpr.max())
+    scale = 1.0 / math.sqrt(spec.d)
+    t0 = time.perf_counter()
+    ref = oracle.verify(kv, qv, scale, threads=threads)
+    S = ref["crit"].astype(np.float32)
+    idx, cnt = oracle.topk(S.reshape(-1, S.shape[-1]), lens.numpy(), kpr, k_max, rows_per_group=spec.h_kv)
+    idx = idx.reshape(len(reqs), spec.h_kv, k_max)
+    cnt = cnt.reshape(len(reqs), spec.h_kv)
+    for j in range(spec.k):
+        oracle.draft(kv, qd[j], idx, cnt, scale, threads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = M.round_kv_bytes(lens.tolist(), kpr.tolist(), spec.h_kv, spec.d, spec.elem_bytes, spec.k)
+    return dt, nbytes
+
+
+def cpu_baseline(layers, budget_s: float = 12.0) -> dict:
+    import oracle
+    threads = oracle.default_threads()
+    B = layers[0].spec.batch
+    total_t, total_b, done = 0.0, 0, []
+    for li, layer in enumerate(layers):
+        for b in range(B):
+            dt, nb = oracle_round_time(layer, [b], threads)
+            total_t += dt
+            total_b += nb
+            done.append((li, b))
+            if total_t >= budget_s:
+                break
+        if total_t >= budget_s:
+            break
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(done)} (layer, request) rounds of verify + select + {layers[0].spec.k} drafts, "
+                      f"{total_t:.1f} s of float64 oracle time on {threads} threads"}
+
+
+# --------------------------------------------------------------------------------------------
+# Arms.
+# --------------------------------------------------------------------------------------------
+
+
+def run_reference(args, spec, rank, world):
+    """The reference arm: the float64 CPU oracle as it stands, each step one bounded sample."""
+    import oracle
+    if rank != 0:
+        return None
+    layers = make_layers(spec, 1, W.spec_seed(spec.name), "cpu")
+    layer = layers[0]
+    threads = oracle.default_threads()
+    reqs = list(range(min(args.ref_requests, spec.batch)))
+    for _ in range(args.warmup):
+        oracle_round_time(layer, reqs[:1], threads)
+    tt, tb = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_round_time(layer, reqs, threads)
+        tt += dt
+        tb += nb
+    value = tb / tt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{spec.name}: {spec.batch} requests, L~U[{spec.len_lo},{spec.len_hi}], "
+                                   f"{spec.h_q}/{spec.h_kv} heads, d={spec.d}, bf16 paged (16), k={spec.k}, top-K 5%",
+                       "sample_per_step": f"requests 0..{len(reqs) - 1} of layer 0, one round"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{len(reqs)} requests x 1 round per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+def run_ours(args, spec, rank, world, local):
+    from sparse_self_speculative_verify_gb300 import KVCache, SpecRound, ssd_status
+    from sparse_self_speculative_verify_gb300 import build as libbuild
+    from sparse_self_speculative_verify_gb300 import binding
+
+    libbuild.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    seed = rank_seed(W.spec_seed(spec.name), rank)
+    layers = make_layers(spec, args.layers, seed, dev)
+    scale = 1.0 / math.sqrt(spec.d)
+    k_max = max(int(l.k_per_req.max()) for l in layers)
+    rounds = [SpecRound(KVCache.from_workload(l), spec.h_q, spec.n_cand, k_max, scale) for l in layers]
+    outs = [torch.empty((spec.k, spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=dev) for _ in layers]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for r, l in zip(rounds, layers):
+            r.verify(l.q_verify)
+            r.select(l.k_per_req)
+        for j in range(spec.k):
+            for r, l, o in zip(rounds, layers, outs):
+                r.draft(l.q_draft[j], out=o[j])
+
+    launches_per_step = args.layers * (2 + 1 + spec.k)
+    with torch.cuda.stream(stream):
+        step()  # eager warm-up (also sets kernel attributes outside capture)
+    stream.synchronize()
+    assert ssd_status() == 0, "device status fault in warm-up"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    stream.synchronize()
+
+    # Work per step (this rank).
+    lens = layers[0].seq_lens.cpu().tolist()
+    kv_step = sum(M.round_kv_bytes(lens, l.k_per_req.cpu().tolist(), spec.h_kv, spec.d, spec.elem_bytes, spec.k)
+                  for l in layers)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    barrier()
+    clocks = ClockSampler(gpu_id_for(dev))
+    clocks.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_total = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    barrier()
+    ms_total = max_over_ranks(ms_total, dev)
+    bytes_all = sum_over_ranks(float(kv_step * args.steps), dev)
+    value = bytes_all / (ms_total * 1e-3) / 1e9
+    ms_step = ms_total / args.steps
+    rounds_per_s = world * args.layers / (ms_step * 1e-3)
+    assert ssd_status() == 0, "device status fault in the timed region"
+
+    # Dominant call: ssd_verify_attn (verify kernel + finalize), timed per launch with events on
+    # its stream, layers cycled (cold L2).
+    reps = max(2, min(args.steps, 10))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(reps * args.layers)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(reps * args.layers)]
+    with torch.cuda.stream(stream):
+        for i in range(reps * args.layers):
+            r, l = rounds[i % args.layers], layers[i % args.layers]
+            starts[i].record(stream)
+            r.verify(l.q_verify, stream=stream)
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    v_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    peaks = measured_peaks()
+    v_bytes = M.verify_call_bytes(lens, spec.batch, spec.h_q, spec.h_kv, spec.d, spec.elem_bytes, spec.n_cand)
+    achieved = v_bytes / (v_ms * 1e-3) / 1e9
+    units = sum(lens) * spec.h_kv
+    roofline = {"bound": "hbm", "kernel": "ssd_verify_attn (verify_mma_kernel + finalize_kernel)",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(units),
+                "peak_source": peaks["source"], "launch_ms": v_ms, "algorithmic_bytes": v_bytes,
+                "verify_tflops": M.verify_flops(lens, spec.h_q, spec.d, spec.n_cand) / (v_ms * 1e-3) / 1e12}
+
+    # End to end through the API with host buffers: per step, the queries of every layer (and the
+    # lengths / page table) go host -> device, the attention outputs device -> host.
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)  # noqa: E731
+    h_in = [(pin(l.q_verify), pin(l.q_draft)) for l in layers]
+    h_meta = (pin(layers[0].seq_lens), pin(layers[0].page_table))
+    h_out = [(torch.empty(r.out_v.shape, pin_memory=True), torch.empty(o.shape, pin_memory=True))
+             for r, o in zip(rounds, outs)]
+    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_in) + \
+        sum(t.numel() * t.element_size() for t in h_meta)
+    d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for (qv, qd), l in zip(h_in, layers):
+                l.q_verify.copy_(qv, non_blocking=True)
+                l.q_draft.copy_(qd, non_blocking=True)
+            layers[0].seq_lens.copy_(h_meta[0], non_blocking=True)
+            layers[0].page_table.copy_(h_meta[1], non_blocking=True)
+            graph.replay()
+            for (ov, od), r, o in zip(h_out, rounds, outs):
+                ov.copy_(r.out_v, non_blocking=True)
+                od.copy_(o, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_value = sum_over_ranks(float(kv_step * e2e_steps), dev) / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(layers, args.cpu_budget)
+    if rank != 0:
+        return None
+    return {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "rounds_per_s": rounds_per_s,
+            "hbm_frac": value / peaks["hbm_gbs"],
+            "config": {"workload": f"{spec.name}: {spec.batch} requests, L~U[{spec.len_lo},{spec.len_hi}], "
+                                   f"{spec.h_q}/{spec.h_kv} heads, d={spec.d}, bf16 paged KV (page {spec.page_size}, "
+                                   f"shuffled), k={spec.k}, top-K ceil(5% L)",
+                       "layers": args.layers, "kv_bytes_per_step_per_gpu": kv_step,
+                       "step": "per layer: verify+criticality, select; then k drafts of every layer",
+                       "l2": f"inputs larger than L2: {args.layers} layers x "
+                             f"{M.verify_kv_bytes(lens, spec.h_kv, spec.d, spec.elem_bytes) / 1e6:.0f} MB KV, cycled",
+                       "timing": "CUDA graph of one step, replayed; CUDA events on the replay stream"},
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="qwen3_8b", choices=sorted(W.SPECS))
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-requests", type=int, default=2)
+    args = ap.parse_args(argv)
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    spec = W.SPECS[args.config]
+    if args.impl == "reference":
+        line = run_reference(args, spec, rank, world)
+    else:
+        line = run_ours(args, spec, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

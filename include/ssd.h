@@ -1,0 +1,211 @@
+/*
+ * ssd.h -- C ABI of libssd: GPU attention for sparse self-speculative decoding (sm_103a).
+ *
+ * One speculative round over a paged KV cache (SparseSpec, "Accelerating Large-Scale Reasoning
+ * Model Inference: Self-Speculative Decoding with Sparse Attention", §4.1 PillarAttn, §2.3, §3.2):
+ *   1. ssd_verify_attn  -- full attention of the k+1 candidate tokens of each request over its whole
+ *                          cache, causal among the candidates; the same pass emits every KV token's
+ *                          criticality (softmax probability summed over the query heads of the KV
+ *                          group and the k+1 verify positions).
+ *   2. ssd_select_topk  -- Top-K of the criticality per (request, KV head), ties to the lower index.
+ *   3. ssd_draft_attn   -- the next k drafts: single-query attention over the selected tokens only.
+ * plus the unified verify/draft launch (§4.2 "fused attention") and the block-granular variant
+ * (SpecSA post, overlap-aware grouped query execution; SparDA §2 max-pooling to a block grid).
+ *
+ * Conventions (all calls):
+ *  - Every pointer argument named as "device" is device memory of the current CUDA device; host
+ *    pointers are only the ssd_paged_kv struct itself and scalar outputs of ssd_status.
+ *  - The caller owns all memory.  The library allocates nothing, keeps no pointer after a call
+ *    returns, and takes scratch space only from the caller's workspace, sized by the matching
+ *    ssd_*_workspace_bytes() query.  A workspace must be zero-filled once after allocation (the
+ *    library leaves its counters at zero after every call) and must not be shared by calls that
+ *    may run concurrently.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *    Argument errors are detected on the host and returned before anything is launched; launch
+ *    failures return SSD_ERR_CUDA.  Data-dependent faults found on the device (a page id outside
+ *    the pool, a token index >= its request's length, a length outside [0, max_seq_len], K > k_max)
+ *    never trap: the offending load is skipped (zero-filled) and a bit is set in a device status
+ *    word that ssd_status() reports.
+ *  - The library never aborts, prints or traps.  ssd_last_error() returns a thread-local message
+ *    for the last failing call on the calling thread.
+ *  - Layouts are dense and row-major unless a stride argument says otherwise.
+ *  - Notation: B requests, H_q query heads, H_kv KV heads, G = H_q / H_kv, d head dim (64 or 128),
+ *    n_cand = k + 1, R = G * n_cand rows per (request, KV head) (R <= 64).  Query head h reads KV
+ *    head h / G.  Request b holds L_b = seq_lens[b] tokens, its candidates at positions
+ *    L_b - n_cand .. L_b - 1; candidate i sees tokens t <= L_b - n_cand + i.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ssd_stream_t; /* == cudaStream_t */
+
+enum ssd_status_code {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1, /* null pointer, bad size or stride, inconsistent shapes */
+  SSD_ERR_UNSUPPORTED = 2, /* dtype, head dim, page size or group shape outside what is built */
+  SSD_ERR_WORKSPACE = 3,   /* workspace null or smaller than the query function says */
+  SSD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  SSD_ERR_TIMEOUT = 5      /* reserved: a bounded device wait expired */
+};
+
+enum ssd_dtype { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 };
+
+/* Device status word bits (ssd_status). */
+enum ssd_device_fault {
+  SSD_FAULT_PAGE = 1u,     /* a page id outside [0, num_pages) */
+  SSD_FAULT_SEQLEN = 2u,   /* seq_lens[b] outside [0, max_seq_len] or shorter than n_cand */
+  SSD_FAULT_INDEX = 4u,    /* a draft index outside [0, L_b) */
+  SSD_FAULT_KMAX = 8u,     /* a requested K larger than k_max (output truncated to k_max) */
+  SSD_FAULT_UNION = 16u    /* a block union larger than umax (output truncated) */
+};
+
+/*
+ * Paged KV cache (SparseSpec §4.2: PagedAttention; a page of size 1 turns full attention into the
+ * sparse token-list case, so both share one pipeline).
+ *   pool        device, [num_pages][2][h_kv][page_size][d] of `dtype`; index 0 = K, 1 = V.  Each
+ *               (page, K|V, head) block of page_size * d elements is contiguous.  16-byte aligned.
+ *   page_table  device int32 [batch][max_pages]: request b's token t lives in page
+ *               page_table[b][t / page_size], slot t % page_size.  Entries past a request's last
+ *               page are never read.
+ *   seq_lens    device int32 [batch].
+ *   max_seq_len host upper bound of seq_lens (sizes grids and workspaces);
+ *               max_seq_len <= max_pages * page_size.
+ */
+typedef struct ssd_paged_kv {
+  const void *pool;
+  int dtype;
+  int64_t num_pages;
+  int page_size; /* power of two */
+  int h_kv;
+  int d; /* 64 or 128 */
+  const int32_t *page_table;
+  int max_pages;
+  const int32_t *seq_lens;
+  int batch;
+  int max_seq_len;
+} ssd_paged_kv;
+
+/* Thread-local message describing the last failing call on this thread ("" if none). */
+const char *ssd_last_error(void);
+
+/* ABI version: (major << 16) | minor. */
+int ssd_version(void);
+
+/* Synchronises `stream`, then returns in *status the OR of all device fault bits raised by
+ * kernels of this library on the current device since the previous ssd_status call, and clears
+ * them.  Returns SSD_ERR_CUDA if the synchronisation reports an error. */
+int ssd_status(ssd_stream_t stream, uint32_t *status);
+
+/* ---------------------------------------------------------------------------------------------
+ * Verify attention with fused criticality.
+ * SparseSpec §4.1 (PillarAttn): the verify step runs full attention over the whole cache; its
+ * kernel dumps the attention scores, caching logits and the log-sum-exp to rematerialise them;
+ * the scores are reduced over the heads of a GQA group and the verify positions.  SpecAttn
+ * (abstract): KV criticality is a byproduct of verification.
+ *
+ *   q        device [batch][n_cand][h_q][d] of kv->dtype (candidate i = verify position i).
+ *   scale    softmax scale applied to q.k (typically 1/sqrt(d)); natural-base softmax.
+ *   out      device float [batch][n_cand][h_q][d]: attention output.
+ *   lse      device float [batch][n_cand][h_q] or NULL: natural-log log-sum-exp of the scaled logits.
+ *   scores   device float [batch][h_kv][scores_stride] or NULL: scores[b][g][t] =
+ *            sum over the G heads h of group g and candidates i of softmax_{b,h,i}(t) (0 where t is
+ *            not visible to i).  Entries t >= L_b are not written.  scores_stride >= max_seq_len.
+ *   bscores  device float [batch][h_kv][n_cand][bscores_stride] or NULL (block mode): for every
+ *            candidate i, the per-candidate criticality sum over h of softmax_{b,h,i}(t) max-pooled
+ *            over blocks of block_size tokens (block j = tokens [j*bs, min((j+1)*bs, L_b))).
+ *            Blocks >= ceil(L_b / bs) are not written.  block_size must be 64 when bscores != NULL.
+ *   workspace device, >= ssd_verify_workspace_bytes(kv, h_q, n_cand) bytes, 256-byte aligned.
+ */
+size_t ssd_verify_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand);
+int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
+                    float *lse, float *scores, int64_t scores_stride, float *bscores,
+                    int64_t bscores_stride, int block_size, void *workspace, size_t workspace_bytes,
+                    ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Top-K selection (SparseSpec §4.1: "Top-K on the dumped scores" gives the sparse pattern; §3.2,
+ * §5.4: about 5% of the tokens).  Rows r = 0 .. n_groups*rows_per_group-1 of the score matrix
+ * (device float, row stride `stride` elements) belong to group r / rows_per_group; row r has
+ * n_r = ceil(lens[group] / len_div) entries and keeps K_r = min(ks[group], n_r) of them: the K_r
+ * largest values, equal values broken toward the lower index.  idx (device int32 [rows][k_max])
+ * receives the kept indices in ascending order, -1 padded; cnt (device int32 [rows]) receives K_r.
+ * lens and ks are device int32 [n_groups].  max_len (host) bounds n_r.  Scores must not be NaN;
+ * -0.0 ranks equal to +0.0.  Token level: rows_per_group = h_kv, lens = seq_lens, len_div = 1.
+ */
+int ssd_select_topk(const float *scores, int64_t stride, const int32_t *lens, const int32_t *ks,
+                    int n_groups, int rows_per_group, int len_div, int max_len, int32_t *idx, int k_max,
+                    int32_t *cnt, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Sparse draft attention (SparseSpec §4.1: each of the k drafts after a verify loads only the
+ * selected tokens; §4.2: sparse attention is PagedAttention at page size 1).
+ *   q    device [batch][h_q][d] of kv->dtype (one draft query per request).
+ *   idx  device int32 [batch][h_kv][k_max], cnt device int32 [batch][h_kv]: the token list of
+ *        each (request, KV head); each entry must be in [0, L_b).  Duplicates count twice.
+ *   out  device float [batch][h_q][d]; lse device float [batch][h_q] or NULL.  An empty list
+ *        gives out = 0 and lse = -inf.
+ */
+size_t ssd_draft_workspace_bytes(const ssd_paged_kv *kv, int h_q, int k_max);
+int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
+                   const int32_t *cnt, float scale, float *out, float *lse, void *workspace,
+                   size_t workspace_bytes, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Unified launch (SparseSpec §4.2: requests of both phases in one batch; a persistent fused kernel
+ * dispatches verify and draft work to their own tile code in one launch).  phase (device uint8
+ * [batch]): 1 = verify, 0 = draft.  Verify-phase requests take q_verify/out_verify/lse_verify/
+ * scores exactly as ssd_verify_attn; draft-phase requests take q_draft/idx/cnt/out_draft/lse_draft
+ * exactly as ssd_draft_attn.  Rows of the other phase are left untouched.
+ */
+size_t ssd_unified_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand, int k_max);
+int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, const void *q_verify,
+                     const void *q_draft, int h_q, int n_cand, const int32_t *idx, int k_max,
+                     const int32_t *cnt, float scale, float *out_verify, float *lse_verify,
+                     float *scores, int64_t scores_stride, float *out_draft, float *lse_draft,
+                     void *workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Block-granular variant (SpecSA post: overlap-aware grouped query execution -- candidates with
+ * overlapping sparse layouts run together and share KV blocks; hierarchical layout management).
+ *
+ * ssd_block_union: for each unit u (= request * h_kv + KV head), the union of the n_cand
+ * candidates' block lists blocks (device int32 [units][n_cand][kb], bcnt valid entries each, as
+ * written by ssd_select_topk with rows_per_group = h_kv * n_cand) in ascending order: uidx (device
+ * int32 [units][umax], -1 padded), umask (device uint32 [units][umax], bit i = candidate i chose the
+ * block) and ucnt (device int32 [units]).  Block ids must be in [0, nblk_max); n_cand <= 32.
+ *
+ * ssd_block_sparse_attn: candidate i of request b attends to the tokens of its own blocks that
+ * it can see (t < L_b and t <= L_b - n_cand + i); each union block is loaded once for all
+ * candidates and heads of the unit.  q/out/lse as in ssd_verify_attn.  block_size must be 64.
+ */
+int ssd_block_union(const int32_t *blocks, const int32_t *bcnt, int n_units, int n_cand, int kb,
+                    int nblk_max, int32_t *uidx, uint32_t *umask, int32_t *ucnt, int umax,
+                    ssd_stream_t stream);
+size_t ssd_block_sparse_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand, int umax);
+int ssd_block_sparse_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand,
+                          const int32_t *uidx, const uint32_t *umask, const int32_t *ucnt, int umax,
+                          int block_size, float scale, float *out, float *lse, void *workspace,
+                          size_t workspace_bytes, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Split-KV combine (the log-sum-exp merge the verify and draft passes use internally).
+ * o_parts device float [n_rows][n_splits][d] (each split's normalised output), lse_parts device
+ * float [n_rows][n_splits] (natural-log LSE of each split; -inf for an empty split).  Writes
+ * out [n_rows][d] = sum_j exp(lse_j - lse*) o_j and lse [n_rows] = log sum_j exp(lse_j) (NULL to
+ * skip); all-empty rows give out = 0, lse = -inf.
+ */
+int ssd_combine(const float *o_parts, const float *lse_parts, int n_rows, int n_splits, int d,
+                float *out, float *lse, ssd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H_ */

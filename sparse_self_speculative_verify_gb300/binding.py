@@ -1,0 +1,383 @@
+"""Thin Python binding of libssd (the C ABI in include/ssd.h).
+
+Argument marshalling only: tensors are checked for device/dtype/contiguity, turned into raw
+pointers and passed with torch's current CUDA stream.  Every step of the computation runs in the
+CUDA kernels of libssd.so; there is no fallback.  If the library has not been built, every call
+raises ``LibraryNotBuilt`` -- build it with ``sparse_self_speculative_verify_gb300.build.build()``.
+
+PyTorch supplies device memory (outputs and zero-initialised workspaces) and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = range(6)
+SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
+FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION = 1, 2, 4, 8, 16
+
+EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
+            "ssd_select_topk", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_unified_workspace_bytes",
+            "ssd_unified_attn", "ssd_block_union", "ssd_block_sparse_workspace_bytes", "ssd_block_sparse_attn",
+            "ssd_combine"]
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class SSDError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class PagedKVStruct(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("dtype", ctypes.c_int), ("num_pages", ctypes.c_int64),
+                ("page_size", ctypes.c_int), ("h_kv", ctypes.c_int), ("d", ctypes.c_int),
+                ("page_table", ctypes.c_void_p), ("max_pages", ctypes.c_int), ("seq_lens", ctypes.c_void_p),
+                ("batch", ctypes.c_int), ("max_seq_len", ctypes.c_int)]
+
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load(path: Optional[str] = None):
+    """Load libssd.so (no build step).  Raises LibraryNotBuilt when it is missing."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None and path is None:
+            return _LIB
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise LibraryNotBuilt(f"{p} does not exist; build it with sparse_self_speculative_verify_gb300.build.build()")
+        L = ctypes.CDLL(p)
+        P, I, I64, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        KV = ctypes.POINTER(PagedKVStruct)
+        sig = {
+            "ssd_last_error": ([], ctypes.c_char_p),
+            "ssd_version": ([], I),
+            "ssd_status": ([P, ctypes.POINTER(ctypes.c_uint32)], I),
+            "ssd_verify_workspace_bytes": ([KV, I, I], S),
+            "ssd_verify_attn": ([KV, P, I, I, F, P, P, P, I64, P, I64, I, P, S, P], I),
+            "ssd_select_topk": ([P, I64, P, P, I, I, I, I, P, I, P, P], I),
+            "ssd_draft_workspace_bytes": ([KV, I, I], S),
+            "ssd_draft_attn": ([KV, P, I, P, I, P, F, P, P, P, S, P], I),
+            "ssd_unified_workspace_bytes": ([KV, I, I, I], S),
+            "ssd_unified_attn": ([KV, P, P, P, I, I, P, I, P, F, P, P, P, I64, P, P, P, S, P], I),
+            "ssd_block_union": ([P, P, I, I, I, I, P, P, P, I, P], I),
+            "ssd_block_sparse_workspace_bytes": ([KV, I, I, I], S),
+            "ssd_block_sparse_attn": ([KV, P, I, I, P, P, P, I, I, F, P, P, P, S, P], I),
+            "ssd_combine": ([P, P, I, I, I, P, P, P], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        if path is None:
+            _LIB = L
+        return L
+
+
+def _lib():
+    return _LIB if _LIB is not None else load()
+
+
+def _check(rc: int):
+    if rc != SSD_OK:
+        raise SSDError(rc, _lib().ssd_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+# ------------------------------------------------------------------------------------------------
+# Paged KV cache handle and workspaces.
+# ------------------------------------------------------------------------------------------------
+
+
+@dataclass
+class KVCache:
+    """pool [num_pages, 2, h_kv, page_size, d] (bf16 or fp32), page_table [B, max_pages] int32,
+    seq_lens [B] int32, max_seq_len (host int, >= every seq_len)."""
+    pool: torch.Tensor
+    page_table: torch.Tensor
+    seq_lens: torch.Tensor
+    max_seq_len: int
+
+    def __post_init__(self):
+        _need(self.pool, "pool")
+        _need(self.page_table, "page_table", torch.int32, self.pool.device)
+        _need(self.seq_lens, "seq_lens", torch.int32, self.pool.device)
+        if self.pool.dim() != 5 or self.pool.shape[1] != 2:
+            raise ValueError("pool must be [num_pages, 2, h_kv, page_size, d]")
+        if self.pool.dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError("pool must be bf16 or fp32")
+        self._struct = PagedKVStruct(
+            self.pool.data_ptr(), SSD_DTYPE_BF16 if self.pool.dtype == torch.bfloat16 else SSD_DTYPE_F32,
+            self.pool.shape[0], self.pool.shape[3], self.pool.shape[2], self.pool.shape[4],
+            self.page_table.data_ptr(), self.page_table.shape[1], self.seq_lens.data_ptr(),
+            self.seq_lens.shape[0], int(self.max_seq_len))
+
+    @property
+    def h_kv(self) -> int:
+        return self.pool.shape[2]
+
+    @property
+    def d(self) -> int:
+        return self.pool.shape[4]
+
+    @property
+    def batch(self) -> int:
+        return self.seq_lens.shape[0]
+
+    @property
+    def device(self):
+        return self.pool.device
+
+    def ref(self):
+        return ctypes.byref(self._struct)
+
+    @classmethod
+    def from_workload(cls, w) -> "KVCache":
+        return cls(w.pool, w.page_table, w.seq_lens, w.max_seq_len)
+
+
+class Workspace:
+    """Zero-initialised device scratch buffers, grown on demand, one per (device, name).  The
+    library returns its counters to zero after each call, so a buffer is zeroed only once."""
+
+    def __init__(self):
+        self._bufs = {}
+
+    def get(self, device, name: str, nbytes: int) -> torch.Tensor:
+        key = (str(device), name)
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(int(nbytes), 256) + 256, dtype=torch.uint8, device=device)
+            self._bufs[key] = buf
+        return buf
+
+    @staticmethod
+    def aligned(buf: torch.Tensor) -> int:
+        p = buf.data_ptr()
+        return (p + 255) & ~255
+
+
+_DEFAULT_WS = Workspace()
+
+
+def _ws(kv_device, name, nbytes, workspace: Optional[Workspace]):
+    ws = (workspace or _DEFAULT_WS).get(kv_device, name, nbytes)
+    base = Workspace.aligned(ws)
+    avail = ws.data_ptr() + ws.numel() - base
+    return ctypes.c_void_p(base), avail
+
+
+# ------------------------------------------------------------------------------------------------
+# Calls (same names as the C ABI).
+# ------------------------------------------------------------------------------------------------
+
+
+def ssd_version() -> int:
+    return _lib().ssd_version()
+
+
+def ssd_status(stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(_lib().ssd_status(_stream(stream), ctypes.byref(v)))
+    return v.value
+
+
+def ssd_verify_attn(kv: KVCache, q: torch.Tensor, n_cand: int, scale: float, *, out=None, lse=None,
+                    scores: Optional[torch.Tensor] = None, bscores: Optional[torch.Tensor] = None,
+                    block_size: int = 64, want_scores: bool = True, want_lse: bool = True,
+                    workspace: Optional[Workspace] = None, stream=None) -> dict:
+    """Verify attention over the paged cache with fused criticality.  q [B, n_cand, h_q, d]."""
+    _need(q, "q", kv.pool.dtype, kv.device)
+    B, nc, h_q, d = q.shape
+    assert nc == n_cand and B == kv.batch and d == kv.d
+    dev = kv.device
+    if out is None:
+        out = torch.empty((B, nc, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, nc, h_q), dtype=torch.float32, device=dev)
+    if scores is None and want_scores:
+        scores = torch.zeros((B, kv.h_kv, max(kv.max_seq_len, 1)), dtype=torch.float32, device=dev)
+    for t, n in ((out, "out"), (lse, "lse"), (scores, "scores"), (bscores, "bscores")):
+        if t is not None:
+            _need(t, n, torch.float32, dev)
+    L = _lib()
+    need = L.ssd_verify_workspace_bytes(kv.ref(), h_q, n_cand)
+    wsp, avail = _ws(dev, "verify", need, workspace)
+    _check(L.ssd_verify_attn(kv.ref(), _ptr(q), h_q, n_cand, float(scale), _ptr(out), _ptr(lse), _ptr(scores),
+                             scores.shape[-1] if scores is not None else 0, _ptr(bscores),
+                             bscores.shape[-1] if bscores is not None else 0, block_size, wsp, avail,
+                             _stream(stream)))
+    return {"out": out, "lse": lse, "scores": scores, "bscores": bscores}
+
+
+def ssd_select_topk(scores: torch.Tensor, lens: torch.Tensor, ks: torch.Tensor, k_max: int, rows_per_group: int,
+                    len_div: int = 1, max_len: Optional[int] = None, *, idx=None, cnt=None, stream=None):
+    """Top-K per row of a [n_rows, stride] (or [..., stride]) fp32 score tensor."""
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    _need(lens, "lens", torch.int32, dev)
+    _need(ks, "ks", torch.int32, dev)
+    stride = scores.shape[-1]
+    n_rows = scores.numel() // stride
+    n_groups = lens.shape[0]
+    assert n_groups * rows_per_group == n_rows and ks.shape[0] == n_groups
+    if max_len is None:
+        max_len = stride
+    if idx is None:
+        idx = torch.empty((n_rows, max(k_max, 0)), dtype=torch.int32, device=dev)
+    if cnt is None:
+        cnt = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(cnt, "cnt", torch.int32, dev)
+    _check(_lib().ssd_select_topk(_ptr(scores), stride, _ptr(lens), _ptr(ks), n_groups, rows_per_group, len_div,
+                                  int(max_len), _ptr(idx), k_max, _ptr(cnt), _stream(stream)))
+    return idx, cnt
+
+
+def ssd_draft_attn(kv: KVCache, q: torch.Tensor, idx: torch.Tensor, cnt: torch.Tensor, scale: float, *, out=None,
+                   lse=None, want_lse: bool = True, workspace: Optional[Workspace] = None, stream=None) -> dict:
+    """Single-query attention over the selected tokens.  q [B, h_q, d]; idx [B, h_kv, k_max]."""
+    _need(q, "q", kv.pool.dtype, kv.device)
+    dev = kv.device
+    _need(idx, "idx", torch.int32, dev)
+    _need(cnt, "cnt", torch.int32, dev)
+    B, h_q, d = q.shape
+    k_max = idx.shape[-1]
+    if out is None:
+        out = torch.empty((B, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h_q), dtype=torch.float32, device=dev)
+    L = _lib()
+    need = L.ssd_draft_workspace_bytes(kv.ref(), h_q, k_max)
+    wsp, avail = _ws(dev, "draft", need, workspace)
+    _check(L.ssd_draft_attn(kv.ref(), _ptr(q), h_q, _ptr(idx), k_max, _ptr(cnt), float(scale), _ptr(out), _ptr(lse),
+                            wsp, avail, _stream(stream)))
+    return {"out": out, "lse": lse}
+
+
+def ssd_unified_attn(kv: KVCache, phase: torch.Tensor, q_verify: torch.Tensor, q_draft: torch.Tensor, n_cand: int,
+                     idx: torch.Tensor, cnt: torch.Tensor, scale: float, *, out_verify=None, lse_verify=None,
+                     scores=None, out_draft=None, lse_draft=None, want_scores: bool = True,
+                     workspace: Optional[Workspace] = None, stream=None) -> dict:
+    """Mixed batch: verify-phase requests (phase == 1) and draft-phase requests (phase == 0) in one
+    persistent launch, then the verify finalize."""
+    dev = kv.device
+    _need(phase, "phase", torch.uint8, dev)
+    _need(q_verify, "q_verify", kv.pool.dtype, dev)
+    _need(q_draft, "q_draft", kv.pool.dtype, dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(cnt, "cnt", torch.int32, dev)
+    B, nc, h_q, d = q_verify.shape
+    k_max = idx.shape[-1]
+    if out_verify is None:
+        out_verify = torch.zeros((B, nc, h_q, d), dtype=torch.float32, device=dev)
+    if lse_verify is None:
+        lse_verify = torch.zeros((B, nc, h_q), dtype=torch.float32, device=dev)
+    if scores is None and want_scores:
+        scores = torch.zeros((B, kv.h_kv, max(kv.max_seq_len, 1)), dtype=torch.float32, device=dev)
+    if out_draft is None:
+        out_draft = torch.zeros((B, h_q, d), dtype=torch.float32, device=dev)
+    if lse_draft is None:
+        lse_draft = torch.zeros((B, h_q), dtype=torch.float32, device=dev)
+    L = _lib()
+    need = L.ssd_unified_workspace_bytes(kv.ref(), h_q, n_cand, k_max)
+    wsp, avail = _ws(dev, "unified", need, workspace)
+    _check(L.ssd_unified_attn(kv.ref(), _ptr(phase), _ptr(q_verify), _ptr(q_draft), h_q, n_cand, _ptr(idx), k_max,
+                              _ptr(cnt), float(scale), _ptr(out_verify), _ptr(lse_verify), _ptr(scores),
+                              scores.shape[-1] if scores is not None else 0, _ptr(out_draft), _ptr(lse_draft), wsp,
+                              avail, _stream(stream)))
+    return {"out_verify": out_verify, "lse_verify": lse_verify, "scores": scores, "out_draft": out_draft,
+            "lse_draft": lse_draft}
+
+
+def ssd_block_union(blocks: torch.Tensor, bcnt: torch.Tensor, nblk_max: int, umax: Optional[int] = None, *,
+                    stream=None):
+    """Union of the candidates' block sets.  blocks [units, n_cand, kb], bcnt [units, n_cand]."""
+    _need(blocks, "blocks", torch.int32)
+    dev = blocks.device
+    _need(bcnt, "bcnt", torch.int32, dev)
+    U, nc, kb = blocks.shape
+    um = umax or nc * kb
+    uidx = torch.empty((U, um), dtype=torch.int32, device=dev)
+    umask = torch.empty((U, um), dtype=torch.int32, device=dev)  # uint32 bit patterns
+    ucnt = torch.empty((U,), dtype=torch.int32, device=dev)
+    _check(_lib().ssd_block_union(_ptr(blocks), _ptr(bcnt), U, nc, kb, nblk_max, _ptr(uidx), _ptr(umask), _ptr(ucnt),
+                                  um, _stream(stream)))
+    return uidx, umask, ucnt
+
+
+def ssd_block_sparse_attn(kv: KVCache, q: torch.Tensor, n_cand: int, uidx: torch.Tensor, umask: torch.Tensor,
+                          ucnt: torch.Tensor, scale: float, block_size: int = 64, *, out=None, lse=None,
+                          workspace: Optional[Workspace] = None, stream=None) -> dict:
+    """Block-sparse attention of the candidates over their union blocks (each loaded once)."""
+    dev = kv.device
+    _need(q, "q", kv.pool.dtype, dev)
+    _need(uidx, "uidx", torch.int32, dev)
+    _need(umask, "umask", torch.int32, dev)
+    _need(ucnt, "ucnt", torch.int32, dev)
+    B, nc, h_q, d = q.shape
+    umax = uidx.shape[-1]
+    if out is None:
+        out = torch.empty((B, nc, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((B, nc, h_q), dtype=torch.float32, device=dev)
+    L = _lib()
+    need = L.ssd_block_sparse_workspace_bytes(kv.ref(), h_q, n_cand, umax)
+    wsp, avail = _ws(dev, "block", need, workspace)
+    _check(L.ssd_block_sparse_attn(kv.ref(), _ptr(q), h_q, n_cand, _ptr(uidx), _ptr(umask), _ptr(ucnt), umax,
+                                   block_size, float(scale), _ptr(out), _ptr(lse), wsp, avail, _stream(stream)))
+    return {"out": out, "lse": lse}
+
+
+def ssd_combine(o_parts: torch.Tensor, lse_parts: torch.Tensor, *, out=None, lse=None, stream=None):
+    """LSE merge of split partials: o_parts [rows, splits, d], lse_parts [rows, splits]."""
+    _need(o_parts, "o_parts", torch.float32)
+    dev = o_parts.device
+    _need(lse_parts, "lse_parts", torch.float32, dev)
+    R, S, d = o_parts.shape
+    if out is None:
+        out = torch.empty((R, d), dtype=torch.float32, device=dev)
+    if lse is None:
+        lse = torch.empty((R,), dtype=torch.float32, device=dev)
+    _check(_lib().ssd_combine(_ptr(o_parts), _ptr(lse_parts), R, S, d, _ptr(out), _ptr(lse), _stream(stream)))
+    return out, lse

@@ -1,0 +1,109 @@
+// ssd_draft.cu -- sparse draft attention (SparseSpec §4.1: the k drafts after a verify attend only
+// the tokens it selected; §4.2: sparse attention = PagedAttention over a token list).
+#include "ssd_draft_tile.cuh"
+#include "ssd_host.h"
+
+namespace ssd {
+
+template <int D, typename T, int GMAX>
+__global__ void __launch_bounds__(128) draft_kernel(DraftArgs a) {
+  extern __shared__ __align__(128) char smem[];
+  draft_item<D, T, GMAX>(a, blockIdx.y, blockIdx.x, smem);
+}
+
+int draft_gmax(int G) { return G <= 4 ? 4 : (G <= 8 ? 8 : 16); }
+
+template <int D, typename T, int GMAX>
+static int launch_draft(const DraftArgs &a, dim3 grid, cudaStream_t st) {
+  constexpr int smem = DraftCfg<D, T, GMAX>::SMEM;
+  static_assert(2 * DraftCfg<D, T, GMAX>::TILE >= (128 / (D / 2)) * GMAX * D * 4, "reduction area");
+  int rc = ensure_smem<draft_kernel<D, T, GMAX>>(smem);
+  if (rc) return rc;
+  draft_kernel<D, T, GMAX><<<grid, 128, smem, st>>>(a);
+  return check_launch("draft_kernel");
+}
+
+template <int D, typename T>
+static int dispatch_g(int gmax, const DraftArgs &a, dim3 grid, cudaStream_t st) {
+  if (gmax == 4) return launch_draft<D, T, 4>(a, grid, st);
+  if (gmax == 8) return launch_draft<D, T, 8>(a, grid, st);
+  return launch_draft<D, T, 16>(a, grid, st);
+}
+
+int launch_draft_any(int dtype, int D, const DraftArgs &a, dim3 grid, cudaStream_t st) {
+  const int gmax = draft_gmax(a.G);
+  if (dtype == SSD_DTYPE_BF16)
+    return D == 128 ? dispatch_g<128, __nv_bfloat16>(gmax, a, grid, st) : dispatch_g<64, __nv_bfloat16>(gmax, a, grid, st);
+  return D == 128 ? dispatch_g<128, float>(gmax, a, grid, st) : dispatch_g<64, float>(gmax, a, grid, st);
+}
+
+// Workspace of the draft partials: o [units][C_max][GMAX][D], lse [units][C_max][GMAX], counters [units].
+size_t draft_ws_bytes(int units, int C_max, int gmax, int D) {
+  Carver c(nullptr);
+  c.take<float>((size_t)units * C_max * gmax * D);
+  c.take<float>((size_t)units * C_max * gmax);
+  c.take<unsigned>((size_t)units);
+  return c.off;
+}
+
+void draft_ws_carve(void *ws, int units, int C_max, int gmax, int D, DraftArgs &a) {
+  Carver c(ws);
+  a.o_parts = c.take<float>((size_t)units * C_max * gmax * D);
+  a.lse_parts = c.take<float>((size_t)units * C_max * gmax);
+  a.counters = c.take<unsigned>((size_t)units);
+}
+
+int draft_checks(const ssd_paged_kv *kv, int h_q, const void *q, const int32_t *idx, int k_max, const int32_t *cnt,
+                 const float *out, const char *who) {
+  if (!q || !idx || !cnt || !out) return fail(SSD_ERR_INVALID_ARG, "%s: q, idx, cnt and out must be non-NULL", who);
+  if (h_q <= 0 || h_q % kv->h_kv) return fail(SSD_ERR_INVALID_ARG, "%s: h_q %d not a multiple of h_kv", who, h_q);
+  if (h_q / kv->h_kv > 16) return fail(SSD_ERR_UNSUPPORTED, "%s: group size %d > 16", who, h_q / kv->h_kv);
+  if (k_max < 0) return fail(SSD_ERR_INVALID_ARG, "%s: k_max < 0", who);
+  if ((int64_t)kv->batch * kv->h_kv > 65535) return fail(SSD_ERR_UNSUPPORTED, "%s: batch*h_kv above 65535", who);
+  return SSD_OK;
+}
+
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" size_t ssd_draft_workspace_bytes(const ssd_paged_kv *kv, int h_q, int k_max) {
+  if (!kv || kv->h_kv <= 0 || h_q <= 0 || k_max < 0 || kv->batch < 0 || (kv->d != 64 && kv->d != 128)) return 0;
+  return draft_ws_bytes(kv->batch * kv->h_kv, cdiv(k_max > 0 ? k_max : 1, kDraftChunk), draft_gmax(h_q / kv->h_kv),
+                        kv->d);
+}
+
+extern "C" int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
+                              const int32_t *cnt, float scale, float *out, float *lse, void *workspace,
+                              size_t workspace_bytes, ssd_stream_t stream) {
+  const char *who = "ssd_draft_attn";
+  KVView v;
+  int rc = validate_kv(kv, &v, who);
+  if (rc) return rc;
+  if ((rc = draft_checks(kv, h_q, q, idx, k_max, cnt, out, who))) return rc;
+  const size_t need = ssd_draft_workspace_bytes(kv, h_q, k_max);
+  if (!workspace || workspace_bytes < need)
+    return fail(SSD_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", who, workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(SSD_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  if (kv->batch == 0) return SSD_OK;
+  unsigned *status = device_status();
+  if (!status) return SSD_ERR_CUDA;
+  const int units = kv->batch * kv->h_kv;
+  const int C_max = cdiv(k_max > 0 ? k_max : 1, kDraftChunk);
+  DraftArgs a{};
+  a.kv = v;
+  a.q = q;
+  a.h_q = h_q;
+  a.G = h_q / kv->h_kv;
+  a.k_max = k_max;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.scale_log2 = scale * kLog2e;
+  a.C_max = C_max;
+  a.out = out;
+  a.lse = lse;
+  a.status = status;
+  draft_ws_carve(workspace, units, C_max, draft_gmax(a.G), kv->d, a);
+  return launch_draft_any(kv->dtype, kv->d, a, dim3(C_max, units), reinterpret_cast<cudaStream_t>(stream));
+}

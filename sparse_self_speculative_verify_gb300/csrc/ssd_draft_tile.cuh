@@ -1,0 +1,249 @@
+// ssd_draft_tile.cuh -- one draft work item: up to kDraftChunk selected tokens of one (request b,
+// KV head g), all G query heads of the group.
+//
+// SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
+// Sparse Attention") §4.1: the k drafts after a verify load and attend only the critical tokens the
+// verify selected; §4.2: sparse attention is PagedAttention with page size 1, i.e. attention over an
+// explicit token list.  A single query row per head carries too little reuse for tensor cores, so
+// the item runs on CUDA cores in fp32: the selected K and V rows are gathered into swizzled shared
+// memory with 16-byte cp.async (one K row = one contiguous 256-byte line of the page), every K/V
+// element is reused by the G heads of the group, and the chunk's partial result is merged with the
+// other chunks of the same (request, KV head) by the last chunk to finish (atomic ticket, no wait).
+#pragma once
+
+#include "ssd_common.cuh"
+
+namespace ssd {
+
+struct DraftArgs {
+  KVView kv;
+  const void *q;  // [B][h_q][D]
+  int h_q, G, k_max;
+  const int32_t *idx;  // [B][h_kv][k_max]
+  const int32_t *cnt;  // [B][h_kv]
+  float scale_log2;
+  int C_max;           // chunks per unit in the partial arrays
+  float *o_parts;      // [units][C_max][G][D]
+  float *lse_parts;    // [units][C_max][G]
+  unsigned *counters;  // [units], zero between calls
+  float *out;          // [B][h_q][D]
+  float *lse;          // [B][h_q] or nullptr
+  const uint8_t *phase;  // unified launch: draft items only for phase == 0 (nullptr otherwise)
+  unsigned *status;
+};
+
+template <int D, typename T, int GMAX>
+struct DraftCfg {
+  static constexpr int ROWB = D * (int)sizeof(T);  // bytes of one K or V row
+  static constexpr int CPR = ROWB / 16;
+  static constexpr int TILE = kDraftChunk * ROWB;
+  static constexpr int SMEM = 2 * TILE + (GMAX * D + GMAX * kDraftChunk + 2 * GMAX) * 4;
+};
+
+__device__ __forceinline__ int draft_chunks(int n) { return n <= 0 ? 1 : cdiv(n, kDraftChunk); }
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4 &v, float *f);
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4 &v, float *f) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4 &v, float *f) {
+  f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+}
+
+template <int D, typename T, int GMAX>
+__device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chunk, char *smem) {
+  using C = DraftCfg<D, T, GMAX>;
+  constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h_kv = a.kv.h_kv;
+  const int b = unit / h_kv, g = unit % h_kv, G = a.G;
+  const int L = effective_len(a.kv, b, 0, a.status);
+  int n_all = a.cnt[unit];
+  if (n_all < 0 || n_all > a.k_max) {
+    atomicOr(a.status, (unsigned)SSD_FAULT_KMAX);
+    n_all = n_all < 0 ? 0 : a.k_max;
+  }
+  const int n_chunks = draft_chunks(n_all);
+  if (chunk >= n_chunks) return;
+  const int j0 = chunk * kDraftChunk;
+  const int n = min(kDraftChunk, n_all - j0);  // may be 0 for an empty list
+
+  char *sKt = smem;
+  char *sVt = smem + C::TILE;
+  float *sQ = reinterpret_cast<float *>(smem + 2 * C::TILE);  // [GMAX][D]
+  float *sS = sQ + GMAX * D;                                   // [GMAX][kDraftChunk]
+  float *sM = sS + GMAX * kDraftChunk;                         // [GMAX]
+  float *sL = sM + GMAX;                                       // [GMAX]
+
+  // Gather the chunk's K and V rows.
+  const int32_t *tok = a.idx + (int64_t)unit * a.k_max + j0;
+  const int64_t v_off = (int64_t)h_kv * a.kv.page_size * D;
+  for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
+    int j = c / C::CPR, ch = c % C::CPR;
+    const T *kr = nullptr;
+    if (j < n) {
+      int t = __ldg(tok + j);
+      if (t >= 0 && t < L) kr = kv_row<D, T>(a.kv, b, 0, g, t, a.status);
+      else if (ch == 0) atomicOr(a.status, (unsigned)SSD_FAULT_INDEX);
+    }
+    uint32_t off = j * C::ROWB + swz_chunk(j, ch) * 16;
+    cp_async16(smem_u32(sKt + off), kr ? (const void *)(kr + ch * EPC) : a.kv.pool, kr ? 16 : 0);
+    cp_async16(smem_u32(sVt + off), kr ? (const void *)(kr + v_off + ch * EPC) : a.kv.pool, kr ? 16 : 0);
+  }
+  cp_async_commit();
+  const T *q = reinterpret_cast<const T *>(a.q);
+  for (int e = tid; e < G * D; e += blockDim.x) {
+    int hl = e / D, dd = e % D;
+    sQ[e] = to_f32<T>(q[((int64_t)b * a.h_q + g * G + hl) * D + dd]);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // Logits: thread pair (2j, 2j+1) computes token j, one half of d each.
+  {
+    const int j = tid >> 1, half = tid & 1;
+    float acc[GMAX];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < C::CPR / 2; ++c) {
+      int ch = half * (C::CPR / 2) + c;
+      uint4 raw = *reinterpret_cast<const uint4 *>(sKt + j * C::ROWB + swz_chunk(j, ch) * 16);
+      float kf[EPC];
+      unpack16<T>(raw, kf);
+      const int d0 = ch * EPC;
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (h < G) {
+          const float *qh = sQ + h * D + d0;
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) acc[h] = fmaf(qh[e], kf[e], acc[h]);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      float s = acc[h] + __shfl_xor_sync(0xffffffffu, acc[h], 1);
+      if (half == 0 && h < G) sS[h * kDraftChunk + j] = (j < n) ? s * a.scale_log2 : -INFINITY;
+    }
+  }
+  __syncthreads();
+
+  // Softmax over the chunk, one warp per head.
+  for (int h = warp; h < G; h += blockDim.x / 32) {
+    float v0 = sS[h * kDraftChunk + lane], v1 = sS[h * kDraftChunk + lane + 32];
+    float m = warp_max(fmaxf(v0, v1));
+    float base = (m == -INFINITY) ? 0.f : m;
+    float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
+    sS[h * kDraftChunk + lane] = p0;
+    sS[h * kDraftChunk + lane + 32] = p1;
+    float l = warp_sum(p0 + p1);
+    if (lane == 0) {
+      sM[h] = m;
+      sL[h] = l;
+    }
+  }
+  __syncthreads();
+
+  // O = P V: thread = (pair of d columns, token part).
+  constexpr int NPAIR = D / 2;
+  constexpr int PARTS = 128 / NPAIR;
+  constexpr int TPP = kDraftChunk / PARTS;  // tokens per part
+  const int dp = tid % NPAIR, part = tid / NPAIR;
+  float acc0[GMAX], acc1[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) acc0[h] = acc1[h] = 0.f;
+  {
+    const int byte = dp * 2 * (int)sizeof(T);
+    const int ch = byte / 16, within = byte % 16;
+    for (int jj = 0; jj < TPP; ++jj) {
+      int j = part * TPP + jj;
+      const char *src = sVt + j * C::ROWB + swz_chunk(j, ch) * 16 + within;
+      float v0, v1;
+      if (sizeof(T) == 2) {
+        uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+        v0 = bf16_lo(w);
+        v1 = bf16_hi(w);
+      } else {
+        float2 w = *reinterpret_cast<const float2 *>(src);
+        v0 = w.x;
+        v1 = w.y;
+      }
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (h < G) {
+          float p = sS[h * kDraftChunk + j];
+          acc0[h] = fmaf(p, v0, acc0[h]);
+          acc1[h] = fmaf(p, v1, acc1[h]);
+        }
+      }
+    }
+  }
+  __syncthreads();  // K tile is free: reuse it for the part reduction
+  float *red = reinterpret_cast<float *>(sKt);  // [PARTS][GMAX][D]
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    if (h < G) {
+      red[(part * GMAX + h) * D + 2 * dp] = acc0[h];
+      red[(part * GMAX + h) * D + 2 * dp + 1] = acc1[h];
+    }
+  }
+  __syncthreads();
+
+  const bool single = (n_chunks == 1);
+  const int64_t prow = ((int64_t)unit * a.C_max + chunk) * GMAX;
+  for (int e = tid; e < G * D; e += blockDim.x) {
+    int h = e / D, dd = e % D;
+    float s = 0.f;
+#pragma unroll
+    for (int p = 0; p < PARTS; ++p) s += red[(p * GMAX + h) * D + dd];
+    float l = sL[h];
+    bool empty = !(l > 0.f);
+    float ov = empty ? 0.f : s / l;
+    float lv = empty ? -INFINITY : (sM[h] + __log2f(l)) * kLn2;
+    if (single) {
+      int64_t row = (int64_t)b * a.h_q + g * G + h;
+      a.out[row * D + dd] = ov;
+      if (dd == 0 && a.lse) a.lse[row] = lv;
+    } else {
+      a.o_parts[(prow + h) * D + dd] = ov;
+      if (dd == 0) a.lse_parts[prow + h] = lv;
+    }
+  }
+  if (single) return;
+
+  // Last chunk of this unit to finish merges all chunks (no waiting on other blocks).
+  __threadfence();
+  __syncthreads();
+  __shared__ unsigned s_last;
+  if (tid == 0) s_last = (atomicAdd(a.counters + unit, 1u) == (unsigned)(n_chunks - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int e = tid; e < G * D; e += blockDim.x) {
+    int h = e / D, dd = e % D;
+    float M = -INFINITY;
+    for (int c = 0; c < n_chunks; ++c)
+      M = fmaxf(M, __ldcg(a.lse_parts + ((int64_t)unit * a.C_max + c) * GMAX + h));
+    float acc = 0.f, wsum = 0.f;
+    if (M != -INFINITY) {
+      for (int c = 0; c < n_chunks; ++c) {
+        int64_t pr = ((int64_t)unit * a.C_max + c) * GMAX + h;
+        float w = fast_exp2((__ldcg(a.lse_parts + pr) - M) * kLog2e);
+        wsum += w;
+        acc = fmaf(w, __ldcg(a.o_parts + pr * D + dd), acc);
+      }
+    }
+    int64_t row = (int64_t)b * a.h_q + g * G + h;
+    a.out[row * D + dd] = (wsum > 0.f) ? acc / wsum : 0.f;
+    if (dd == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? M + __logf(wsum) : -INFINITY;
+  }
+  if (tid == 0) a.counters[unit] = 0u;
+}
+
+}  // namespace ssd

@@ -1,0 +1,62 @@
+// ssd_host.h -- host-side helpers shared by the libssd translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ssd.h"
+#include "ssd_common.cuh"
+
+namespace ssd {
+
+// Records a formatted message as the calling thread's last error and returns `code`.
+int fail(int code, const char *fmt, ...);
+// Maps a pending CUDA launch error to SSD_ERR_CUDA (clearing it); SSD_OK otherwise.
+int check_launch(const char *what);
+// Device status word of the current device (nullptr + error message on failure).
+unsigned *device_status();
+// Number of SMs of the current device (cached).
+int sm_count();
+// Validates the cache description; fills `v`.  `need_mask` lists the accepted dtypes as bits.
+int validate_kv(const ssd_paged_kv *kv, KVView *v, const char *who);
+
+// Raises the dynamic shared-memory limit of `Kernel` to at least `bytes` on the current device;
+// the attribute call is made only when the limit has to grow, so launches during CUDA-graph
+// capture (after an eager warm-up) make no attribute calls.
+template <auto Kernel>
+int ensure_smem(int bytes) {
+  static int set_bytes[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return fail(SSD_ERR_CUDA, "no current CUDA device");
+  }
+  if (set_bytes[dev] >= bytes) return SSD_OK;
+  cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SSD_ERR_CUDA, "cudaFuncSetAttribute(%d bytes): %s", bytes, cudaGetErrorString(e));
+  }
+  set_bytes[dev] = bytes;
+  return SSD_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Carves consecutive 256-byte aligned regions out of a workspace.
+struct Carver {
+  char *base;
+  size_t off = 0;
+  explicit Carver(void *p) : base(static_cast<char *>(p)) {}
+  template <typename T>
+  T *take(size_t count) {
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off = align256(off + count * sizeof(T));
+    return p;
+  }
+};
+
+}  // namespace ssd

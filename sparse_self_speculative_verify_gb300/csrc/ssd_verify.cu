@@ -1,0 +1,410 @@
+// ssd_verify.cu -- verify attention with fused criticality, the split-KV finalize (LSE combine +
+// criticality rematerialisation + block max-pool), the block-sparse union pass and the public
+// split combine.
+//
+// SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
+// Sparse Attention") §4.1 PillarAttn: the verify kernel dumps the attention scores while it runs,
+// caching logits and LSE to rematerialise them; scores are reduced over the GQA group's heads and
+// the verify positions.  SpecSA post, "overlap-aware grouped query execution": candidates whose
+// sparse layouts overlap run together so shared KV blocks are loaded once.  SparDA §2: fine scores
+// are max-pooled onto the coarser selection grid.
+#include "ssd_host.h"
+#include "ssd_verify_tile.cuh"
+
+namespace ssd {
+
+// ------------------------------------------------------------------------------------------------
+// Verify kernels: grid (split, unit); one work item per block.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ int clamp_len(const KVView &kv, int b) {
+  int L = kv.seq_lens[b];
+  return L < 0 ? 0 : (L > kv.max_seq_len ? kv.max_seq_len : L);
+}
+
+template <int D, int NRT, bool BLOCKS>
+__global__ void __launch_bounds__(128, 2) verify_mma_kernel(VerifyArgs a) {
+  extern __shared__ __align__(128) char smem[];
+  const int unit = blockIdx.y, split = blockIdx.x;
+  if (BLOCKS) {
+    int nu = min(max(a.ucnt[unit], 0), a.umax);
+    if (split >= block_splits(nu)) return;
+  } else {
+    if (split >= verify_splits(clamp_len(a.kv, unit / a.kv.h_kv))) return;
+  }
+  verify_item_mma<D, NRT, BLOCKS>(a, unit, split, smem);
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) verify_simt_kernel(VerifyArgs a) {
+  extern __shared__ __align__(128) char smem[];
+  const int unit = blockIdx.y, split = blockIdx.x;
+  if (split >= verify_splits(clamp_len(a.kv, unit / a.kv.h_kv))) return;
+  verify_item_simt<D>(a, unit, split, smem);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Finalize: grid (n_tok_ctas + 1, unit).  Every block first merges the unit's split LSEs per row;
+// the last block of a unit combines the outputs, the others rematerialise the criticality of
+// kFinTok tokens each: crit[t] = sum_r e[r][t] * 2^(m_ref[r][t/16] - LSE2_r).
+// ------------------------------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f) {
+  __shared__ float sLn[kMaxRows];
+  __shared__ float sL2[kMaxRows];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int u = blockIdx.y, b = u / f.h_kv, g = u % f.h_kv;
+  if (f.phase && f.phase[b] == 0) return;
+  int L = f.seq_lens[b];
+  L = L < 0 ? 0 : (L > f.max_seq_len ? f.max_seq_len : L);
+  const int ns = f.ucnt ? block_splits(min(max(f.ucnt[u], 0), f.umax)) : verify_splits(L);
+  const int64_t pbase = (int64_t)u * f.S_max * f.R;
+  for (int r = tid; r < f.R; r += blockDim.x) {
+    float M = -INFINITY;
+    for (int j = 0; j < ns; ++j) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
+    float s = 0.f;
+    if (M != -INFINITY)
+      for (int j = 0; j < ns; ++j) s += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
+    float ln = (M == -INFINITY) ? -INFINITY : M + __logf(s);
+    sLn[r] = ln;
+    sL2[r] = ln * kLog2e;
+  }
+  __syncthreads();
+
+  if (blockIdx.x == gridDim.x - 1) {
+    const int D = f.D;
+    for (int idx = tid; idx < f.R * D; idx += blockDim.x) {
+      int r = idx / D, dd = idx % D;
+      float ln = sLn[r], acc = 0.f;
+      if (ln != -INFINITY)
+        for (int j = 0; j < ns; ++j) {
+          int64_t pr = pbase + (int64_t)j * f.R + r;
+          float w = fast_exp2((f.lse_parts[pr] - ln) * kLog2e);
+          acc = fmaf(w, f.o_parts[pr * D + dd], acc);
+        }
+      int i = r / f.G, hl = r % f.G;
+      int64_t row = ((int64_t)b * f.n_c + i) * f.h_q + g * f.G + hl;
+      f.out[row * D + dd] = acc;
+      if (dd == 0 && f.lse) f.lse[row] = ln;
+    }
+    return;
+  }
+  if (!f.side_p) return;
+
+  const int t0 = blockIdx.x * kFinTok + tid * 8;
+  const bool valid = t0 < L;
+  const int nref = f.Lpad / kRefGroup;
+  float crit[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) crit[k] = 0.f;
+  for (int i = 0; i < f.n_c; ++i) {
+    float cc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cc[k] = 0.f;
+    if (valid) {
+      for (int hl = 0; hl < f.G; ++hl) {
+        int r = i * f.G + hl;
+        float l2 = sL2[r];
+        if (l2 == -INFINITY) continue;
+        int64_t rr = (int64_t)u * f.R + r;
+        float coef = fast_exp2(f.side_m[rr * nref + t0 / kRefGroup] - l2);
+        uint4 raw = *reinterpret_cast<const uint4 *>(f.side_p + rr * f.Lpad + t0);
+        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float2 pf = __half22float2(h2[k]);
+          cc[2 * k] = fmaf(pf.x, coef, cc[2 * k]);
+          cc[2 * k + 1] = fmaf(pf.y, coef, cc[2 * k + 1]);
+        }
+      }
+    }
+    if (f.bscores) {
+      float m = cc[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) m = fmaxf(m, cc[k]);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      if ((lane & 7) == 0 && valid)
+        f.bscores[((int64_t)u * f.n_c + i) * f.bstride + t0 / kBlockTokens] = m;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) crit[k] += cc[k];
+  }
+  if (f.scores && valid) {
+    float *dst = f.scores + (int64_t)u * f.scores_stride + t0;
+    if (t0 + 8 <= L && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
+      reinterpret_cast<float4 *>(dst)[0] = make_float4(crit[0], crit[1], crit[2], crit[3]);
+      reinterpret_cast<float4 *>(dst)[1] = make_float4(crit[4], crit[5], crit[6], crit[7]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (t0 + k < L) dst[k] = crit[k];
+    }
+  }
+}
+
+int launch_finalize(const FinalizeArgs &f, int n_tok, int units, cudaStream_t st) {
+  finalize_kernel<<<dim3(n_tok + 1, units), kFinThreads, 0, st>>>(f);
+  return check_launch("finalize_kernel");
+}
+
+// Public split combine: one block per row.
+__global__ void __launch_bounds__(128) combine_kernel(const float *o_parts, const float *lse_parts, int n_splits,
+                                                     int d, float *out, float *lse) {
+  const int row = blockIdx.x;
+  const float *lp = lse_parts + (int64_t)row * n_splits;
+  float M = -INFINITY;
+  for (int j = 0; j < n_splits; ++j) M = fmaxf(M, lp[j]);
+  float s = 0.f;
+  if (M != -INFINITY)
+    for (int j = 0; j < n_splits; ++j) s += fast_exp2((lp[j] - M) * kLog2e);
+  const float ln = (M == -INFINITY) ? -INFINITY : M + __logf(s);
+  for (int dd = threadIdx.x; dd < d; dd += blockDim.x) {
+    float acc = 0.f;
+    if (ln != -INFINITY)
+      for (int j = 0; j < n_splits; ++j)
+        acc = fmaf(fast_exp2((lp[j] - ln) * kLog2e), o_parts[((int64_t)row * n_splits + j) * d + dd], acc);
+    out[(int64_t)row * d + dd] = acc;
+  }
+  if (threadIdx.x == 0 && lse) lse[row] = ln;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Host side.
+// ------------------------------------------------------------------------------------------------
+static int rows_per_tile(int R) { return R <= 16 ? 1 : (R <= 32 ? 2 : 4); }
+
+template <int D, int NRT, bool BLOCKS>
+static int launch_mma(const VerifyArgs &a, dim3 grid, cudaStream_t st) {
+  constexpr int smem = VerifyMmaCfg<D, NRT>::SMEM;
+  int rc = ensure_smem<verify_mma_kernel<D, NRT, BLOCKS>>(smem);
+  if (rc) return rc;
+  verify_mma_kernel<D, NRT, BLOCKS><<<grid, 128, smem, st>>>(a);
+  return check_launch("verify_mma_kernel");
+}
+
+template <bool BLOCKS>
+static int dispatch_mma(int D, int NRT, const VerifyArgs &a, dim3 grid, cudaStream_t st) {
+  if (D == 128) {
+    if (NRT == 1) return launch_mma<128, 1, BLOCKS>(a, grid, st);
+    if (NRT == 2) return launch_mma<128, 2, BLOCKS>(a, grid, st);
+    return launch_mma<128, 4, BLOCKS>(a, grid, st);
+  }
+  if (NRT == 1) return launch_mma<64, 1, BLOCKS>(a, grid, st);
+  if (NRT == 2) return launch_mma<64, 2, BLOCKS>(a, grid, st);
+  return launch_mma<64, 4, BLOCKS>(a, grid, st);
+}
+
+template <int D>
+static int launch_simt(const VerifyArgs &a, dim3 grid, cudaStream_t st) {
+  constexpr int smem = VerifySimtCfg<D>::SMEM;
+  int rc = ensure_smem<verify_simt_kernel<D>>(smem);
+  if (rc) return rc;
+  verify_simt_kernel<D><<<grid, 128, smem, st>>>(a);
+  return check_launch("verify_simt_kernel");
+}
+
+struct VerifyLayout {
+  int G, R, units, S_max, Lpad;
+  size_t o_off, lse_off, sp_off, sm_off, total;
+};
+
+static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int S_max) {
+  VerifyLayout l{};
+  l.G = h_q / kv->h_kv;
+  l.R = l.G * n_cand;
+  l.units = kv->batch * kv->h_kv;
+  l.S_max = S_max;
+  l.Lpad = cdiv(kv->max_seq_len > 0 ? kv->max_seq_len : 1, kStageTokens) * kStageTokens;
+  Carver c(nullptr);
+  size_t rows = (size_t)l.units * l.S_max * l.R;
+  l.o_off = c.off;
+  c.take<float>(rows * kv->d);
+  l.lse_off = c.off;
+  c.take<float>(rows);
+  l.sp_off = c.off;
+  c.take<__half>((size_t)l.units * l.R * l.Lpad);
+  l.sm_off = c.off;
+  c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
+  l.total = c.off;
+  return l;
+}
+
+static int verify_common_checks(const ssd_paged_kv *kv, int h_q, int n_cand, const void *q, const float *out,
+                                const char *who) {
+  if (!q || !out) return fail(SSD_ERR_INVALID_ARG, "%s: q and out must be non-NULL", who);
+  if (h_q <= 0 || h_q % kv->h_kv) return fail(SSD_ERR_INVALID_ARG, "%s: h_q %d not a multiple of h_kv %d", who, h_q, kv->h_kv);
+  if (n_cand < 1) return fail(SSD_ERR_INVALID_ARG, "%s: n_cand %d < 1", who, n_cand);
+  if ((h_q / kv->h_kv) * n_cand > kMaxRows)
+    return fail(SSD_ERR_UNSUPPORTED, "%s: G*n_cand = %d exceeds %d", who, (h_q / kv->h_kv) * n_cand, kMaxRows);
+  if (!aligned16(q)) return fail(SSD_ERR_INVALID_ARG, "%s: q must be 16-byte aligned", who);
+  if ((int64_t)kv->batch * kv->h_kv > 65535) return fail(SSD_ERR_UNSUPPORTED, "%s: batch*h_kv above 65535", who);
+  return SSD_OK;
+}
+
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" size_t ssd_verify_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand) {
+  if (!kv || kv->h_kv <= 0 || h_q <= 0 || n_cand <= 0 || kv->batch < 0 || kv->max_seq_len < 0) return 0;
+  return verify_layout(kv, h_q, n_cand, cdiv(kv->max_seq_len, kSplitTokens)).total;
+}
+
+extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
+                               float *lse, float *scores, int64_t scores_stride, float *bscores,
+                               int64_t bscores_stride, int block_size, void *workspace, size_t workspace_bytes,
+                               ssd_stream_t stream) {
+  const char *who = "ssd_verify_attn";
+  KVView v;
+  int rc = validate_kv(kv, &v, who);
+  if (rc) return rc;
+  if ((rc = verify_common_checks(kv, h_q, n_cand, q, out, who))) return rc;
+  if (scores && scores_stride < kv->max_seq_len)
+    return fail(SSD_ERR_INVALID_ARG, "%s: scores_stride %lld < max_seq_len %d", who, (long long)scores_stride, kv->max_seq_len);
+  if (bscores) {
+    if (block_size != kBlockTokens) return fail(SSD_ERR_UNSUPPORTED, "%s: block_size %d (only 64)", who, block_size);
+    if (bscores_stride < cdiv(kv->max_seq_len, kBlockTokens))
+      return fail(SSD_ERR_INVALID_ARG, "%s: bscores_stride too small", who);
+  }
+  const VerifyLayout lay = verify_layout(kv, h_q, n_cand, cdiv(kv->max_seq_len, kSplitTokens));
+  if (!workspace || workspace_bytes < lay.total)
+    return fail(SSD_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", who, workspace_bytes, lay.total);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(SSD_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  if (kv->batch == 0 || kv->max_seq_len == 0) return SSD_OK;
+  unsigned *status = device_status();
+  if (!status) return SSD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  const bool crit = scores || bscores;
+
+  VerifyArgs a{};
+  a.kv = v;
+  a.q = q;
+  a.h_q = h_q;
+  a.n_c = n_cand;
+  a.G = lay.G;
+  a.R = lay.R;
+  a.scale_log2 = scale * kLog2e;
+  a.S_max = lay.S_max;
+  a.Lpad = lay.Lpad;
+  a.o_parts = reinterpret_cast<float *>(ws + lay.o_off);
+  a.lse_parts = reinterpret_cast<float *>(ws + lay.lse_off);
+  a.side_p = crit ? reinterpret_cast<__half *>(ws + lay.sp_off) : nullptr;
+  a.side_m = crit ? reinterpret_cast<float *>(ws + lay.sm_off) : nullptr;
+  a.status = status;
+  dim3 grid(lay.S_max, lay.units);
+  if (kv->dtype == SSD_DTYPE_BF16)
+    rc = dispatch_mma<false>(kv->d, rows_per_tile(lay.R), a, grid, st);
+  else
+    rc = kv->d == 128 ? launch_simt<128>(a, grid, st) : launch_simt<64>(a, grid, st);
+  if (rc) return rc;
+
+  FinalizeArgs f{};
+  f.seq_lens = kv->seq_lens;
+  f.max_seq_len = kv->max_seq_len;
+  f.h_kv = kv->h_kv;
+  f.h_q = h_q;
+  f.n_c = n_cand;
+  f.G = lay.G;
+  f.R = lay.R;
+  f.D = kv->d;
+  f.S_max = lay.S_max;
+  f.Lpad = lay.Lpad;
+  f.o_parts = a.o_parts;
+  f.lse_parts = a.lse_parts;
+  f.side_p = a.side_p;
+  f.side_m = a.side_m;
+  f.out = out;
+  f.lse = lse;
+  f.scores = scores;
+  f.scores_stride = scores_stride;
+  f.bscores = bscores;
+  f.bstride = bscores_stride;
+  const int n_tok = crit ? cdiv(kv->max_seq_len, kFinTok) : 0;
+  return launch_finalize(f, n_tok, lay.units, st);
+}
+
+extern "C" size_t ssd_block_sparse_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand, int umax) {
+  if (!kv || kv->h_kv <= 0 || h_q <= 0 || n_cand <= 0 || umax <= 0 || kv->batch < 0) return 0;
+  const int G = h_q / kv->h_kv, R = G * n_cand;
+  const size_t rows = (size_t)kv->batch * kv->h_kv * cdiv(umax, kBlocksPerItem) * R;
+  Carver c(nullptr);
+  c.take<float>(rows * kv->d);
+  c.take<float>(rows);
+  return c.off;
+}
+
+extern "C" int ssd_block_sparse_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, const int32_t *uidx,
+                                     const uint32_t *umask, const int32_t *ucnt, int umax, int block_size, float scale,
+                                     float *out, float *lse, void *workspace, size_t workspace_bytes,
+                                     ssd_stream_t stream) {
+  const char *who = "ssd_block_sparse_attn";
+  KVView v;
+  int rc = validate_kv(kv, &v, who);
+  if (rc) return rc;
+  if ((rc = verify_common_checks(kv, h_q, n_cand, q, out, who))) return rc;
+  if (kv->dtype != SSD_DTYPE_BF16) return fail(SSD_ERR_UNSUPPORTED, "%s: bf16 caches only", who);
+  if (block_size != kBlockTokens) return fail(SSD_ERR_UNSUPPORTED, "%s: block_size %d (only 64)", who, block_size);
+  if (n_cand > 32) return fail(SSD_ERR_UNSUPPORTED, "%s: n_cand %d > 32", who, n_cand);
+  if (!uidx || !umask || !ucnt || umax <= 0) return fail(SSD_ERR_INVALID_ARG, "%s: union arrays / umax", who);
+  const size_t need = ssd_block_sparse_workspace_bytes(kv, h_q, n_cand, umax);
+  if (!workspace || workspace_bytes < need)
+    return fail(SSD_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", who, workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(SSD_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  if (kv->batch == 0) return SSD_OK;
+  unsigned *status = device_status();
+  if (!status) return SSD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int G = h_q / kv->h_kv, R = G * n_cand, units = kv->batch * kv->h_kv;
+  const int S_max = cdiv(umax, kBlocksPerItem);
+  Carver c(workspace);
+  VerifyArgs a{};
+  a.kv = v;
+  a.q = q;
+  a.h_q = h_q;
+  a.n_c = n_cand;
+  a.G = G;
+  a.R = R;
+  a.scale_log2 = scale * kLog2e;
+  a.S_max = S_max;
+  a.Lpad = 0;
+  a.o_parts = c.take<float>((size_t)units * S_max * R * kv->d);
+  a.lse_parts = c.take<float>((size_t)units * S_max * R);
+  a.uidx = uidx;
+  a.umask = umask;
+  a.ucnt = ucnt;
+  a.umax = umax;
+  a.status = status;
+  rc = dispatch_mma<true>(kv->d, rows_per_tile(R), a, dim3(S_max, units), st);
+  if (rc) return rc;
+  FinalizeArgs f{};
+  f.seq_lens = kv->seq_lens;
+  f.max_seq_len = kv->max_seq_len;
+  f.h_kv = kv->h_kv;
+  f.h_q = h_q;
+  f.n_c = n_cand;
+  f.G = G;
+  f.R = R;
+  f.D = kv->d;
+  f.S_max = S_max;
+  f.o_parts = a.o_parts;
+  f.lse_parts = a.lse_parts;
+  f.ucnt = ucnt;
+  f.umax = umax;
+  f.out = out;
+  f.lse = lse;
+  return launch_finalize(f, 0, units, st);
+}
+
+extern "C" int ssd_combine(const float *o_parts, const float *lse_parts, int n_rows, int n_splits, int d, float *out,
+                           float *lse, ssd_stream_t stream) {
+  if (!o_parts || !lse_parts || !out) return fail(SSD_ERR_INVALID_ARG, "ssd_combine: NULL pointer");
+  if (n_rows < 0 || n_splits < 0 || d <= 0) return fail(SSD_ERR_INVALID_ARG, "ssd_combine: bad sizes");
+  if (n_rows == 0) return SSD_OK;
+  if (n_rows > (1 << 30)) return fail(SSD_ERR_UNSUPPORTED, "ssd_combine: too many rows");
+  combine_kernel<<<n_rows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(o_parts, lse_parts, n_splits, d, out, lse);
+  return check_launch("combine_kernel");
+}

@@ -1,0 +1,61 @@
+"""One speculative round on one attention layer: verify (with criticality) -> Top-K select -> k
+sparse drafts, with every buffer allocated once so the round can be replayed or captured in a CUDA
+graph.
+
+SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
+Sparse Attention") §4.1: the sparse pattern is refreshed by every verify and stays fixed for the k
+drafts that follow it (the refresh stride equals k); §2.3 / §3.2: a round is k drafts plus one
+verify of the k+1 positions.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class SpecRound:
+    def __init__(self, kv: B.KVCache, h_q: int, n_cand: int, k_max: int, scale: Optional[float] = None,
+                 workspace: Optional[B.Workspace] = None):
+        self.kv = kv
+        self.h_q = h_q
+        self.n_cand = n_cand
+        self.k_max = k_max
+        self.scale = scale if scale is not None else 1.0 / math.sqrt(kv.d)
+        dev = kv.device
+        Bsz, hkv, d = kv.batch, kv.h_kv, kv.d
+        self.ws = workspace or B.Workspace()
+        self.out_v = torch.empty((Bsz, n_cand, h_q, d), dtype=torch.float32, device=dev)
+        self.lse_v = torch.empty((Bsz, n_cand, h_q), dtype=torch.float32, device=dev)
+        self.scores = torch.zeros((Bsz, hkv, max(kv.max_seq_len, 1)), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((Bsz * hkv, k_max), dtype=torch.int32, device=dev)
+        self.cnt = torch.empty((Bsz * hkv,), dtype=torch.int32, device=dev)
+        self.out_d = torch.empty((Bsz, h_q, d), dtype=torch.float32, device=dev)
+        self.lse_d = torch.empty((Bsz, h_q), dtype=torch.float32, device=dev)
+
+    def verify(self, q_verify: torch.Tensor, stream=None):
+        return B.ssd_verify_attn(self.kv, q_verify, self.n_cand, self.scale, out=self.out_v, lse=self.lse_v,
+                                 scores=self.scores, workspace=self.ws, stream=stream)
+
+    def select(self, k_per_req: torch.Tensor, stream=None):
+        return B.ssd_select_topk(self.scores, self.kv.seq_lens, k_per_req, self.k_max, self.kv.h_kv,
+                                 max_len=self.kv.max_seq_len, idx=self.idx, cnt=self.cnt, stream=stream)
+
+    def draft(self, q_draft: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
+        return B.ssd_draft_attn(self.kv, q_draft, self.idx.view(self.kv.batch, self.kv.h_kv, self.k_max),
+                                self.cnt.view(self.kv.batch, self.kv.h_kv), self.scale,
+                                out=out if out is not None else self.out_d, lse=self.lse_d, workspace=self.ws,
+                                stream=stream)
+
+    def run(self, q_verify: torch.Tensor, q_drafts: torch.Tensor, k_per_req: torch.Tensor,
+            draft_outs: Optional[torch.Tensor] = None, stream=None):
+        """verify -> select -> len(q_drafts) drafts.  draft_outs [k, B, h_q, d] keeps every draft's
+        output (else each overwrites ``out_d``)."""
+        self.verify(q_verify, stream)
+        self.select(k_per_req, stream)
+        for j in range(q_drafts.shape[0]):
+            self.draft(q_drafts[j], out=None if draft_outs is None else draft_outs[j], stream=stream)

@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports every function include/ssd.h declares, and rejects bad
+arguments on the host (no kernel is launched by these calls)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_self_speculative_verify_gb300 import binding
+from sparse_self_speculative_verify_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.ssd_version() == 0x10000
+
+
+def _kv(**over):
+    d = dict(pool=16, dtype=binding.SSD_DTYPE_BF16, num_pages=10, page_size=16, h_kv=8, d=128, page_table=256,
+             max_pages=4, seq_lens=512, batch=2, max_seq_len=64)
+    d.update(over)
+    return binding.PagedKVStruct(**d)
+
+
+def test_workspace_queries(lib):
+    kv = _kv()
+    vb = lib.ssd_verify_workspace_bytes(ctypes.byref(kv), 32, 5)
+    assert vb > 0 and vb % 256 == 0
+    kv2 = _kv(max_seq_len=128, max_pages=8)
+    assert lib.ssd_verify_workspace_bytes(ctypes.byref(kv2), 32, 5) > vb
+    assert lib.ssd_verify_workspace_bytes(None, 32, 5) == 0
+    assert lib.ssd_draft_workspace_bytes(ctypes.byref(kv), 32, 410) > lib.ssd_draft_workspace_bytes(ctypes.byref(kv), 32, 64)
+    assert lib.ssd_unified_workspace_bytes(ctypes.byref(kv), 32, 5, 64) >= vb
+    assert lib.ssd_block_sparse_workspace_bytes(ctypes.byref(kv), 32, 5, 80) > 0
+
+
+CASES = [
+    ("null kv", dict(kv=None), binding.SSD_ERR_INVALID_ARG),
+    ("bad dtype", dict(kvo=dict(dtype=7)), binding.SSD_ERR_UNSUPPORTED),
+    ("bad head dim", dict(kvo=dict(d=96)), binding.SSD_ERR_UNSUPPORTED),
+    ("page size not pow2", dict(kvo=dict(page_size=12)), binding.SSD_ERR_UNSUPPORTED),
+    ("max_seq_len > pages", dict(kvo=dict(max_seq_len=65)), binding.SSD_ERR_INVALID_ARG),
+    ("unaligned pool", dict(kvo=dict(pool=24)), binding.SSD_ERR_INVALID_ARG),
+    ("h_q not multiple", dict(h_q=30), binding.SSD_ERR_INVALID_ARG),
+    ("too many rows", dict(h_q=128, n_cand=5), binding.SSD_ERR_UNSUPPORTED),
+    ("null q", dict(q=None), binding.SSD_ERR_INVALID_ARG),
+    ("short workspace", dict(ws_bytes=100), binding.SSD_ERR_WORKSPACE),
+    ("scores stride", dict(scores=4096, scores_stride=10), binding.SSD_ERR_INVALID_ARG),
+    ("block size", dict(bscores=4096, bscores_stride=4, block_size=32), binding.SSD_ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,over,code", CASES, ids=[c[0] for c in CASES])
+def test_verify_argument_errors(lib, name, over, code):
+    kv = _kv(**over.get("kvo", {}))
+    kvp = None if "kv" in over and over["kv"] is None else ctypes.byref(kv)
+    ws_bytes = over.get("ws_bytes", 1 << 40)
+    rc = lib.ssd_verify_attn(kvp, over.get("q", 4096), over.get("h_q", 32), over.get("n_cand", 5), 0.1, 8192, None,
+                             over.get("scores"), over.get("scores_stride", 0), over.get("bscores"),
+                             over.get("bscores_stride", 0), over.get("block_size", 64), 1 << 20, ws_bytes, None)
+    assert rc == code, lib.ssd_last_error()
+    assert lib.ssd_last_error()
+
+
+def test_select_argument_errors(lib):
+    assert lib.ssd_select_topk(None, 10, 1, 1, 1, 1, 1, 10, 1, 4, 1, None) == binding.SSD_ERR_INVALID_ARG
+    assert lib.ssd_select_topk(4096, 5, 16, 16, 1, 1, 1, 10, 64, 4, 64, None) == binding.SSD_ERR_INVALID_ARG
+    assert lib.ssd_select_topk(4096, 10, 16, 16, 1, 0, 1, 10, 64, 4, 64, None) == binding.SSD_ERR_INVALID_ARG
+    # Zero rows: nothing to do, no device work.
+    assert lib.ssd_select_topk(4096, 10, 16, 16, 0, 1, 1, 10, 64, 4, 64, None) == binding.SSD_OK
+
+
+def test_draft_and_union_argument_errors(lib):
+    kv = _kv()
+    assert lib.ssd_draft_attn(ctypes.byref(kv), None, 32, 16, 8, 16, 0.1, 16, None, 1 << 20, 1 << 40,
+                              None) == binding.SSD_ERR_INVALID_ARG
+    assert lib.ssd_draft_attn(ctypes.byref(kv), 16, 8 * 17, 16, 8, 16, 0.1, 16, None, 1 << 20, 1 << 40,
+                              None) == binding.SSD_ERR_UNSUPPORTED  # group of 17 heads
+    assert lib.ssd_block_union(16, 16, 4, 33, 16, 2048, 16, 16, 16, 80, None) == binding.SSD_ERR_UNSUPPORTED
+    assert lib.ssd_combine(None, 16, 4, 2, 128, 16, None, None) == binding.SSD_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(binding.LibraryNotBuilt):
+        binding.load(str(tmp_path / "missing.so"))

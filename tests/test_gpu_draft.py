@@ -1,0 +1,90 @@
+"""Sparse draft attention on the GPU against the float64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_self_speculative_verify_gb300 import KVCache, ssd_draft_attn, ssd_status, ssd_verify_attn
+from sparse_self_speculative_verify_gb300 import workloads as W
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _draft(w, idx, cnt, q=None):
+    _gpu.lib()
+    kv = KVCache.from_workload(w)
+    q = w.q_draft[0] if q is None else q
+    r = ssd_draft_attn(kv, q, idx.to(DEV), cnt.to(DEV), _gpu.scale_of(w.spec))
+    torch.cuda.synchronize()
+    assert ssd_status() == 0
+    return r
+
+
+def _check(w, r, idx, cnt, reqs=None, q=None):
+    kv_h, reqs = _gpu.host_subset(w, reqs)
+    q = (w.q_draft[0] if q is None else q).cpu()[reqs]
+    ref = oracle.draft(kv_h, q, idx[reqs], cnt[reqs], _gpu.scale_of(w.spec))
+    _gpu.assert_out(r["out"].cpu().numpy()[reqs], ref["out"], "draft out")
+    _gpu.assert_lse(r["lse"].cpu().numpy()[reqs], ref["lse"])
+
+
+CASES = [
+    # (spec name, overrides, lens, k per request, k_max)
+    ("qwen3_8b", dict(batch=3), [2049, 700, 64], [103, 35, 64], 128),       # 1-2 chunks per unit
+    ("qwen3_8b", dict(batch=2), [8192, 5000], [410, 250], 410),               # 7 chunks: last-arriver merge
+    ("qwen3_8b", dict(batch=2, h_q=40), [3000, 1200], [150, 0], 150),         # G = 5, one empty list
+    ("qwen3_8b", dict(batch=2, h_q=128, h_kv=8), [600, 1000], [30, 300], 300),  # G = 16
+    ("qwen3_8b", dict(batch=2, d=64, page_size=32), [1000, 333], [65, 17], 65),
+    ("tiny", dict(), [512, 512], [64, 64], 64),                               # fp32, d = 64
+    ("tiny", dict(d=128, page_size=16, shuffled=True), [700, 129], [100, 7], 100),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-{'_'.join(map(str, c[2]))}-k{c[4]}")
+def test_draft_random_sets(case):
+    name, over, lens, ks, k_max = case
+    spec = W.scaled_spec(W.SPECS[name], name="d", **over)
+    w = W.make_workload(spec, seed=31 + k_max, device=DEV, lengths=lens)
+    idx, cnt = W.random_index_sets(w.seq_lens, spec.h_kv, torch.tensor(ks, dtype=torch.int32), k_max, seed=k_max)
+    _check(w, _draft(w, idx, cnt), idx, cnt)
+
+
+def test_draft_repeat_calls_identical():
+    """Consecutive calls reuse the workspace counters: results are bit-identical."""
+    spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="rep", batch=2)
+    w = W.make_workload(spec, seed=2, device=DEV, lengths=[8000, 4000])
+    idx, cnt = W.random_index_sets(w.seq_lens, spec.h_kv, torch.tensor([400, 200], dtype=torch.int32), 400, seed=3)
+    a = _draft(w, idx, cnt)["out"].clone()
+    b = _draft(w, idx, cnt)["out"]
+    assert torch.equal(a, b)
+
+
+def test_draft_select_all_equals_verify_single_candidate():
+    """With every index selected, the draft is dense single-query attention: it matches the GPU
+    verify with n_cand = 1 on the same query (and the oracle)."""
+    spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="all", batch=2, k=0)
+    w = W.make_workload(spec, seed=5, device=DEV, lengths=[1500, 700])
+    k_max = 1500
+    idx = torch.full((2, spec.h_kv, k_max), -1, dtype=torch.int32)
+    cnt = torch.zeros((2, spec.h_kv), dtype=torch.int32)
+    for b, L in enumerate([1500, 700]):
+        idx[b, :, :L] = torch.arange(L, dtype=torch.int32)
+        cnt[b] = L
+    q = w.q_verify[:, 0].contiguous()
+    r = _draft(w, idx, cnt, q=q)
+    v = ssd_verify_attn(KVCache.from_workload(w), w.q_verify, 1, _gpu.scale_of(spec))
+    torch.cuda.synchronize()
+    _gpu.assert_out(r["out"].cpu().numpy(), v["out"][:, 0].cpu().numpy(), "draft vs verify", tol=1e-3)
+    _check(w, r, idx, cnt, q=q)
+
+
+def test_draft_full_size_qwen3_8b():
+    """Full-size Qwen3-8B shape with 5% random index sets; every output against the oracle."""
+    spec = W.SPECS["qwen3_8b"]
+    w = W.make_workload(spec, device=DEV)
+    k_max = int(w.k_per_req.max())
+    idx, cnt = W.random_index_sets(w.seq_lens, spec.h_kv, w.k_per_req, k_max, seed=77)
+    _check(w, _draft(w, idx, cnt), idx, cnt)

@@ -1,0 +1,87 @@
+"""A whole speculative round (verify -> select -> k drafts) on the full-size Qwen3-8B-shaped
+workload, as the benchmark runs it, plus its CUDA-graph replay."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_self_speculative_verify_gb300 import KVCache, SpecRound, ssd_draft_attn, ssd_status
+from sparse_self_speculative_verify_gb300 import workloads as W
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _round(w):
+    _gpu.lib()
+    spec = w.spec
+    kv = KVCache.from_workload(w)
+    k_max = int(w.k_per_req.max())
+    rnd = SpecRound(kv, spec.h_q, spec.n_cand, k_max, _gpu.scale_of(spec))
+    outs = torch.empty((spec.k, spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=DEV)
+    rnd.run(w.q_verify, w.q_draft, w.k_per_req, draft_outs=outs)
+    torch.cuda.synchronize()
+    assert ssd_status() == 0
+    return rnd, outs
+
+
+def test_round_qwen3_8b_full_size():
+    spec = W.SPECS["qwen3_8b"]
+    w = W.make_workload(spec, device=DEV)
+    rnd, outs = _round(w)
+    reqs = [1, 17, 31]
+    kv_h, reqs = _gpu.host_subset(w, reqs)
+    scale = _gpu.scale_of(spec)
+    ref = oracle.verify(kv_h, w.q_verify.cpu()[reqs], scale)
+    _gpu.assert_out(rnd.out_v.cpu().numpy()[reqs], ref["out"], "verify out")
+    lens = kv_h.seq_lens
+    _gpu.assert_scores(rnd.scores.cpu().numpy()[reqs], ref["crit"], lens)
+    # The GPU's selection (from its own scores) is a valid top-K of the oracle's scores.
+    k_max = rnd.k_max
+    idx = rnd.idx.view(spec.batch, spec.h_kv, k_max).cpu().numpy()[reqs].reshape(-1, k_max)
+    cnt = rnd.cnt.view(spec.batch, spec.h_kv).cpu().numpy()[reqs].reshape(-1)
+    kpr = w.k_per_req.cpu().numpy()[reqs]
+    _gpu.assert_valid_topk(idx, cnt, ref["crit"].reshape(-1, ref["crit"].shape[-1]), kpr, lens, spec.h_kv)
+    # Drafts on the oracle's selection (fp32 scores, oracle top-K) against the oracle drafts.
+    S = ref["crit"].astype(np.float32)
+    oidx, ocnt = oracle.topk(S.reshape(-1, S.shape[-1]), lens, kpr, k_max, rows_per_group=spec.h_kv)
+    oidx = oidx.reshape(len(reqs), spec.h_kv, k_max)
+    ocnt = ocnt.reshape(len(reqs), spec.h_kv)
+    full_idx = torch.zeros((spec.batch, spec.h_kv, k_max), dtype=torch.int32)
+    full_cnt = torch.zeros((spec.batch, spec.h_kv), dtype=torch.int32)
+    full_idx[reqs] = torch.from_numpy(oidx)
+    full_cnt[reqs] = torch.from_numpy(ocnt)
+    kv = KVCache.from_workload(w)
+    for j in range(spec.k):
+        g = ssd_draft_attn(kv, w.q_draft[j], full_idx.to(DEV), full_cnt.to(DEV), scale)
+        dref = oracle.draft(kv_h, w.q_draft[j].cpu()[reqs], oidx, ocnt, scale)
+        torch.cuda.synchronize()
+        _gpu.assert_out(g["out"].cpu().numpy()[reqs], dref["out"], f"draft {j}")
+
+
+def test_round_graph_replay_matches_eager():
+    spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="graph", batch=4)
+    w = W.make_workload(spec, seed=3, device=DEV, lengths=[2100, 4097, 300, 1000])
+    rnd, outs = _round(w)
+    eager = (rnd.out_v.clone(), rnd.scores.clone(), rnd.idx.clone(), outs.clone())
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        rnd.run(w.q_verify, w.q_draft, w.k_per_req, draft_outs=outs)  # warm-up on the capture stream
+        torch.cuda.synchronize()
+        rnd.out_v.zero_()
+        outs.zero_()
+        with torch.cuda.graph(g, stream=s):
+            rnd.run(w.q_verify, w.q_draft, w.k_per_req, draft_outs=outs)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ssd_status() == 0
+    assert torch.equal(rnd.out_v, eager[0])
+    assert torch.equal(rnd.scores, eager[1])
+    assert torch.equal(rnd.idx, eager[2])
+    assert torch.equal(outs, eager[3])
