@@ -112,9 +112,10 @@ class ClockSampler:
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) == len(CLOCK_FIELDS):
-                self.rows.append(parts)
+                self.rows.append((time.time(), parts))
 
-    def stop(self) -> dict:
+    def stop(self, t_begin: float = 0.0, t_end: float = float("inf")) -> dict:
+        """Stops sampling; summarises the samples taken between t_begin and t_end (host time)."""
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -126,7 +127,9 @@ class ClockSampler:
         sm = []
         smax = None
         reasons = set()
-        for r in self.rows:
+        for ts, r in self.rows:
+            if ts < t_begin or ts > t_end:
+                continue
             try:
                 sm.append(float(r[0]))
                 smax = float(r[1])
@@ -340,14 +343,16 @@ def run_ours(args, spec, rank, world, local):
     time.sleep(0.3)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
+    t_begin = time.time()
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for _ in range(args.steps):
             graph.replay()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
+    t_end = time.time()
     ms_total = ev0.elapsed_time(ev1)
-    clk = clocks.stop()
+    clk = clocks.stop(t_begin, t_end)
     barrier()
     ms_total = max_over_ranks(ms_total, dev)
     bytes_all = sum_over_ranks(float(kv_step * args.steps), dev)
@@ -436,7 +441,7 @@ def run_ours(args, spec, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen3_8b", choices=sorted(W.SPECS))

@@ -225,23 +225,46 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int e = tid; e < G * D; e += blockDim.x) {
-    int h = e / D, dd = e % D;
+  // Per head: LSE over the chunks (one warp, lanes over chunks).
+  const int64_t cbase = (int64_t)unit * a.C_max * GMAX;
+  for (int h = warp; h < G; h += blockDim.x / 32) {
     float M = -INFINITY;
-    for (int c = 0; c < n_chunks; ++c)
-      M = fmaxf(M, __ldcg(a.lse_parts + ((int64_t)unit * a.C_max + c) * GMAX + h));
-    float acc = 0.f, wsum = 0.f;
+    for (int c = lane; c < n_chunks; c += 32) M = fmaxf(M, __ldcg(a.lse_parts + cbase + (int64_t)c * GMAX + h));
+    M = warp_max(M);
+    float s = 0.f;
+    if (M != -INFINITY)
+      for (int c = lane; c < n_chunks; c += 32)
+        s += fast_exp2((__ldcg(a.lse_parts + cbase + (int64_t)c * GMAX + h) - M) * kLog2e);
+    s = warp_sum(s);
+    if (lane == 0) {
+      sM[h] = M;
+      sL[h] = s;
+    }
+  }
+  __syncthreads();
+  // Outputs: one float4 of d per thread, chunks unrolled (independent loads).
+  for (int e = tid; e < G * (D / 4); e += blockDim.x) {
+    const int h = e / (D / 4), q4 = e % (D / 4);
+    const float M = sM[h], s = sL[h];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
+#pragma unroll 4
       for (int c = 0; c < n_chunks; ++c) {
-        int64_t pr = ((int64_t)unit * a.C_max + c) * GMAX + h;
-        float w = fast_exp2((__ldcg(a.lse_parts + pr) - M) * kLog2e);
-        wsum += w;
-        acc = fmaf(w, __ldcg(a.o_parts + pr * D + dd), acc);
+        const int64_t pr = cbase + (int64_t)c * GMAX + h;
+        const float w = fast_exp2((__ldcg(a.lse_parts + pr) - M) * kLog2e);
+        const float4 o = __ldcg(reinterpret_cast<const float4 *>(a.o_parts + pr * D) + q4);
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
       }
     }
-    int64_t row = (int64_t)b * a.h_q + g * G + h;
-    a.out[row * D + dd] = (wsum > 0.f) ? acc / wsum : 0.f;
-    if (dd == 0 && a.lse) a.lse[row] = (wsum > 0.f) ? M + __logf(wsum) : -INFINITY;
+    const bool ok = s > 0.f;
+    const float inv = ok ? 1.f / s : 0.f;
+    const int64_t row = (int64_t)b * a.h_q + g * G + h;
+    reinterpret_cast<float4 *>(a.out + row * D)[q4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (q4 == 0 && a.lse) a.lse[row] = ok ? M + __logf(s) : -INFINITY;
   }
   if (tid == 0) a.counters[unit] = 0u;
 }

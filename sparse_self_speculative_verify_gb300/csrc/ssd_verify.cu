@@ -43,49 +43,63 @@ __global__ void __launch_bounds__(128) verify_simt_kernel(VerifyArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Finalize: grid (n_tok_ctas + 1, unit).  Every block first merges the unit's split LSEs per row;
-// the last block of a unit combines the outputs, the others rematerialise the criticality of
-// kFinTok tokens each: crit[t] = sum_r e[r][t] * 2^(m_ref[r][t/16] - LSE2_r).
+// Finalize: grid (n_tok + n_comb, unit).  Every block first merges the unit's split LSEs per row
+// (one warp per row, lanes over splits); blocks x >= n_tok combine the split outputs of kFinRows
+// rows each (one float4 of d per thread, splits unrolled), blocks x < n_tok rematerialise the
+// criticality of kFinTok tokens each: crit[t] = sum_r e[r][t] * 2^(m_ref[r][t/16] - LSE2_r).
 // ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ int fin_rows_per_cta(int D) { return kFinThreads / (D / 4); }
 
-__global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f) {
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, int n_tok) {
   __shared__ float sLn[kMaxRows];
   __shared__ float sL2[kMaxRows];
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = blockIdx.y, b = u / f.h_kv, g = u % f.h_kv;
   if (f.phase && f.phase[b] == 0) return;
   int L = f.seq_lens[b];
   L = L < 0 ? 0 : (L > f.max_seq_len ? f.max_seq_len : L);
   const int ns = f.ucnt ? block_splits(min(max(f.ucnt[u], 0), f.umax)) : verify_splits(L);
   const int64_t pbase = (int64_t)u * f.S_max * f.R;
-  for (int r = tid; r < f.R; r += blockDim.x) {
+  for (int r = warp; r < f.R; r += kFinThreads / 32) {
     float M = -INFINITY;
-    for (int j = 0; j < ns; ++j) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
+    for (int j = lane; j < ns; j += 32) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
+    M = warp_max(M);
     float s = 0.f;
     if (M != -INFINITY)
-      for (int j = 0; j < ns; ++j) s += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
-    float ln = (M == -INFINITY) ? -INFINITY : M + __logf(s);
-    sLn[r] = ln;
-    sL2[r] = ln * kLog2e;
+      for (int j = lane; j < ns; j += 32) s += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
+    s = warp_sum(s);
+    if (lane == 0) {
+      float ln = (M == -INFINITY) ? -INFINITY : M + __logf(s);
+      sLn[r] = ln;
+      sL2[r] = ln * kLog2e;
+    }
   }
   __syncthreads();
 
-  if (blockIdx.x == gridDim.x - 1) {
-    const int D = f.D;
-    for (int idx = tid; idx < f.R * D; idx += blockDim.x) {
-      int r = idx / D, dd = idx % D;
-      float ln = sLn[r], acc = 0.f;
-      if (ln != -INFINITY)
-        for (int j = 0; j < ns; ++j) {
-          int64_t pr = pbase + (int64_t)j * f.R + r;
-          float w = fast_exp2((f.lse_parts[pr] - ln) * kLog2e);
-          acc = fmaf(w, f.o_parts[pr * D + dd], acc);
-        }
-      int i = r / f.G, hl = r % f.G;
-      int64_t row = ((int64_t)b * f.n_c + i) * f.h_q + g * f.G + hl;
-      f.out[row * D + dd] = acc;
-      if (dd == 0 && f.lse) f.lse[row] = ln;
+  if ((int)blockIdx.x >= n_tok) {
+    const int D = f.D, tpr = D / 4, rpc = fin_rows_per_cta(D);
+    const int r = ((int)blockIdx.x - n_tok) * rpc + tid / tpr, q4 = tid % tpr;
+    if (r >= f.R) return;
+    const float ln = sLn[r];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ln != -INFINITY) {
+      const float *lp = f.lse_parts + pbase + r;
+      const float4 *op = reinterpret_cast<const float4 *>(f.o_parts + (pbase + r) * D) + q4;
+      const int64_t ostep = (int64_t)f.R * D / 4;
+#pragma unroll 4
+      for (int j = 0; j < ns; ++j) {
+        float w = fast_exp2((lp[(int64_t)j * f.R] - ln) * kLog2e);
+        float4 o = op[j * ostep];
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+      }
     }
+    const int i = r / f.G, hl = r % f.G;
+    const int64_t row = ((int64_t)b * f.n_c + i) * f.h_q + g * f.G + hl;
+    reinterpret_cast<float4 *>(f.out + row * D)[q4] = acc;
+    if (q4 == 0 && f.lse) f.lse[row] = ln;
     return;
   }
   if (!f.side_p) return;
@@ -93,42 +107,42 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f) {
   const int t0 = blockIdx.x * kFinTok + tid * 8;
   const bool valid = t0 < L;
   const int nref = f.Lpad / kRefGroup;
-  float crit[8];
+  float crit[8], cc[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) crit[k] = 0.f;
-  for (int i = 0; i < f.n_c; ++i) {
-    float cc[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) cc[k] = 0.f;
+  for (int k = 0; k < 8; ++k) crit[k] = cc[k] = 0.f;
+  const int64_t rbase = (int64_t)u * f.R;
+#pragma unroll 4
+  for (int r = 0; r < f.R; ++r) {
     if (valid) {
-      for (int hl = 0; hl < f.G; ++hl) {
-        int r = i * f.G + hl;
-        float l2 = sL2[r];
-        if (l2 == -INFINITY) continue;
-        int64_t rr = (int64_t)u * f.R + r;
-        float coef = fast_exp2(f.side_m[rr * nref + t0 / kRefGroup] - l2);
-        uint4 raw = *reinterpret_cast<const uint4 *>(f.side_p + rr * f.Lpad + t0);
-        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+      const float l2 = sL2[r];
+      const float ref = f.side_m[(rbase + r) * nref + t0 / kRefGroup];
+      const uint4 raw = *reinterpret_cast<const uint4 *>(f.side_p + (rbase + r) * f.Lpad + t0);
+      const float coef = (l2 == -INFINITY) ? 0.f : fast_exp2(ref - l2);
+      const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float2 pf = __half22float2(h2[k]);
-          cc[2 * k] = fmaf(pf.x, coef, cc[2 * k]);
-          cc[2 * k + 1] = fmaf(pf.y, coef, cc[2 * k + 1]);
-        }
+      for (int k = 0; k < 4; ++k) {
+        float2 pf = __half22float2(h2[k]);
+        cc[2 * k] = fmaf(pf.x, coef, cc[2 * k]);
+        cc[2 * k + 1] = fmaf(pf.y, coef, cc[2 * k + 1]);
       }
     }
-    if (f.bscores) {
-      float m = cc[0];
+    if ((r + 1) % f.G == 0) {  // candidate r / G complete
+      if (f.bscores) {
+        float m = cc[0];
 #pragma unroll
-      for (int k = 1; k < 8; ++k) m = fmaxf(m, cc[k]);
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-      if ((lane & 7) == 0 && valid)
-        f.bscores[((int64_t)u * f.n_c + i) * f.bstride + t0 / kBlockTokens] = m;
+        for (int k = 1; k < 8; ++k) m = fmaxf(m, cc[k]);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        if ((lane & 7) == 0 && valid)
+          f.bscores[((int64_t)u * f.n_c + r / f.G) * f.bstride + t0 / kBlockTokens] = m;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        crit[k] += cc[k];
+        cc[k] = 0.f;
+      }
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) crit[k] += cc[k];
   }
   if (f.scores && valid) {
     float *dst = f.scores + (int64_t)u * f.scores_stride + t0;
@@ -144,7 +158,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f) {
 }
 
 int launch_finalize(const FinalizeArgs &f, int n_tok, int units, cudaStream_t st) {
-  finalize_kernel<<<dim3(n_tok + 1, units), kFinThreads, 0, st>>>(f);
+  const int n_comb = cdiv(f.R, kFinThreads / (f.D / 4));
+  finalize_kernel<<<dim3(n_tok + n_comb, units), kFinThreads, 0, st>>>(f, n_tok);
   return check_launch("finalize_kernel");
 }
 
