@@ -378,7 +378,7 @@ def run_ours(args, spec, rank, world, local):
     v_bytes = M.verify_call_bytes(lens, spec.batch, spec.h_q, spec.h_kv, spec.d, spec.elem_bytes, spec.n_cand)
     achieved = v_bytes / (v_ms * 1e-3) / 1e9
     units = sum(lens) * spec.h_kv
-    roofline = {"bound": "hbm", "kernel": "ssd_verify_attn (verify_mma_kernel + finalize_kernel)",
+    roofline = {"bound": "hbm", "kernel": "ssd_verify_attn (verify_tc_kernel + finalize_kernel)",
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(units),
                 "peak_source": peaks["source"], "launch_ms": v_ms, "algorithmic_bytes": v_bytes,

@@ -63,7 +63,8 @@ enum ssd_device_fault {
   SSD_FAULT_SEQLEN = 2u,   /* seq_lens[b] outside [0, max_seq_len] or shorter than n_cand */
   SSD_FAULT_INDEX = 4u,    /* a draft index outside [0, L_b) */
   SSD_FAULT_KMAX = 8u,     /* a requested K larger than k_max (output truncated to k_max) */
-  SSD_FAULT_UNION = 16u    /* a block union larger than umax (output truncated) */
+  SSD_FAULT_UNION = 16u,   /* a block union larger than umax (output truncated) */
+  SSD_FAULT_TIMEOUT = 32u  /* a bounded wait inside a kernel expired; that block's outputs are invalid */
 };
 
 /*

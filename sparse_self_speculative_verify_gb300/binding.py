@@ -22,7 +22,7 @@ from . import build as _build
 
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = range(6)
 SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
-FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION = 1, 2, 4, 8, 16
+FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT = 1, 2, 4, 8, 16, 32
 
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
             "ssd_select_topk", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_unified_workspace_bytes",

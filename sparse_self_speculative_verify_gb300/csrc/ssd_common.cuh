@@ -16,6 +16,8 @@ constexpr int kSplitTokens = 512;
 constexpr int kStageTokens = 64;
 // Criticality side values carry one log2-domain reference per (row, kRefGroup tokens).
 constexpr int kRefGroup = 16;
+// Row length of the criticality side buffer is a multiple of this (the largest tile that writes it).
+constexpr int kSideAlign = 128;
 // Draft work item: up to kDraftChunk selected tokens of one (request, KV head).
 constexpr int kDraftChunk = 64;
 // Tokens per union block in the block-granular path.

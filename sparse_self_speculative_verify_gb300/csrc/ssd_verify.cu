@@ -104,55 +104,60 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   }
   if (!f.side_p) return;
 
-  const int t0 = blockIdx.x * kFinTok + tid * 8;
-  const bool valid = t0 < L;
+  // Criticality: one token per thread.  coef[r][j] = 2^(m_ref[r][group j] - LSE2_r) for the
+  // kFinGroups 16-token groups of this block, then crit[t] = sum_r e[t][r] * coef[r][t / 16].
+  __shared__ float s_coef[kMaxRows * kFinGroups];
+  __shared__ unsigned s_bmax[kMaxRows / 1 * (kFinTok / kBlockTokens)];
+  const int tb0 = blockIdx.x * kFinTok;
+  if (tb0 >= L) return;
   const int nref = f.Lpad / kRefGroup;
-  float crit[8], cc[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) crit[k] = cc[k] = 0.f;
   const int64_t rbase = (int64_t)u * f.R;
-#pragma unroll 4
-  for (int r = 0; r < f.R; ++r) {
-    if (valid) {
-      const float l2 = sL2[r];
-      const float ref = f.side_m[(rbase + r) * nref + t0 / kRefGroup];
-      const uint4 raw = *reinterpret_cast<const uint4 *>(f.side_p + (rbase + r) * f.Lpad + t0);
-      const float coef = (l2 == -INFINITY) ? 0.f : fast_exp2(ref - l2);
-      const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+  for (int e = tid; e < f.R * kFinGroups; e += kFinThreads) {
+    const int r = e / kFinGroups, j = e % kFinGroups;
+    if (tb0 + j * kRefGroup >= L) continue;
+    const float l2 = sL2[r];
+    const float ref = f.side_m[(rbase + r) * nref + tb0 / kRefGroup + j];
+    s_coef[r * kFinGroups + j] = (l2 == -INFINITY) ? 0.f : fast_exp2(ref - l2);
+  }
+  if (f.bscores)
+    for (int e = tid; e < f.n_c * (kFinTok / kBlockTokens); e += kFinThreads) s_bmax[e] = 0u;
+  __syncthreads();
+  const int t = tb0 + tid;
+  const bool valid = t < L;
+  const int grp = tid / kRefGroup;
+  const __half *sp = f.side_p + ((int64_t)u * f.Lpad + t) * f.RS;
+  float crit = 0.f, cc = 0.f;
+  int cand = 0, in_cand = 0;
+  for (int c = 0; c < f.RS; c += 8) {
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (valid) raw = *reinterpret_cast<const uint4 *>(sp + c);
+    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float2 pf = __half22float2(h2[k]);
-        cc[2 * k] = fmaf(pf.x, coef, cc[2 * k]);
-        cc[2 * k + 1] = fmaf(pf.y, coef, cc[2 * k + 1]);
-      }
-    }
-    if ((r + 1) % f.G == 0) {  // candidate r / G complete
-      if (f.bscores) {
-        float m = cc[0];
-#pragma unroll
-        for (int k = 1; k < 8; ++k) m = fmaxf(m, cc[k]);
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        if ((lane & 7) == 0 && valid)
-          f.bscores[((int64_t)u * f.n_c + r / f.G) * f.bstride + t0 / kBlockTokens] = m;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        crit[k] += cc[k];
-        cc[k] = 0.f;
+    for (int e = 0; e < 8; ++e) {
+      const int r = c + e;
+      if (r < f.R) {
+        const float2 pf = __half22float2(h2[e >> 1]);
+        cc = fmaf((e & 1) ? pf.y : pf.x, s_coef[r * kFinGroups + grp], cc);
+        if (++in_cand == f.G) {  // candidate `cand` complete
+          if (f.bscores) {
+            const float m = warp_max(valid ? cc : 0.f);
+            if (lane == 0) atomicMax(&s_bmax[cand * (kFinTok / kBlockTokens) + tid / kBlockTokens], __float_as_uint(m));
+          }
+          crit += cc;
+          cc = 0.f;
+          in_cand = 0;
+          ++cand;
+        }
       }
     }
   }
-  if (f.scores && valid) {
-    float *dst = f.scores + (int64_t)u * f.scores_stride + t0;
-    if (t0 + 8 <= L && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
-      reinterpret_cast<float4 *>(dst)[0] = make_float4(crit[0], crit[1], crit[2], crit[3]);
-      reinterpret_cast<float4 *>(dst)[1] = make_float4(crit[4], crit[5], crit[6], crit[7]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (t0 + k < L) dst[k] = crit[k];
+  if (f.scores && valid) f.scores[(int64_t)u * f.scores_stride + t] = crit;
+  if (f.bscores) {
+    __syncthreads();
+    for (int e = tid; e < f.n_c * (kFinTok / kBlockTokens); e += kFinThreads) {
+      const int i = e / (kFinTok / kBlockTokens), j = e % (kFinTok / kBlockTokens);
+      const int blk = tb0 / kBlockTokens + j;
+      if (blk * kBlockTokens < L) f.bscores[((int64_t)u * f.n_c + i) * f.bstride + blk] = __uint_as_float(s_bmax[e]);
     }
   }
 }
@@ -187,6 +192,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *o_parts, cons
 // ------------------------------------------------------------------------------------------------
 // Host side.
 // ------------------------------------------------------------------------------------------------
+bool verify_tc_supported(const ssd_paged_kv *kv, int R);
+int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st);
+
 static int rows_per_tile(int R) { return R <= 16 ? 1 : (R <= 32 ? 2 : 4); }
 
 template <int D, int NRT, bool BLOCKS>
@@ -230,7 +238,7 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   l.R = l.G * n_cand;
   l.units = kv->batch * kv->h_kv;
   l.S_max = S_max;
-  l.Lpad = cdiv(kv->max_seq_len > 0 ? kv->max_seq_len : 1, kStageTokens) * kStageTokens;
+  l.Lpad = cdiv(kv->max_seq_len > 0 ? kv->max_seq_len : 1, kSideAlign) * kSideAlign;
   Carver c(nullptr);
   size_t rows = (size_t)l.units * l.S_max * l.R;
   l.o_off = c.off;
@@ -238,7 +246,7 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   l.lse_off = c.off;
   c.take<float>(rows);
   l.sp_off = c.off;
-  c.take<__half>((size_t)l.units * l.R * l.Lpad);
+  c.take<__half>((size_t)l.units * l.Lpad * (cdiv(l.R, 8) * 8));
   l.sm_off = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
   l.total = c.off;
@@ -252,7 +260,7 @@ static int verify_common_checks(const ssd_paged_kv *kv, int h_q, int n_cand, con
   if (n_cand < 1) return fail(SSD_ERR_INVALID_ARG, "%s: n_cand %d < 1", who, n_cand);
   if ((h_q / kv->h_kv) * n_cand > kMaxRows)
     return fail(SSD_ERR_UNSUPPORTED, "%s: G*n_cand = %d exceeds %d", who, (h_q / kv->h_kv) * n_cand, kMaxRows);
-  if (!aligned16(q)) return fail(SSD_ERR_INVALID_ARG, "%s: q must be 16-byte aligned", who);
+  if (!aligned16(q) || !aligned16(out)) return fail(SSD_ERR_INVALID_ARG, "%s: q and out must be 16-byte aligned", who);
   if ((int64_t)kv->batch * kv->h_kv > 65535) return fail(SSD_ERR_UNSUPPORTED, "%s: batch*h_kv above 65535", who);
   return SSD_OK;
 }
@@ -304,13 +312,16 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   a.scale_log2 = scale * kLog2e;
   a.S_max = lay.S_max;
   a.Lpad = lay.Lpad;
+  a.RS = cdiv(lay.R, 8) * 8;
   a.o_parts = reinterpret_cast<float *>(ws + lay.o_off);
   a.lse_parts = reinterpret_cast<float *>(ws + lay.lse_off);
   a.side_p = crit ? reinterpret_cast<__half *>(ws + lay.sp_off) : nullptr;
   a.side_m = crit ? reinterpret_cast<float *>(ws + lay.sm_off) : nullptr;
   a.status = status;
   dim3 grid(lay.S_max, lay.units);
-  if (kv->dtype == SSD_DTYPE_BF16)
+  if (verify_tc_supported(kv, lay.R))
+    rc = launch_verify_tc(kv, a, st);
+  else if (kv->dtype == SSD_DTYPE_BF16)
     rc = dispatch_mma<false>(kv->d, rows_per_tile(lay.R), a, grid, st);
   else
     rc = kv->d == 128 ? launch_simt<128>(a, grid, st) : launch_simt<64>(a, grid, st);
@@ -327,6 +338,7 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   f.D = kv->d;
   f.S_max = lay.S_max;
   f.Lpad = lay.Lpad;
+  f.RS = cdiv(lay.R, 8) * 8;
   f.o_parts = a.o_parts;
   f.lse_parts = a.lse_parts;
   f.side_p = a.side_p;

@@ -1,0 +1,711 @@
+// ssd_verify_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) verify kernel for bf16 caches with d = 128.
+//
+// SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
+// Sparse Attention") §4.1: the verify step is full attention of the k+1 candidates over the whole
+// cache, and the same kernel dumps what is needed to rematerialise the attention scores (cached
+// logits + LSE).  Same work items, partials and criticality side values as the mma.sync tile in
+// ssd_verify_tile.cuh; the finalize pass is shared.
+//
+// One persistent block per SM walks the work items (splits of 512 tokens of one (request, KV head))
+// assigned to it, tile by tile (128 tokens):
+//  * warp 8 streams K and V tiles with TMA (one box per page and 64-column panel, 128-byte swizzle,
+//    L2 evict-first) into a ring of 32 KB slots; the item's page ids are read once per item by the
+//    whole warp and each lane issues its own boxes.  It also writes the item's query rows.
+//  * warp 9 (one thread) issues the MMAs:  S^T[t][r] = K[t][:] . Q[r][:]    (M = 128 tokens, N = NP)
+//                                          O^T[d][n] += V[:][d] . P^T[:][n]  (M = 128 = d,   N = 2 NP)
+//    where n < NP carries the bf16 high part of the probabilities and n >= NP the bf16 residual, so
+//    P keeps about 16 bits.  S is double-buffered in TMEM; QK of tile i+1 is issued before PV of i.
+//  * warps 0-3 and 4-7 are two softmax warpgroups: TMEM lane t is token t of the tile (for S) and
+//    head dimension d = t (for O); warpgroup w owns rows [w*NP/2, (w+1)*NP/2).  The two groups are
+//    independent (rows never mix), so each scheduler runs two softmax warps.
+//  * The softmax keeps a lazily updated per-row reference m_ref (log2 domain): probabilities are
+//    2^(s - m_ref) <= 2^8; only when a logit exceeds m_ref + 8 does a group agree on a new reference
+//    (warp vote, then a transposed warp reduction) and rescale its running sums and its columns of
+//    the TMEM accumulator.  Padded rows carry m_ref = +inf, so full tiles need no masking.  The fp16
+//    side values for the criticality are these probabilities (token-major rows), with m_ref stored
+//    once per 16 tokens.
+//  * All waits are bounded (about one second); on expiry the block raises SSD_FAULT_TIMEOUT in the
+//    status word, drains its own copies and MMAs, frees its tensor memory and exits.  Abort
+//    decisions are warp-uniform, and the softmax groups synchronise through mbarriers (bounded), not
+//    hardware named barriers.
+#include "ssd_host.h"
+#include "ssd_sm100.cuh"
+#include "ssd_verify_tile.cuh"
+
+namespace ssd {
+using namespace sm100;
+
+constexpr int kTcTile = 128;
+constexpr int kTcWarps = 10;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcSoftmax = 256;  // two warpgroups
+constexpr int kTcProducerWarp = 8;
+constexpr int kTcMmaWarp = 9;
+constexpr int kTcMaxBatch = 2048;
+constexpr int kSlotBytes = kTcTile * 256;  // one K or V tile: 2 panels x 128 rows x 128 B
+constexpr int kPanelBytes = kTcTile * 128;
+constexpr float kLazy = 8.f;
+
+template <int NP>
+struct TcCfg {
+  static_assert(NP == 32 || NP == 64, "row padding");
+  static constexpr int CW = NP / 2;  // columns (rows of the GQA group) per softmax warpgroup
+  static constexpr int NSLOT = NP == 32 ? 5 : 3;
+  static constexpr int P_BYTES = kTcTile * (2 * NP) * 2;
+  static constexpr int Q_PANEL = NP * 128;
+  static constexpr int Q_BYTES = 2 * Q_PANEL;
+  static constexpr int TMEM_COLS = 4 * NP;
+  static constexpr int OFF_P = NSLOT * kSlotBytes;
+  static constexpr int OFF_Q = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_MISC = OFF_Q + 2 * Q_BYTES;
+  // misc: 32 mbarriers, flags, per-row arrays, reduction scratch, the per-request item prefix
+  static constexpr int MISC = 32 * 8 + 64 + NP * 4 * 3 + 2 * 4 * 32 * 4 + (kTcMaxBatch + 1) * 4;
+  static constexpr int SMEM = OFF_MISC + MISC + 1024;
+};
+
+struct TcSmem {
+  uint64_t *full, *empty, *s_full, *s_empty, *p_full, *p_empty, *o_full, *o_empty, *q_full, *q_empty, *drain, *grp;
+  uint32_t *tmem;
+  int *abort;
+  int *vote;  // [2 groups][4]
+  float *mref, *alpha, *lsum, *red;  // red: [2 groups][4 warps][32]
+  int *pre;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(uint64_t *b) { return smem_u32(b); }
+
+struct TcItem {
+  int b, g, split, L, t0, t1, ntiles;
+};
+
+// Item -> (request, head, split): items of request b are pre[b] .. pre[b+1]-1, ordered (head, split).
+__device__ __forceinline__ TcItem tc_decode(int item, const int *pre, int B, const VerifyArgs &a) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (pre[mid] <= item) lo = mid; else hi = mid;
+  }
+  TcItem it;
+  it.b = lo;
+  const int r = item - pre[lo];
+  const int ns = (pre[lo + 1] - pre[lo]) / a.kv.h_kv;
+  it.g = r / ns;
+  it.split = r % ns;
+  int L = a.kv.seq_lens[lo];
+  it.L = L < 0 ? 0 : (L > a.kv.max_seq_len ? a.kv.max_seq_len : L);
+  it.t0 = it.split * kSplitTokens;
+  it.t1 = min(it.t0 + kSplitTokens, it.L);
+  it.ntiles = cdiv(it.t1 - it.t0, kTcTile);
+  return it;
+}
+
+// Reduces v[N] (N = 16 or 32) over the 32 lanes of the warp; afterwards lane l holds the result for
+// column l % N.
+template <int N, bool MAX>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int ofs = 16; ofs >= N; ofs >>= 1) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[k], ofs);
+      v[k] = MAX ? fmaxf(v[k], o) : v[k] + o;
+    }
+  }
+#pragma unroll
+  for (int ofs = N / 2; ofs >= 1; ofs >>= 1) {
+    const bool upper = (lane & ofs) != 0;
+#pragma unroll
+    for (int k = 0; k < ofs; ++k) {
+      const float send = upper ? v[k] : v[k + ofs];
+      const float keep = upper ? v[k + ofs] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, ofs);
+      v[k] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
+// Bounded arrive-and-wait over the 128 threads of one softmax warpgroup.
+__device__ __forceinline__ bool group_sync(uint64_t *bar, volatile int *abort, uint32_t &phase) {
+  mbar_arrive(bar_addr(bar));
+  const bool ok = mbar_wait(bar_addr(bar), phase, abort);
+  phase ^= 1u;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-uniform bounded wait: every lane gets the same verdict, so an aborting warp leaves its loops
+// together (no lane is stranded at a warp-collective instruction).
+__device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile int *abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v) {
+  if constexpr (N == 16) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  } else {
+    static_assert(N == 32, "16 or 32 columns");
+    tmem_ld32(taddr, v);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float *v) {
+  if constexpr (N == 16) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+  } else {
+    static_assert(N == 32, "16 or 32 columns");
+    tmem_st32(taddr, v);
+  }
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    verify_tc_kernel(const __grid_constant__ CUtensorMap kvmap, VerifyArgs a, int box_rows) {
+  using C = TcCfg<NP>;
+  constexpr int CW = C::CW;
+  extern __shared__ __align__(1024) char smem_raw[];
+  char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int B = a.kv.batch, h_kv = a.kv.h_kv;
+
+  TcSmem s;
+  {
+    char *m = sm + C::OFF_MISC;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(m);
+    s.full = bars;
+    s.empty = bars + 5;
+    s.s_full = bars + 10;
+    s.s_empty = bars + 12;
+    s.p_full = bars + 14;
+    s.p_empty = bars + 16;
+    s.o_full = bars + 18;
+    s.o_empty = bars + 19;
+    s.q_full = bars + 20;
+    s.q_empty = bars + 22;
+    s.drain = bars + 24;
+    s.grp = bars + 25;  // [2]
+    m += 32 * 8;
+    s.tmem = reinterpret_cast<uint32_t *>(m);
+    s.abort = reinterpret_cast<int *>(s.tmem + 1);
+    s.vote = s.abort + 1;  // [8]
+    m += 64;
+    s.mref = reinterpret_cast<float *>(m);
+    s.alpha = s.mref + NP;
+    s.lsum = s.alpha + NP;
+    s.red = s.lsum + NP;
+    s.pre = reinterpret_cast<int *>(s.red + 2 * 4 * 32);
+  }
+
+  // Per-request item counts and their prefix (chunked block scan).
+  {
+    constexpr int CH = cdiv(kTcMaxBatch + 1, kTcThreads);
+    int loc[CH];
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const int b = tid * CH + k;
+      int c = 0;
+      if (b < B) {
+        int L = a.kv.seq_lens[b];
+        if (L < a.n_c || L > a.kv.max_seq_len) {
+          if (blockIdx.x == 0) atomicOr(a.status, (unsigned)SSD_FAULT_SEQLEN);
+          L = L < 0 ? 0 : (L > a.kv.max_seq_len ? a.kv.max_seq_len : L);
+        }
+        c = h_kv * verify_splits(L);
+      }
+      loc[k] = c;
+      sum += c;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    __shared__ int s_wsum[kTcWarps];
+    if (lane == 31) s_wsum[warp] = incl;
+    if (tid == 0) {
+      *s.abort = 0;
+      for (int k = 0; k < 8; ++k) s.vote[k] = 0;
+      for (int k = 0; k < C::NSLOT; ++k) {
+        mbar_init(bar_addr(s.full + k), 1);
+        mbar_init(bar_addr(s.empty + k), 1);
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(bar_addr(s.s_full + k), 1);
+        mbar_init(bar_addr(s.s_empty + k), kTcSoftmax);
+        mbar_init(bar_addr(s.p_full + k), kTcSoftmax);
+        mbar_init(bar_addr(s.p_empty + k), 1);
+        mbar_init(bar_addr(s.q_full + k), 32);
+        mbar_init(bar_addr(s.q_empty + k), 1);
+        mbar_init(bar_addr(s.grp + k), 128);
+      }
+      mbar_init(bar_addr(s.o_full), 1);
+      mbar_init(bar_addr(s.o_empty), kTcSoftmax);
+      mbar_init(bar_addr(s.drain), 1);
+      mbar_init_fence();
+    }
+    if (warp == kTcMmaWarp) {
+      tmem_alloc(smem_u32(s.tmem), C::TMEM_COLS);
+      tmem_relinquish();
+    }
+    if (warp == kTcProducerWarp && lane == 0) tma_prefetch_desc(&kvmap);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    int off = 0;
+    for (int w = 0; w < warp; ++w) off += s_wsum[w];
+    off += incl - sum;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const int b = tid * CH + k;
+      if (b <= B) s.pre[b] = off;
+      off += loc[k];
+    }
+    __syncthreads();
+  }
+  const uint32_t tm = *s.tmem;
+  const int n_items = s.pre[B];
+  const int G = a.G, R = a.R, n_c = a.n_c;
+
+  if (warp == kTcProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer + query rows
+    // Control flow stays warp-uniform: lane 0 waits, the verdict is broadcast.
+    const uint64_t pol = policy_evict_first();
+    const int ps = a.kv.page_size, lps = a.kv.log2_ps;
+    uint32_t fill = 0;
+    int jl = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++jl) {
+      const TcItem it = tc_decode(item, s.pre, B, a);
+      // Page ids of the item's boxes, read once by the whole warp: box j (tokens t0 + j*box_rows)
+      // lives in lane j % 32, register j / 32 (at most 512 / 8 = 64 boxes per item).
+      int32_t pid_reg[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = it.t0 + (h * 32 + lane) * box_rows;
+        pid_reg[h] = t < it.t1 ? __ldg(a.kv.page_table + (int64_t)it.b * a.kv.max_pages + (t >> lps)) : -1;
+      }
+      // Query rows of this item (rows >= R are zero), K-major 128-byte swizzled panels.
+      const bool qok = lane == 0 ? mbar_wait(bar_addr(s.q_empty + (jl & 1)), ((jl >> 1) & 1) ^ 1, s.abort) : true;
+      if (!__shfl_sync(0xffffffffu, qok, 0)) { ok = false; break; }
+      {
+        char *qb = sm + C::OFF_Q + (jl & 1) * C::Q_BYTES;
+        const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+        for (int e = lane; e < NP * 16; e += 32) {
+          const int r = e >> 4, ch = e & 15, panel = ch >> 3, c = ch & 7;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (r < R) {
+            const int i = r / G, hl = r % G;
+            v = __ldg(reinterpret_cast<const uint4 *>(q + (((int64_t)it.b * n_c + i) * a.h_q + it.g * G + hl) * 128) + ch);
+          }
+          *reinterpret_cast<uint4 *>(qb + panel * C::Q_PANEL + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar_addr(s.q_full + (jl & 1)));
+      }
+      const int boxes_per_tile = kTcTile / box_rows;
+      for (int k = 0; ok && k < it.ntiles; ++k) {
+        const int tb = it.t0 + k * kTcTile, tend = min(tb + kTcTile, it.t1);
+        // Lane j < boxes_per_tile handles box j of this tile.
+        const int jb = k * boxes_per_tile + lane;
+        const int32_t p0 = __shfl_sync(0xffffffffu, pid_reg[0], jb & 31);
+        const int32_t p1 = __shfl_sync(0xffffffffu, pid_reg[1], jb & 31);
+        const int32_t pid = (jb >> 5) ? p1 : p0;
+        const int t = tb + lane * box_rows;
+        const bool in_tile = lane < boxes_per_tile && t < tend;
+        const bool good = in_tile && pid >= 0 && (int64_t)pid < a.kv.num_pages;
+        if (in_tile && !good) atomicOr(a.status, (unsigned)SSD_FAULT_PAGE);
+        const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, good));
+        for (int kv = 0; kv < 2; ++kv, ++fill) {
+          const int slot = fill % C::NSLOT;
+          const uint32_t use = fill / C::NSLOT;
+          const bool eok = lane == 0 ? mbar_wait(bar_addr(s.empty + slot), (use & 1) ^ 1, s.abort) : true;
+          if (!__shfl_sync(0xffffffffu, eok, 0)) { ok = false; break; }
+          const uint32_t fb = bar_addr(s.full + slot);
+          if (lane == 0) mbar_arrive_expect_tx(fb, nbox * (uint32_t)box_rows * 256u);
+          __syncwarp();
+          if (good) {
+            const int row = (int)((((int64_t)pid * 2 + kv) * h_kv + it.g) * ps + (t & (ps - 1)));
+            const uint32_t dst = sbase + slot * kSlotBytes + (t - tb) * 128;
+            tma_load_3d(dst, &kvmap, 0, 0, row, fb, pol);
+            tma_load_3d(dst + kPanelBytes, &kvmap, 0, 1, row, fb, pol);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // Drain: every fill issued so far must land before the block's shared memory is released.
+      for (uint32_t f = fill > (uint32_t)C::NSLOT ? fill - C::NSLOT : 0; f < fill; ++f) {
+        volatile int never = 0;
+        mbar_wait(bar_addr(s.full + (f % C::NSLOT)), (f / C::NSLOT) & 1, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kTcMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16_f32(128, NP, 0, 0);
+      const uint32_t id_pv = idesc_bf16_f32(128, 2 * NP, 1, 1);
+      const uint32_t o_col = tm + 2 * NP;
+      uint32_t i = 0;
+      int jl = 0;
+      bool ok = true;
+      bool pend = false, pfirst = false, plast = false;
+      uint32_t pi = 0;
+      int pj = 0;
+      auto issue_pv = [&](uint32_t ti, bool first, bool last, int tj) -> bool {
+        const uint32_t vf = 2 * ti + 1;
+        const int vslot = vf % C::NSLOT;
+        if (!mbar_wait(bar_addr(s.full + vslot), (vf / C::NSLOT) & 1, s.abort)) return false;
+        if (!mbar_wait(bar_addr(s.p_full + (ti & 1)), (ti >> 1) & 1, s.abort)) return false;
+        if (first && !mbar_wait(bar_addr(s.o_empty), (tj & 1) ^ 1, s.abort)) return false;
+        tc_fence_after();
+        const uint32_t va = sbase + vslot * kSlotBytes;
+        const uint32_t pa = sbase + C::OFF_P + (ti & 1) * C::P_BYTES;
+#pragma unroll
+        for (int st = 0; st < kTcTile / 16; ++st) {
+          const uint64_t ad = smem_desc(va + st * 2048, kPanelBytes, 1024);
+          const uint64_t bd = smem_desc(pa + st * 2048, kPanelBytes, 1024);
+          mma_bf16_ss(o_col, ad, bd, id_pv, (first && st == 0) ? 0u : 1u);
+        }
+        mma_commit(bar_addr(s.empty + vslot));
+        mma_commit(bar_addr(s.p_empty + (ti & 1)));
+        if (last) mma_commit(bar_addr(s.o_full));
+        return true;
+      };
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++jl) {
+        const TcItem it = tc_decode(item, s.pre, B, a);
+        if (!mbar_wait(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1, s.abort)) { ok = false; break; }
+        const uint32_t qa = sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES;
+        for (int k = 0; k < it.ntiles; ++k, ++i) {
+          const uint32_t kf = 2 * i;
+          const int kslot = kf % C::NSLOT;
+          if (!mbar_wait(bar_addr(s.full + kslot), (kf / C::NSLOT) & 1, s.abort)) { ok = false; break; }
+          if (!mbar_wait(bar_addr(s.s_empty + (i & 1)), ((i >> 1) & 1) ^ 1, s.abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t ka = sbase + kslot * kSlotBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = smem_desc(ka + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = smem_desc(qa + (kk >> 2) * C::Q_PANEL + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ss(tm + (i & 1) * NP, ad, bd, id_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar_addr(s.s_full + (i & 1)));
+          mma_commit(bar_addr(s.empty + kslot));
+          if (k == it.ntiles - 1) mma_commit(bar_addr(s.q_empty + (jl & 1)));
+          if (pend && !issue_pv(pi, pfirst, plast, pj)) { ok = false; break; }
+          pend = true;
+          pi = i;
+          pfirst = (k == 0);
+          plast = (k == it.ntiles - 1);
+          pj = jl;
+        }
+      }
+      if (ok && pend) issue_pv(pi, pfirst, plast, pj);
+      // Drain every MMA this thread issued before the tensor memory is released.
+      mma_commit(bar_addr(s.drain));
+      volatile int never = 0;
+      mbar_wait(bar_addr(s.drain), 0, &never);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax + epilogue
+    const int wg = warp >> 2, tw = tid & 127, wiw = warp & 3;  // group, lane of TMEM, warp in group
+    const int c0 = wg * CW;                                      // first row of this group
+    uint64_t *grp = s.grp + wg;
+    int *vote = s.vote + wg * 4;
+    float *red = s.red + wg * 4 * 32;
+    const uint32_t lane_base = (uint32_t)(wiw * 32) << 16;
+    const int nref = a.Lpad / kRefGroup;
+    const int RS = a.RS;
+    uint32_t i = 0, gph = 0;
+    int jl = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++jl) {
+      const TcItem it = tc_decode(item, s.pre, B, a);
+      const int u = it.b * h_kv + it.g;
+      const int lim_base = it.L - n_c;  // row r sees t <= lim_base + r / G
+      if (tw < CW) s.mref[c0 + tw] = (c0 + tw < R) ? -INFINITY : INFINITY;
+      float lsum[CW];
+#pragma unroll
+      for (int j = 0; j < CW; ++j) lsum[j] = 0.f;
+      if (!group_sync(grp, s.abort, gph)) goto out;
+      for (int k = 0; k < it.ntiles; ++k, ++i) {
+        const int tb = it.t0 + k * kTcTile, t = tb + tw;
+        const uint32_t vf = 2 * i + 1;
+        const int vslot = vf % C::NSLOT;
+        // Token validity from the page table itself (loaded before the wait so its latency hides
+        // behind it): the K slot may already be refilled once QK has consumed it, so the softmax
+        // never waits on that slot.
+        int32_t pid = 0;
+        if (t < it.t1) pid = __ldg(a.kv.page_table + (int64_t)it.b * a.kv.max_pages + (t >> a.kv.log2_ps));
+        if (!wwait(bar_addr(s.s_full + (i & 1)), (i >> 1) & 1, s.abort)) goto out;
+        tc_fence_after();
+        float x[CW];
+        tmem_ld_cols<CW>(tm + lane_base + (i & 1) * NP + c0, x);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(bar_addr(s.s_empty + (i & 1)));
+        const bool valid = t < it.t1 && pid >= 0 && (int64_t)pid < a.kv.num_pages;
+        const bool causal = tb + kTcTile - 1 > lim_base;
+        const bool masked = causal || !__all_sync(0xffffffffu, valid);
+        float mr[CW];
+#pragma unroll
+        for (int j = 0; j < CW; j += 4) *reinterpret_cast<float4 *>(mr + j) = *reinterpret_cast<const float4 *>(s.mref + c0 + j);
+        // d = scale * s - m_ref (log2 domain); -inf where the row cannot see the token.
+        float dl[CW];
+        if (masked) {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            const int r = c0 + j;
+            const bool vis = valid && r < R && (!causal || t <= lim_base + r / G);
+            x[j] = vis ? x[j] * a.scale_log2 : -INFINITY;
+            dl[j] = x[j] - mr[j];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) dl[j] = fmaf(x[j], a.scale_log2, -mr[j]);  // padded rows: -inf
+        }
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) need |= dl[j] > kLazy;
+        if (__any_sync(0xffffffffu, need) && lane == 0) vote[i & 3] = 1;
+        if (!group_sync(grp, s.abort, gph)) goto out;
+        const bool any = vote[i & 3] != 0;
+        if (tw == 0) vote[(i + 2) & 3] = 0;
+        if (any) {
+          // New reference: per-row maximum of the tile (over the group's 128 tokens).
+          float v[CW];
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            const int r = c0 + j;
+            if (!masked) x[j] = r < R ? x[j] * a.scale_log2 : -INFINITY;
+            v[j] = x[j];
+          }
+          const float mx = transpose_reduce<CW, true>(v);
+          if (lane < CW) red[wiw * 32 + lane] = mx;
+          if (!group_sync(grp, s.abort, gph)) goto out;
+          if (tw < CW) {
+            const int r = c0 + tw;
+            const float m_old = s.mref[r];
+            const float mt = fmaxf(fmaxf(red[tw], red[32 + tw]), fmaxf(red[64 + tw], red[96 + tw]));
+            if (r < R) {
+              const float m_new = fmaxf(m_old, mt);
+              s.alpha[r] = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - m_new);
+              s.mref[r] = m_new;
+            } else {
+              s.alpha[r] = 1.f;
+            }
+          }
+          if (!group_sync(grp, s.abort, gph)) goto out;
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            lsum[j] *= s.alpha[c0 + j];
+            mr[j] = s.mref[c0 + j];
+            dl[j] = x[j] - mr[j];
+          }
+          if (k > 0) {
+            // Rescale this group's columns of the accumulator once the previous PV has landed.
+            const uint32_t pj = i - 1;
+            if (!wwait(bar_addr(s.p_empty + (pj & 1)), (pj >> 1) & 1, s.abort)) goto out;
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float o[CW];
+              const uint32_t col = tm + lane_base + 2 * NP + h * NP + c0;
+              tmem_ld_cols<CW>(col, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < CW; ++j) o[j] *= s.alpha[c0 + j];
+              tmem_st_cols<CW>(col, o);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+          }
+        }
+        // Probabilities (<= 2^kLazy; exp2(-inf) = 0), running sums, side values, P tile.
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          x[j] = fast_exp2(dl[j]);
+          lsum[j] += x[j];
+        }
+        if (a.side_p != nullptr) {
+          // Token-major fp16 row of RS values; this group writes its rows that fall below RS.
+          __half *sp = a.side_p + ((int64_t)u * a.Lpad + t) * RS + c0;
+#pragma unroll
+          for (int j = 0; j < CW; j += 8) {
+            if (c0 + j < RS) {
+              uint4 pk;
+              pk.x = pack_half(x[j], x[j + 1]);
+              pk.y = pack_half(x[j + 2], x[j + 3]);
+              pk.z = pack_half(x[j + 4], x[j + 5]);
+              pk.w = pack_half(x[j + 6], x[j + 7]);
+              *reinterpret_cast<uint4 *>(sp + j) = pk;
+            }
+          }
+          // References: one per (row, 16 tokens); CW rows x 8 groups entries per warpgroup.
+#pragma unroll
+          for (int e = tw; e < CW * (kTcTile / kRefGroup); e += 128) {
+            const int r = c0 + e / (kTcTile / kRefGroup), gi = e % (kTcTile / kRefGroup);
+            if (r < R) {
+              const float m = s.mref[r];
+              a.side_m[((int64_t)u * R + r) * nref + tb / kRefGroup + gi] = (m == -INFINITY) ? 0.f : m;
+            }
+          }
+        }
+        if (!wwait(bar_addr(s.p_empty + (i & 1)), ((i >> 1) & 1) ^ 1, s.abort)) goto out;
+        {
+          char *prow = sm + C::OFF_P + (i & 1) * C::P_BYTES + tw * 128;
+#pragma unroll
+          for (int c8 = 0; c8 < CW / 8; ++c8) {
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_bf16(x[8 * c8 + 2 * e], x[8 * c8 + 2 * e + 1], h[e], l[e]);
+            // Columns n = c0 + 8*c8 .. +7 (high part) and NP + c0 + 8*c8 .. (residual); 64 columns
+            // per 128-byte swizzle atom.
+            const int nh = c0 + 8 * c8, nl = NP + c0 + 8 * c8;
+            *reinterpret_cast<uint4 *>(prow + (nh >> 6) * kPanelBytes + ((((nh & 63) >> 3) ^ (tw & 7)) << 4)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(prow + (nl >> 6) * kPanelBytes + ((((nl & 63) >> 3) ^ (tw & 7)) << 4)) =
+                make_uint4(l[0], l[1], l[2], l[3]);
+          }
+        }
+        if (wg == 0) {
+          // An invalid token's V row may hold bytes past the sequence (or a skipped page): zero it
+          // once the tile has landed, so that 0 * garbage cannot reach the accumulator.
+          if (__any_sync(0xffffffffu, !valid)) {
+            if (!wwait(bar_addr(s.full + vslot), (vf / C::NSLOT) & 1, s.abort)) goto out;
+          }
+          if (!valid) {
+            char *vrow = sm + vslot * kSlotBytes + tw * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4 *>(vrow + kPanelBytes + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar_addr(s.p_full + (i & 1)));
+      }
+      // Epilogue: O (high + residual columns) and the row sums -> the split's normalised partial.
+      {
+        if (!wwait(bar_addr(s.o_full), jl & 1, s.abort)) goto out;
+        tc_fence_after();
+        float o[CW];
+        {
+          float hi[CW], lo[CW];
+          tmem_ld_cols<CW>(tm + lane_base + 2 * NP + c0, hi);
+          tmem_ld_cols<CW>(tm + lane_base + 3 * NP + c0, lo);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CW; ++j) o[j] = hi[j] + lo[j];
+        }
+        tc_fence_before();
+        mbar_arrive(bar_addr(s.o_empty));
+        const float ls = transpose_reduce<CW, false>(lsum);
+        if (lane < CW) red[wiw * 32 + lane] = ls;
+        if (!group_sync(grp, s.abort, gph)) goto out;
+        if (tw < CW) s.lsum[c0 + tw] = red[tw] + red[32 + tw] + red[64 + tw] + red[96 + tw];
+        if (!group_sync(grp, s.abort, gph)) goto out;
+        const int64_t prow = ((int64_t)u * a.S_max + it.split) * R;
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          const int r = c0 + j;
+          if (r < R) {
+            const float l = s.lsum[r];
+            a.o_parts[(prow + r) * 128 + tw] = l > 0.f ? o[j] / l : 0.f;
+          }
+        }
+        if (tw < CW && c0 + tw < R) {
+          const int r = c0 + tw;
+          const float l = s.lsum[r], m = s.mref[r];
+          a.lse_parts[prow + r] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        }
+        if (!group_sync(grp, s.abort, gph)) goto out;
+      }
+    }
+  out:;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0 && *reinterpret_cast<volatile int *>(s.abort)) atomicOr(a.status, (unsigned)SSD_FAULT_TIMEOUT);
+  if (warp == kTcMmaWarp) tmem_dealloc(tm, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Host side.
+// ------------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+bool verify_tc_supported(const ssd_paged_kv *kv, int R) {
+  return kv->dtype == SSD_DTYPE_BF16 && kv->d == 128 && kv->page_size >= 8 && R <= 64 && kv->batch <= kTcMaxBatch &&
+         (int64_t)kv->num_pages * 2 * kv->h_kv * kv->page_size < (1ll << 31);
+}
+
+template <int NP>
+static int launch_tc(const CUtensorMap &map, const VerifyArgs &a, int box_rows, int grid, cudaStream_t st) {
+  constexpr int smem = TcCfg<NP>::SMEM;
+  int rc = ensure_smem<verify_tc_kernel<NP>>(smem);
+  if (rc) return rc;
+  verify_tc_kernel<NP><<<grid, kTcThreads, smem, st>>>(map, a, box_rows);
+  return check_launch("verify_tc_kernel");
+}
+
+int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const int box_rows = kv->page_size < kTcTile ? kv->page_size : kTcTile;
+  CUtensorMap map;
+  cuuint64_t dims[3] = {64, 2, (cuuint64_t)kv->num_pages * 2 * kv->h_kv * kv->page_size};
+  cuuint64_t strides[2] = {128, 256};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv->pool), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  const int64_t items_max = (int64_t)kv->batch * kv->h_kv * a.S_max;
+  const int grid = (int)(items_max < sm_count() ? items_max : sm_count());
+  if (grid <= 0) return SSD_OK;
+  return a.R <= 32 ? launch_tc<32>(map, a, box_rows, grid, st) : launch_tc<64>(map, a, box_rows, grid, st);
+}
+
+}  // namespace ssd

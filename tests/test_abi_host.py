@@ -47,7 +47,7 @@ def test_workspace_queries(lib):
     kv = _kv()
     vb = lib.ssd_verify_workspace_bytes(ctypes.byref(kv), 32, 5)
     assert vb > 0 and vb % 256 == 0
-    kv2 = _kv(max_seq_len=128, max_pages=8)
+    kv2 = _kv(max_seq_len=1024, max_pages=64)
     assert lib.ssd_verify_workspace_bytes(ctypes.byref(kv2), 32, 5) > vb
     assert lib.ssd_verify_workspace_bytes(None, 32, 5) == 0
     assert lib.ssd_draft_workspace_bytes(ctypes.byref(kv), 32, 410) > lib.ssd_draft_workspace_bytes(ctypes.byref(kv), 32, 64)
