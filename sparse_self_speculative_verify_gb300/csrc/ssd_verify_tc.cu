@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int r = c0 + j;
             const bool vis = valid && r < R && (!causal || t <= lim_base + r / G);
             x[j] = vis ? x[j] * a.scale_log2 : -INFINITY;
-            dl[j] = x[j] - mr[j];
+            dl[j] = vis ? x[j] - mr[j] : -INFINITY;  // never -inf - (-inf)
           }
         } else {
 #pragma unroll
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int j = 0; j < CW; ++j) {
             lsum[j] *= s.alpha[c0 + j];
             mr[j] = s.mref[c0 + j];
-            dl[j] = x[j] - mr[j];
+            dl[j] = (x[j] == -INFINITY) ? -INFINITY : x[j] - mr[j];
           }
           if (k > 0) {
             // Rescale this group's columns of the accumulator once the previous PV has landed.

@@ -85,6 +85,7 @@ def assert_scores(got, ref, lens, what="scores"):
     for b, L in enumerate(lens):
         g = np.asarray(got[b, :, :L], np.float64)
         r = np.asarray(ref[b, :, :L], np.float64)
+        assert np.isfinite(g).all(), f"{what}: request {b}: non-finite scores"
         d = np.abs(g - r)
         lim = SCORE_RTOL * np.abs(r) + SCORE_ATOL
         bad = d > lim
