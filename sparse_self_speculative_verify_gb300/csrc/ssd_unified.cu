@@ -121,7 +121,7 @@ static UniLayout uni_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int k_m
   l.v_lse = c.off;
   c.take<float>(rows);
   l.v_sp = c.off;
-  c.take<__half>((size_t)l.units * l.Lpad * (cdiv(l.R, 8) * 8));
+  c.take<__half>((size_t)l.units * l.R * l.Lpad);
   l.v_sm = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
   l.d_off = c.off;
@@ -205,7 +205,6 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
   va.scale_log2 = scale * kLog2e;
   va.S_max = lay.S_max;
   va.Lpad = lay.Lpad;
-  va.RS = cdiv(lay.R, 8) * 8;
   va.o_parts = reinterpret_cast<float *>(ws + lay.v_o);
   va.lse_parts = reinterpret_cast<float *>(ws + lay.v_lse);
   va.side_p = scores ? reinterpret_cast<__half *>(ws + lay.v_sp) : nullptr;
@@ -241,7 +240,6 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
   f.D = kv->d;
   f.S_max = lay.S_max;
   f.Lpad = lay.Lpad;
-  f.RS = cdiv(lay.R, 8) * 8;
   f.o_parts = va.o_parts;
   f.lse_parts = va.lse_parts;
   f.side_p = va.side_p;

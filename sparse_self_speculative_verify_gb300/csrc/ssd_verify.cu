@@ -104,12 +104,11 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   }
   if (!f.side_p) return;
 
-  // Criticality: one token per thread.  coef[r][j] = 2^(m_ref[r][group j] - LSE2_r) for the
-  // kFinGroups 16-token groups of this block, then crit[t] = sum_r e[t][r] * coef[r][t / 16].
-  __shared__ float s_coef[kMaxRows * kFinGroups];
-  __shared__ unsigned s_bmax[kMaxRows / 1 * (kFinTok / kBlockTokens)];
+  // Criticality: eight consecutive tokens per thread.  coef[r][j] = 2^(m_ref[r][group j] - LSE2_r)
+  // for the kFinGroups 16-token groups of this block, then crit[t] = sum_r e[r][t] * coef[r][t/16].
   const int tb0 = blockIdx.x * kFinTok;
   if (tb0 >= L) return;
+  __shared__ float s_coef[kMaxRows * kFinGroups];
   const int nref = f.Lpad / kRefGroup;
   const int64_t rbase = (int64_t)u * f.R;
   for (int e = tid; e < f.R * kFinGroups; e += kFinThreads) {
@@ -119,45 +118,66 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     const float ref = f.side_m[(rbase + r) * nref + tb0 / kRefGroup + j];
     s_coef[r * kFinGroups + j] = (l2 == -INFINITY) ? 0.f : fast_exp2(ref - l2);
   }
-  if (f.bscores)
-    for (int e = tid; e < f.n_c * (kFinTok / kBlockTokens); e += kFinThreads) s_bmax[e] = 0u;
   __syncthreads();
-  const int t = tb0 + tid;
-  const bool valid = t < L;
-  const int grp = tid / kRefGroup;
-  const __half *sp = f.side_p + ((int64_t)u * f.Lpad + t) * f.RS;
-  float crit = 0.f, cc = 0.f;
-  int cand = 0, in_cand = 0;
-  for (int c = 0; c < f.RS; c += 8) {
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (valid) raw = *reinterpret_cast<const uint4 *>(sp + c);
-    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+  const int t0 = tb0 + tid * 8;
+  const bool valid = t0 < L;
+  const int grp = tid >> 1;  // 8 tokens = half a 16-token group
+  const __half *sp = f.side_p + rbase * f.Lpad + t0;
+  float crit[8], cc[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int r = c + e;
-      if (r < f.R) {
-        const float2 pf = __half22float2(h2[e >> 1]);
-        cc = fmaf((e & 1) ? pf.y : pf.x, s_coef[r * kFinGroups + grp], cc);
-        if (++in_cand == f.G) {  // candidate `cand` complete
-          if (f.bscores) {
-            const float m = warp_max(valid ? cc : 0.f);
-            if (lane == 0) atomicMax(&s_bmax[cand * (kFinTok / kBlockTokens) + tid / kBlockTokens], __float_as_uint(m));
-          }
-          crit += cc;
-          cc = 0.f;
-          in_cand = 0;
-          ++cand;
+  for (int k = 0; k < 8; ++k) crit[k] = cc[k] = 0.f;
+  if (f.bscores == nullptr) {
+#pragma unroll 4
+    for (int r = 0; r < f.R; ++r) {
+      const uint4 raw = valid ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad)) : make_uint4(0, 0, 0, 0);
+      const float c = s_coef[r * kFinGroups + grp];
+      const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 pf = __half22float2(h2[k]);
+        crit[2 * k] = fmaf(pf.x, c, crit[2 * k]);
+        crit[2 * k + 1] = fmaf(pf.y, c, crit[2 * k + 1]);
+      }
+    }
+  } else {
+    for (int i = 0; i < f.n_c; ++i) {
+#pragma unroll 4
+      for (int hl = 0; hl < f.G; ++hl) {
+        const int r = i * f.G + hl;
+        const uint4 raw = valid ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad)) : make_uint4(0, 0, 0, 0);
+        const float c = s_coef[r * kFinGroups + grp];
+        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 pf = __half22float2(h2[k]);
+          cc[2 * k] = fmaf(pf.x, c, cc[2 * k]);
+          cc[2 * k + 1] = fmaf(pf.y, c, cc[2 * k + 1]);
         }
+      }
+      // Candidate i's block maximum: 64 tokens = 8 lanes x 8 tokens.
+      float m = cc[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) m = fmaxf(m, cc[k]);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      if ((lane & 7) == 0 && valid) f.bscores[((int64_t)u * f.n_c + i) * f.bstride + t0 / kBlockTokens] = m;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        crit[k] += cc[k];
+        cc[k] = 0.f;
       }
     }
   }
-  if (f.scores && valid) f.scores[(int64_t)u * f.scores_stride + t] = crit;
-  if (f.bscores) {
-    __syncthreads();
-    for (int e = tid; e < f.n_c * (kFinTok / kBlockTokens); e += kFinThreads) {
-      const int i = e / (kFinTok / kBlockTokens), j = e % (kFinTok / kBlockTokens);
-      const int blk = tb0 / kBlockTokens + j;
-      if (blk * kBlockTokens < L) f.bscores[((int64_t)u * f.n_c + i) * f.bstride + blk] = __uint_as_float(s_bmax[e]);
+  if (f.scores && valid) {
+    float *dst = f.scores + (int64_t)u * f.scores_stride + t0;
+    if (t0 + 8 <= L && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
+      reinterpret_cast<float4 *>(dst)[0] = make_float4(crit[0], crit[1], crit[2], crit[3]);
+      reinterpret_cast<float4 *>(dst)[1] = make_float4(crit[4], crit[5], crit[6], crit[7]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (t0 + k < L) dst[k] = crit[k];
     }
   }
 }
@@ -246,7 +266,7 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   l.lse_off = c.off;
   c.take<float>(rows);
   l.sp_off = c.off;
-  c.take<__half>((size_t)l.units * l.Lpad * (cdiv(l.R, 8) * 8));
+  c.take<__half>((size_t)l.units * l.R * l.Lpad);
   l.sm_off = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
   l.total = c.off;
@@ -312,7 +332,6 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   a.scale_log2 = scale * kLog2e;
   a.S_max = lay.S_max;
   a.Lpad = lay.Lpad;
-  a.RS = cdiv(lay.R, 8) * 8;
   a.o_parts = reinterpret_cast<float *>(ws + lay.o_off);
   a.lse_parts = reinterpret_cast<float *>(ws + lay.lse_off);
   a.side_p = crit ? reinterpret_cast<__half *>(ws + lay.sp_off) : nullptr;
@@ -338,7 +357,6 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   f.D = kv->d;
   f.S_max = lay.S_max;
   f.Lpad = lay.Lpad;
-  f.RS = cdiv(lay.R, 8) * 8;
   f.o_parts = a.o_parts;
   f.lse_parts = a.lse_parts;
   f.side_p = a.side_p;

@@ -332,16 +332,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int32_t p1 = __shfl_sync(0xffffffffu, pid_reg[1], jb & 31);
         const int32_t pid = (jb >> 5) ? p1 : p0;
         const int t = tb + lane * box_rows;
-        const bool in_tile = lane < boxes_per_tile && t < tend;
-        const bool good = in_tile && pid >= 0 && (int64_t)pid < a.kv.num_pages;
-        if (in_tile && !good) atomicOr(a.status, (unsigned)SSD_FAULT_PAGE);
+        const bool in_tile = lane < boxes_per_tile;
+        const bool page_ok = pid >= 0 && (int64_t)pid < a.kv.num_pages;
+        const int nvalid = in_tile ? max(0, min(box_rows, tend - t)) : 0;  // rows of this box in [tb, tend)
+        if (nvalid > 0 && !page_ok) atomicOr(a.status, (unsigned)SSD_FAULT_PAGE);
+        // Full boxes of a good page go through TMA; every other box of the tile (the request's
+        // partial last page, boxes past its end, skipped pages) is written by the warp with plain
+        // copies and zeros, in the same swizzled layout, so the MMA never reads stale or garbage rows.
+        const bool good = in_tile && nvalid == box_rows && page_ok;
         const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, good));
+        const uint32_t gmask = __ballot_sync(0xffffffffu, in_tile && !good);
         for (int kv = 0; kv < 2; ++kv, ++fill) {
           const int slot = fill % C::NSLOT;
           const uint32_t use = fill / C::NSLOT;
           const bool eok = lane == 0 ? mbar_wait(bar_addr(s.empty + slot), (use & 1) ^ 1, s.abort) : true;
           if (!__shfl_sync(0xffffffffu, eok, 0)) { ok = false; break; }
           const uint32_t fb = bar_addr(s.full + slot);
+          for (uint32_t gm = gmask; gm != 0; gm &= gm - 1) {
+            const int j = __ffs(gm) - 1;
+            const int nv = __shfl_sync(0xffffffffu, nvalid, j);
+            const bool okp = __shfl_sync(0xffffffffu, page_ok, j);
+            const int32_t pj = __shfl_sync(0xffffffffu, pid, j);
+            const int bt = tb + j * box_rows;
+            const __nv_bfloat16 *pool = reinterpret_cast<const __nv_bfloat16 *>(a.kv.pool);
+            for (int e = lane; e < box_rows * 16; e += 32) {
+              const int rr = e >> 4, ch = e & 15, panel = ch >> 3, c = ch & 7;
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (rr < nv && okp) {
+                const int64_t row = (((int64_t)pj * 2 + kv) * h_kv + it.g) * ps + ((bt + rr) & (ps - 1));
+                v = __ldg(reinterpret_cast<const uint4 *>(pool + row * 128) + ch);
+              }
+              const int trow = bt - tb + rr;
+              *reinterpret_cast<uint4 *>(sm + slot * kSlotBytes + panel * kPanelBytes + trow * 128 +
+                                         ((c ^ (trow & 7)) << 4)) = v;
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
           if (lane == 0) mbar_arrive_expect_tx(fb, nbox * (uint32_t)box_rows * 256u);
           __syncwarp();
           if (good) {
@@ -438,7 +465,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float *red = s.red + wg * 4 * 32;
     const uint32_t lane_base = (uint32_t)(wiw * 32) << 16;
     const int nref = a.Lpad / kRefGroup;
-    const int RS = a.RS;
     uint32_t i = 0, gph = 0;
     int jl = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++jl) {
@@ -452,13 +478,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!group_sync(grp, s.abort, gph)) goto out;
       for (int k = 0; k < it.ntiles; ++k, ++i) {
         const int tb = it.t0 + k * kTcTile, t = tb + tw;
-        const uint32_t vf = 2 * i + 1;
-        const int vslot = vf % C::NSLOT;
-        // Token validity from the page table itself (loaded before the wait so its latency hides
-        // behind it): the K slot may already be refilled once QK has consumed it, so the softmax
-        // never waits on that slot.
-        int32_t pid = 0;
-        if (t < it.t1) pid = __ldg(a.kv.page_table + (int64_t)it.b * a.kv.max_pages + (t >> a.kv.log2_ps));
         if (!wwait(bar_addr(s.s_full + (i & 1)), (i >> 1) & 1, s.abort)) goto out;
         tc_fence_after();
         float x[CW];
@@ -466,7 +485,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(bar_addr(s.s_empty + (i & 1)));
-        const bool valid = t < it.t1 && pid >= 0 && (int64_t)pid < a.kv.num_pages;
+        // Rows past the sequence and rows of skipped pages hold zeros in the K/V slots (the producer
+        // fills them), so only t < t1 matters here.
+        const bool valid = t < it.t1;
         const bool causal = tb + kTcTile - 1 > lim_base;
         const bool masked = causal || !__all_sync(0xffffffffu, valid);
         float mr[CW];
@@ -550,19 +571,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           lsum[j] += x[j];
         }
         if (a.side_p != nullptr) {
-          // Token-major fp16 row of RS values; this group writes its rows that fall below RS.
-          __half *sp = a.side_p + ((int64_t)u * a.Lpad + t) * RS + c0;
+          // fp16 side values, row-major per (unit, row): each warp store covers 32 consecutive tokens.
+          __half *sp = a.side_p + ((int64_t)u * R + c0) * a.Lpad + t;
 #pragma unroll
-          for (int j = 0; j < CW; j += 8) {
-            if (c0 + j < RS) {
-              uint4 pk;
-              pk.x = pack_half(x[j], x[j + 1]);
-              pk.y = pack_half(x[j + 2], x[j + 3]);
-              pk.z = pack_half(x[j + 4], x[j + 5]);
-              pk.w = pack_half(x[j + 6], x[j + 7]);
-              *reinterpret_cast<uint4 *>(sp + j) = pk;
-            }
-          }
+          for (int j = 0; j < CW; ++j)
+            if (c0 + j < R) sp[(int64_t)j * a.Lpad] = __float2half_rn(x[j]);
           // References: one per (row, 16 tokens); CW rows x 8 groups entries per warpgroup.
 #pragma unroll
           for (int e = tw; e < CW * (kTcTile / kRefGroup); e += 128) {
@@ -588,21 +601,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 make_uint4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<uint4 *>(prow + (nl >> 6) * kPanelBytes + ((((nl & 63) >> 3) ^ (tw & 7)) << 4)) =
                 make_uint4(l[0], l[1], l[2], l[3]);
-          }
-        }
-        if (wg == 0) {
-          // An invalid token's V row may hold bytes past the sequence (or a skipped page): zero it
-          // once the tile has landed, so that 0 * garbage cannot reach the accumulator.
-          if (__any_sync(0xffffffffu, !valid)) {
-            if (!wwait(bar_addr(s.full + vslot), (vf / C::NSLOT) & 1, s.abort)) goto out;
-          }
-          if (!valid) {
-            char *vrow = sm + vslot * kSlotBytes + tw * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4 *>(vrow + kPanelBytes + c * 16) = make_uint4(0, 0, 0, 0);
-            }
           }
         }
         fence_proxy_async_smem();

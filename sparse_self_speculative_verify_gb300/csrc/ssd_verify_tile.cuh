@@ -29,10 +29,9 @@ struct VerifyArgs {
   float scale_log2;  // softmax scale * log2(e)
   int S_max;         // splits per unit in the partial arrays
   int Lpad;          // tokens per unit in the side buffers (multiple of kSideAlign)
-  int RS;            // R rounded up to 8: fp16 values per token in side_p
   float *o_parts;    // [units][S_max][R][D], normalised by the split's own sum
   float *lse_parts;  // [units][S_max][R], natural log; -inf for an empty split
-  __half *side_p;    // [units][Lpad][RS] token-major, or nullptr (no criticality)
+  __half *side_p;    // [units][R][Lpad], or nullptr (no criticality)
   float *side_m;     // [units][R][Lpad / kRefGroup]
   // Block-sparse token source (union of candidate block sets); nullptr for contiguous splits.
   const int32_t *uidx;
@@ -246,18 +245,12 @@ __device__ __forceinline__ void verify_item_mma(const VerifyArgs &a, int unit, i
     // Criticality side values: e = 2^(s - base) as fp16, and base once per 16 tokens.
     if (!BLOCKS && a.side_p != nullptr) {
       const int tw0 = base + tg * TW;
-      __half *sp = a.side_p + ((int64_t)unit * a.Lpad + tw0 + 2 * tq) * a.RS;
+      __half *sp0 = a.side_p + ((int64_t)unit * R + r0) * a.Lpad + tw0 + 2 * tq;
+      __half *sp1 = a.side_p + ((int64_t)unit * R + r1) * a.Lpad + tw0 + 2 * tq;
 #pragma unroll
       for (int n = 0; n < TW / 8; ++n) {
-        __half *s2 = sp + (int64_t)n * 8 * a.RS;
-        if (st0) {
-          s2[r0] = __float2half_rn(sacc[n][0]);
-          s2[a.RS + r0] = __float2half_rn(sacc[n][1]);
-        }
-        if (st1) {
-          s2[r1] = __float2half_rn(sacc[n][2]);
-          s2[a.RS + r1] = __float2half_rn(sacc[n][3]);
-        }
+        if (st0) *reinterpret_cast<uint32_t *>(sp0 + n * 8) = pack_half(sacc[n][0], sacc[n][1]);
+        if (st1) *reinterpret_cast<uint32_t *>(sp1 + n * 8) = pack_half(sacc[n][2], sacc[n][3]);
       }
       if (tq == 0) {
         const int nref = a.Lpad / kRefGroup;
@@ -409,8 +402,8 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
   if (a.side_p != nullptr) {
     const int nref = a.Lpad / kRefGroup;
     for (int e = tid; e < R * n; e += blockDim.x) {
-      int j = e / R, r = e % R;
-      a.side_p[((int64_t)unit * a.Lpad + t0 + j) * a.RS + r] = __float2half_rn(sS[r * kSplitTokens + j]);
+      int r = e / n, j = e % n;
+      a.side_p[((int64_t)unit * R + r) * a.Lpad + t0 + j] = __float2half_rn(sS[r * kSplitTokens + j]);
     }
     for (int e = tid; e < R * cdiv(n, kRefGroup); e += blockDim.x) {
       int r = e / cdiv(n, kRefGroup), j = e % cdiv(n, kRefGroup);
@@ -461,10 +454,10 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
 struct FinalizeArgs {
   const int32_t *seq_lens;
   int max_seq_len, h_kv, h_q, n_c, G, R, D;
-  int S_max, Lpad, RS;
+  int S_max, Lpad;
   const float *o_parts;
   const float *lse_parts;
-  const __half *side_p;   // [units][Lpad][RS]
+  const __half *side_p;   // [units][R][Lpad]
   const float *side_m;    // [units][R][Lpad / kRefGroup]
   const int32_t *ucnt;    // block-sparse pass: splits per unit from the union size
   const uint8_t *phase;   // unified launch: units of draft-phase requests are skipped
@@ -477,7 +470,7 @@ struct FinalizeArgs {
   int64_t bstride;
 };
 constexpr int kFinThreads = 256;
-constexpr int kFinTok = kFinThreads;  // one token per thread
+constexpr int kFinTok = kFinThreads * 8;  // eight consecutive tokens per thread
 constexpr int kFinGroups = kFinTok / kRefGroup;
 
 // Launches the finalize pass: grid (n_tok + n_comb, units); implemented in ssd_verify.cu.
