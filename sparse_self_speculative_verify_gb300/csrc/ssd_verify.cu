@@ -249,7 +249,7 @@ static int launch_simt(const VerifyArgs &a, dim3 grid, cudaStream_t st) {
 
 struct VerifyLayout {
   int G, R, units, S_max, Lpad;
-  size_t o_off, lse_off, sp_off, sm_off, total;
+  size_t o_off, lse_off, sp_off, sm_off, ctr_off, total;
 };
 
 static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int S_max) {
@@ -269,6 +269,8 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   c.take<__half>((size_t)l.units * l.R * l.Lpad);
   l.sm_off = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
+  l.ctr_off = c.off;  // item counter of the tensor-core kernel
+  c.take<int>(1);
   l.total = c.off;
   return l;
 }
@@ -337,6 +339,7 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   a.side_p = crit ? reinterpret_cast<__half *>(ws + lay.sp_off) : nullptr;
   a.side_m = crit ? reinterpret_cast<float *>(ws + lay.sm_off) : nullptr;
   a.status = status;
+  a.sched = reinterpret_cast<int *>(ws + lay.ctr_off);
   dim3 grid(lay.S_max, lay.units);
   if (verify_tc_supported(kv, lay.R))
     rc = launch_verify_tc(kv, a, st);

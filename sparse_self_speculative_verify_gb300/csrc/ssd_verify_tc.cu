@@ -6,15 +6,20 @@
 // logits + LSE).  Same work items, partials and criticality side values as the mma.sync tile in
 // ssd_verify_tile.cuh; the finalize pass is shared.
 //
-// One persistent block per SM walks the work items (splits of 512 tokens of one (request, KV head))
-// assigned to it, tile by tile (128 tokens):
-//  * warp 8 streams K and V tiles with TMA (one box per page and 64-column panel, 128-byte swizzle,
-//    L2 evict-first) into a ring of 32 KB slots; the item's page ids are read once per item by the
-//    whole warp and each lane issues its own boxes.  It also writes the item's query rows.
+// One persistent block per SM works through work items (splits of 512 tokens of one (request, KV
+// head)), tile by tile (128 tokens).  Its first item is blockIdx.x; later ones come from a global
+// counter, so the items spread over the blocks by how fast each block actually runs.
+//  * warp 8 draws the items, hands their numbers to the other warps through a small shared ring, and
+//    streams K and V tiles with TMA (one box per page and 64-column panel, 128-byte swizzle, L2
+//    evict-first) into a ring of 32 KB slots; the next item's page ids are read one item ahead by
+//    the whole warp and each lane issues its own boxes.  Boxes that TMA cannot take whole (a
+//    request's partial last page, a skipped page) are written by the warp with plain copies and
+//    zeros.  The item's query rows arrive by one 4-D TMA box per 64-column panel.
 //  * warp 9 (one thread) issues the MMAs:  S^T[t][r] = K[t][:] . Q[r][:]    (M = 128 tokens, N = NP)
 //                                          O^T[d][n] += V[:][d] . P^T[:][n]  (M = 128 = d,   N = 2 NP)
 //    where n < NP carries the bf16 high part of the probabilities and n >= NP the bf16 residual, so
-//    P keeps about 16 bits.  S is double-buffered in TMEM; QK of tile i+1 is issued before PV of i.
+//    P keeps about 16 bits.  S is double-buffered in TMEM; PV of tile i is issued as soon as its
+//    probabilities are in shared memory, QK of tile i+1 as soon as its K tile has landed.
 //  * warps 0-3 and 4-7 are two softmax warpgroups: TMEM lane t is token t of the tile (for S) and
 //    head dimension d = t (for O); warpgroup w owns rows [w*NP/2, (w+1)*NP/2).  The two groups are
 //    independent (rows never mix), so each scheduler runs two softmax warps.
@@ -22,8 +27,8 @@
 //    2^(s - m_ref) <= 2^8; only when a logit exceeds m_ref + 8 does a group agree on a new reference
 //    (warp vote, then a transposed warp reduction) and rescale its running sums and its columns of
 //    the TMEM accumulator.  Padded rows carry m_ref = +inf, so full tiles need no masking.  The fp16
-//    side values for the criticality are these probabilities (token-major rows), with m_ref stored
-//    once per 16 tokens.
+//    side values for the criticality are these probabilities, stored row-major per (request, KV
+//    head) as [row][token], with m_ref stored once per 16 tokens.
 //  * All waits are bounded (about one second); on expiry the block raises SSD_FAULT_TIMEOUT in the
 //    status word, drains its own copies and MMAs, frees its tensor memory and exits.  Abort
 //    decisions are warp-uniform, and the softmax groups synchronise through mbarriers (bounded), not
@@ -41,7 +46,8 @@ constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcSoftmax = 256;  // two warpgroups
 constexpr int kTcProducerWarp = 8;
 constexpr int kTcMmaWarp = 9;
-constexpr int kTcMaxBatch = 2048;
+constexpr int kTcMaxBatch = 1024;
+constexpr int kTcItemRing = 8;  // item numbers handed from the producer to the other roles
 constexpr int kSlotBytes = kTcTile * 256;  // one K or V tile: 2 panels x 128 rows x 128 B
 constexpr int kPanelBytes = kTcTile * 128;
 constexpr float kLazy = 8.f;
@@ -58,18 +64,22 @@ struct TcCfg {
   static constexpr int OFF_P = NSLOT * kSlotBytes;
   static constexpr int OFF_Q = OFF_P + 2 * P_BYTES;
   static constexpr int OFF_MISC = OFF_Q + 2 * Q_BYTES;
-  // misc: 32 mbarriers, flags, per-row arrays, reduction scratch, the per-request item prefix
-  static constexpr int MISC = 32 * 8 + 64 + NP * 4 * 3 + 2 * 4 * 32 * 4 + (kTcMaxBatch + 1) * 4;
+  // misc: 48 mbarriers, flags and the item ring, per-row arrays, reduction scratch, the per-request
+  // item prefix and lengths
+  static constexpr int MISC = 48 * 8 + 128 + NP * 4 * 2 + 2 * 4 * 32 * 4 + (2 * kTcMaxBatch + 1) * 4;
   static constexpr int SMEM = OFF_MISC + MISC + 1024;
 };
 
 struct TcSmem {
   uint64_t *full, *empty, *s_full, *s_empty, *p_full, *p_empty, *o_full, *o_empty, *q_full, *q_empty, *drain, *grp;
+  uint64_t *item_full;  // [kTcItemRing]
   uint32_t *tmem;
   int *abort;
-  int *vote;  // [2 groups][4]
-  float *mref, *alpha, *lsum, *red;  // red: [2 groups][4 warps][32]
-  int *pre;
+  int *vote;   // [2 groups][4]
+  int *items;  // [kTcItemRing] item numbers in processing order; n_items ends the sequence
+  float *mref, *alpha, *red;  // red: [2 groups][4 warps][32]
+  int *pre;  // [B+1] item prefix per request
+  int *len;  // [B] clamped sequence lengths
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint64_t *b) { return smem_u32(b); }
@@ -79,7 +89,7 @@ struct TcItem {
 };
 
 // Item -> (request, head, split): items of request b are pre[b] .. pre[b+1]-1, ordered (head, split).
-__device__ __forceinline__ TcItem tc_decode(int item, const int *pre, int B, const VerifyArgs &a) {
+__device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int *len, int B, const VerifyArgs &a) {
   int lo = 0, hi = B;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -91,8 +101,7 @@ __device__ __forceinline__ TcItem tc_decode(int item, const int *pre, int B, con
   const int ns = (pre[lo + 1] - pre[lo]) / a.kv.h_kv;
   it.g = r / ns;
   it.split = r % ns;
-  int L = a.kv.seq_lens[lo];
-  it.L = L < 0 ? 0 : (L > a.kv.max_seq_len ? a.kv.max_seq_len : L);
+  it.L = len[lo];
   it.t0 = it.split * kSplitTokens;
   it.t1 = min(it.t0 + kSplitTokens, it.L);
   it.ntiles = cdiv(it.t1 - it.t0, kTcTile);
@@ -178,7 +187,8 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float *v) {
 
 template <int NP>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    verify_tc_kernel(const __grid_constant__ CUtensorMap kvmap, VerifyArgs a, int box_rows) {
+    verify_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap,
+                     VerifyArgs a, int box_rows) {
   using C = TcCfg<NP>;
   constexpr int CW = C::CW;
   extern __shared__ __align__(1024) char smem_raw[];
@@ -203,16 +213,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s.q_empty = bars + 22;
     s.drain = bars + 24;
     s.grp = bars + 25;  // [2]
-    m += 32 * 8;
+    s.item_full = bars + 32;
+    m += 48 * 8;
     s.tmem = reinterpret_cast<uint32_t *>(m);
     s.abort = reinterpret_cast<int *>(s.tmem + 1);
     s.vote = s.abort + 1;  // [8]
-    m += 64;
+    s.items = s.vote + 8;
+    m += 128;
     s.mref = reinterpret_cast<float *>(m);
     s.alpha = s.mref + NP;
-    s.lsum = s.alpha + NP;
-    s.red = s.lsum + NP;
+    s.red = s.alpha + NP;  // 16-byte aligned (float4 reads)
     s.pre = reinterpret_cast<int *>(s.red + 2 * 4 * 32);
+    s.len = s.pre + kTcMaxBatch + 1;
   }
 
   // Per-request item counts and their prefix (chunked block scan).
@@ -231,6 +243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           L = L < 0 ? 0 : (L > a.kv.max_seq_len ? a.kv.max_seq_len : L);
         }
         c = h_kv * verify_splits(L);
+        s.len[b] = L;
       }
       loc[k] = c;
       sum += c;
@@ -255,20 +268,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bar_addr(s.s_empty + k), kTcSoftmax);
         mbar_init(bar_addr(s.p_full + k), kTcSoftmax);
         mbar_init(bar_addr(s.p_empty + k), 1);
-        mbar_init(bar_addr(s.q_full + k), 32);
+        mbar_init(bar_addr(s.q_full + k), 1);
         mbar_init(bar_addr(s.q_empty + k), 1);
         mbar_init(bar_addr(s.grp + k), 128);
       }
       mbar_init(bar_addr(s.o_full), 1);
       mbar_init(bar_addr(s.o_empty), kTcSoftmax);
       mbar_init(bar_addr(s.drain), 1);
+      for (int k = 0; k < kTcItemRing; ++k) mbar_init(bar_addr(s.item_full + k), 1);
       mbar_init_fence();
     }
     if (warp == kTcMmaWarp) {
       tmem_alloc(smem_u32(s.tmem), C::TMEM_COLS);
       tmem_relinquish();
     }
-    if (warp == kTcProducerWarp && lane == 0) tma_prefetch_desc(&kvmap);
+    if (warp == kTcProducerWarp && lane == 0) {
+      tma_prefetch_desc(&kvmap);
+      tma_prefetch_desc(&qmap);
+    }
+    // Query buffers start zeroed: the TMA writes rows < R only, padded rows must read as zero.
+    for (int e = tid; e < 2 * C::Q_BYTES / 16; e += kTcThreads)
+      reinterpret_cast<uint4 *>(sm + C::OFF_Q)[e] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -295,34 +316,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t fill = 0;
     int jl = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++jl) {
-      const TcItem it = tc_decode(item, s.pre, B, a);
-      // Page ids of the item's boxes, read once by the whole warp: box j (tokens t0 + j*box_rows)
-      // lives in lane j % 32, register j / 32 (at most 512 / 8 = 64 boxes per item).
-      int32_t pid_reg[2];
+    // Page ids of an item's boxes, read by the whole warp one item ahead of use: box j (tokens
+    // t0 + j*box_rows) lives in lane j % 32, register j / 32 (at most 512 / 8 = 64 boxes per item).
+    auto load_pids = [&](int item_idx, int32_t(&dst)[2]) {
+      dst[0] = dst[1] = -1;
+      if (item_idx < n_items) {
+        const TcItem nx = tc_decode(item_idx, s.pre, s.len, B, a);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int t = it.t0 + (h * 32 + lane) * box_rows;
-        pid_reg[h] = t < it.t1 ? __ldg(a.kv.page_table + (int64_t)it.b * a.kv.max_pages + (t >> lps)) : -1;
+        for (int h = 0; h < 2; ++h) {
+          const int t = nx.t0 + (h * 32 + lane) * box_rows;
+          if (t < nx.t1) dst[h] = __ldg(a.kv.page_table + (int64_t)nx.b * a.kv.max_pages + (t >> lps));
+        }
       }
-      // Query rows of this item (rows >= R are zero), K-major 128-byte swizzled panels.
+    };
+    // Work distribution: the block's first item is blockIdx.x, every later one is drawn from a global
+    // counter (items gridDim.x, gridDim.x + 1, ...), so blocks that run ahead take more items. The
+    // draw for item j+2 is issued at the start of item j and read one item later, when item j+1's
+    // page ids are fetched, so the atomic's latency stays hidden. Lane 0 holds the raw draws.
+    int cur = blockIdx.x;
+    int nxt = n_items, raw = 0;
+    if (cur < n_items) {
+      if (lane == 0) raw = atomicAdd(a.sched, 1);
+      nxt = min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items);
+    }
+    int32_t pid_next[2];
+    load_pids(cur, pid_next);
+    for (;; ++jl) {
+      // Hand the item number to the MMA and softmax roles (n_items ends their loops). The slot
+      // written here last held item jl - kTcItemRing, which every role has read by now: this warp
+      // has passed the query-buffer wait of item jl - 1, so the MMA issuer is done with item jl - 3
+      // and the softmax warps (which read the S tile two tiles back) have begun item jl - 5 at least.
+      if (lane == 0) {
+        s.items[jl % kTcItemRing] = cur;
+        mbar_arrive(bar_addr(s.item_full + jl % kTcItemRing));
+      }
+      if (cur >= n_items || !ok) break;
+      const TcItem it = tc_decode(cur, s.pre, s.len, B, a);
+      int32_t pid_reg[2] = {pid_next[0], pid_next[1]};
+      load_pids(nxt, pid_next);
+      if (nxt < n_items && lane == 0) raw = atomicAdd(a.sched, 1);
+      // Query rows of this item: one 4-D TMA box per 64-column panel (d x 1 x G heads x n_c
+      // candidates lands as rows r = i*G + h, 128-byte swizzled); rows >= R stay zero.
       const bool qok = lane == 0 ? mbar_wait(bar_addr(s.q_empty + (jl & 1)), ((jl >> 1) & 1) ^ 1, s.abort) : true;
       if (!__shfl_sync(0xffffffffu, qok, 0)) { ok = false; break; }
-      {
-        char *qb = sm + C::OFF_Q + (jl & 1) * C::Q_BYTES;
-        const __nv_bfloat16 *q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-        for (int e = lane; e < NP * 16; e += 32) {
-          const int r = e >> 4, ch = e & 15, panel = ch >> 3, c = ch & 7;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (r < R) {
-            const int i = r / G, hl = r % G;
-            v = __ldg(reinterpret_cast<const uint4 *>(q + (((int64_t)it.b * n_c + i) * a.h_q + it.g * G + hl) * 128) + ch);
-          }
-          *reinterpret_cast<uint4 *>(qb + panel * C::Q_PANEL + r * 128 + ((c ^ (r & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(bar_addr(s.q_full + (jl & 1)));
+      if (lane == 0) {
+        const uint32_t qf = bar_addr(s.q_full + (jl & 1));
+        const uint32_t qb = sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES;
+        mbar_arrive_expect_tx(qf, 2u * R * 128u);
+        tma_load_4d(qb, &qmap, 0, 0, it.g * G, it.b * n_c, qf);
+        tma_load_4d(qb + C::Q_PANEL, &qmap, 0, 1, it.g * G, it.b * n_c, qf);
       }
+      __syncwarp();
       const int boxes_per_tile = kTcTile / box_rows;
       for (int k = 0; ok && k < it.ntiles; ++k) {
         const int tb = it.t0 + k * kTcTile, tend = min(tb + kTcTile, it.t1);
@@ -380,6 +424,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
         }
       }
+      const bool drew = nxt < n_items;
+      cur = nxt;
+      nxt = drew ? min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items) : n_items;
     }
     if (!ok && lane == 0) {
       // Drain: every fill issued so far must land before the block's shared memory is released.
@@ -421,15 +468,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (last) mma_commit(bar_addr(s.o_full));
         return true;
       };
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++jl) {
-        const TcItem it = tc_decode(item, s.pre, B, a);
-        if (!mbar_wait(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1, s.abort)) { ok = false; break; }
+      // The pending PV (previous tile) is issued as soon as its inputs are ready, even while the
+      // next QK still waits for its K tile (e.g. at an item boundary).
+      auto pv_ready = [&]() -> bool {
+        const uint32_t vf = 2 * pi + 1;
+        return mbar_try_wait(bar_addr(s.full + vf % C::NSLOT), (vf / C::NSLOT) & 1) &&
+               mbar_try_wait(bar_addr(s.p_full + (pi & 1)), (pi >> 1) & 1) &&
+               (!pfirst || mbar_try_wait(bar_addr(s.o_empty), (pj & 1) ^ 1));
+      };
+      auto wait_or_pv = [&](uint32_t bar, uint32_t parity) -> bool {
+        const long long t0 = clock64();
+        for (;;) {
+          if (pend && pv_ready()) {
+            issue_pv(pi, pfirst, plast, pj);
+            pend = false;
+          }
+          if (mbar_try_wait_sleep(bar, parity, pend ? 200u : 20000u)) return true;
+          if (*s.abort) return false;
+          if (clock64() - t0 > 2000000000ll) {
+            *s.abort = 1;
+            return false;
+          }
+        }
+      };
+      for (; ok; ++jl) {
+        if (!wait_or_pv(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1)) { ok = false; break; }
+        const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
+        if (item >= n_items) break;
+        const TcItem it = tc_decode(item, s.pre, s.len, B, a);
+        if (!wait_or_pv(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1)) { ok = false; break; }
         const uint32_t qa = sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES;
         for (int k = 0; k < it.ntiles; ++k, ++i) {
           const uint32_t kf = 2 * i;
           const int kslot = kf % C::NSLOT;
-          if (!mbar_wait(bar_addr(s.full + kslot), (kf / C::NSLOT) & 1, s.abort)) { ok = false; break; }
-          if (!mbar_wait(bar_addr(s.s_empty + (i & 1)), ((i >> 1) & 1) ^ 1, s.abort)) { ok = false; break; }
+          if (!wait_or_pv(bar_addr(s.full + kslot), (kf / C::NSLOT) & 1)) { ok = false; break; }
+          if (!wait_or_pv(bar_addr(s.s_empty + (i & 1)), ((i >> 1) & 1) ^ 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t ka = sbase + kslot * kSlotBytes;
 #pragma unroll
@@ -467,8 +540,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nref = a.Lpad / kRefGroup;
     uint32_t i = 0, gph = 0;
     int jl = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++jl) {
-      const TcItem it = tc_decode(item, s.pre, B, a);
+    for (;; ++jl) {
+      if (!wwait(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1, s.abort)) goto out;
+      const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
+      if (item >= n_items) break;
+      const TcItem it = tc_decode(item, s.pre, s.len, B, a);
       const int u = it.b * h_kv + it.g;
       const int lim_base = it.L - n_c;  // row r sees t <= lim_base + r / G
       if (tw < CW) s.mref[c0 + tw] = (c0 + tw < R) ? -INFINITY : INFINITY;
@@ -624,23 +700,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float ls = transpose_reduce<CW, false>(lsum);
         if (lane < CW) red[wiw * 32 + lane] = ls;
         if (!group_sync(grp, s.abort, gph)) goto out;
-        if (tw < CW) s.lsum[c0 + tw] = red[tw] + red[32 + tw] + red[64 + tw] + red[96 + tw];
-        if (!group_sync(grp, s.abort, gph)) goto out;
+        // Each thread sums the four warps' partial row sums itself: no second group barrier. The
+        // next write to red comes after the next item's opening group barrier.
         const int64_t prow = ((int64_t)u * a.S_max + it.split) * R;
-#pragma unroll
-        for (int j = 0; j < CW; ++j) {
-          const int r = c0 + j;
-          if (r < R) {
-            const float l = s.lsum[r];
-            a.o_parts[(prow + r) * 128 + tw] = l > 0.f ? o[j] / l : 0.f;
-          }
-        }
         if (tw < CW && c0 + tw < R) {
           const int r = c0 + tw;
-          const float l = s.lsum[r], m = s.mref[r];
-          a.lse_parts[prow + r] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+          float l = 0.f;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) l += red[w * 32 + tw];
+          a.lse_parts[prow + r] = l > 0.f ? (s.mref[r] + __log2f(l)) * kLn2 : -INFINITY;
         }
-        if (!group_sync(grp, s.abort, gph)) goto out;
+#pragma unroll
+        for (int j = 0; j < CW; j += 4) {
+          float4 l4 = *reinterpret_cast<const float4 *>(red + j);
+#pragma unroll
+          for (int w = 1; w < 4; ++w) {
+            const float4 p = *reinterpret_cast<const float4 *>(red + w * 32 + j);
+            l4.x += p.x; l4.y += p.y; l4.z += p.z; l4.w += p.w;
+          }
+          const float l[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (c0 + j + e < R) a.o_parts[(prow + c0 + j + e) * 128 + tw] = l[e] > 0.f ? o[j + e] * (1.f / l[e]) : 0.f;
+        }
       }
     }
   out:;
@@ -679,11 +761,12 @@ bool verify_tc_supported(const ssd_paged_kv *kv, int R) {
 }
 
 template <int NP>
-static int launch_tc(const CUtensorMap &map, const VerifyArgs &a, int box_rows, int grid, cudaStream_t st) {
+static int launch_tc(const CUtensorMap &map, const CUtensorMap &qmap, const VerifyArgs &a, int box_rows, int grid,
+                     cudaStream_t st) {
   constexpr int smem = TcCfg<NP>::SMEM;
   int rc = ensure_smem<verify_tc_kernel<NP>>(smem);
   if (rc) return rc;
-  verify_tc_kernel<NP><<<grid, kTcThreads, smem, st>>>(map, a, box_rows);
+  verify_tc_kernel<NP><<<grid, kTcThreads, smem, st>>>(map, qmap, a, box_rows);
   return check_launch("verify_tc_kernel");
 }
 
@@ -699,11 +782,24 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
   CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv->pool), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  if (r != CUDA_SUCCESS) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled (KV pool) failed (%d)", (int)r);
+  // Queries [B][n_c][h_q][128] as (64-column panel, panel, head, request*candidate); one box holds the
+  // G heads x n_c candidates of a (request, KV head) for one panel.
+  CUtensorMap qmap;
+  cuuint64_t qdims[4] = {64, 2, (cuuint64_t)a.h_q, (cuuint64_t)kv->batch * a.n_c};
+  cuuint64_t qstrides[3] = {128, 256, (cuuint64_t)a.h_q * 256};
+  cuuint32_t qbox[4] = {64, 1, (cuuint32_t)a.G, (cuuint32_t)a.n_c};
+  cuuint32_t qes[4] = {1, 1, 1, 1};
+  r = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(a.q), qdims, qstrides, qbox, qes,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled (queries) failed (%d)", (int)r);
   const int64_t items_max = (int64_t)kv->batch * kv->h_kv * a.S_max;
   const int grid = (int)(items_max < sm_count() ? items_max : sm_count());
   if (grid <= 0) return SSD_OK;
-  return a.R <= 32 ? launch_tc<32>(map, a, box_rows, grid, st) : launch_tc<64>(map, a, box_rows, grid, st);
+  if (!a.sched) return fail(SSD_ERR_INVALID_ARG, "verify_tc_kernel: no item counter");
+  if (cudaMemsetAsync(a.sched, 0, sizeof(int), st) != cudaSuccess) return check_launch("verify_tc_kernel (counter reset)");
+  return a.R <= 32 ? launch_tc<32>(map, qmap, a, box_rows, grid, st) : launch_tc<64>(map, qmap, a, box_rows, grid, st);
 }
 
 }  // namespace ssd

@@ -39,6 +39,7 @@ struct VerifyArgs {
   const int32_t *ucnt;
   int umax;
   unsigned *status;
+  int *sched;  // item counter for dynamic scheduling (tensor-core path), zero at launch
 };
 
 template <int D, int NRT>
