@@ -17,9 +17,11 @@
  *    pointers are only the ssd_paged_kv struct itself and scalar outputs of ssd_status.
  *  - The caller owns all memory.  The library allocates nothing, keeps no pointer after a call
  *    returns, and takes scratch space only from the caller's workspace, sized by the matching
- *    ssd_*_workspace_bytes() query.  A workspace must be zero-filled once after allocation (the
- *    library leaves its counters at zero after every call) and must not be shared by calls that
- *    may run concurrently.
+ *    ssd_*_workspace_bytes() query.  A workspace must be zero-filled once after allocation.  Its
+ *    first 256 KiB hold only the library's counters, which every call returns to zero, so one
+ *    workspace may then serve calls of any entry point and shape one after another (zero it again
+ *    after a call that raised SSD_FAULT_TIMEOUT).  It must not be shared by calls that may run
+ *    concurrently.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *    Argument errors are detected on the host and returned before anything is launched; launch
  *    failures return SSD_ERR_CUDA.  Data-dependent faults found on the device (a page id outside

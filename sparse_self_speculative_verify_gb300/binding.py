@@ -178,7 +178,8 @@ class KVCache:
 
 class Workspace:
     """Zero-initialised device scratch buffers, grown on demand, one per (device, name).  The
-    library returns its counters to zero after each call, so a buffer is zeroed only once."""
+    library keeps its counters in a fixed area at the start of a workspace and returns them to zero
+    after each call, so a buffer is zeroed only once and serves calls of any shape in turn."""
 
     def __init__(self):
         self._bufs = {}

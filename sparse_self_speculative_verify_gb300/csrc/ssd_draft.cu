@@ -37,20 +37,20 @@ int launch_draft_any(int dtype, int D, const DraftArgs &a, dim3 grid, cudaStream
   return D == 128 ? dispatch_g<128, float>(gmax, a, grid, st) : dispatch_g<64, float>(gmax, a, grid, st);
 }
 
-// Workspace of the draft partials: o [units][C_max][GMAX][D], lse [units][C_max][GMAX], counters [units].
-size_t draft_ws_bytes(int units, int C_max, int gmax, int D) {
+// Draft partials: o [units][C_max][GMAX][D], lse [units][C_max][GMAX].  The per-unit arrival
+// counters live in the workspace's counter area (slot = unit).
+size_t draft_data_bytes(int units, int C_max, int gmax, int D) {
   Carver c(nullptr);
   c.take<float>((size_t)units * C_max * gmax * D);
   c.take<float>((size_t)units * C_max * gmax);
-  c.take<unsigned>((size_t)units);
   return c.off;
 }
 
-void draft_ws_carve(void *ws, int units, int C_max, int gmax, int D, DraftArgs &a) {
-  Carver c(ws);
+void draft_carve(unsigned *counters, void *data, int units, int C_max, int gmax, int D, DraftArgs &a) {
+  Carver c(data);
   a.o_parts = c.take<float>((size_t)units * C_max * gmax * D);
   a.lse_parts = c.take<float>((size_t)units * C_max * gmax);
-  a.counters = c.take<unsigned>((size_t)units);
+  a.counters = counters;
 }
 
 int draft_checks(const ssd_paged_kv *kv, int h_q, const void *q, const int32_t *idx, int k_max, const int32_t *cnt,
@@ -69,8 +69,8 @@ using namespace ssd;
 
 extern "C" size_t ssd_draft_workspace_bytes(const ssd_paged_kv *kv, int h_q, int k_max) {
   if (!kv || kv->h_kv <= 0 || h_q <= 0 || k_max < 0 || kv->batch < 0 || (kv->d != 64 && kv->d != 128)) return 0;
-  return draft_ws_bytes(kv->batch * kv->h_kv, cdiv(k_max > 0 ? k_max : 1, kDraftChunk), draft_gmax(h_q / kv->h_kv),
-                        kv->d);
+  return kCounterBytes + draft_data_bytes(kv->batch * kv->h_kv, cdiv(k_max > 0 ? k_max : 1, kDraftChunk),
+                                          draft_gmax(h_q / kv->h_kv), kv->d);
 }
 
 extern "C" int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
@@ -104,6 +104,7 @@ extern "C" int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, co
   a.out = out;
   a.lse = lse;
   a.status = status;
-  draft_ws_carve(workspace, units, C_max, draft_gmax(a.G), kv->d, a);
+  draft_carve(static_cast<unsigned *>(workspace), static_cast<char *>(workspace) + kCounterBytes, units, C_max,
+              draft_gmax(a.G), kv->d, a);
   return launch_draft_any(kv->dtype, kv->d, a, dim3(C_max, units), reinterpret_cast<cudaStream_t>(stream));
 }

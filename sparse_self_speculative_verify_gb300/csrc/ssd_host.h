@@ -43,6 +43,14 @@ int ensure_smem(int bytes) {
   return SSD_OK;
 }
 
+// Every workspace begins with a counter area: kCounterSlots 32-bit counters for arrival counting
+// and work distribution, at offsets that depend on nothing but the counter's index.  Nothing else is
+// stored there and every kernel returns the counters it used to zero when it completes, so a
+// workspace zero-filled once stays valid for any later sequence of calls, of any entry point and
+// shape.  (Data regions move with the shape; counters placed among them would not stay zero.)
+constexpr int kCounterSlots = 65536;
+constexpr size_t kCounterBytes = size_t(kCounterSlots) * 4;
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

@@ -18,8 +18,8 @@
 namespace ssd {
 
 int draft_gmax(int G);
-size_t draft_ws_bytes(int units, int C_max, int gmax, int D);
-void draft_ws_carve(void *ws, int units, int C_max, int gmax, int D, DraftArgs &a);
+size_t draft_data_bytes(int units, int C_max, int gmax, int D);
+void draft_carve(unsigned *counters, void *data, int units, int C_max, int gmax, int D, DraftArgs &a);
 int draft_checks(const ssd_paged_kv *kv, int h_q, const void *q, const int32_t *idx, int k_max, const int32_t *cnt,
                  const float *out, const char *who);
 
@@ -115,6 +115,7 @@ static UniLayout uni_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int k_m
   l.C_max = cdiv(k_max > 0 ? k_max : 1, kDraftChunk);
   l.gmax = draft_gmax(l.G);
   Carver c(nullptr);
+  c.take<unsigned>(kCounterSlots);  // counter area (draft arrival counters)
   size_t rows = (size_t)l.units * l.S_max * l.R;
   l.v_o = c.off;
   c.take<float>(rows * kv->d);
@@ -125,7 +126,7 @@ static UniLayout uni_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int k_m
   l.v_sm = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
   l.d_off = c.off;
-  l.total = l.d_off + draft_ws_bytes(l.units, l.C_max, l.gmax, kv->d);
+  l.total = l.d_off + draft_data_bytes(l.units, l.C_max, l.gmax, kv->d);
   return l;
 }
 
@@ -224,7 +225,7 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
   da.lse = lse_draft;
   da.phase = phase;
   da.status = status;
-  draft_ws_carve(ws + lay.d_off, lay.units, lay.C_max, lay.gmax, kv->d, da);
+  draft_carve(reinterpret_cast<unsigned *>(ws), ws + lay.d_off, lay.units, lay.C_max, lay.gmax, kv->d, da);
   const int nrt = lay.R <= 16 ? 1 : (lay.R <= 32 ? 2 : 4);
   rc = kv->d == 128 ? uni_rows<128>(nrt, lay.gmax, va, da, phase, st) : uni_rows<64>(nrt, lay.gmax, va, da, phase, st);
   if (rc) return rc;

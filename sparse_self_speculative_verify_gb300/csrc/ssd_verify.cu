@@ -260,6 +260,8 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   l.S_max = S_max;
   l.Lpad = cdiv(kv->max_seq_len > 0 ? kv->max_seq_len : 1, kSideAlign) * kSideAlign;
   Carver c(nullptr);
+  l.ctr_off = c.off;  // counter area (item counter of the tensor-core kernel)
+  c.take<unsigned>(kCounterSlots);
   size_t rows = (size_t)l.units * l.S_max * l.R;
   l.o_off = c.off;
   c.take<float>(rows * kv->d);
@@ -269,8 +271,6 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   c.take<__half>((size_t)l.units * l.R * l.Lpad);
   l.sm_off = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
-  l.ctr_off = c.off;  // item counter of the tensor-core kernel
-  c.take<int>(1);
   l.total = c.off;
   return l;
 }

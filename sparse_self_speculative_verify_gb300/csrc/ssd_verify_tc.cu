@@ -428,6 +428,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       cur = nxt;
       nxt = drew ? min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items) : n_items;
     }
+    // Every draw this warp issued has returned (also after an abort) before the block counts itself
+    // finished below, so the counter reset cannot overtake a draw.
+    const int last_draw = __shfl_sync(0xffffffffu, raw, 0);
+    asm volatile("" ::"r"(last_draw));
     if (!ok && lane == 0) {
       // Drain: every fill issued so far must land before the block's shared memory is released.
       for (uint32_t f = fill > (uint32_t)C::NSLOT ? fill - C::NSLOT : 0; f < fill; ++f) {
@@ -732,6 +736,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   if (tid == 0 && *reinterpret_cast<volatile int *>(s.abort)) atomicOr(a.status, (unsigned)SSD_FAULT_TIMEOUT);
   if (warp == kTcMmaWarp) tmem_dealloc(tm, C::TMEM_COLS);
+  // The last block to finish returns the item counter and the finished count to zero for the next
+  // call (the counter area's contract).  Every block's draws completed before its count.
+  if (tid == 0 && atomicAdd(a.sched + 1, 1) == (int)gridDim.x - 1) {
+    __threadfence();
+    atomicExch(a.sched, 0);
+    atomicExch(a.sched + 1, 0);
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -798,7 +809,6 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
   const int grid = (int)(items_max < sm_count() ? items_max : sm_count());
   if (grid <= 0) return SSD_OK;
   if (!a.sched) return fail(SSD_ERR_INVALID_ARG, "verify_tc_kernel: no item counter");
-  if (cudaMemsetAsync(a.sched, 0, sizeof(int), st) != cudaSuccess) return check_launch("verify_tc_kernel (counter reset)");
   return a.R <= 32 ? launch_tc<32>(map, qmap, a, box_rows, grid, st) : launch_tc<64>(map, qmap, a, box_rows, grid, st);
 }
 

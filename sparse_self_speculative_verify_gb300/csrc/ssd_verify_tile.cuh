@@ -39,7 +39,8 @@ struct VerifyArgs {
   const int32_t *ucnt;
   int umax;
   unsigned *status;
-  int *sched;  // item counter for dynamic scheduling (tensor-core path), zero at launch
+  int *sched;  // [2] in the counter area: next-item counter and finished-block count (tensor-core
+               // path); zero at launch, and the last block to finish returns both to zero
 };
 
 template <int D, int NRT>

@@ -62,6 +62,23 @@ def test_draft_repeat_calls_identical():
     assert torch.equal(a, b)
 
 
+def test_draft_workspace_reused_across_shapes():
+    """One workspace serves calls of different shapes in turn: the counters of the second call sit
+    where the first call left partial outputs, and each call clears them before its kernel."""
+    from sparse_self_speculative_verify_gb300 import Workspace
+    ws = Workspace()
+    specs = [(W.scaled_spec(W.SPECS["qwen3_8b"], name="wsa", batch=3), [8192, 6000, 300], [410, 300, 20], 410),
+             (W.scaled_spec(W.SPECS["qwen3_8b"], name="wsb", batch=2, h_q=40), [3000, 5000], [150, 250], 250)]
+    for n, (spec, lens, ks, k_max) in enumerate(specs + specs[:1]):
+        w = W.make_workload(spec, seed=40 + n % 2, device=DEV, lengths=lens)
+        idx, cnt = W.random_index_sets(w.seq_lens, spec.h_kv, torch.tensor(ks, dtype=torch.int32), k_max, seed=n % 2)
+        r = ssd_draft_attn(KVCache.from_workload(w), w.q_draft[0], idx.to(DEV), cnt.to(DEV), _gpu.scale_of(spec),
+                           workspace=ws)
+        torch.cuda.synchronize()
+        assert ssd_status() == 0
+        _check(w, r, idx, cnt)
+
+
 def test_draft_select_all_equals_verify_single_candidate():
     """With every index selected, the draft is dense single-query attention: it matches the GPU
     verify with n_cand = 1 on the same query (and the oracle)."""
