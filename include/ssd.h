@@ -161,6 +161,31 @@ int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t
                    size_t workspace_bytes, ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * ssd_draft_attn_static: ssd_draft_attn without a workspace.  The paper has no counterpart; this
+ * is a library convenience.  It exists for callers that cannot allocate device memory where they
+ * run the draft step: a plugin inside another runtime that owns all device allocations and passes
+ * in only input and output buffers, or a serving loop that must not call cudaMalloc / cudaFree
+ * (which can synchronise the whole device) while other streams are running.
+ *
+ * Same arguments, results and device-side fault reporting as ssd_draft_attn, minus workspace and
+ * workspace_bytes.  The scratch is one built-in device array of SSD_DRAFT_STATIC_SCRATCH_BYTES
+ * (16 MiB), held on every device that loads the library until the process exits.  The call
+ * allocates and frees nothing.
+ *  - A batch whose scratch does not fit returns SSD_ERR_WORKSPACE before anything is launched;
+ *    use ssd_draft_attn for it.  The scratch is 4 bytes per (request, KV head) rounded up to 256,
+ *    plus ssd_draft_workspace_bytes for the same arguments minus its 256 KiB counter area.
+ *  - The first call on each device looks up the array's device address (with that device current)
+ *    and keeps it; make that first call before any stream capture on the device.
+ *  - Every call on a device uses the same array, which keeps the previous call's contents; the
+ *    parts that must start at zero are cleared on `stream` before the kernel runs.  Calls whose
+ *    work can overlap on the GPU (different streams with no ordering between them) race on the
+ *    array and give wrong results: order them on one stream or with events.
+ */
+#define SSD_DRAFT_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+int ssd_draft_attn_static(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
+                          const int32_t *cnt, float scale, float *out, float *lse, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Unified launch (SparseSpec §4.2: requests of both phases in one batch; a persistent fused kernel
  * dispatches verify and draft work to their own tile code in one launch).  phase (device uint8
  * [batch]): 1 = verify, 0 = draft.  Verify-phase requests take q_verify/out_verify/lse_verify/

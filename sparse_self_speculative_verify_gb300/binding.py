@@ -25,7 +25,8 @@ SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
 FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT = 1, 2, 4, 8, 16, 32
 
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
-            "ssd_select_topk", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_unified_workspace_bytes",
+            "ssd_select_topk", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
+            "ssd_unified_workspace_bytes",
             "ssd_unified_attn", "ssd_block_union", "ssd_block_sparse_workspace_bytes", "ssd_block_sparse_attn",
             "ssd_combine"]
 
@@ -76,6 +77,7 @@ def load(path: Optional[str] = None):
             "ssd_select_topk": ([P, I64, P, P, I, I, I, I, P, I, P, P], I),
             "ssd_draft_workspace_bytes": ([KV, I, I], S),
             "ssd_draft_attn": ([KV, P, I, P, I, P, F, P, P, P, S, P], I),
+            "ssd_draft_attn_static": ([KV, P, I, P, I, P, F, P, P, P], I),
             "ssd_unified_workspace_bytes": ([KV, I, I, I], S),
             "ssd_unified_attn": ([KV, P, P, P, I, I, P, I, P, F, P, P, P, I64, P, P, P, S, P], I),
             "ssd_block_union": ([P, P, I, I, I, I, P, P, P, I, P], I),
@@ -293,6 +295,27 @@ def ssd_draft_attn(kv: KVCache, q: torch.Tensor, idx: torch.Tensor, cnt: torch.T
     wsp, avail = _ws(dev, "draft", need, workspace)
     _check(L.ssd_draft_attn(kv.ref(), _ptr(q), h_q, _ptr(idx), k_max, _ptr(cnt), float(scale), _ptr(out), _ptr(lse),
                             wsp, avail, _stream(stream)))
+    return {"out": out, "lse": lse}
+
+
+def ssd_draft_attn_static(kv: KVCache, q: torch.Tensor, idx: torch.Tensor, cnt: torch.Tensor, scale: float, *,
+                          out=None, lse=None, want_lse: bool = True, stream=None) -> dict:
+    """ssd_draft_attn without a workspace: the scratch is the library's built-in device array
+    (SSD_DRAFT_STATIC_SCRATCH_BYTES), so nothing is allocated for it.  For callers that cannot
+    allocate device memory where they run the draft step.  Calls that can overlap on the GPU share
+    that array and race; the first call on a device must come before any stream capture there."""
+    _need(q, "q", kv.pool.dtype, kv.device)
+    dev = kv.device
+    _need(idx, "idx", torch.int32, dev)
+    _need(cnt, "cnt", torch.int32, dev)
+    B, h_q, d = q.shape
+    k_max = idx.shape[-1]
+    if out is None:
+        out = torch.empty((B, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h_q), dtype=torch.float32, device=dev)
+    _check(_lib().ssd_draft_attn_static(kv.ref(), _ptr(q), h_q, _ptr(idx), k_max, _ptr(cnt), float(scale), _ptr(out),
+                                        _ptr(lse), _stream(stream)))
     return {"out": out, "lse": lse}
 
 
