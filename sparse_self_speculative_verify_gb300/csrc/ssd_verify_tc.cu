@@ -192,7 +192,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using C = TcCfg<NP>;
   constexpr int CW = C::CW;
   extern __shared__ __align__(1024) char smem_raw[];
-  char *sm = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Rounded up to 1024 bytes by pointer arithmetic on the shared array, so every derived pointer is
+  // still known to address shared memory (plain shared loads and stores, not generic ones).
+  char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.kv.batch, h_kv = a.kv.h_kv;
@@ -259,6 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
       *s.abort = 0;
       for (int k = 0; k < 8; ++k) s.vote[k] = 0;
+      for (int r = 0; r < NP; ++r) s.mref[r] = r < a.R ? -INFINITY : INFINITY;  // first item's references
       for (int k = 0; k < C::NSLOT; ++k) {
         mbar_init(bar_addr(s.full + k), 1);
         mbar_init(bar_addr(s.empty + k), 1);
@@ -399,16 +402,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int32_t pj = __shfl_sync(0xffffffffu, pid, j);
             const int bt = tb + j * box_rows;
             const __nv_bfloat16 *pool = reinterpret_cast<const __nv_bfloat16 *>(a.kv.pool);
-            for (int e = lane; e < box_rows * 16; e += 32) {
-              const int rr = e >> 4, ch = e & 15, panel = ch >> 3, c = ch & 7;
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (rr < nv && okp) {
-                const int64_t row = (((int64_t)pj * 2 + kv) * h_kv + it.g) * ps + ((bt + rr) & (ps - 1));
-                v = __ldg(reinterpret_cast<const uint4 *>(pool + row * 128) + ch);
+            // 16-byte chunks e = row * 16 + chunk; each lane loads eight before it stores any, so
+            // one memory latency covers 256 chunks (16 rows).
+            const int nchunk = box_rows * 16;
+            for (int e0 = 0; e0 < nchunk; e0 += 256) {
+              uint4 v[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int e = e0 + u * 32 + lane, rr = e >> 4;
+                v[u] = make_uint4(0, 0, 0, 0);
+                if (e < nchunk && rr < nv && okp) {
+                  const int64_t row = (((int64_t)pj * 2 + kv) * h_kv + it.g) * ps + ((bt + rr) & (ps - 1));
+                  v[u] = __ldg(reinterpret_cast<const uint4 *>(pool + row * 128) + (e & 15));
+                }
               }
-              const int trow = bt - tb + rr;
-              *reinterpret_cast<uint4 *>(sm + slot * kSlotBytes + panel * kPanelBytes + trow * 128 +
-                                         ((c ^ (trow & 7)) << 4)) = v;
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int e = e0 + u * 32 + lane;
+                if (e < nchunk) {
+                  const int rr = e >> 4, ch = e & 15, panel = ch >> 3, c = ch & 7, trow = bt - tb + rr;
+                  *reinterpret_cast<uint4 *>(sm + slot * kSlotBytes + panel * kPanelBytes + trow * 128 +
+                                             ((c ^ (trow & 7)) << 4)) = v[u];
+                }
+              }
             }
           }
           fence_proxy_async_smem();
@@ -474,11 +490,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       // The pending PV (previous tile) is issued as soon as its inputs are ready, even while the
       // next QK still waits for its K tile (e.g. at an item boundary).
+      // While a PV is pending both conditions are polled without suspending the thread (a
+      // suspended wait may wake late); otherwise the thread sleeps in the barrier.
       auto pv_ready = [&]() -> bool {
         const uint32_t vf = 2 * pi + 1;
-        return mbar_try_wait(bar_addr(s.full + vf % C::NSLOT), (vf / C::NSLOT) & 1) &&
-               mbar_try_wait(bar_addr(s.p_full + (pi & 1)), (pi >> 1) & 1) &&
-               (!pfirst || mbar_try_wait(bar_addr(s.o_empty), (pj & 1) ^ 1));
+        return mbar_test_wait(bar_addr(s.full + vf % C::NSLOT), (vf / C::NSLOT) & 1) &&
+               mbar_test_wait(bar_addr(s.p_full + (pi & 1)), (pi >> 1) & 1) &&
+               (!pfirst || mbar_test_wait(bar_addr(s.o_empty), (pj & 1) ^ 1));
       };
       auto wait_or_pv = [&](uint32_t bar, uint32_t parity) -> bool {
         const long long t0 = clock64();
@@ -487,7 +505,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             issue_pv(pi, pfirst, plast, pj);
             pend = false;
           }
-          if (mbar_try_wait_sleep(bar, parity, pend ? 200u : 20000u)) return true;
+          if (pend ? mbar_test_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u)) return true;
           if (*s.abort) return false;
           if (clock64() - t0 > 2000000000ll) {
             *s.abort = 1;
@@ -544,18 +562,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nref = a.Lpad / kRefGroup;
     uint32_t i = 0, gph = 0;
     int jl = 0;
+    // The item sequence comes from the producer's ring.  Each item's per-row references start at
+    // -inf (padded rows +inf): in shared memory, the thread that owns a row resets it at the end of
+    // the previous item (the same thread reads it first in the next item's reference update, and
+    // every other reader comes after a group barrier); the first tile takes the start values from
+    // registers.  So no group barrier is needed between items.
+    int item = n_items;
+    TcItem it{};
+    if (!wwait(bar_addr(s.item_full), 0, s.abort)) goto out;
+    item = *reinterpret_cast<volatile int *>(s.items);
+    if (item < n_items) it = tc_decode(item, s.pre, s.len, B, a);
     for (;; ++jl) {
-      if (!wwait(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1, s.abort)) goto out;
-      const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
       if (item >= n_items) break;
-      const TcItem it = tc_decode(item, s.pre, s.len, B, a);
       const int u = it.b * h_kv + it.g;
       const int lim_base = it.L - n_c;  // row r sees t <= lim_base + r / G
-      if (tw < CW) s.mref[c0 + tw] = (c0 + tw < R) ? -INFINITY : INFINITY;
       float lsum[CW];
 #pragma unroll
       for (int j = 0; j < CW; ++j) lsum[j] = 0.f;
-      if (!group_sync(grp, s.abort, gph)) goto out;
       for (int k = 0; k < it.ntiles; ++k, ++i) {
         const int tb = it.t0 + k * kTcTile, t = tb + tw;
         if (!wwait(bar_addr(s.s_full + (i & 1)), (i >> 1) & 1, s.abort)) goto out;
@@ -571,8 +594,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool causal = tb + kTcTile - 1 > lim_base;
         const bool masked = causal || !__all_sync(0xffffffffu, valid);
         float mr[CW];
+        if (k == 0) {
 #pragma unroll
-        for (int j = 0; j < CW; j += 4) *reinterpret_cast<float4 *>(mr + j) = *reinterpret_cast<const float4 *>(s.mref + c0 + j);
+          for (int j = 0; j < CW; ++j) mr[j] = c0 + j < R ? -INFINITY : INFINITY;
+        } else {
+#pragma unroll
+          for (int j = 0; j < CW; j += 4) *reinterpret_cast<float4 *>(mr + j) = *reinterpret_cast<const float4 *>(s.mref + c0 + j);
+        }
         // d = scale * s - m_ref (log2 domain); -inf where the row cannot see the token.
         float dl[CW];
         if (masked) {
@@ -686,6 +714,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar_addr(s.p_full + (i & 1)));
       }
+      // The next item (published by the producer once this item's tiles were issued), decoded while
+      // the last PV of this item completes.
+      const uint32_t nj = (uint32_t)jl + 1;
+      if (!wwait(bar_addr(s.item_full + nj % kTcItemRing), (nj / kTcItemRing) & 1, s.abort)) goto out;
+      const int next_item = *reinterpret_cast<volatile int *>(s.items + nj % kTcItemRing);
+      TcItem nx{};
+      if (next_item < n_items) nx = tc_decode(next_item, s.pre, s.len, B, a);
       // Epilogue: O (high + residual columns) and the row sums -> the split's normalised partial.
       {
         if (!wwait(bar_addr(s.o_full), jl & 1, s.abort)) goto out;
@@ -704,16 +739,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float ls = transpose_reduce<CW, false>(lsum);
         if (lane < CW) red[wiw * 32 + lane] = ls;
         if (!group_sync(grp, s.abort, gph)) goto out;
-        // Each thread sums the four warps' partial row sums itself: no second group barrier. The
-        // next write to red comes after the next item's opening group barrier.
-        const int64_t prow = ((int64_t)u * a.S_max + it.split) * R;
-        if (tw < CW && c0 + tw < R) {
-          const int r = c0 + tw;
-          float l = 0.f;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) l += red[w * 32 + tw];
-          a.lse_parts[prow + r] = l > 0.f ? (s.mref[r] + __log2f(l)) * kLn2 : -INFINITY;
-        }
+        // Each thread sums the four warps' partial row sums itself (all shared reads before the global
+        // stores): no second group barrier.  The next write to red comes after the next item's first
+        // vote barrier.
+        float inv[CW];
 #pragma unroll
         for (int j = 0; j < CW; j += 4) {
           float4 l4 = *reinterpret_cast<const float4 *>(red + j);
@@ -722,12 +751,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float4 p = *reinterpret_cast<const float4 *>(red + w * 32 + j);
             l4.x += p.x; l4.y += p.y; l4.z += p.z; l4.w += p.w;
           }
-          const float l[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (c0 + j + e < R) a.o_parts[(prow + c0 + j + e) * 128 + tw] = l[e] > 0.f ? o[j + e] * (1.f / l[e]) : 0.f;
+          inv[j] = l4.x; inv[j + 1] = l4.y; inv[j + 2] = l4.z; inv[j + 3] = l4.w;
         }
+        const int64_t prow = ((int64_t)u * a.S_max + it.split) * R;
+        if (tw < CW) {
+          const int r = c0 + tw;
+          if (r < R) {
+            float l = 0.f;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) l += red[w * 32 + tw];
+            a.lse_parts[prow + r] = l > 0.f ? (s.mref[r] + __log2f(l)) * kLn2 : -INFINITY;
+          }
+          s.mref[r] = r < R ? -INFINITY : INFINITY;  // the next item's starting reference
+        }
+#pragma unroll
+        for (int j = 0; j < CW; ++j) inv[j] = inv[j] > 0.f ? __fdividef(1.f, inv[j]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < CW; ++j)
+          if (c0 + j < R) a.o_parts[(prow + c0 + j) * 128 + tw] = o[j] * inv[j];
       }
+      item = next_item;
+      it = nx;
     }
   out:;
   }
