@@ -160,9 +160,15 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+# Sources of the dominant call (ssd_verify_attn: tensor-core verify kernel + finalize); a change to
+# any of them makes the committed DRAM-traffic capture stale.
+VERIFY_SOURCES = ("ssd_common.cuh", "ssd_host.h", "ssd_sm100.cuh", "ssd_verify.cu", "ssd_verify_tc.cu",
+                  "ssd_verify_tile.cuh")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "sparse_self_speculative_verify_gb300", "csrc", "*"))):
+    for p in sorted(os.path.join(ROOT, "sparse_self_speculative_verify_gb300", "csrc", n) for n in VERIFY_SOURCES):
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())

@@ -37,7 +37,7 @@ struct DraftCfg {
   static constexpr int ROWB = D * (int)sizeof(T);  // bytes of one K or V row
   static constexpr int CPR = ROWB / 16;
   static constexpr int TILE = kDraftChunk * ROWB;
-  static constexpr int SMEM = 2 * TILE + (GMAX * D + GMAX * kDraftChunk + 2 * GMAX) * 4;
+  static constexpr int SMEM = 2 * TILE + (GMAX * D + GMAX * kDraftChunk + 2 * GMAX) * 4 + kDraftChunk * 8;
 };
 
 __device__ __forceinline__ int draft_chunks(int n) { return n <= 0 ? 1 : cdiv(n, kDraftChunk); }
@@ -62,6 +62,12 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h_kv = a.kv.h_kv;
   const int b = unit / h_kv, g = unit % h_kv, G = a.G;
+  // The list length, the request length and this chunk's token indices are loaded together (none
+  // depends on another), so a block waits for one memory latency before it can resolve its rows.
+  const int j0 = chunk * kDraftChunk;
+  const int32_t *tok = a.idx + (int64_t)unit * a.k_max + j0;
+  int t_mine = -1;
+  if (tid < kDraftChunk && j0 + tid < a.k_max) t_mine = __ldg(tok + tid);
   const int L = effective_len(a.kv, b, 0, a.status);
   int n_all = a.cnt[unit];
   if (n_all < 0 || n_all > a.k_max) {
@@ -70,7 +76,6 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   }
   const int n_chunks = draft_chunks(n_all);
   if (chunk >= n_chunks) return;
-  const int j0 = chunk * kDraftChunk;
   const int n = min(kDraftChunk, n_all - j0);  // may be 0 for an empty list
 
   char *sKt = smem;
@@ -79,18 +84,32 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   float *sS = sQ + GMAX * D;                                   // [GMAX][kDraftChunk]
   float *sM = sS + GMAX * kDraftChunk;                         // [GMAX]
   float *sL = sM + GMAX;                                       // [GMAX]
+  int64_t *sRow = reinterpret_cast<int64_t *>(sL + GMAX);       // [kDraftChunk] K row element offset, -1: none
 
-  // Gather the chunk's K and V rows.
-  const int32_t *tok = a.idx + (int64_t)unit * a.k_max + j0;
+  // Each token's K row, resolved once by its own thread (index check, page-table lookup).
+  if (tid < kDraftChunk) {
+    int64_t row = -1;
+    if (tid < n) {
+      if (t_mine >= 0 && t_mine < L) {
+        const int32_t p = __ldg(a.kv.page_table + (int64_t)b * a.kv.max_pages + (t_mine >> a.kv.log2_ps));
+        if (p >= 0 && (int64_t)p < a.kv.num_pages)
+          row = ((((int64_t)p * 2) * h_kv + g) * a.kv.page_size + (t_mine & (a.kv.page_size - 1))) * D;
+        else
+          atomicOr(a.status, (unsigned)SSD_FAULT_PAGE);
+      } else {
+        atomicOr(a.status, (unsigned)SSD_FAULT_INDEX);
+      }
+    }
+    sRow[tid] = row;
+  }
+  __syncthreads();
+
+  // Gather the chunk's K and V rows (rows of skipped tokens are zero-filled).
   const int64_t v_off = (int64_t)h_kv * a.kv.page_size * D;
   for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
     int j = c / C::CPR, ch = c % C::CPR;
-    const T *kr = nullptr;
-    if (j < n) {
-      int t = __ldg(tok + j);
-      if (t >= 0 && t < L) kr = kv_row<D, T>(a.kv, b, 0, g, t, a.status);
-      else if (ch == 0) atomicOr(a.status, (unsigned)SSD_FAULT_INDEX);
-    }
+    const int64_t row = sRow[j];
+    const T *kr = row >= 0 ? reinterpret_cast<const T *>(a.kv.pool) + row : nullptr;
     uint32_t off = j * C::ROWB + swz_chunk(j, ch) * 16;
     cp_async16(smem_u32(sKt + off), kr ? (const void *)(kr + ch * EPC) : a.kv.pool, kr ? 16 : 0);
     cp_async16(smem_u32(sVt + off), kr ? (const void *)(kr + v_off + ch * EPC) : a.kv.pool, kr ? 16 : 0);
