@@ -57,6 +57,10 @@ def _load(path: str):
     L.oracle_block_maxpool.argtypes = [P, I64, P, I, I, I, I, P, I64]
     L.oracle_block_union.argtypes = [P, P, I, I, I, P, P, P, I]
     L.oracle_block_attn.argtypes = [P, I, I64, I, I, I, P, I, P, I, P, I, I, I, P, P, I, I, D, P, P, I]
+    L.oracle_kv_append.argtypes = [P, I, I64, I, I, I, P, I, P, I, I, P, P, I, P]
+    L.oracle_kv_advance.argtypes = [P, P, I, I]
+    L.oracle_kv_append.restype = I
+    L.oracle_kv_advance.restype = I
     for fn in ("oracle_verify", "oracle_draft", "oracle_topk", "oracle_block_maxpool",
                "oracle_block_union", "oracle_block_attn"):
         getattr(L, fn).restype = ctypes.c_int
@@ -235,3 +239,29 @@ def _use_library(path: str | None):
     planted mistakes."""
     global _LIB
     _LIB = None if path is None else _load(path)
+
+
+def kv_append(pool, page_table, seq_lens, max_seq_len: int, k_new, v_new):
+    """KV append (ssd_oracle.c, oracle_kv_append; reading R8): returns (new pool, written[b]).
+    pool [P][2][h_kv][page][d] (float32 or bf16 bit patterns as uint16), k_new/v_new [B][n][h_kv][d]
+    of the same element type.  The input pool is not modified."""
+    pool = np.array(_np(pool), copy=True, order="C")
+    esize = pool.dtype.itemsize
+    pt = _np(page_table, np.int32)
+    lens = _np(seq_lens, np.int32)
+    kn = np.ascontiguousarray(_np(k_new).view(pool.dtype))
+    vn = np.ascontiguousarray(_np(v_new).view(pool.dtype))
+    B, n, h_kv, d = kn.shape
+    ok = np.zeros(B, np.int32)
+    _check(_lib().oracle_kv_append(_ptr(pool), esize, pool.shape[0], pool.shape[3], h_kv, d, _ptr(pt), pt.shape[1],
+                                   _ptr(lens), B, int(max_seq_len), _ptr(kn), _ptr(vn), n, _ptr(ok)), "kv_append")
+    return pool, ok
+
+
+def kv_advance(seq_lens, delta, max_seq_len: int) -> np.ndarray:
+    """Length advance (ssd_oracle.c, oracle_kv_advance; reading R8): seq_lens + delta where the
+    result stays in [0, max_seq_len], else unchanged."""
+    lens = np.array(_np(seq_lens, np.int32), copy=True)
+    dl = _np(delta, np.int32)
+    _check(_lib().oracle_kv_advance(_ptr(lens), _ptr(dl), lens.shape[0], int(max_seq_len)), "kv_advance")
+    return lens

@@ -19,6 +19,8 @@
  *        blocks execute together over the shared blocks.
  *  [SD]  "SparDA: Sparse Decoupled Attention ...", §2 training strategy: fine scores are max-pooled
  *        to the coarser selection grid.
+ *  [SSR] "SpecSA" forum post, "refresh/reuse NSA kernel fusion" and "branch handling": the KV of
+ *        accepted tokens is kept for later queries and the KV of rejected tokens is dropped.
  *
  * Readings of points the pages leave open (each one is listed in the design notes as well):
  *  R1  Request b holds L_b tokens including its n_c = k+1 candidates at positions L_b-n_c .. L_b-1.
@@ -33,6 +35,12 @@
  *      block_size tokens; each candidate keeps its own top blocks; the union of a group's candidate
  *      block sets is loaded once, and candidate i attends only its own blocks (causal as R1).
  *  R7  An empty token set gives output 0 and lse = -inf.
+ *  R8  KV append writes token j of request b (its K and V rows for every KV head) at position
+ *      seq_lens[b] + j through the page table; a position at or past max_seq_len, or a page id
+ *      outside the pool, skips the request (nothing of it is written).  Advancing adds delta[b] to
+ *      seq_lens[b]; a result outside [0, max_seq_len] leaves it unchanged.  Accepting a of the n_c
+ *      candidates of a verify is an advance by -(n_c - a): the rejected candidates' KV stays in the
+ *      pages but lies past the request's length.
  *
  * Element types: 0 = float32, 1 = bfloat16 (converted exactly to double).
  * KV pool layout [num_pages][2][h_kv][page_size][d]; index 0 = K, 1 = V.
@@ -482,4 +490,52 @@ int oracle_block_attn(const void *pool, int dtype, int64_t num_pages, int page_s
   size_t scratch = (size_t)(Lmax + 1) * sizeof(int32_t) + (size_t)Lmax / block + 64 +
                    (size_t)(Lmax + 1) * sizeof(double);
   return orc_run(orc_battn_unit, &c, batch * h_kv, nthreads, scratch);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * KV append and length advance (R8, [SSR]).  Plain element copies, no arithmetic.
+ *   pool       [num_pages][2][h_kv][page_size][d], element size esize bytes, modified in place
+ *   k_new/v_new [batch][n_new][h_kv][d]
+ *   ok[b]      set to 1 when request b was written, 0 when it was skipped
+ */
+int oracle_kv_append(void *pool, int esize, int64_t num_pages, int page_size, int h_kv, int d,
+                     const int32_t *page_table, int max_pages, const int32_t *seq_lens, int batch,
+                     int max_seq_len, const void *k_new, const void *v_new, int n_new, int32_t *ok) {
+  if (!pool || (esize != 2 && esize != 4) || page_size <= 0 || h_kv <= 0 || d <= 0 || n_new < 0 || batch < 0)
+    return -1;
+  const int64_t row_bytes = (int64_t)d * esize;
+  for (int b = 0; b < batch; ++b) {
+    ok[b] = 0;
+    const int L = seq_lens[b];
+    int good = L >= 0 && (int64_t)L + n_new <= max_seq_len;
+    for (int j = 0; good && j < n_new; ++j) {
+      const int t = L + j, pj = t / page_size;
+      if (pj >= max_pages) { good = 0; break; }
+      const int32_t p = page_table[(int64_t)b * max_pages + pj];
+      if (p < 0 || (int64_t)p >= num_pages) good = 0;
+    }
+    if (!good) continue;
+    for (int j = 0; j < n_new; ++j) {
+      const int t = L + j;
+      const int32_t p = page_table[(int64_t)b * max_pages + t / page_size];
+      for (int g = 0; g < h_kv; ++g) {
+        for (int which = 0; which < 2; ++which) {
+          const int64_t dst = ((((int64_t)p * 2 + which) * h_kv + g) * page_size + t % page_size) * row_bytes;
+          const int64_t src = ((((int64_t)b * n_new + j) * h_kv) + g) * row_bytes;
+          memcpy((char *)pool + dst, (const char *)(which ? v_new : k_new) + src, (size_t)row_bytes);
+        }
+      }
+    }
+    ok[b] = 1;
+  }
+  return 0;
+}
+
+int oracle_kv_advance(int32_t *seq_lens, const int32_t *delta, int batch, int max_seq_len) {
+  if (!seq_lens || !delta || batch < 0) return -1;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t v = (int64_t)seq_lens[b] + delta[b];
+    if (v >= 0 && v <= max_seq_len) seq_lens[b] = (int32_t)v;
+  }
+  return 0;
 }

@@ -342,6 +342,76 @@ def pin_block_attn(orc):
             np.testing.assert_allclose(bsub["out"][0, i, h], p @ V, rtol=0, atol=1e-13)
 
 
+def _kv_case(rng, lens, n, h_kv=2, d=8, ps=4, shuffle_seed=3):
+    """Full sequences of L + n tokens, their paged cache, and the 'before' cache in which the last n
+    slots of every request are blank (NaN): appending those n tokens must reproduce the full cache."""
+    Ks = [rng.standard_normal((h_kv, L + n, d)).astype(np.float32) for L in lens]
+    Vs = [rng.standard_normal((h_kv, L + n, d)).astype(np.float32) for L in lens]
+    full, pt, full_lens = paged_from_contiguous(Ks, Vs, ps, shuffle_seed=shuffle_seed)
+    before = full.copy()
+    for b, L in enumerate(lens):
+        for t in range(L, L + n):
+            before[pt[b, t // ps], :, :, t % ps, :] = np.nan
+    k_new = np.stack([Ks[b][:, L:L + n, :].transpose(1, 0, 2) for b, L in enumerate(lens)])
+    v_new = np.stack([Vs[b][:, L:L + n, :].transpose(1, 0, 2) for b, L in enumerate(lens)])
+    return Ks, Vs, full, before, pt, full_lens, k_new, v_new
+
+
+def pin_kv_append_composes(orc):
+    """Appending each request's next n tokens to a paged cache reproduces the cache built directly
+    from the longer sequences (every other pool element untouched), and verifying with the appended
+    tokens as the candidates equals brute force on the contiguous sequences.  Appending nothing
+    changes nothing."""
+    rng = np.random.default_rng(53)
+    lens, n, G = [5, 9], 3, 2
+    Ks, Vs, full, before, pt, full_lens, k_new, v_new = _kv_case(rng, lens, n)
+    max_len = pt.shape[1] * 4
+    after, ok = orc.kv_append(before, pt, np.array(lens, np.int32), max_len, k_new, v_new)
+    assert ok.tolist() == [1, 1]
+    np.testing.assert_array_equal(after, full)
+    q = rng.standard_normal((2, n, 2 * G, 8)).astype(np.float32)
+    res = orc.verify(orc.PagedKV(after, pt, full_lens), q, 0.3)
+    ref_out, _, _ = brute_verify(Ks, Vs, q, 0.3)
+    assert np.allclose(res["out"], ref_out, rtol=0, atol=1e-12)
+    same, ok0 = orc.kv_append(before, pt, np.array(lens, np.int32), max_len, k_new[:, :0], v_new[:, :0])
+    assert ok0.tolist() == [1, 1]
+    np.testing.assert_array_equal(same, before)
+
+
+def pin_kv_append_skips(orc):
+    """A request whose new tokens would pass max_seq_len, or reach a skipped page, is left
+    untouched; the others are written."""
+    rng = np.random.default_rng(59)
+    lens, n = [10, 4, 2], 3
+    _, _, full, before, pt, _, k_new, v_new = _kv_case(rng, lens, n)
+    pt = pt.copy()
+    pt[2, (lens[2] + 1) // 4] = -1  # request 2: its second new token falls in a missing page
+    after, ok = orc.kv_append(before, pt, np.array(lens, np.int32), 12, k_new, v_new)
+    assert ok.tolist() == [0, 1, 0]
+    for b, L in enumerate(lens):
+        for t in range(L, L + n):
+            p = pt[b, t // 4]
+            if p < 0:
+                continue
+            want = full if b == 1 else before
+            np.testing.assert_array_equal(after[p, :, :, t % 4, :], want[p, :, :, t % 4, :])
+
+
+def pin_kv_advance(orc):
+    """Advancing by +n then -n is the identity; a result outside [0, max_seq_len] leaves the
+    length unchanged; accepting a of n_c candidates is an advance by -(n_c - a)."""
+    lens = np.array([5, 9, 0, 12], np.int32)
+    up = orc.kv_advance(lens, np.array([3, 3, 3, 1], np.int32), 12)
+    assert up.tolist() == [8, 12, 3, 12]
+    back = orc.kv_advance(up, np.array([-3, -3, -3, 0], np.int32), 12)
+    assert back.tolist() == [5, 9, 0, 12]
+    assert orc.kv_advance(lens, np.array([-6, 0, -1, 0], np.int32), 12).tolist() == [5, 9, 0, 12]
+    n_c, accepted = 5, np.array([2, 5, 0, 1], np.int32)
+    cand = orc.kv_advance(np.array([10, 10, 10, 10], np.int32), np.full(4, n_c, np.int32), 64)
+    assert orc.kv_advance(cand, -(n_c - accepted), 64).tolist() == (10 + accepted).tolist()
+
+
 ALL_PINS = [pin_softmax_closed_form, pin_brute_force, pin_identical_keys, pin_crit_sums, pin_causality,
             pin_paging_invariance, pin_gqa_equals_mha, pin_draft_select_all, pin_draft_subset, pin_topk,
-            pin_block_maxpool, pin_block_union, pin_block_attn]
+            pin_block_maxpool, pin_block_union, pin_block_attn, pin_kv_append_composes, pin_kv_append_skips,
+            pin_kv_advance]

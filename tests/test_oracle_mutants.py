@@ -32,6 +32,9 @@ MUTANTS = {
                              "umask[(int64_t)u * umax + m - 1] |= 1u;"),
     "block_attn_no_causal": ("int last = L - c->n_c + i, n = 0;", "int last = L - 1, n = 0;"),
     "page_slot_wrong": ("(t % kv->page_size)) * kv->d;", "(t / kv->page_size) % kv->page_size) * kv->d;"),
+    "append_slot_shifted": ("* page_size + t % page_size) * row_bytes;", "* page_size + (t + 1) % page_size) * row_bytes;"),
+    "append_k_v_swapped": ("(which ? v_new : k_new)", "(which ? k_new : v_new)"),
+    "advance_no_range_check": ("if (v >= 0 && v <= max_seq_len) seq_lens[b] = (int32_t)v;", "seq_lens[b] = (int32_t)v;"),
 }
 
 
