@@ -161,6 +161,29 @@ int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t
                    size_t workspace_bytes, ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * KV append and length advance (SpecSA post, "refresh/reuse NSA kernel fusion" and "branch
+ * handling": the KV of accepted tokens is kept, that of rejected tokens dropped; SparseSpec §2.3: a
+ * verify checks the k drafts plus one bonus position).  With this library's verify convention the
+ * n_cand candidates of request b sit at positions L_b - n_cand .. L_b - 1, so a round is:
+ *   ssd_kv_append(candidates' K/V) -> ssd_kv_advance(+n_cand) -> verify / select / drafts ->
+ *   ssd_kv_advance(-(n_cand - accepted_b)).
+ * The rejected candidates' rows stay in their pages past the request's end, where nothing reads them.
+ *
+ * ssd_kv_append: writes token j (0 <= j < n_new) of request b at position seq_lens[b] + j.
+ *   k_new, v_new  device [batch][n_new][h_kv][d] of kv->dtype, 16-byte aligned.  kv->pool is written
+ *                 (the struct's const qualifier notwithstanding); seq_lens is only read.
+ *   The caller allocates the pages: page_table must map every new position.  A request whose new
+ *   positions would pass max_seq_len (SSD_FAULT_SEQLEN) or use a page id outside the pool
+ *   (SSD_FAULT_PAGE) is skipped as a whole; the others are written.
+ * ssd_kv_advance: seq_lens[b] += delta[b] (device int32 arrays of `batch`); a result outside
+ *   [0, max_seq_len] leaves seq_lens[b] unchanged and raises SSD_FAULT_SEQLEN.
+ */
+int ssd_kv_append(const ssd_paged_kv *kv, const void *k_new, const void *v_new, int n_new,
+                  ssd_stream_t stream);
+int ssd_kv_advance(int32_t *seq_lens, const int32_t *delta, int batch, int max_seq_len,
+                   ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * ssd_draft_attn_static: ssd_draft_attn without a workspace.  The paper has no counterpart; this
  * is a library convenience.  It exists for callers that cannot allocate device memory where they
  * run the draft step: a plugin inside another runtime that owns all device allocations and passes

@@ -26,7 +26,7 @@ FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT = 
 
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
             "ssd_select_topk", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
-            "ssd_unified_workspace_bytes",
+            "ssd_unified_workspace_bytes", "ssd_kv_append", "ssd_kv_advance",
             "ssd_unified_attn", "ssd_block_union", "ssd_block_sparse_workspace_bytes", "ssd_block_sparse_attn",
             "ssd_combine"]
 
@@ -78,6 +78,8 @@ def load(path: Optional[str] = None):
             "ssd_draft_workspace_bytes": ([KV, I, I], S),
             "ssd_draft_attn": ([KV, P, I, P, I, P, F, P, P, P, S, P], I),
             "ssd_draft_attn_static": ([KV, P, I, P, I, P, F, P, P, P], I),
+            "ssd_kv_append": ([KV, P, P, I, P], I),
+            "ssd_kv_advance": ([P, P, I, I, P], I),
             "ssd_unified_workspace_bytes": ([KV, I, I, I], S),
             "ssd_unified_attn": ([KV, P, P, P, I, I, P, I, P, F, P, P, P, I64, P, P, P, S, P], I),
             "ssd_block_union": ([P, P, I, I, I, I, P, P, P, I, P], I),
@@ -317,6 +319,28 @@ def ssd_draft_attn_static(kv: KVCache, q: torch.Tensor, idx: torch.Tensor, cnt: 
     _check(_lib().ssd_draft_attn_static(kv.ref(), _ptr(q), h_q, _ptr(idx), k_max, _ptr(cnt), float(scale), _ptr(out),
                                         _ptr(lse), _stream(stream)))
     return {"out": out, "lse": lse}
+
+
+def ssd_kv_append(kv: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """Writes k_new / v_new [B, n_new, h_kv, d] (the pool's dtype) at positions seq_lens[b] + j of
+    every request; kv.pool is modified in place, kv.seq_lens is not."""
+    _need(k_new, "k_new", kv.pool.dtype, kv.device)
+    _need(v_new, "v_new", kv.pool.dtype, kv.device)
+    if k_new.shape != v_new.shape or k_new.dim() != 4 or k_new.shape[0] != kv.batch or \
+            k_new.shape[2] != kv.h_kv or k_new.shape[3] != kv.d:
+        raise ValueError("k_new and v_new must both be [batch, n_new, h_kv, d]")
+    _check(_lib().ssd_kv_append(kv.ref(), _ptr(k_new), _ptr(v_new), k_new.shape[1], _stream(stream)))
+
+
+def ssd_kv_advance(seq_lens: torch.Tensor, delta: torch.Tensor, max_seq_len: int, stream=None) -> None:
+    """seq_lens += delta in place on the device (results outside [0, max_seq_len] are left as they
+    were and flagged in the device status)."""
+    _need(seq_lens, "seq_lens", torch.int32, seq_lens.device)
+    _need(delta, "delta", torch.int32, seq_lens.device)
+    if delta.shape != seq_lens.shape:
+        raise ValueError("delta must have the shape of seq_lens")
+    _check(_lib().ssd_kv_advance(_ptr(seq_lens), _ptr(delta), seq_lens.shape[0], int(max_seq_len),
+                                 _stream(stream)))
 
 
 def ssd_unified_attn(kv: KVCache, phase: torch.Tensor, q_verify: torch.Tensor, q_draft: torch.Tensor, n_cand: int,

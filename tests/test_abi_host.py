@@ -101,6 +101,19 @@ def test_draft_and_union_argument_errors(lib):
     assert lib.ssd_combine(None, 16, 4, 2, 128, 16, None, None) == binding.SSD_ERR_INVALID_ARG
 
 
+def test_kv_append_and_advance_argument_errors(lib):
+    kv = _kv()
+    E, OK = binding.SSD_ERR_INVALID_ARG, binding.SSD_OK
+    assert lib.ssd_kv_append(ctypes.byref(kv), None, 4096, 2, None) == E  # no k_new
+    assert lib.ssd_kv_append(ctypes.byref(kv), 4096, 4096, -1, None) == E  # negative count
+    assert lib.ssd_kv_append(ctypes.byref(kv), 4104, 4096, 2, None) == E  # k_new not 16-byte aligned
+    assert lib.ssd_kv_append(None, 4096, 4096, 2, None) == E
+    assert lib.ssd_kv_append(ctypes.byref(kv), 4096, 4096, 0, None) == OK  # nothing to append, no launch
+    assert lib.ssd_kv_advance(None, 4096, 4, 100, None) == E
+    assert lib.ssd_kv_advance(4096, 4096, -1, 100, None) == E
+    assert lib.ssd_kv_advance(4096, 4096, 0, 100, None) == OK  # empty batch, no launch
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(binding.LibraryNotBuilt):
         binding.load(str(tmp_path / "missing.so"))
