@@ -61,6 +61,10 @@ def _load(path: str):
     L.oracle_kv_advance.argtypes = [P, P, I, I]
     L.oracle_kv_append.restype = I
     L.oracle_kv_advance.restype = I
+    L.oracle_phase_assign.argtypes = [P, I, I, P]
+    L.oracle_phase_flags.argtypes = [P, I, I, I64, P]
+    L.oracle_phase_assign.restype = I
+    L.oracle_phase_flags.restype = I
     for fn in ("oracle_verify", "oracle_draft", "oracle_topk", "oracle_block_maxpool",
                "oracle_block_union", "oracle_block_attn"):
         getattr(L, fn).restype = ctypes.c_int
@@ -265,3 +269,20 @@ def kv_advance(seq_lens, delta, max_seq_len: int) -> np.ndarray:
     dl = _np(delta, np.int32)
     _check(_lib().oracle_kv_advance(_ptr(lens), _ptr(dl), lens.shape[0], int(max_seq_len)), "kv_advance")
     return lens
+
+
+def phase_assign(counts, n_new: int):
+    """Greedy phase-offset assignment (ssd_oracle.c, oracle_phase_assign; reading R9): returns
+    (new counts, offsets of the n_new arriving requests)."""
+    c = np.array(_np(counts, np.int32), copy=True)
+    out = np.zeros(max(n_new, 1), np.int32)
+    _check(_lib().oracle_phase_assign(_ptr(c), c.shape[0], int(n_new), _ptr(out)), "phase_assign")
+    return c, out[:n_new]
+
+
+def phase_flags(offsets, n_buckets: int, step: int) -> np.ndarray:
+    """1 where request b verifies at `step`, else 0 (ssd_oracle.c, oracle_phase_flags; R9)."""
+    off = _np(offsets, np.int32)
+    out = np.zeros(max(off.shape[0], 1), np.uint8)
+    _check(_lib().oracle_phase_flags(_ptr(off), off.shape[0], int(n_buckets), int(step), _ptr(out)), "phase_flags")
+    return out[:off.shape[0]]

@@ -35,6 +35,10 @@
  *      block_size tokens; each candidate keeps its own top blocks; the union of a group's candidate
  *      block sets is loaded once, and candidate i attends only its own blocks (causal as R1).
  *  R7  An empty token set gives output 0 and lse = -inf.
+ *  R9  Phase assignment ([SS] §4.2, workload-aware scheduling): there is one bucket per phase offset
+ *      (n_buckets = k+1: k draft steps and the verify); an arriving request joins the bucket with the
+ *      fewest live requests, ties to the lowest offset.  At step s a request with offset o is in
+ *      phase (s + o) mod n_buckets; the last phase (n_buckets - 1) is its verify, the others drafts.
  *  R8  KV append writes token j of request b (its K and V rows for every KV head) at position
  *      seq_lens[b] + j through the page table; a position at or past max_seq_len, or a page id
  *      outside the pool, skips the request (nothing of it is written).  Advancing adds delta[b] to
@@ -536,6 +540,33 @@ int oracle_kv_advance(int32_t *seq_lens, const int32_t *delta, int batch, int ma
   for (int b = 0; b < batch; ++b) {
     const int64_t v = (int64_t)seq_lens[b] + delta[b];
     if (v >= 0 && v <= max_seq_len) seq_lens[b] = (int32_t)v;
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Phase assignment and per-step phase flags (R9).
+ *   counts     [n_buckets] live requests per offset, updated in place
+ *   offset_out [n_new] the offset given to each arriving request, in arrival order
+ *   verify_out [batch] 1 when request b verifies at `step`, else 0
+ */
+int oracle_phase_assign(int32_t *counts, int n_buckets, int n_new, int32_t *offset_out) {
+  if (!counts || n_buckets <= 0 || n_new < 0 || (n_new > 0 && !offset_out)) return -1;
+  for (int r = 0; r < n_new; ++r) {
+    int best = 0;
+    for (int o = 1; o < n_buckets; ++o)
+      if (counts[o] < counts[best]) best = o;
+    counts[best] += 1;
+    offset_out[r] = best;
+  }
+  return 0;
+}
+
+int oracle_phase_flags(const int32_t *offsets, int batch, int n_buckets, int64_t step, uint8_t *verify_out) {
+  if (!offsets || !verify_out || batch < 0 || n_buckets <= 0 || step < 0) return -1;
+  for (int b = 0; b < batch; ++b) {
+    if (offsets[b] < 0 || offsets[b] >= n_buckets) return -1;
+    verify_out[b] = (uint8_t)(((step + offsets[b]) % n_buckets) == n_buckets - 1);
   }
   return 0;
 }

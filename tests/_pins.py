@@ -411,7 +411,30 @@ def pin_kv_advance(orc):
     assert orc.kv_advance(cand, -(n_c - accepted), 64).tolist() == (10 + accepted).tolist()
 
 
+def pin_phase_assignment(orc):
+    """Arrivals into empty buckets fill them round-robin (offsets 0, 1, ..., k, 0, ...), so the counts
+    never differ by more than one; an arrival joins the emptiest bucket, ties to the lowest offset;
+    over any n_buckets consecutive steps every request verifies exactly once, and at each step the
+    verifying requests are those of one bucket."""
+    nb = 5
+    c, off = orc.phase_assign(np.zeros(nb, np.int32), 12)
+    assert off.tolist() == [0, 1, 2, 3, 4, 0, 1, 2, 3, 4, 0, 1]
+    assert c.tolist() == [3, 3, 2, 2, 2] and c.max() - c.min() <= 1
+    c2, off2 = orc.phase_assign(np.array([4, 1, 3, 1, 2], np.int32), 3)
+    assert off2.tolist() == [1, 3, 1] and c2.tolist() == [4, 3, 3, 2, 2]
+    # A request that joins at offset 0 drafts for k = nb - 1 steps, then verifies (a speculative
+    # round is k drafts followed by one verify).
+    assert [int(orc.phase_flags(np.array([0], np.int32), nb, s)[0]) for s in range(2 * nb)] == [0, 0, 0, 0, 1] * 2
+    offsets = np.array([0, 1, 2, 3, 4, 0, 1, 2], np.int32)
+    total = np.zeros(len(offsets), np.int64)
+    for step in range(3, 3 + nb):
+        f = orc.phase_flags(offsets, nb, step)
+        total += f
+        assert len(set(offsets[f == 1].tolist())) == 1
+    assert total.tolist() == [1] * len(offsets)
+
+
 ALL_PINS = [pin_softmax_closed_form, pin_brute_force, pin_identical_keys, pin_crit_sums, pin_causality,
             pin_paging_invariance, pin_gqa_equals_mha, pin_draft_select_all, pin_draft_subset, pin_topk,
             pin_block_maxpool, pin_block_union, pin_block_attn, pin_kv_append_composes, pin_kv_append_skips,
-            pin_kv_advance]
+            pin_kv_advance, pin_phase_assignment]

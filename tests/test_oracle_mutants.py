@@ -34,6 +34,8 @@ MUTANTS = {
     "page_slot_wrong": ("(t % kv->page_size)) * kv->d;", "(t / kv->page_size) % kv->page_size) * kv->d;"),
     "append_slot_shifted": ("* page_size + t % page_size) * row_bytes;", "* page_size + (t + 1) % page_size) * row_bytes;"),
     "append_k_v_swapped": ("(which ? v_new : k_new)", "(which ? k_new : v_new)"),
+    "phase_ties_to_highest": ("if (counts[o] < counts[best]) best = o;", "if (counts[o] <= counts[best]) best = o;"),
+    "phase_verify_is_first": ("== n_buckets - 1);", "== 0);"),
     "advance_no_range_check": ("if (v >= 0 && v <= max_seq_len) seq_lens[b] = (int32_t)v;", "seq_lens[b] = (int32_t)v;"),
 }
 
