@@ -223,6 +223,25 @@ int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, const void *q
                      void *workspace, size_t workspace_bytes, ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Phase assignment for the unified batch (SparseSpec §4.2, workload-aware scheduling: requests of
+ * both phases are mixed evenly in every step; a greedy bin-packing keeps one bucket per phase and
+ * gives each arriving request the least loaded one).  A bucket is a phase offset o in
+ * [0, n_buckets) with n_buckets = k + 1: at step s a request with offset o is in phase
+ * (s + o) mod n_buckets, where n_buckets - 1 is its verify and the other phases its k drafts.
+ *
+ * ssd_phase_assign (host only, no CUDA call): counts (host int32 [n_buckets], live requests per
+ *   offset) is updated in place; offset_out (host int32 [n_new]) receives each arriving request's
+ *   offset in arrival order: the bucket with the smallest count, ties to the lowest offset.  The
+ *   caller decrements counts[o] when a request with offset o finishes.
+ * ssd_phase_fill: phase (device uint8 [batch]) = 1 where request b verifies at `step`, 0 where it
+ *   drafts -- the phase array of ssd_unified_attn.  offsets: device int32 [batch]; an offset
+ *   outside [0, n_buckets) gives 0 and raises SSD_FAULT_INDEX.
+ */
+int ssd_phase_assign(int32_t *counts, int n_buckets, int n_new, int32_t *offset_out);
+int ssd_phase_fill(const int32_t *offsets, int batch, int n_buckets, int64_t step, uint8_t *phase,
+                   ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Block-granular variant (SpecSA post: overlap-aware grouped query execution -- candidates with
  * overlapping sparse layouts run together and share KV blocks; hierarchical layout management).
  *

@@ -26,7 +26,7 @@ FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT = 
 
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
             "ssd_select_topk", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
-            "ssd_unified_workspace_bytes", "ssd_kv_append", "ssd_kv_advance",
+            "ssd_unified_workspace_bytes", "ssd_kv_append", "ssd_kv_advance", "ssd_phase_assign", "ssd_phase_fill",
             "ssd_unified_attn", "ssd_block_union", "ssd_block_sparse_workspace_bytes", "ssd_block_sparse_attn",
             "ssd_combine"]
 
@@ -80,6 +80,8 @@ def load(path: Optional[str] = None):
             "ssd_draft_attn_static": ([KV, P, I, P, I, P, F, P, P, P], I),
             "ssd_kv_append": ([KV, P, P, I, P], I),
             "ssd_kv_advance": ([P, P, I, I, P], I),
+            "ssd_phase_assign": ([P, I, I, P], I),
+            "ssd_phase_fill": ([P, I, I, I64, P, P], I),
             "ssd_unified_workspace_bytes": ([KV, I, I, I], S),
             "ssd_unified_attn": ([KV, P, P, P, I, I, P, I, P, F, P, P, P, I64, P, P, P, S, P], I),
             "ssd_block_union": ([P, P, I, I, I, I, P, P, P, I, P], I),
@@ -341,6 +343,30 @@ def ssd_kv_advance(seq_lens: torch.Tensor, delta: torch.Tensor, max_seq_len: int
         raise ValueError("delta must have the shape of seq_lens")
     _check(_lib().ssd_kv_advance(_ptr(seq_lens), _ptr(delta), seq_lens.shape[0], int(max_seq_len),
                                  _stream(stream)))
+
+
+def ssd_phase_assign(counts, n_new: int):
+    """Greedy phase offsets for n_new arriving requests.  counts: host int32 array [k + 1] of live
+    requests per offset (numpy or CPU tensor), updated in place; returns the offsets (int32 numpy)."""
+    import numpy as np
+    c = counts.numpy() if isinstance(counts, torch.Tensor) else counts
+    if not isinstance(c, np.ndarray) or c.dtype != np.int32 or not c.flags["C_CONTIGUOUS"]:
+        raise TypeError("counts must be a contiguous int32 host array")
+    out = np.zeros(max(n_new, 1), np.int32)
+    _check(_lib().ssd_phase_assign(c.ctypes.data_as(ctypes.c_void_p), c.shape[0], int(n_new),
+                                   out.ctypes.data_as(ctypes.c_void_p)))
+    return out[:n_new]
+
+
+def ssd_phase_fill(offsets: torch.Tensor, n_buckets: int, step: int, *, phase=None, stream=None) -> torch.Tensor:
+    """Device phase array for ssd_unified_attn at `step`: 1 = verify, 0 = draft."""
+    _need(offsets, "offsets", torch.int32, offsets.device)
+    if phase is None:
+        phase = torch.empty(offsets.shape, dtype=torch.uint8, device=offsets.device)
+    _need(phase, "phase", torch.uint8, offsets.device)
+    _check(_lib().ssd_phase_fill(_ptr(offsets), offsets.shape[0], int(n_buckets), int(step), _ptr(phase),
+                                 _stream(stream)))
+    return phase
 
 
 def ssd_unified_attn(kv: KVCache, phase: torch.Tensor, q_verify: torch.Tensor, q_draft: torch.Tensor, n_cand: int,
