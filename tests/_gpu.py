@@ -1,5 +1,5 @@
 """Helpers for the GPU parity tests: host copies of (sub)workloads for the oracle, and the
-comparisons with the tolerances the benchmark spec fixes (outputs: max |diff| <= 2e-3; criticality:
+comparisons with the parity tolerances (outputs: max |diff| <= 2e-3; criticality:
 |diff| <= 1e-3 |ref| + 1e-6; indices: bit-exact when both sides select from the same fp32 scores)."""
 
 from __future__ import annotations
