@@ -64,6 +64,8 @@ def _load(path: str):
     L.oracle_phase_assign.argtypes = [P, I, I, P]
     L.oracle_phase_flags.argtypes = [P, I, I, I64, P]
     L.oracle_phase_assign.restype = I
+    L.oracle_topp_k.argtypes = [P, I64, P, D, I, I, I, I, P]
+    L.oracle_topp_k.restype = I
     L.oracle_phase_flags.restype = I
     for fn in ("oracle_verify", "oracle_draft", "oracle_topk", "oracle_block_maxpool",
                "oracle_block_union", "oracle_block_attn"):
@@ -286,3 +288,19 @@ def phase_flags(offsets, n_buckets: int, step: int) -> np.ndarray:
     out = np.zeros(max(off.shape[0], 1), np.uint8)
     _check(_lib().oracle_phase_flags(_ptr(off), off.shape[0], int(n_buckets), int(step), _ptr(out)), "phase_flags")
     return out[:off.shape[0]]
+
+
+def topp(scores, lens, p: float, k_max: int, rows_per_group: int = 1, len_div: int = 1):
+    """Top-p selection (ssd_oracle.c, oracle_topp_k then oracle_topk; reading R10): per row the
+    smallest set of largest entries whose sum reaches p times the row total, capped at k_max.
+    Returns idx [n_rows, k_max] (ascending, -1 padded), cnt [n_rows] and the per-row K."""
+    s = _np(scores, np.float32)
+    n_rows, stride = s.shape
+    lens_n = _np(lens, np.int32)
+    n_groups = n_rows // rows_per_group
+    assert n_groups * rows_per_group == n_rows and lens_n.size == n_groups
+    kout = np.zeros(n_rows, np.int32)
+    _check(_lib().oracle_topp_k(_ptr(s), stride, _ptr(lens_n), float(p), n_groups, rows_per_group, len_div, k_max,
+                                _ptr(kout)), "topp")
+    idx, cnt = topk(s, np.repeat(lens_n, rows_per_group), kout, k_max, 1, len_div)
+    return idx, cnt, kout

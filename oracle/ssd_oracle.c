@@ -39,6 +39,10 @@
  *      (n_buckets = k+1: k draft steps and the verify); an arriving request joins the bucket with the
  *      fewest live requests, ties to the lowest offset.  At step s a request with offset o is in
  *      phase (s + o) mod n_buckets; the last phase (n_buckets - 1) is its verify, the others drafts.
+ *  R10 Top-p (variable K): a row keeps the smallest number K of its largest entries (ties toward
+ *      the lower index) whose sum reaches p times the row's total, both sums in double precision,
+ *      the prefix taken in that descending order; K = 0 when p times the total is not positive;
+ *      K is capped at k_max.  The kept set is then exactly the Top-K set of R4 with that K.
  *  R8  KV append writes token j of request b (its K and V rows for every KV head) at position
  *      seq_lens[b] + j through the page table; a position at or past max_seq_len, or a page id
  *      outside the pool, skips the request (nothing of it is written).  Advancing adds delta[b] to
@@ -567,6 +571,41 @@ int oracle_phase_flags(const int32_t *offsets, int batch, int n_buckets, int64_t
   for (int b = 0; b < batch; ++b) {
     if (offsets[b] < 0 || offsets[b] >= n_buckets) return -1;
     verify_out[b] = (uint8_t)(((step + offsets[b]) % n_buckets) == n_buckets - 1);
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * Top-p entry counts (R10).  kout[r] = min(K_p(r), k_max) for every row r (rows grouped as in
+ * oracle_topk: row r uses lens[r / rows_per_group] and has ceil(len / len_div) entries).
+ */
+int oracle_topp_k(const float *scores, int64_t stride, const int32_t *lens, double p, int n_groups,
+                  int rows_per_group, int len_div, int k_max, int32_t *kout) {
+  if (!scores || !lens || !kout || rows_per_group <= 0 || len_div <= 0 || k_max < 0 || !(p >= 0.0)) return ORC_EARG;
+  const int64_t n_rows = (int64_t)n_groups * rows_per_group;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int n = (lens[r / rows_per_group] + len_div - 1) / len_div;
+    if (n < 0 || (int64_t)n > stride) return ORC_EARG;
+    orc_pair *pairs = (orc_pair *)malloc((size_t)(n > 0 ? n : 1) * sizeof(orc_pair));
+    if (!pairs) return ORC_ENOMEM;
+    double total = 0.0;
+    for (int t = 0; t < n; ++t) {
+      const float v = scores[r * stride + t];
+      if (v != v || v < 0.f) {
+        free(pairs);
+        return ORC_EARG; /* scores are non-negative probabilities, never NaN */
+      }
+      pairs[t].v = v;
+      pairs[t].i = t;
+    }
+    qsort(pairs, (size_t)n, sizeof(orc_pair), orc_cmp_desc);
+    for (int t = 0; t < n; ++t) total += (double)pairs[t].v;
+    const double target = p * total;
+    int k = 0;
+    double acc = 0.0;
+    while (k < n && acc < target) acc += (double)pairs[k++].v;
+    kout[r] = k < k_max ? k : k_max;
+    free(pairs);
   }
   return 0;
 }

@@ -434,7 +434,39 @@ def pin_phase_assignment(orc):
     assert total.tolist() == [1] * len(offsets)
 
 
+def pin_topp(orc):
+    """Top-p against a brute-force prefix search on sorted rows; p = 1 keeps exactly the non-zero
+    entries; equal entries keep ceil(p n) of them, the lowest indices; K never decreases with p;
+    K is capped at k_max; a zero row keeps nothing."""
+    rng = np.random.default_rng(73)
+    s = rng.random((6, 40)).astype(np.float32) ** 3
+    s[1, 20:] = 0.0
+    s[2, :] = 0.25
+    s[3, :] = 0.0
+    lens = np.array([40, 40, 40, 40, 17, 1], np.int32)
+    for p in (0.0, 0.1, 0.5, 0.9, 0.999, 1.0):
+        idx, cnt, k = orc.topp(s, lens, p, 40)
+        for r in range(6):
+            n = lens[r]
+            order = sorted(range(n), key=lambda t: (-float(s[r, t]), t))
+            vals = [float(s[r, t]) for t in order]
+            target, acc, kk = p * sum(vals), 0.0, 0
+            while kk < n and acc < target:
+                acc += vals[kk]
+                kk += 1
+            assert k[r] == kk and cnt[r] == kk
+            assert sorted(idx[r, :kk].tolist()) == sorted(order[:kk]) and idx[r, :kk].tolist() == sorted(order[:kk])
+    _, _, k1 = orc.topp(s, lens, 1.0, 40)
+    assert k1[1] == 20 and k1[3] == 0
+    _, _, kq = orc.topp(s, lens, 0.3, 40)
+    assert kq[2] == 12  # 0.3 * 40 equal entries
+    ks = [orc.topp(s, lens, p, 40)[2] for p in (0.2, 0.4, 0.6, 0.8)]
+    assert all((a <= b).all() for a, b in zip(ks, ks[1:]))
+    _, capped, kc = orc.topp(s, lens, 1.0, 5)
+    assert kc.max() <= 5 and capped.max() <= 5
+
+
 ALL_PINS = [pin_softmax_closed_form, pin_brute_force, pin_identical_keys, pin_crit_sums, pin_causality,
             pin_paging_invariance, pin_gqa_equals_mha, pin_draft_select_all, pin_draft_subset, pin_topk,
             pin_block_maxpool, pin_block_union, pin_block_attn, pin_kv_append_composes, pin_kv_append_skips,
-            pin_kv_advance, pin_phase_assignment]
+            pin_kv_advance, pin_phase_assignment, pin_topp]

@@ -36,6 +36,9 @@ MUTANTS = {
     "append_k_v_swapped": ("(which ? v_new : k_new)", "(which ? k_new : v_new)"),
     "phase_ties_to_highest": ("if (counts[o] < counts[best]) best = o;", "if (counts[o] <= counts[best]) best = o;"),
     "phase_verify_is_first": ("== n_buckets - 1);", "== 0);"),
+    "topp_strict_reach": ("while (k < n && acc < target) acc += (double)pairs[k++].v;",
+                          "while (k < n && acc <= target) acc += (double)pairs[k++].v;"),
+    "topp_no_cap": ("kout[r] = k < k_max ? k : k_max;", "kout[r] = k;"),
     "advance_no_range_check": ("if (v >= 0 && v <= max_seq_len) seq_lens[b] = (int32_t)v;", "seq_lens[b] = (int32_t)v;"),
 }
 
