@@ -7,7 +7,8 @@
  *                          cache, causal among the candidates; the same pass emits every KV token's
  *                          criticality (softmax probability summed over the query heads of the KV
  *                          group and the k+1 verify positions).
- *   2. ssd_select_topk  -- Top-K of the criticality per (request, KV head), ties to the lower index.
+ *   2. ssd_select_topk  -- Top-K of the criticality per (request, KV head), ties to the lower index
+ *                          (ssd_select_topp: the same with a per-row K from a top-p budget).
  *   3. ssd_draft_attn   -- the next k drafts: single-query attention over the selected tokens only.
  * plus the unified verify/draft launch (§4.2 "fused attention") and the block-granular variant
  * (SpecSA post, overlap-aware grouped query execution; SparDA §2 max-pooling to a block grid).
@@ -66,7 +67,8 @@ enum ssd_device_fault {
   SSD_FAULT_INDEX = 4u,    /* a draft index outside [0, L_b) */
   SSD_FAULT_KMAX = 8u,     /* a requested K larger than k_max (output truncated to k_max) */
   SSD_FAULT_UNION = 16u,   /* a block union larger than umax (output truncated) */
-  SSD_FAULT_TIMEOUT = 32u  /* a bounded wait inside a kernel expired; that block's outputs are invalid */
+  SSD_FAULT_TIMEOUT = 32u, /* a bounded wait inside a kernel expired; that block's outputs are invalid */
+  SSD_FAULT_VALUE = 64u    /* a score that must be >= 0 (top-p selection) was negative or NaN */
 };
 
 /*
@@ -145,6 +147,23 @@ int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, 
 int ssd_select_topk(const float *scores, int64_t stride, const int32_t *lens, const int32_t *ks,
                     int n_groups, int rows_per_group, int len_div, int max_len, int32_t *idx, int k_max,
                     int32_t *cnt, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Top-p selection: a per-row budget instead of a fixed K (SparseSpec §3.2 and §3.3 measure the
+ * draft against "oracle top-k" attention and cite adaptive sparsity by hierarchical top-p pruning,
+ * Twilight; §4.1: the selected set is the top of the verify scores).  Row r (same grouping, lengths and len_div as ssd_select_topk) keeps
+ * K_r = min(K_p, k_max) entries, where K_p is the smallest count of the row's largest entries
+ * (equal values toward the lower index) whose sum reaches p times the row's total; the kept set
+ * is the Top-K_r set, written to idx / cnt exactly as ssd_select_topk writes it.  k_rows (device
+ * int32 [rows]) receives K_r.  p is in [0, 1]; p = 0, an empty row or an all-zero row keeps
+ * nothing.  Scores must be >= 0 (criticality is a sum of probabilities): a row holding a negative
+ * value or NaN keeps nothing and raises SSD_FAULT_VALUE.  Sums are exact 64-bit fixed point in
+ * units of 2^(ceil(log2 n_r) - 62) times the power of two just above the row's maximum; smaller
+ * values round down to that unit.  Two kernels on `stream`: the counts, then the Top-K pass.
+ */
+int ssd_select_topp(const float *scores, int64_t stride, const int32_t *lens, float p, int n_groups,
+                    int rows_per_group, int len_div, int max_len, int32_t *idx, int k_max, int32_t *cnt,
+                    int32_t *k_rows, ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Sparse draft attention (SparseSpec §4.1: each of the k drafts after a verify loads only the

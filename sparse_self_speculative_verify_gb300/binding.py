@@ -22,10 +22,10 @@ from . import build as _build
 
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_WORKSPACE, SSD_ERR_CUDA, SSD_ERR_TIMEOUT = range(6)
 SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
-FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT = 1, 2, 4, 8, 16, 32
+FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT, FAULT_VALUE = 1, 2, 4, 8, 16, 32, 64
 
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
-            "ssd_select_topk", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
+            "ssd_select_topk", "ssd_select_topp", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
             "ssd_unified_workspace_bytes", "ssd_kv_append", "ssd_kv_advance", "ssd_phase_assign", "ssd_phase_fill",
             "ssd_unified_attn", "ssd_block_union", "ssd_block_sparse_workspace_bytes", "ssd_block_sparse_attn",
             "ssd_combine"]
@@ -75,6 +75,7 @@ def load(path: Optional[str] = None):
             "ssd_verify_workspace_bytes": ([KV, I, I], S),
             "ssd_verify_attn": ([KV, P, I, I, F, P, P, P, I64, P, I64, I, P, S, P], I),
             "ssd_select_topk": ([P, I64, P, P, I, I, I, I, P, I, P, P], I),
+            "ssd_select_topp": ([P, I64, P, F, I, I, I, I, P, I, P, P, P], I),
             "ssd_draft_workspace_bytes": ([KV, I, I], S),
             "ssd_draft_attn": ([KV, P, I, P, I, P, F, P, P, P, S, P], I),
             "ssd_draft_attn_static": ([KV, P, I, P, I, P, F, P, P, P], I),
@@ -279,6 +280,33 @@ def ssd_select_topk(scores: torch.Tensor, lens: torch.Tensor, ks: torch.Tensor, 
     _check(_lib().ssd_select_topk(_ptr(scores), stride, _ptr(lens), _ptr(ks), n_groups, rows_per_group, len_div,
                                   int(max_len), _ptr(idx), k_max, _ptr(cnt), _stream(stream)))
     return idx, cnt
+
+
+def ssd_select_topp(scores: torch.Tensor, lens: torch.Tensor, p: float, k_max: int, rows_per_group: int,
+                    len_div: int = 1, max_len: Optional[int] = None, *, idx=None, cnt=None, k_rows=None,
+                    stream=None):
+    """Top-p per row: the fewest largest entries whose sum reaches p times the row total, at most
+    k_max.  Returns (idx, cnt, k_rows); k_rows is the per-row count before the Top-K pass."""
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    _need(lens, "lens", torch.int32, dev)
+    stride = scores.shape[-1]
+    n_rows = scores.numel() // stride
+    n_groups = lens.shape[0]
+    assert n_groups * rows_per_group == n_rows
+    if max_len is None:
+        max_len = stride
+    if idx is None:
+        idx = torch.empty((n_rows, max(k_max, 0)), dtype=torch.int32, device=dev)
+    if cnt is None:
+        cnt = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    if k_rows is None:
+        k_rows = torch.empty((n_rows,), dtype=torch.int32, device=dev)
+    for t, name in ((idx, "idx"), (cnt, "cnt"), (k_rows, "k_rows")):
+        _need(t, name, torch.int32, dev)
+    _check(_lib().ssd_select_topp(_ptr(scores), stride, _ptr(lens), float(p), n_groups, rows_per_group, len_div,
+                                  int(max_len), _ptr(idx), k_max, _ptr(cnt), _ptr(k_rows), _stream(stream)))
+    return idx, cnt, k_rows
 
 
 def ssd_draft_attn(kv: KVCache, q: torch.Tensor, idx: torch.Tensor, cnt: torch.Tensor, scale: float, *, out=None,

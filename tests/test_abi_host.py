@@ -91,6 +91,17 @@ def test_select_argument_errors(lib):
     assert lib.ssd_select_topk(4096, 10, 16, 16, 0, 1, 1, 10, 64, 4, 64, None) == binding.SSD_OK
 
 
+def test_select_topp_argument_errors(lib):
+    E = binding.SSD_ERR_INVALID_ARG
+    # scores, stride, lens, p, n_groups, rows_per_group, len_div, max_len, idx, k_max, cnt, k_rows
+    assert lib.ssd_select_topp(4096, 10, 16, 0.5, 1, 1, 1, 10, 64, 4, 64, None, None) == E  # k_rows NULL
+    for bad_p in (-0.25, 1.25, float("nan")):
+        assert lib.ssd_select_topp(4096, 10, 16, bad_p, 1, 1, 1, 10, 64, 4, 64, 128, None) == E
+    assert lib.ssd_select_topp(4096, 5, 16, 0.5, 1, 1, 1, 10, 64, 4, 64, 128, None) == E  # stride < max_len
+    assert lib.ssd_select_topp(4096, 10, 16, 0.5, 1, 1, 0, 10, 64, 4, 64, 128, None) == E  # len_div 0
+    assert lib.ssd_select_topp(4096, 10, 16, 0.5, 0, 1, 1, 10, 64, 4, 64, 128, None) == binding.SSD_OK
+
+
 def test_draft_and_union_argument_errors(lib):
     kv = _kv()
     assert lib.ssd_draft_attn(ctypes.byref(kv), None, 32, 16, 8, 16, 0.1, 16, None, 1 << 20, 1 << 40,
