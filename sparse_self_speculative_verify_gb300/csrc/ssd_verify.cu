@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   if (f.phase && f.phase[b] == 0) return;
   int L = f.seq_lens[b];
   L = L < 0 ? 0 : (L > f.max_seq_len ? f.max_seq_len : L);
-  const int ns = f.ucnt ? block_splits(min(max(f.ucnt[u], 0), f.umax)) : verify_splits(L);
+  const int ns = f.ucnt ? block_splits(min(max(f.ucnt[u], 0), f.umax))
+                        : verify_splits(L, f.split_len ? *f.split_len : kSplitTokens);
   const int64_t pbase = (int64_t)u * f.S_max * f.R;
   for (int r = warp; r < f.R; r += kFinThreads / 32) {
     float M = -INFINITY;
@@ -249,7 +250,7 @@ static int launch_simt(const VerifyArgs &a, dim3 grid, cudaStream_t st) {
 
 struct VerifyLayout {
   int G, R, units, S_max, Lpad;
-  size_t o_off, lse_off, sp_off, sm_off, ctr_off, total;
+  size_t o_off, lse_off, sp_off, sm_off, split_off, ctr_off, total;
 };
 
 static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int S_max) {
@@ -271,6 +272,8 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   c.take<__half>((size_t)l.units * l.R * l.Lpad);
   l.sm_off = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
+  l.split_off = c.off;
+  c.take<int>(1);
   l.total = c.off;
   return l;
 }
@@ -341,8 +344,11 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   a.status = status;
   a.sched = reinterpret_cast<int *>(ws + lay.ctr_off);
   dim3 grid(lay.S_max, lay.units);
-  if (verify_tc_supported(kv, lay.R))
+  const bool tc = verify_tc_supported(kv, lay.R);
+  if (tc) {
+    a.split_out = reinterpret_cast<int *>(ws + lay.split_off);
     rc = launch_verify_tc(kv, a, st);
+  }
   else if (kv->dtype == SSD_DTYPE_BF16)
     rc = dispatch_mma<false>(kv->d, rows_per_tile(lay.R), a, grid, st);
   else
@@ -370,6 +376,7 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   f.scores_stride = scores_stride;
   f.bscores = bscores;
   f.bstride = bscores_stride;
+  f.split_len = tc ? a.split_out : nullptr;
   const int n_tok = crit ? cdiv(kv->max_seq_len, kFinTok) : 0;
   return launch_finalize(f, n_tok, lay.units, st);
 }

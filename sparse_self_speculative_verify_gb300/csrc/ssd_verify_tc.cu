@@ -6,7 +6,7 @@
 // logits + LSE).  Same work items, partials and criticality side values as the mma.sync tile in
 // ssd_verify_tile.cuh; the finalize pass is shared.
 //
-// One persistent block per SM works through work items (splits of 512 tokens of one (request, KV
+// One persistent block per SM works through work items (splits of 512 to 2048 tokens of one (request, KV
 // head)), tile by tile (128 tokens).  Its first item is blockIdx.x; later ones come from a global
 // counter, so the items spread over the blocks by how fast each block actually runs.
 //  * warp 8 draws the items, hands their numbers to the other warps through a small shared ring, and
@@ -48,6 +48,11 @@ constexpr int kTcProducerWarp = 8;
 constexpr int kTcMmaWarp = 9;
 constexpr int kTcMaxBatch = 1024;
 constexpr int kTcItemRing = 8;  // item numbers handed from the producer to the other roles
+// Split length: each item ends with an epilogue and a pipeline refill that cost a few thousand
+// cycles, so items are made as long as load balance allows: about kTcItemsPerBlock items per block
+// over the batch's actual tokens, a multiple of the tile, between kSplitTokens and kTcMaxSplit.
+constexpr int kTcItemsPerBlock = 6;
+constexpr int kTcMaxSplit = 2048;
 constexpr int kSlotBytes = kTcTile * 256;  // one K or V tile: 2 panels x 128 rows x 128 B
 constexpr int kPanelBytes = kTcTile * 128;
 constexpr float kLazy = 8.f;
@@ -89,7 +94,8 @@ struct TcItem {
 };
 
 // Item -> (request, head, split): items of request b are pre[b] .. pre[b+1]-1, ordered (head, split).
-__device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int *len, int B, const VerifyArgs &a) {
+__device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int *len, int B, const VerifyArgs &a,
+                                           int split_len) {
   int lo = 0, hi = B;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -102,8 +108,8 @@ __device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int 
   it.g = r / ns;
   it.split = r % ns;
   it.L = len[lo];
-  it.t0 = it.split * kSplitTokens;
-  it.t1 = min(it.t0 + kSplitTokens, it.L);
+  it.t0 = it.split * split_len;
+  it.t1 = min(it.t0 + split_len, it.L);
   it.ntiles = cdiv(it.t1 - it.t0, kTcTile);
   return it;
 }
@@ -229,35 +235,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s.len = s.pre + kTcMaxBatch + 1;
   }
 
-  // Per-request item counts and their prefix (chunked block scan).
+  // Per-request lengths, the split length, item counts and their prefix (chunked block scan).
+  int split_len;
   {
     constexpr int CH = cdiv(kTcMaxBatch + 1, kTcThreads);
     int loc[CH];
-    int sum = 0;
+    long long tok = 0;
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
       const int b = tid * CH + k;
-      int c = 0;
+      int L = 0;
       if (b < B) {
-        int L = a.kv.seq_lens[b];
+        L = a.kv.seq_lens[b];
         if (L < a.n_c || L > a.kv.max_seq_len) {
           if (blockIdx.x == 0) atomicOr(a.status, (unsigned)SSD_FAULT_SEQLEN);
           L = L < 0 ? 0 : (L > a.kv.max_seq_len ? a.kv.max_seq_len : L);
         }
-        c = h_kv * verify_splits(L);
         s.len[b] = L;
       }
-      loc[k] = c;
-      sum += c;
+      loc[k] = L;
+      tok += L;
     }
-    int incl = sum;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
+    for (int o = 16; o >= 1; o >>= 1) tok += __shfl_xor_sync(0xffffffffu, tok, o);
+    __shared__ long long s_wtok[kTcWarps];
     __shared__ int s_wsum[kTcWarps];
-    if (lane == 31) s_wsum[warp] = incl;
+    if (lane == 0) s_wtok[warp] = tok;
     if (tid == 0) {
       *s.abort = 0;
       for (int k = 0; k < 8; ++k) s.vote[k] = 0;
@@ -296,6 +299,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    {
+      long long total = 0;
+      for (int w = 0; w < kTcWarps; ++w) total += s_wtok[w];
+      long long per = total * h_kv / ((long long)gridDim.x * kTcItemsPerBlock) / kTcTile * kTcTile;
+      split_len = (int)min(max(per, (long long)kSplitTokens), (long long)kTcMaxSplit);
+    }
+    if (blockIdx.x == 0 && tid == 0) *a.split_out = split_len;
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      loc[k] = h_kv * verify_splits(loc[k], split_len);
+      sum += loc[k];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
     int off = 0;
     for (int w = 0; w < warp; ++w) off += s_wsum[w];
     off += incl - sum;
@@ -320,13 +344,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int jl = 0;
     bool ok = true;
     // Page ids of an item's boxes, read by the whole warp one item ahead of use: box j (tokens
-    // t0 + j*box_rows) lives in lane j % 32, register j / 32 (at most 512 / 8 = 64 boxes per item).
-    auto load_pids = [&](int item_idx, int32_t(&dst)[2]) {
-      dst[0] = dst[1] = -1;
-      if (item_idx < n_items) {
-        const TcItem nx = tc_decode(item_idx, s.pre, s.len, B, a);
+    // t0 + j*box_rows) lives in lane j % 32, register j / 32 (boxes hold at least 8 rows).
+    constexpr int kPidRegs = kTcMaxSplit / (8 * 32);
+    auto load_pids = [&](int item_idx, int32_t(&dst)[kPidRegs]) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kPidRegs; ++h) dst[h] = -1;
+      if (item_idx < n_items) {
+        const TcItem nx = tc_decode(item_idx, s.pre, s.len, B, a, split_len);
+#pragma unroll
+        for (int h = 0; h < kPidRegs; ++h) {
           const int t = nx.t0 + (h * 32 + lane) * box_rows;
           if (t < nx.t1) dst[h] = __ldg(a.kv.page_table + (int64_t)nx.b * a.kv.max_pages + (t >> lps));
         }
@@ -342,7 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) raw = atomicAdd(a.sched, 1);
       nxt = min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items);
     }
-    int32_t pid_next[2];
+    int32_t pid_next[kPidRegs];
     load_pids(cur, pid_next);
     for (;; ++jl) {
       // Hand the item number to the MMA and softmax roles (n_items ends their loops). The slot
@@ -354,8 +380,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive(bar_addr(s.item_full + jl % kTcItemRing));
       }
       if (cur >= n_items || !ok) break;
-      const TcItem it = tc_decode(cur, s.pre, s.len, B, a);
-      int32_t pid_reg[2] = {pid_next[0], pid_next[1]};
+      const TcItem it = tc_decode(cur, s.pre, s.len, B, a, split_len);
+      int32_t pid_reg[kPidRegs];
+#pragma unroll
+      for (int h = 0; h < kPidRegs; ++h) pid_reg[h] = pid_next[h];
       load_pids(nxt, pid_next);
       if (nxt < n_items && lane == 0) raw = atomicAdd(a.sched, 1);
       // Query rows of this item: one 4-D TMA box per 64-column panel (d x 1 x G heads x n_c
@@ -375,9 +403,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int tb = it.t0 + k * kTcTile, tend = min(tb + kTcTile, it.t1);
         // Lane j < boxes_per_tile handles box j of this tile.
         const int jb = k * boxes_per_tile + lane;
-        const int32_t p0 = __shfl_sync(0xffffffffu, pid_reg[0], jb & 31);
-        const int32_t p1 = __shfl_sync(0xffffffffu, pid_reg[1], jb & 31);
-        const int32_t pid = (jb >> 5) ? p1 : p0;
+        int32_t pid = -1;
+#pragma unroll
+        for (int h = 0; h < kPidRegs; ++h) {
+          const int32_t ph = __shfl_sync(0xffffffffu, pid_reg[h], jb & 31);
+          if ((jb >> 5) == h) pid = ph;
+        }
         const int t = tb + lane * box_rows;
         const bool in_tile = lane < boxes_per_tile;
         const bool page_ok = pid >= 0 && (int64_t)pid < a.kv.num_pages;
@@ -517,7 +548,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!wait_or_pv(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1)) { ok = false; break; }
         const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
         if (item >= n_items) break;
-        const TcItem it = tc_decode(item, s.pre, s.len, B, a);
+        const TcItem it = tc_decode(item, s.pre, s.len, B, a, split_len);
         if (!wait_or_pv(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1)) { ok = false; break; }
         const uint32_t qa = sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES;
         for (int k = 0; k < it.ntiles; ++k, ++i) {
@@ -571,7 +602,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TcItem it{};
     if (!wwait(bar_addr(s.item_full), 0, s.abort)) goto out;
     item = *reinterpret_cast<volatile int *>(s.items);
-    if (item < n_items) it = tc_decode(item, s.pre, s.len, B, a);
+    if (item < n_items) it = tc_decode(item, s.pre, s.len, B, a, split_len);
     for (;; ++jl) {
       if (item >= n_items) break;
       const int u = it.b * h_kv + it.g;
@@ -720,7 +751,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!wwait(bar_addr(s.item_full + nj % kTcItemRing), (nj / kTcItemRing) & 1, s.abort)) goto out;
       const int next_item = *reinterpret_cast<volatile int *>(s.items + nj % kTcItemRing);
       TcItem nx{};
-      if (next_item < n_items) nx = tc_decode(next_item, s.pre, s.len, B, a);
+      if (next_item < n_items) nx = tc_decode(next_item, s.pre, s.len, B, a, split_len);
       // Epilogue: O (high + residual columns) and the row sums -> the split's normalised partial.
       {
         if (!wwait(bar_addr(s.o_full), jl & 1, s.abort)) goto out;

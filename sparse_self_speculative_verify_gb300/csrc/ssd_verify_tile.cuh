@@ -41,6 +41,7 @@ struct VerifyArgs {
   unsigned *status;
   int *sched;  // [2] in the counter area: next-item counter and finished-block count (tensor-core
                // path); zero at launch, and the last block to finish returns both to zero
+  int *split_out;  // tensor-core path: receives the split length it chose (read by the finalize)
 };
 
 template <int D, int NRT>
@@ -59,7 +60,7 @@ struct VerifyMmaCfg {
 };
 
 // Number of work items (splits) of one unit.
-__device__ __forceinline__ int verify_splits(int L) { return cdiv(L, kSplitTokens); }
+__device__ __forceinline__ int verify_splits(int L, int split = kSplitTokens) { return cdiv(L, split); }
 __device__ __forceinline__ int block_splits(int ucnt) { return cdiv(ucnt, kBlocksPerItem); }
 
 template <int D, int NRT, bool BLOCKS>
@@ -462,6 +463,7 @@ struct FinalizeArgs {
   const __half *side_p;   // [units][R][Lpad]
   const float *side_m;    // [units][R][Lpad / kRefGroup]
   const int32_t *ucnt;    // block-sparse pass: splits per unit from the union size
+  const int *split_len;   // tensor-core verify: the split length it chose; nullptr = kSplitTokens
   const uint8_t *phase;   // unified launch: units of draft-phase requests are skipped
   int umax;
   float *out;
