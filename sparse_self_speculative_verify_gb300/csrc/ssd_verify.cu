@@ -43,41 +43,101 @@ __global__ void __launch_bounds__(128) verify_simt_kernel(VerifyArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Finalize: grid (n_tok + n_comb, unit).  Every block first merges the unit's split LSEs per row
-// (one warp per row, lanes over splits); blocks x >= n_tok combine the split outputs of kFinRows
-// rows each (one float4 of d per thread, splits unrolled), blocks x < n_tok rematerialise the
-// criticality of kFinTok tokens each: crit[t] = sum_r e[r][t] * 2^(m_ref[r][t/16] - LSE2_r).
+// Finalize: grid (n_tok + n_comb, unit).  Every block merges the unit's split LSEs per row (one warp
+// per row, lanes over splits); blocks x >= n_tok combine the split outputs of kFinRows rows each
+// (one float4 of d per thread, splits unrolled), blocks x < n_tok rematerialise the criticality of
+// kFinTok tokens each: crit[t] = sum_r e[r][t] * 2^(m_ref[r][t/16] - LSE2_r).  A token block past
+// the unit's length exits first; the others issue their first kFinAhead rows of side values and
+// their reference values before the LSE merge (neither depends on it), so one memory latency
+// covers the merge, the references and the first rows.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ int fin_rows_per_cta(int D) { return kFinThreads / (D / 4); }
+
+constexpr int kFinAhead = 5;  // side-value rows loaded per batch
+
+__device__ __forceinline__ void fin_fma_row(const uint4 &raw, float c, float (&acc)[8]) {
+  const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 pf = __half22float2(h2[k]);
+    acc[2 * k] = fmaf(pf.x, c, acc[2 * k]);
+    acc[2 * k + 1] = fmaf(pf.y, c, acc[2 * k + 1]);
+  }
+}
 
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, int n_tok) {
   __shared__ float sLn[kMaxRows];
   __shared__ float sL2[kMaxRows];
+  __shared__ __align__(16) float s_coef[kMaxRows * kFinGroups];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = blockIdx.y, b = u / f.h_kv, g = u % f.h_kv;
   if (f.phase && f.phase[b] == 0) return;
   int L = f.seq_lens[b];
   L = L < 0 ? 0 : (L > f.max_seq_len ? f.max_seq_len : L);
+  const bool tok = (int)blockIdx.x < n_tok;
+  const int tb0 = blockIdx.x * kFinTok;
+  if (tok && (!f.side_p || tb0 >= L)) return;
   const int ns = f.ucnt ? block_splits(min(max(f.ucnt[u], 0), f.umax))
                         : verify_splits(L, f.split_len ? *f.split_len : kSplitTokens);
   const int64_t pbase = (int64_t)u * f.S_max * f.R;
-  for (int r = warp; r < f.R; r += kFinThreads / 32) {
-    float M = -INFINITY;
-    for (int j = lane; j < ns; j += 32) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
-    M = warp_max(M);
-    float s = 0.f;
-    if (M != -INFINITY)
-      for (int j = lane; j < ns; j += 32) s += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
-    s = warp_sum(s);
-    if (lane == 0) {
-      float ln = (M == -INFINITY) ? -INFINITY : M + __logf(s);
-      sLn[r] = ln;
-      sL2[r] = ln * kLog2e;
+  const int64_t rbase = (int64_t)u * f.R;
+  const int nref = f.Lpad / kRefGroup;
+
+  // Early loads of a token block: its first rows of side values and its reference values.
+  const int t0 = tb0 + tid * 8;
+  const bool valid = tok && t0 < L;
+  const bool fast = tok && f.bscores == nullptr;
+  const __half *sp = tok ? f.side_p + rbase * f.Lpad + t0 : nullptr;
+  uint4 raw[kFinAhead];
+  if (fast) {
+#pragma unroll
+    for (int k = 0; k < kFinAhead; ++k)
+      raw[k] = (valid && k < f.R) ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)k * f.Lpad)) : make_uint4(0, 0, 0, 0);
+  }
+  if (tok) {
+    // References straight into the coefficient table (16 bytes = 4 groups per copy; a row's
+    // references start 16-byte aligned since Lpad is a multiple of 128 tokens).  Groups at or past
+    // L are not fetched: no stored score reads their coefficient.
+    for (int e = tid; e < f.R * (kFinGroups / 4); e += kFinThreads) {
+      const int r = e / (kFinGroups / 4), j4 = (e % (kFinGroups / 4)) * 4;
+      if (tb0 + j4 * kRefGroup < L)
+        cp_async16(smem_u32(s_coef + r * kFinGroups + j4), f.side_m + (rbase + r) * nref + tb0 / kRefGroup + j4, 16);
+    }
+    cp_async_commit();
+  }
+
+  // LSE merge: warp w takes rows w, w + kFinWarps, ...; lane j holds split j (a loop when ns > 32).
+  {
+    constexpr int kFinWarps = kFinThreads / 32;
+    float v[kMaxRows / kFinWarps];
+#pragma unroll
+    for (int q = 0; q < kMaxRows / kFinWarps; ++q) {
+      const int r = warp + kFinWarps * q;
+      v[q] = (r < f.R && lane < ns) ? f.lse_parts[pbase + (int64_t)lane * f.R + r] : -INFINITY;
+    }
+#pragma unroll
+    for (int q = 0; q < kMaxRows / kFinWarps; ++q) {
+      const int r = warp + kFinWarps * q;
+      if (r >= f.R) break;
+      float M = v[q];
+      for (int j = lane + 32; j < ns; j += 32) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
+      M = warp_max(M);
+      float sum = 0.f;
+      if (M != -INFINITY) {
+        sum = lane < ns ? fast_exp2((v[q] - M) * kLog2e) : 0.f;
+        for (int j = lane + 32; j < ns; j += 32) sum += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) {
+        const float ln = (M == -INFINITY) ? -INFINITY : M + __logf(sum);
+        sLn[r] = ln;
+        sL2[r] = ln * kLog2e;
+      }
     }
   }
   __syncthreads();
 
-  if ((int)blockIdx.x >= n_tok) {
+  if (!tok) {
     const int D = f.D, tpr = D / 4, rpc = fin_rows_per_cta(D);
     const int r = ((int)blockIdx.x - n_tok) * rpc + tid / tpr, q4 = tid % tpr;
     if (r >= f.R) return;
@@ -103,57 +163,40 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     if (q4 == 0 && f.lse) f.lse[row] = ln;
     return;
   }
-  if (!f.side_p) return;
 
-  // Criticality: eight consecutive tokens per thread.  coef[r][j] = 2^(m_ref[r][group j] - LSE2_r)
-  // for the kFinGroups 16-token groups of this block, then crit[t] = sum_r e[r][t] * coef[r][t/16].
-  const int tb0 = blockIdx.x * kFinTok;
-  if (tb0 >= L) return;
-  __shared__ float s_coef[kMaxRows * kFinGroups];
-  const int nref = f.Lpad / kRefGroup;
-  const int64_t rbase = (int64_t)u * f.R;
+  // Criticality: coef[r][j] = 2^(m_ref[r][group j] - LSE2_r) for the kFinGroups 16-token groups of
+  // this block, then crit[t] = sum_r e[r][t] * coef[r][t/16], eight consecutive tokens per thread.
+  cp_async_wait<0>();
+  __syncthreads();
   for (int e = tid; e < f.R * kFinGroups; e += kFinThreads) {
-    const int r = e / kFinGroups, j = e % kFinGroups;
-    if (tb0 + j * kRefGroup >= L) continue;
-    const float l2 = sL2[r];
-    const float ref = f.side_m[(rbase + r) * nref + tb0 / kRefGroup + j];
-    s_coef[r * kFinGroups + j] = (l2 == -INFINITY) ? 0.f : fast_exp2(ref - l2);
+    const float l2 = sL2[e / kFinGroups];
+    s_coef[e] = (l2 == -INFINITY) ? 0.f : fast_exp2(s_coef[e] - l2);
   }
   __syncthreads();
-  const int t0 = tb0 + tid * 8;
-  const bool valid = t0 < L;
   const int grp = tid >> 1;  // 8 tokens = half a 16-token group
-  const __half *sp = f.side_p + rbase * f.Lpad + t0;
   float crit[8], cc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) crit[k] = cc[k] = 0.f;
-  if (f.bscores == nullptr) {
-#pragma unroll 4
-    for (int r = 0; r < f.R; ++r) {
-      const uint4 raw = valid ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad)) : make_uint4(0, 0, 0, 0);
-      const float c = s_coef[r * kFinGroups + grp];
-      const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+  if (fast) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 pf = __half22float2(h2[k]);
-        crit[2 * k] = fmaf(pf.x, c, crit[2 * k]);
-        crit[2 * k + 1] = fmaf(pf.y, c, crit[2 * k + 1]);
-      }
+    for (int k = 0; k < kFinAhead; ++k)
+      if (k < f.R) fin_fma_row(raw[k], s_coef[k * kFinGroups + grp], crit);
+    for (int r0 = kFinAhead; r0 < f.R; r0 += kFinAhead) {
+#pragma unroll
+      for (int k = 0; k < kFinAhead; ++k)
+        raw[k] = (valid && r0 + k < f.R) ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)(r0 + k) * f.Lpad))
+                                         : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int k = 0; k < kFinAhead; ++k)
+        if (r0 + k < f.R) fin_fma_row(raw[k], s_coef[(r0 + k) * kFinGroups + grp], crit);
     }
   } else {
     for (int i = 0; i < f.n_c; ++i) {
 #pragma unroll 4
       for (int hl = 0; hl < f.G; ++hl) {
         const int r = i * f.G + hl;
-        const uint4 raw = valid ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad)) : make_uint4(0, 0, 0, 0);
-        const float c = s_coef[r * kFinGroups + grp];
-        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 pf = __half22float2(h2[k]);
-          cc[2 * k] = fmaf(pf.x, c, cc[2 * k]);
-          cc[2 * k + 1] = fmaf(pf.y, c, cc[2 * k + 1]);
-        }
+        const uint4 rw = valid ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad)) : make_uint4(0, 0, 0, 0);
+        fin_fma_row(rw, s_coef[r * kFinGroups + grp], cc);
       }
       // Candidate i's block maximum: 64 tokens = 8 lanes x 8 tokens.
       float m = cc[0];
