@@ -51,6 +51,36 @@ class SpecRound:
                                 out=out if out is not None else self.out_d, lse=self.lse_d, workspace=self.ws,
                                 stream=stream)
 
+    def draft_oracle_topk(self, q_draft: torch.Tensor, k_per_req: torch.Tensor, out: Optional[torch.Tensor] = None,
+                          stream=None) -> dict:
+        """Draft with the "oracle top-k" pattern (SparseSpec §3.3, the reference the pages measure
+        drafts against): the draft query selects by its own exact criticality instead of by the last
+        verify's.  Three calls: a verify pass with the draft query as the single candidate (it sees
+        the whole cache) gives that criticality and the dense output; Top-K selects K_b tokens per
+        (request, KV head); the sparse draft attends them.  Buffers are allocated on first use.
+        Returns the sparse draft's ``out`` / ``lse`` plus ``dense`` (the full-attention output) and
+        the selection ``idx`` / ``cnt``."""
+        kv = self.kv
+        Bsz, hkv, d = kv.batch, kv.h_kv, kv.d
+        if not hasattr(self, "_o_scores"):
+            dev = kv.device
+            self._o_dense = torch.empty((Bsz, 1, self.h_q, d), dtype=torch.float32, device=dev)
+            self._o_lse = torch.empty((Bsz, 1, self.h_q), dtype=torch.float32, device=dev)
+            self._o_scores = torch.zeros((Bsz, hkv, max(kv.max_seq_len, 1)), dtype=torch.float32, device=dev)
+            self._o_idx = torch.empty((Bsz * hkv, self.k_max), dtype=torch.int32, device=dev)
+            self._o_cnt = torch.empty((Bsz * hkv,), dtype=torch.int32, device=dev)
+            self._o_out = torch.empty((Bsz, self.h_q, d), dtype=torch.float32, device=dev)
+            self._o_lse_d = torch.empty((Bsz, self.h_q), dtype=torch.float32, device=dev)
+        B.ssd_verify_attn(kv, q_draft.view(Bsz, 1, self.h_q, d), 1, self.scale, out=self._o_dense, lse=self._o_lse,
+                          scores=self._o_scores, workspace=self.ws, stream=stream)
+        B.ssd_select_topk(self._o_scores, kv.seq_lens, k_per_req, self.k_max, hkv, max_len=kv.max_seq_len,
+                          idx=self._o_idx, cnt=self._o_cnt, stream=stream)
+        o = out if out is not None else self._o_out
+        B.ssd_draft_attn(kv, q_draft, self._o_idx.view(Bsz, hkv, self.k_max), self._o_cnt.view(Bsz, hkv), self.scale,
+                         out=o, lse=self._o_lse_d, workspace=self.ws, stream=stream)
+        return {"out": o, "lse": self._o_lse_d, "dense": self._o_dense.view(Bsz, self.h_q, d),
+                "scores": self._o_scores, "idx": self._o_idx, "cnt": self._o_cnt}
+
     def run(self, q_verify: torch.Tensor, q_drafts: torch.Tensor, k_per_req: torch.Tensor,
             draft_outs: Optional[torch.Tensor] = None, stream=None):
         """verify -> select -> len(q_drafts) drafts.  draft_outs [k, B, h_q, d] keeps every draft's

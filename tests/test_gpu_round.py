@@ -85,3 +85,49 @@ def test_round_graph_replay_matches_eager():
     assert torch.equal(rnd.scores, eager[1])
     assert torch.equal(rnd.idx, eager[2])
     assert torch.equal(outs, eager[3])
+
+
+def _oracle_topk_case(lengths, seed, select_all=False):
+    spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="otk", batch=len(lengths))
+    w = W.make_workload(spec, seed=seed, device=DEV, lengths=lengths)
+    _gpu.lib()
+    kv = KVCache.from_workload(w)
+    scale = _gpu.scale_of(spec)
+    kpr = w.seq_lens.clone() if select_all else w.k_per_req
+    k_max = int(kpr.max())
+    rnd = SpecRound(kv, spec.h_q, spec.n_cand, k_max, scale)
+    qd = w.q_draft[0]
+    r = rnd.draft_oracle_topk(qd, kpr)
+    torch.cuda.synchronize()
+    assert ssd_status() == 0
+    kv_h, _ = _gpu.host_subset(w)
+    return spec, w, kv_h, scale, kpr.cpu().numpy(), k_max, r
+
+
+def test_oracle_topk_draft_matches_oracle():
+    """'Oracle top-k' draft: the draft query's own criticality (a verify with one candidate, which
+    sees the whole cache) selects its tokens.  Dense output and scores against the oracle's, the
+    selection bit-exact against the oracle's Top-K of the GPU's scores, the sparse output against
+    the oracle draft on that selection."""
+    spec, w, kv_h, scale, kpr, k_max, r = _oracle_topk_case([3000, 1029, 4500], 21)
+    qd = w.q_draft[0].cpu()
+    ref = oracle.verify(kv_h, qd[:, None], scale)
+    lens = kv_h.seq_lens
+    _gpu.assert_out(r["dense"].cpu().numpy(), ref["out"][:, 0], "dense")
+    _gpu.assert_scores(r["scores"].cpu().numpy(), ref["crit"], lens)
+    S = r["scores"].cpu().numpy()
+    oidx, ocnt = oracle.topk(S.reshape(-1, S.shape[-1]), lens, kpr, k_max, rows_per_group=spec.h_kv)
+    np.testing.assert_array_equal(r["idx"].cpu().numpy(), oidx)
+    np.testing.assert_array_equal(r["cnt"].cpu().numpy(), ocnt)
+    # The selection is also a valid Top-K of the oracle's own scores.
+    _gpu.assert_valid_topk(oidx, ocnt, ref["crit"].reshape(-1, ref["crit"].shape[-1]), kpr, lens, spec.h_kv)
+    B = spec.batch
+    dref = oracle.draft(kv_h, qd, oidx.reshape(B, spec.h_kv, k_max), ocnt.reshape(B, spec.h_kv), scale)
+    _gpu.assert_out(r["out"].cpu().numpy(), dref["out"], "oracle top-k draft")
+
+
+def test_oracle_topk_draft_selecting_all_is_dense():
+    """With K_b = L_b every token is selected, so the sparse draft equals the dense attention."""
+    spec, w, kv_h, scale, kpr, k_max, r = _oracle_topk_case([700, 129, 1500], 22, select_all=True)
+    assert r["cnt"].cpu().numpy().tolist() == np.repeat(kpr, spec.h_kv).tolist()
+    _gpu.assert_out(r["out"].cpu().numpy(), r["dense"].cpu().numpy(), "select-all draft vs dense")
