@@ -135,6 +135,20 @@ int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, 
                     ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Verify with the selection fused into its criticality pass (SparseSpec §4.1: Top-K is applied to
+ * the scores the verify dumps; fusing removes the separate select launch and its read of the
+ * scores).  Same arguments and results as ssd_verify_attn with scores (no block scores), plus the
+ * Top-K that ssd_select_topk(scores, scores_stride, seq_lens, ks, batch, h_kv, 1, max_seq_len, idx,
+ * k_max, cnt) would write: ks is device int32 [batch] (K per request), idx device int32
+ * [batch][h_kv][k_max] (ascending, -1 padded), cnt device int32 [batch][h_kv]; K > k_max raises
+ * SSD_FAULT_KMAX and keeps k_max.  The workspace is ssd_verify_workspace_bytes(kv, h_q, n_cand);
+ * batch * h_kv must be at most 65534 (its counters share the workspace's counter area).
+ */
+int ssd_verify_select(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
+                      float *lse, float *scores, int64_t scores_stride, const int32_t *ks, int32_t *idx, int k_max,
+                      int32_t *cnt, void *workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Top-K selection (SparseSpec §4.1: "Top-K on the dumped scores" gives the sparse pattern; §3.2,
  * §5.4: about 5% of the tokens).  Rows r = 0 .. n_groups*rows_per_group-1 of the score matrix
  * (device float, row stride `stride` elements) belong to group r / rows_per_group; row r has

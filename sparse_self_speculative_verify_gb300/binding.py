@@ -25,6 +25,7 @@ SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
 FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT, FAULT_VALUE = 1, 2, 4, 8, 16, 32, 64
 
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
+            "ssd_verify_select",
             "ssd_select_topk", "ssd_select_topp", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
             "ssd_unified_workspace_bytes", "ssd_kv_append", "ssd_kv_advance", "ssd_phase_assign", "ssd_phase_fill",
             "ssd_unified_attn", "ssd_block_union", "ssd_block_sparse_workspace_bytes", "ssd_block_sparse_attn",
@@ -74,6 +75,7 @@ def load(path: Optional[str] = None):
             "ssd_status": ([P, ctypes.POINTER(ctypes.c_uint32)], I),
             "ssd_verify_workspace_bytes": ([KV, I, I], S),
             "ssd_verify_attn": ([KV, P, I, I, F, P, P, P, I64, P, I64, I, P, S, P], I),
+            "ssd_verify_select": ([KV, P, I, I, F, P, P, P, I64, P, P, I, P, P, S, P], I),
             "ssd_select_topk": ([P, I64, P, P, I, I, I, I, P, I, P, P], I),
             "ssd_select_topp": ([P, I64, P, F, I, I, I, I, P, I, P, P, P], I),
             "ssd_draft_workspace_bytes": ([KV, I, I], S),
@@ -256,6 +258,38 @@ def ssd_verify_attn(kv: KVCache, q: torch.Tensor, n_cand: int, scale: float, *, 
                              bscores.shape[-1] if bscores is not None else 0, block_size, wsp, avail,
                              _stream(stream)))
     return {"out": out, "lse": lse, "scores": scores, "bscores": bscores}
+
+
+def ssd_verify_select(kv: KVCache, q: torch.Tensor, n_cand: int, scale: float, ks: torch.Tensor, k_max: int, *,
+                      out=None, lse=None, scores=None, idx=None, cnt=None, want_lse: bool = True,
+                      workspace: Optional[Workspace] = None, stream=None) -> dict:
+    """Verify with the Top-K selection fused into its criticality pass.  q [B, n_cand, h_q, d];
+    ks [B] int32 (K per request); idx [B * h_kv, k_max], cnt [B * h_kv]."""
+    _need(q, "q", kv.pool.dtype, kv.device)
+    B, nc, h_q, d = q.shape
+    assert nc == n_cand and B == kv.batch and d == kv.d
+    dev = kv.device
+    _need(ks, "ks", torch.int32, dev)
+    if out is None:
+        out = torch.empty((B, nc, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, nc, h_q), dtype=torch.float32, device=dev)
+    if scores is None:
+        scores = torch.zeros((B, kv.h_kv, max(kv.max_seq_len, 1)), dtype=torch.float32, device=dev)
+    if idx is None:
+        idx = torch.empty((B * kv.h_kv, max(k_max, 0)), dtype=torch.int32, device=dev)
+    if cnt is None:
+        cnt = torch.empty((B * kv.h_kv,), dtype=torch.int32, device=dev)
+    for t, n, dt in ((out, "out", torch.float32), (lse, "lse", torch.float32), (scores, "scores", torch.float32),
+                     (idx, "idx", torch.int32), (cnt, "cnt", torch.int32)):
+        if t is not None:
+            _need(t, n, dt, dev)
+    L = _lib()
+    need = L.ssd_verify_workspace_bytes(kv.ref(), h_q, n_cand)
+    wsp, avail = _ws(dev, "verify", need, workspace)
+    _check(L.ssd_verify_select(kv.ref(), _ptr(q), h_q, n_cand, float(scale), _ptr(out), _ptr(lse), _ptr(scores),
+                               scores.shape[-1], _ptr(ks), _ptr(idx), k_max, _ptr(cnt), wsp, avail, _stream(stream)))
+    return {"out": out, "lse": lse, "scores": scores, "idx": idx, "cnt": cnt}
 
 
 def ssd_select_topk(scores: torch.Tensor, lens: torch.Tensor, ks: torch.Tensor, k_max: int, rows_per_group: int,

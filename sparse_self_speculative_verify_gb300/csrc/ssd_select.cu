@@ -7,54 +7,17 @@
 // and the hierarchical layout representation: the candidates' block sets are merged into one
 // ordered union with a per-block candidate mask.
 //
-// Selection is an exact radix select on the order-preserving 32-bit key of each fp32 score (four
-// 8-bit MSB-first histogram passes find the K-th largest key tau), followed by a stream compaction
-// in index order that keeps every key > tau and the lowest-index keys == tau until K are kept, so
-// ties go to the lower index and the output comes out sorted.
+// One block selects one row with topk_row (ssd_topk.cuh: exact radix select, ties to the lower
+// index, output sorted).
 #include "ssd_host.h"
+#include "ssd_topk.cuh"
 
 namespace ssd {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelItems = 4;
 constexpr int kSelTile = kSelThreads * kSelItems;
 constexpr int kSelSmemRow = 40960;  // rows up to this length are staged in shared memory
-
-// Order-preserving key: unsigned order of the keys = numeric order of the floats; -0.0 == +0.0.
-__device__ __forceinline__ uint32_t score_key(float x) {
-  uint32_t u = __float_as_uint(x);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Exclusive block-wide prefix sum of one value per thread; *total receives the sum.
-__device__ __forceinline__ int block_excl_scan(int v, int *s_warp, int *s_total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kSelWarps ? s_warp[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += t;
-    }
-    if (lane < kSelWarps) s_warp[lane] = wi - w;
-    if (lane == kSelWarps - 1) *s_total = wi;
-  }
-  __syncthreads();
-  int res = s_warp[warp] + incl - v;
-  __syncthreads();
-  return res;
-}
 
 struct TopkArgs {
   const float *scores;
@@ -72,13 +35,8 @@ struct TopkArgs {
 template <bool IN_SMEM>
 __global__ void __launch_bounds__(kSelThreads) topk_kernel(TopkArgs p) {
   extern __shared__ uint32_t s_keys[];
-  __shared__ uint32_t s_hist[kSelWarps][256];
-  __shared__ uint32_t s_tot[256];
-  __shared__ int s_warp[kSelWarps];
-  __shared__ int s_total;
-  __shared__ uint32_t s_digit;
-  __shared__ int s_rem;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ TopkScratch<kSelThreads> sc;
+  const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
   const int grp = (int)(row / p.rows_per_group);
   int raw_len = p.lens[grp];
@@ -101,106 +59,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(TopkArgs p) {
   }
   auto key = [&](int t) -> uint32_t { return IN_SMEM ? s_keys[t] : score_key(__ldg(src + t)); };
 
-  if (K == n) {
-    for (int t = tid; t < n; t += kSelThreads) out[t] = t;
-  } else if (K > 0) {
-    uint32_t prefix = 0, mask = 0;
-    int rem = K;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      for (int e = tid; e < kSelWarps * 256; e += kSelThreads) (&s_hist[0][0])[e] = 0u;
-      __syncthreads();
-      for (int t = tid; t < n; t += kSelThreads) {
-        uint32_t k = key(t);
-        if ((k & mask) == prefix) atomicAdd(&s_hist[warp][(k >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      if (tid < 256) {
-        uint32_t s = 0;
-#pragma unroll
-        for (int w = 0; w < kSelWarps; ++w) s += s_hist[w][tid];
-        s_tot[tid] = s;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // Lane l owns bins 255-8l .. 248-8l (descending).
-        uint32_t c[8];
-        uint32_t sum = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          c[j] = s_tot[255 - 8 * lane - j];
-          sum += c[j];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        const uint32_t excl = incl - sum;
-        unsigned hit = __ballot_sync(0xffffffffu, incl >= (uint32_t)rem);
-        int f = __ffs(hit) - 1;
-        if (lane == f) {
-          uint32_t run = excl;
-          for (int j = 0; j < 8; ++j) {
-            if (run + c[j] >= (uint32_t)rem) {
-              s_digit = 255u - 8u * lane - j;
-              s_rem = rem - (int)run;
-              break;
-            }
-            run += c[j];
-          }
-        }
-      }
-      __syncthreads();
-      prefix |= s_digit << shift;
-      mask |= 0xffu << shift;
-      rem = s_rem;
-      __syncthreads();
-    }
-    const uint32_t tau = prefix;
-    const int need_eq = rem;
-    int base_eq = 0, base_sel = 0;
-    for (int start = 0; start < n; start += kSelTile) {
-      const int t_first = start + tid * kSelItems;
-      uint32_t kk[kSelItems];
-      int c_eq = 0;
-#pragma unroll
-      for (int e = 0; e < kSelItems; ++e) {
-        int t = t_first + e;
-        kk[e] = t < n ? key(t) : 0u;
-        c_eq += (t < n && kk[e] == tau) ? 1 : 0;
-      }
-      const int ex_eq = block_excl_scan(c_eq, s_warp, &s_total);
-      const int tot_eq = s_total;
-      int run = base_eq + ex_eq;
-      unsigned sel = 0;
-#pragma unroll
-      for (int e = 0; e < kSelItems; ++e) {
-        int t = t_first + e;
-        if (t < n) {
-          if (kk[e] == tau) {
-            if (run < need_eq) sel |= 1u << e;
-            ++run;
-          } else if (kk[e] > tau) {
-            sel |= 1u << e;
-          }
-        }
-      }
-      const int ex_sel = block_excl_scan(__popc(sel), s_warp, &s_total);
-      const int tot_sel = s_total;
-      int pos = base_sel + ex_sel;
-#pragma unroll
-      for (int e = 0; e < kSelItems; ++e)
-        if ((sel >> e) & 1u) {
-          if (pos < K) out[pos] = t_first + e;
-          ++pos;
-        }
-      base_eq += tot_eq;
-      base_sel += tot_sel;
-    }
-  }
-  for (int j = K + tid; j < p.k_max; j += kSelThreads) out[j] = -1;
+  topk_row<kSelThreads>(key, n, K, out, p.k_max, sc);
   if (tid == 0) p.cnt[row] = K;
 }
 
@@ -433,7 +292,7 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(UnionArgs p) {
     int c = 0;
 #pragma unroll
     for (int e = 0; e < kSelItems; ++e) c += (j0 + e < p.nblk_max && s_mask[j0 + e]) ? 1 : 0;
-    int pos = base + block_excl_scan(c, s_warp, &s_total);
+    int pos = base + block_excl_scan<kSelWarps>(c, s_warp, &s_total);
     const int tot = s_total;
 #pragma unroll
     for (int e = 0; e < kSelItems; ++e) {

@@ -1,0 +1,175 @@
+// ssd_topk.cuh -- exact Top-K of one score row by one thread block (shared by the select kernels
+// and the finalize's fused selection).
+//
+// SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
+// Sparse Attention") §4.1: Top-K over the dumped, GQA-reduced verify scores gives the sparse pattern.
+// An exact radix select on the order-preserving 32-bit key of each fp32 score (four 8-bit MSB-first
+// histogram passes find the K-th largest key tau), then a stream compaction in index order that keeps
+// every key > tau and the lowest-index keys == tau until K are kept: ties go to the lower index and
+// the output comes out sorted.
+#pragma once
+
+#include "ssd_common.cuh"
+
+namespace ssd {
+
+constexpr int kSelItems = 4;
+
+// Order-preserving key: unsigned order of the keys = numeric order of the floats; -0.0 == +0.0.
+__device__ __forceinline__ uint32_t score_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive block-wide prefix sum of one value per thread; *total receives the sum.
+template <int NW>
+__device__ __forceinline__ int block_excl_scan(int v, int *s_warp, int *s_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NW ? s_warp[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    if (lane < NW) s_warp[lane] = wi - w;
+    if (lane == NW - 1) *s_total = wi;
+  }
+  __syncthreads();
+  int res = s_warp[warp] + incl - v;
+  __syncthreads();
+  return res;
+}
+
+// Scratch of topk_row for an NT-thread block.
+template <int NT>
+struct TopkScratch {
+  uint32_t hist[NT / 32][256];
+  uint32_t tot[256];
+  int warp[NT / 32];
+  int total;
+  uint32_t digit;
+  int rem;
+};
+
+// Writes the K (0 <= K <= n) largest of the n keys key(0..n-1) to out[0..K) in ascending index order
+// (equal keys toward the lower index) and -1 to out[K..k_max).  Every thread of the NT-thread block
+// calls it; `key` must give every thread the same value for the same index.
+template <int NT, typename KeyFn>
+__device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, int k_max, TopkScratch<NT> &sc) {
+  static_assert(NT >= 256 && NT % 32 == 0, "one thread per histogram bin");
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (K == n) {
+    for (int t = tid; t < n; t += NT) out[t] = t;
+  } else if (K > 0) {
+    uint32_t prefix = 0, mask = 0;
+    int rem = K;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int e = tid; e < NW * 256; e += NT) (&sc.hist[0][0])[e] = 0u;
+      __syncthreads();
+      for (int t = tid; t < n; t += NT) {
+        uint32_t k = key(t);
+        if ((k & mask) == prefix) atomicAdd(&sc.hist[warp][(k >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid < 256) {
+        uint32_t s = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s += sc.hist[w][tid];
+        sc.tot[tid] = s;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // Lane l owns bins 255-8l .. 248-8l (descending).
+        uint32_t c[8];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = sc.tot[255 - 8 * lane - j];
+          sum += c[j];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const uint32_t excl = incl - sum;
+        unsigned hit = __ballot_sync(0xffffffffu, incl >= (uint32_t)rem);
+        int f = __ffs(hit) - 1;
+        if (lane == f) {
+          uint32_t run = excl;
+          for (int j = 0; j < 8; ++j) {
+            if (run + c[j] >= (uint32_t)rem) {
+              sc.digit = 255u - 8u * lane - j;
+              sc.rem = rem - (int)run;
+              break;
+            }
+            run += c[j];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= sc.digit << shift;
+      mask |= 0xffu << shift;
+      rem = sc.rem;
+      __syncthreads();
+    }
+    const uint32_t tau = prefix;
+    const int need_eq = rem;
+    int base_eq = 0, base_sel = 0;
+    for (int start = 0; start < n; start += NT * kSelItems) {
+      const int t_first = start + tid * kSelItems;
+      uint32_t kk[kSelItems];
+      int c_eq = 0;
+#pragma unroll
+      for (int e = 0; e < kSelItems; ++e) {
+        int t = t_first + e;
+        kk[e] = t < n ? key(t) : 0u;
+        c_eq += (t < n && kk[e] == tau) ? 1 : 0;
+      }
+      const int ex_eq = block_excl_scan<NW>(c_eq, sc.warp, &sc.total);
+      const int tot_eq = sc.total;
+      int run = base_eq + ex_eq;
+      unsigned sel = 0;
+#pragma unroll
+      for (int e = 0; e < kSelItems; ++e) {
+        int t = t_first + e;
+        if (t < n) {
+          if (kk[e] == tau) {
+            if (run < need_eq) sel |= 1u << e;
+            ++run;
+          } else if (kk[e] > tau) {
+            sel |= 1u << e;
+          }
+        }
+      }
+      const int ex_sel = block_excl_scan<NW>(__popc(sel), sc.warp, &sc.total);
+      const int tot_sel = sc.total;
+      int pos = base_sel + ex_sel;
+#pragma unroll
+      for (int e = 0; e < kSelItems; ++e)
+        if ((sel >> e) & 1u) {
+          if (pos < K) out[pos] = t_first + e;
+          ++pos;
+        }
+      base_eq += tot_eq;
+      base_sel += tot_sel;
+    }
+  }
+  for (int j = K + tid; j < k_max; j += NT) out[j] = -1;
+}
+
+}  // namespace ssd

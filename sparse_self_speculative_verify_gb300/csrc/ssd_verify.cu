@@ -9,6 +9,7 @@
 // sparse layouts overlap run together so shared KV blocks are loaded once.  SparDA §2: fine scores
 // are max-pooled onto the coarser selection grid.
 #include "ssd_host.h"
+#include "ssd_topk.cuh"
 #include "ssd_verify_tile.cuh"
 
 namespace ssd {
@@ -77,6 +78,10 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   const bool tok = (int)blockIdx.x < n_tok;
   const int tb0 = blockIdx.x * kFinTok;
   if (tok && (!f.side_p || tb0 >= L)) return;
+  if (f.ks && (int)blockIdx.x == n_tok && L == 0) {  // an empty row has no token block: select nothing
+    for (int j = tid; j < f.sel_kmax; j += kFinThreads) f.sel_idx[(int64_t)u * f.sel_kmax + j] = -1;
+    if (tid == 0) f.sel_cnt[u] = 0;
+  }
   const int ns = f.ucnt ? block_splits(min(max(f.ucnt[u], 0), f.umax))
                         : verify_splits(L, f.split_len ? *f.split_len : kSplitTokens);
   const int64_t pbase = (int64_t)u * f.S_max * f.R;
@@ -224,6 +229,31 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
         if (t0 + k < L) dst[k] = crit[k];
     }
   }
+  if (!f.ks) return;
+
+  // Fused selection: the last of the unit's token blocks to finish selects the unit's row (read
+  // back through L2; the other blocks' scores are visible after their fence and the ticket).
+  __threadfence();
+  __syncthreads();  // also: s_coef is free for the selection scratch
+  __shared__ unsigned s_sel_last;
+  if (tid == 0) s_sel_last = atomicAdd(f.sel_ctr + u, 1u) == (unsigned)(cdiv(L, kFinTok) - 1);
+  __syncthreads();
+  if (!s_sel_last) return;
+  __threadfence();
+  int K = f.ks[b];
+  K = K < 0 ? 0 : (K > L ? L : K);
+  if (K > f.sel_kmax) {
+    if (tid == 0) atomicOr(f.status, (unsigned)SSD_FAULT_KMAX);
+    K = f.sel_kmax;
+  }
+  const float *row = f.scores + (int64_t)u * f.scores_stride;
+  auto &sc = *reinterpret_cast<TopkScratch<kFinThreads> *>(s_coef);
+  topk_row<kFinThreads>([&](int t) -> uint32_t { return score_key(__ldcg(row + t)); }, L, K,
+                        f.sel_idx + (int64_t)u * f.sel_kmax, f.sel_kmax, sc);
+  if (tid == 0) {
+    f.sel_cnt[u] = K;
+    f.sel_ctr[u] = 0u;
+  }
 }
 
 int launch_finalize(const FinalizeArgs &f, int n_tok, int units, cudaStream_t st) {
@@ -342,11 +372,10 @@ extern "C" size_t ssd_verify_workspace_bytes(const ssd_paged_kv *kv, int h_q, in
   return verify_layout(kv, h_q, n_cand, cdiv(kv->max_seq_len, kSplitTokens)).total;
 }
 
-extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
-                               float *lse, float *scores, int64_t scores_stride, float *bscores,
-                               int64_t bscores_stride, int block_size, void *workspace, size_t workspace_bytes,
-                               ssd_stream_t stream) {
-  const char *who = "ssd_verify_attn";
+static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
+                       float *lse, float *scores, int64_t scores_stride, float *bscores, int64_t bscores_stride,
+                       int block_size, const int32_t *ks, int32_t *idx, int k_max, int32_t *cnt, void *workspace,
+                       size_t workspace_bytes, ssd_stream_t stream, const char *who) {
   KVView v;
   int rc = validate_kv(kv, &v, who);
   if (rc) return rc;
@@ -363,6 +392,12 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
     return fail(SSD_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", who, workspace_bytes, lay.total);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(SSD_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  if (ks) {
+    if (!scores || bscores) return fail(SSD_ERR_INVALID_ARG, "%s: needs scores and no block scores", who);
+    if (!cnt || (!idx && k_max > 0) || k_max < 0) return fail(SSD_ERR_INVALID_ARG, "%s: idx / cnt / k_max", who);
+    if ((int64_t)kv->batch * kv->h_kv > kCounterSlots - 2)
+      return fail(SSD_ERR_UNSUPPORTED, "%s: batch*h_kv above %d", who, kCounterSlots - 2);
+  }
   if (kv->batch == 0 || kv->max_seq_len == 0) return SSD_OK;
   unsigned *status = device_status();
   if (!status) return SSD_ERR_CUDA;
@@ -420,8 +455,32 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
   f.bscores = bscores;
   f.bstride = bscores_stride;
   f.split_len = tc ? a.split_out : nullptr;
+  f.ks = ks;
+  f.sel_idx = idx;
+  f.sel_cnt = cnt;
+  f.sel_kmax = k_max;
+  f.sel_ctr = reinterpret_cast<unsigned *>(ws + lay.ctr_off) + 2;  // slots 0-1: the tensor-core kernel
+  f.status = status;
   const int n_tok = crit ? cdiv(kv->max_seq_len, kFinTok) : 0;
   return launch_finalize(f, n_tok, lay.units, st);
+}
+
+extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
+                               float *lse, float *scores, int64_t scores_stride, float *bscores,
+                               int64_t bscores_stride, int block_size, void *workspace, size_t workspace_bytes,
+                               ssd_stream_t stream) {
+  return verify_call(kv, q, h_q, n_cand, scale, out, lse, scores, scores_stride, bscores, bscores_stride, block_size,
+                     nullptr, nullptr, 0, nullptr, workspace, workspace_bytes, stream, "ssd_verify_attn");
+}
+
+extern "C" int ssd_verify_select(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
+                                 float *lse, float *scores, int64_t scores_stride, const int32_t *ks, int32_t *idx,
+                                 int k_max, int32_t *cnt, void *workspace, size_t workspace_bytes,
+                                 ssd_stream_t stream) {
+  const char *who = "ssd_verify_select";
+  if (!ks) return fail(SSD_ERR_INVALID_ARG, "%s: ks must be non-NULL", who);
+  return verify_call(kv, q, h_q, n_cand, scale, out, lse, scores, scores_stride, nullptr, 0, kBlockTokens, ks, idx,
+                     k_max, cnt, workspace, workspace_bytes, stream, who);
 }
 
 extern "C" size_t ssd_block_sparse_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand, int umax) {

@@ -472,6 +472,14 @@ struct FinalizeArgs {
   int64_t scores_stride;
   float *bscores;
   int64_t bstride;
+  // Fused Top-K (nullptr ks: none): row u of the scores keeps K = min(ks[b], L_b) tokens, written
+  // as the select pass writes them (sel_idx [units][sel_kmax], sel_cnt [units]).
+  const int32_t *ks;
+  int32_t *sel_idx;
+  int32_t *sel_cnt;
+  int sel_kmax;
+  unsigned *sel_ctr;  // [units] arrivals of a unit's token blocks, in the counter area
+  unsigned *status;
 };
 constexpr int kFinThreads = 256;
 constexpr int kFinTok = kFinThreads * 8;  // eight consecutive tokens per thread

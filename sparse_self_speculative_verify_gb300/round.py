@@ -41,6 +41,12 @@ class SpecRound:
         return B.ssd_verify_attn(self.kv, q_verify, self.n_cand, self.scale, out=self.out_v, lse=self.lse_v,
                                  scores=self.scores, workspace=self.ws, stream=stream)
 
+    def verify_select(self, q_verify: torch.Tensor, k_per_req: torch.Tensor, stream=None):
+        """verify + select in one call: the selection runs inside the criticality pass."""
+        return B.ssd_verify_select(self.kv, q_verify, self.n_cand, self.scale, k_per_req, self.k_max, out=self.out_v,
+                                   lse=self.lse_v, scores=self.scores, idx=self.idx, cnt=self.cnt, workspace=self.ws,
+                                   stream=stream)
+
     def select(self, k_per_req: torch.Tensor, stream=None):
         return B.ssd_select_topk(self.scores, self.kv.seq_lens, k_per_req, self.k_max, self.kv.h_kv,
                                  max_len=self.kv.max_seq_len, idx=self.idx, cnt=self.cnt, stream=stream)
@@ -82,10 +88,14 @@ class SpecRound:
                 "scores": self._o_scores, "idx": self._o_idx, "cnt": self._o_cnt}
 
     def run(self, q_verify: torch.Tensor, q_drafts: torch.Tensor, k_per_req: torch.Tensor,
-            draft_outs: Optional[torch.Tensor] = None, stream=None):
+            draft_outs: Optional[torch.Tensor] = None, stream=None, fused_select: bool = False):
         """verify -> select -> len(q_drafts) drafts.  draft_outs [k, B, h_q, d] keeps every draft's
-        output (else each overwrites ``out_d``)."""
-        self.verify(q_verify, stream)
-        self.select(k_per_req, stream)
+        output (else each overwrites ``out_d``).  fused_select runs the selection inside the verify's
+        criticality pass (one launch fewer, same results)."""
+        if fused_select:
+            self.verify_select(q_verify, k_per_req, stream)
+        else:
+            self.verify(q_verify, stream)
+            self.select(k_per_req, stream)
         for j in range(q_drafts.shape[0]):
             self.draft(q_drafts[j], out=None if draft_outs is None else draft_outs[j], stream=stream)

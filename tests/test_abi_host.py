@@ -83,6 +83,18 @@ def test_verify_argument_errors(lib, name, over, code):
     assert lib.ssd_last_error()
 
 
+def test_verify_select_argument_errors(lib):
+    kv = _kv()
+    E = binding.SSD_ERR_INVALID_ARG
+
+    def call(**o):
+        return lib.ssd_verify_select(ctypes.byref(kv), 4096, 32, 5, 0.1, 8192, None, o.get("scores", 4096),
+                                     o.get("stride", 1 << 16), o.get("ks", 64), o.get("idx", 128), o.get("k_max", 4),
+                                     o.get("cnt", 256), 1 << 20, 1 << 40, None)
+    for over in (dict(ks=None), dict(scores=None), dict(cnt=None), dict(idx=None), dict(k_max=-1), dict(stride=1)):
+        assert call(**over) == E, (over, lib.ssd_last_error())
+
+
 def test_select_argument_errors(lib):
     assert lib.ssd_select_topk(None, 10, 1, 1, 1, 1, 1, 10, 1, 4, 1, None) == binding.SSD_ERR_INVALID_ARG
     assert lib.ssd_select_topk(4096, 5, 16, 16, 1, 1, 1, 10, 64, 4, 64, None) == binding.SSD_ERR_INVALID_ARG
