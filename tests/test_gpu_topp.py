@@ -167,3 +167,31 @@ def test_topp_argument_errors():
             ssd_select_topp(s, lens, bad_p, 4, 1)
     with pytest.raises(binding.SSDError):
         ssd_select_topp(s, lens, 0.5, 4, 1, max_len=11)
+
+
+def test_topp_full_size_on_verify_scores():
+    """The full-size Qwen3-8B verify's criticality rows (32 requests x 8 KV heads, up to 8192 tokens),
+    selected at p = 0.9 in the launch the round would use; sampled rows against the oracle."""
+    _gpu.lib()
+    from sparse_self_speculative_verify_gb300 import KVCache, ssd_verify_attn
+    spec = W.SPECS["qwen3_8b"]
+    w = W.make_workload(spec, device=DEV)
+    kv = KVCache.from_workload(w)
+    r = ssd_verify_attn(kv, w.q_verify, spec.n_cand, _gpu.scale_of(spec))
+    k_max = kv.max_seq_len
+    p32 = float(np.float32(0.9))
+    gi, gc, gk = ssd_select_topp(r["scores"], kv.seq_lens, p32, k_max, spec.h_kv, max_len=kv.max_seq_len)
+    torch.cuda.synchronize()
+    assert ssd_status() == 0
+    S = r["scores"].view(-1, r["scores"].shape[-1]).cpu().numpy()
+    lens = np.repeat(kv.seq_lens.cpu().numpy(), spec.h_kv)
+    rows = [0, 7, 77, 130, 255]
+    sub = S[rows]
+    _, _, ok_k = oracle.topp(sub, lens[rows], p32, k_max)
+    gk, gc, gi = gk.cpu().numpy(), gc.cpu().numpy(), gi.cpu().numpy()
+    for n, rr in enumerate(rows):
+        if ok_k[n] != gk[rr]:
+            assert _count_ok(sub[n, :lens[rr]], p32, int(gk[rr]), k_max), (rr, int(gk[rr]), int(ok_k[n]))
+    oi, oc = oracle.topk(sub, lens[rows], gk[rows], k_max)
+    np.testing.assert_array_equal(gc[rows], oc)
+    np.testing.assert_array_equal(gi[rows], oi)
