@@ -115,16 +115,66 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     cp_async16(smem_u32(sVt + off), kr ? (const void *)(kr + v_off + ch * EPC) : a.kv.pool, kr ? 16 : 0);
   }
   cp_async_commit();
+  // bf16 caches: logits and P V on tensor cores (mma.sync m16n8k16, fp32 accumulate); the queries
+  // stay in registers as B fragments, P goes through bf16 high + residual parts (about 16 bits).
+  constexpr bool TC = sizeof(T) == 2;
+  constexpr int NT8 = (GMAX + 7) / 8;  // 8-wide head tiles
+  constexpr int KS = D / 16;           // 16-wide steps over d
   const T *q = reinterpret_cast<const T *>(a.q);
-  for (int e = tid; e < G * D; e += blockDim.x) {
-    int hl = e / D, dd = e % D;
-    sQ[e] = to_f32<T>(q[((int64_t)b * a.h_q + g * G + hl) * D + dd]);
+  uint32_t qb[TC ? NT8 : 1][TC ? KS : 1][2];
+  if constexpr (TC) {
+    // B fragment of Q^T: head n = 8 nt + lane / 4, dims k0, k0 + 1 and k0 + 8, k0 + 9.
+    const unsigned short *q16 = reinterpret_cast<const unsigned short *>(a.q);
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+      const int hn = nt * 8 + (lane >> 2);
+      const unsigned short *qr = q16 + ((int64_t)b * a.h_q + g * G + (hn < G ? hn : 0)) * D + (lane & 3) * 2;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t v0 = 0, v1 = 0;
+        if (hn < G) {
+          v0 = (uint32_t)__ldg(qr + ks * 16) | ((uint32_t)__ldg(qr + ks * 16 + 1) << 16);
+          v1 = (uint32_t)__ldg(qr + ks * 16 + 8) | ((uint32_t)__ldg(qr + ks * 16 + 9) << 16);
+        }
+        qb[nt][ks][0] = v0;
+        qb[nt][ks][1] = v1;
+      }
+    }
+  } else {
+    for (int e = tid; e < G * D; e += blockDim.x) {
+      int hl = e / D, dd = e % D;
+      sQ[e] = to_f32<T>(q[((int64_t)b * a.h_q + g * G + hl) * D + dd]);
+    }
   }
   cp_async_wait<0>();
   __syncthreads();
 
-  // Logits: thread pair (2j, 2j+1) computes token j, one half of d each.
-  {
+  if constexpr (TC) {
+    // S^T = K Q^T: warp w takes tokens 16w .. 16w + 15; A fragments by ldmatrix from the swizzled K
+    // tile (thread t addresses row (t & 7) + 8 ((t >> 3) & 1), 16-byte chunk 2 ks + (t >> 4)).
+    float acc[NT8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const int ar = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int ch = 2 * ks + (lane >> 4);
+      uint32_t af[4];
+      ldsm_x4(smem_u32(sKt + ar * C::ROWB + swz_chunk(ar, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt) mma_bf16(acc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+    }
+    // c0, c1: token 16w + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3: token + 8.
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = warp * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
+        if (h < G) sS[h * kDraftChunk + j] = (j < n) ? acc[nt][e] * a.scale_log2 : -INFINITY;
+      }
+    }
+  } else {
+    // Logits: thread pair (2j, 2j+1) computes token j, one half of d each.
     const int j = tid >> 1, half = tid & 1;
     float acc[GMAX];
 #pragma unroll
@@ -152,6 +202,9 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     }
   }
   __syncthreads();
+  // P in bf16 high + residual parts [2][GMAX][kDraftChunk] for the tensor-core P V; it takes the
+  // query area, which the tensor-core path does not use.
+  uint16_t *sP = reinterpret_cast<uint16_t *>(sQ);
 
   // Softmax over the chunk, one warp per head.
   for (int h = warp; h < G; h += blockDim.x / 32) {
@@ -161,6 +214,14 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
     sS[h * kDraftChunk + lane] = p0;
     sS[h * kDraftChunk + lane + 32] = p1;
+    if constexpr (TC) {
+      uint32_t hi, lo;
+      split_bf16(p0, p1, hi, lo);
+      sP[h * kDraftChunk + lane] = (uint16_t)(hi & 0xffffu);
+      sP[h * kDraftChunk + lane + 32] = (uint16_t)(hi >> 16);
+      sP[(GMAX + h) * kDraftChunk + lane] = (uint16_t)(lo & 0xffffu);
+      sP[(GMAX + h) * kDraftChunk + lane + 32] = (uint16_t)(lo >> 16);
+    }
     float l = warp_sum(p0 + p1);
     if (lane == 0) {
       sM[h] = m;
@@ -169,9 +230,59 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   }
   __syncthreads();
 
-  // O = P V: thread = (pair of d columns, token part).
   constexpr int NPAIR = D / 2;
-  constexpr int PARTS = 128 / NPAIR;
+  constexpr int PARTS = TC ? 1 : 128 / NPAIR;
+  float *red = reinterpret_cast<float *>(sKt);  // [PARTS][GMAX][D]: the K tile is free after the logits
+  if constexpr (TC) {
+    // O^T = V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ..; A fragments by
+    // transposing ldmatrix from the swizzled V tile, B fragments (P^T) from the bf16 P parts.
+    constexpr int MTW = D / 16 / 4;
+    float o[MTW][NT8][4];
+#pragma unroll
+    for (int mi = 0; mi < MTW; ++mi)
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kDraftChunk / 16; ++ks) {
+      uint32_t bh[NT8][2], bl[NT8][2];
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt) {
+        const int hn = nt * 8 + (lane >> 2), k0 = ks * 16 + (lane & 3) * 2;
+        bh[nt][0] = bh[nt][1] = bl[nt][0] = bl[nt][1] = 0u;
+        if (hn < G) {
+          bh[nt][0] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0);
+          bh[nt][1] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0 + 8);
+          bl[nt][0] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0);
+          bl[nt][1] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0 + 8);
+        }
+      }
+      const int tr = ks * 16 + (lane & 7) + ((lane >> 4) << 3);  // token row of this thread's address
+#pragma unroll
+      for (int mi = 0; mi < MTW; ++mi) {
+        const int ch = 2 * (warp * MTW + mi) + ((lane >> 3) & 1);
+        uint32_t af[4];
+        ldsm_x4_t(smem_u32(sVt + tr * C::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) {
+          mma_bf16(o[mi][nt], af, bh[nt][0], bh[nt][1]);
+          mma_bf16(o[mi][nt], af, bl[nt][0], bl[nt][1]);
+        }
+      }
+    }
+    // c0, c1: d = 16 mt + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3: d + 8.
+#pragma unroll
+    for (int mi = 0; mi < MTW; ++mi)
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int dd = (warp * MTW + mi) * 16 + (lane >> 2) + (e >> 1) * 8;
+          const int h = nt * 8 + (lane & 3) * 2 + (e & 1);
+          if (h < G) red[h * D + dd] = o[mi][nt][e];
+        }
+    __syncthreads();
+  } else {
+  // O = P V: thread = (pair of d columns, token part).
   constexpr int TPP = kDraftChunk / PARTS;  // tokens per part
   const int dp = tid % NPAIR, part = tid / NPAIR;
   float acc0[GMAX], acc1[GMAX];
@@ -204,7 +315,6 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     }
   }
   __syncthreads();  // K tile is free: reuse it for the part reduction
-  float *red = reinterpret_cast<float *>(sKt);  // [PARTS][GMAX][D]
 #pragma unroll
   for (int h = 0; h < GMAX; ++h) {
     if (h < G) {
@@ -213,6 +323,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     }
   }
   __syncthreads();
+  }
 
   const bool single = (n_chunks == 1);
   const int64_t prow = ((int64_t)unit * a.C_max + chunk) * GMAX;
