@@ -162,8 +162,8 @@ def measured_peaks() -> dict:
 
 # Sources of the dominant call (ssd_verify_attn: tensor-core verify kernel + finalize); a change to
 # any of them makes the committed DRAM-traffic capture stale.
-VERIFY_SOURCES = ("ssd_common.cuh", "ssd_host.h", "ssd_sm100.cuh", "ssd_verify.cu", "ssd_verify_tc.cu",
-                  "ssd_verify_tile.cuh")
+VERIFY_SOURCES = ("ssd_common.cuh", "ssd_host.h", "ssd_sm100.cuh", "ssd_topk.cuh", "ssd_verify.cu",
+                  "ssd_verify_tc.cu", "ssd_verify_tile.cuh")
 
 
 def kernel_source_sha() -> str:
