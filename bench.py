@@ -487,6 +487,159 @@ def run_ours(args, spec, rank, world, local):
             "clocks": clk}
 
 
+def _time_calls(fn, reps: int = 20, warm: int = 3) -> float:
+    """Mean device time of fn() in ms with a cold L2: [L2 flush, fn] and [L2 flush] are each captured
+    once as a CUDA graph (after warm-up calls) and replayed `reps` times between CUDA events on their
+    stream; the call's time is the difference, so neither host overhead nor the flush is counted."""
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    flush = W.flush_buffer(torch.device("cuda", torch.cuda.current_device()))
+    with torch.cuda.stream(st):
+        for _ in range(warm):
+            fn()
+    st.synchronize()
+    graphs = []
+    for with_fn in (True, False):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(g, stream=st):
+                flush.fill_(1.0)
+                if with_fn:
+                    fn()
+        graphs.append(g)
+    st.synchronize()
+    ms = []
+    for g in graphs:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            g.replay()
+            e0.record(st)
+            for _ in range(reps):
+                g.replay()
+            e1.record(st)
+        st.synchronize()
+        ms.append(e0.elapsed_time(e1) / reps)
+    return ms[0] - ms[1]
+
+
+def run_rows(args) -> list:
+    """One line per hot-path call on its own workload (the verify, select and draft of the Qwen3-8B
+    round, the unified launch on the Qwen3-14B mixed batch against separate verify and draft calls on
+    the same requests, and the block path on 8 x 131072): device time per call, L2 flushed before
+    each call, and algorithmic bytes."""
+    from sparse_self_speculative_verify_gb300 import binding as Bd
+    from sparse_self_speculative_verify_gb300 import build as libbuild
+    libbuild.build()
+    Bd.load()
+    dev = torch.device("cuda", 0)
+    peak = measured_peaks()["hbm_gbs"]
+    out = []
+
+    def line(row, workload, ms, nbytes, **extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        d = {"row": row, "workload": workload, "us_per_call": ms * 1e3, "algorithmic_bytes": nbytes,
+             "GB_s": gbs, "frac_of_measured_hbm": gbs / peak}
+        d.update(extra)
+        out.append(d)
+
+    # Qwen3-8B round: verify, select, draft.
+    spec = W.SPECS["qwen3_8b"]
+    w = W.make_workload(spec, seed=1002, device=dev)
+    kv = Bd.KVCache.from_workload(w)
+    scale = 1.0 / math.sqrt(spec.d)
+    lens = w.seq_lens.cpu().tolist()
+    kpr = w.k_per_req.cpu().tolist()
+    k_max = max(kpr)
+    ws = Bd.Workspace()
+    r = {}
+
+    def verify():
+        r.update(Bd.ssd_verify_attn(kv, w.q_verify, spec.n_cand, scale, workspace=ws))
+    ms = _time_calls(verify)
+    line("a1-a3 verify + criticality + combine", spec.name, ms,
+         M.verify_call_bytes(lens, spec.batch, spec.h_q, spec.h_kv, spec.d, spec.elem_bytes, spec.n_cand))
+    sel = {}
+
+    def select():
+        sel["idx"], sel["cnt"] = Bd.ssd_select_topk(r["scores"], kv.seq_lens, w.k_per_req, k_max, spec.h_kv,
+                                                    max_len=kv.max_seq_len)
+    ms = _time_calls(select)
+    line("a4 top-K select", spec.name, ms, sum(lens) * spec.h_kv * 4)
+    idx = sel["idx"].view(spec.batch, spec.h_kv, k_max)
+    cnt = sel["cnt"].view(spec.batch, spec.h_kv)
+    ms = _time_calls(lambda: Bd.ssd_draft_attn(kv, w.q_draft[0], idx, cnt, scale, workspace=ws))
+    line("a5 sparse draft", spec.name, ms, M.draft_kv_bytes(kpr, lens, spec.h_kv, spec.d, spec.elem_bytes))
+    del w, kv, r, sel, idx, cnt
+    torch.cuda.empty_cache()
+
+    # Qwen3-14B mixed batch: one unified launch against a verify call and a draft call on the two
+    # request subsets.
+    spec = W.SPECS["qwen3_14b_unified"]
+    w = W.make_workload(spec, seed=1004, device=dev)
+    kv = Bd.KVCache.from_workload(w)
+    scale = 1.0 / math.sqrt(spec.d)
+    k_max = int(w.k_per_req.max())
+    uidx, ucnt = W.random_index_sets(w.seq_lens, spec.h_kv, w.k_per_req, k_max, seed=w.seed)
+    uidx, ucnt = uidx.to(dev), ucnt.to(dev)
+    phase = w.phase.cpu().numpy()
+    lens = w.seq_lens.cpu().tolist()
+    vreq = [b for b in range(spec.batch) if phase[b] == 1]
+    dreq = [b for b in range(spec.batch) if phase[b] == 0]
+    nbytes = (M.verify_kv_bytes([lens[b] for b in vreq], spec.h_kv, spec.d, spec.elem_bytes) +
+              int(ucnt[dreq].sum().item()) * M.kv_bytes_per_token_head(spec.d, spec.elem_bytes))
+    wsu = Bd.Workspace()
+    ms = _time_calls(lambda: Bd.ssd_unified_attn(kv, w.phase, w.q_verify, w.q_draft[0], spec.n_cand, uidx, ucnt,
+                                                 scale, workspace=wsu))
+    vi = torch.tensor(vreq, device=dev)
+    di = torch.tensor(dreq, device=dev)
+    kv_v = Bd.KVCache(kv.pool, kv.page_table[vi].contiguous(), kv.seq_lens[vi].contiguous(), kv.max_seq_len)
+    kv_d = Bd.KVCache(kv.pool, kv.page_table[di].contiguous(), kv.seq_lens[di].contiguous(), kv.max_seq_len)
+    qv = w.q_verify[vi].contiguous()
+    qd = w.q_draft[0][di].contiguous()
+    di_idx, di_cnt = uidx[di].contiguous(), ucnt[di].contiguous()
+
+    def separate():
+        Bd.ssd_verify_attn(kv_v, qv, spec.n_cand, scale, workspace=wsu)
+        Bd.ssd_draft_attn(kv_d, qd, di_idx, di_cnt, scale, workspace=wsu)
+    ms_sep = _time_calls(separate)
+    line("a6 unified launch", spec.name, ms, nbytes, verify_requests=len(vreq), draft_requests=len(dreq),
+         separate_calls_us=ms_sep * 1e3, speedup_over_separate=ms_sep / ms)
+    del w, kv, kv_v, kv_d, uidx, ucnt
+    torch.cuda.empty_cache()
+
+    # Block path on 8 x 131072: per-candidate block scores, block Top-16, union, block-sparse attention.
+    spec = W.SPECS["block_131k"]
+    w = W.make_workload(spec, seed=1005, device=dev)
+    kv = Bd.KVCache.from_workload(w)
+    scale = 1.0 / math.sqrt(spec.d)
+    nb = (kv.max_seq_len + 63) // 64
+    bs = torch.zeros((spec.batch, spec.h_kv, spec.n_cand, nb), device=dev)
+    wsb = Bd.Workspace()
+    lens = w.seq_lens.cpu().tolist()
+    ms_v = _time_calls(lambda: Bd.ssd_verify_attn(kv, w.q_verify, spec.n_cand, scale, bscores=bs, want_scores=False,
+                                                  workspace=wsb), reps=5)
+    kb = spec.top_blocks
+    ks = torch.full((spec.batch,), kb, dtype=torch.int32, device=dev)
+    bi, bc = Bd.ssd_select_topk(bs, kv.seq_lens, ks, kb, spec.h_kv * spec.n_cand, len_div=64, max_len=nb)
+    blocks = bi.view(spec.batch * spec.h_kv, spec.n_cand, kb)
+    bcnt = bc.view(spec.batch * spec.h_kv, spec.n_cand)
+    un = {}
+
+    def union():
+        un["i"], un["m"], un["c"] = Bd.ssd_block_union(blocks, bcnt, nb)
+    ms_u = _time_calls(union)
+    ms_b = _time_calls(lambda: Bd.ssd_block_sparse_attn(kv, w.q_verify, spec.n_cand, un["i"], un["m"], un["c"], scale,
+                                                        workspace=wsb))
+    ublocks = int(un["c"].sum().item())
+    line("a7 block-sparse attention over the union", spec.name, ms_b,
+         ublocks * 64 * M.kv_bytes_per_token_head(spec.d, spec.elem_bytes), union_blocks=ublocks,
+         union_us=ms_u * 1e3, block_scores_verify_us=ms_v * 1e3,
+         block_scores_verify_frac=M.verify_kv_bytes(lens, spec.h_kv, spec.d, spec.elem_bytes) / (ms_v * 1e-3) / 1e9
+         / peak)
+    assert Bd.ssd_status() == 0, "device status fault"
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -498,7 +651,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-requests", type=int, default=2)
+    ap.add_argument("--rows", action="store_true", help="time each hot-path call on its own workload (1 GPU)")
     args = ap.parse_args(argv)
+    if args.rows:
+        for d in run_rows(args):
+            print(json.dumps(d), flush=True)
+        return
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as dist

@@ -8,6 +8,7 @@ namespace ssd {
 template <int D, typename T, int GMAX>
 __global__ void __launch_bounds__(128) draft_kernel(DraftArgs a) {
   extern __shared__ __align__(128) char smem[];
+  if (a.phase && a.phase[blockIdx.y / a.kv.h_kv] != 0) return;  // a verify-phase request of a mixed batch
   draft_item<D, T, GMAX>(a, blockIdx.y, blockIdx.x, smem);
 }
 

@@ -6,11 +6,16 @@
 // (about 1/(k+1) of them verify), and a persistent-style fused attention kernel dispatches verify
 // and draft attention to their own tile code on chip instead of launching two kernels.
 //
-// Each block enumerates the work of the whole batch itself (per-request item counts and prefix sums
-// in shared memory: verify items first, draft items after them, so the long items are started first)
-// and then takes items c, c + grid, c + 2*grid, ...; verify items run the tensor-core split tile,
-// draft items the gather tile.  The verify-phase requests then go through the same finalize pass as
-// ssd_verify_attn.
+// Where the tcgen05 verify applies (bf16, d = 128, pages of 8 or more tokens), the call runs the
+// verify-phase requests through it (its blocks skip draft-phase requests), then the finalize, then
+// the draft kernel over the draft-phase requests (its blocks skip verify-phase requests): the
+// tcgen05 verify holds all of an SM's shared memory, so verify and draft work cannot share a block
+// there, and one mma.sync launch mixing both measured about twice the time of the three launches.
+// Otherwise one persistent launch mixes both: each block enumerates the work of the whole batch
+// itself (per-request item counts and prefix sums in shared memory: verify items first, draft items
+// after them, so the long items are started first) and then takes items c, c + grid, c + 2*grid, ...;
+// verify items run the mma.sync split tile, draft items the gather tile.  In both forms the
+// verify-phase requests then go through the same finalize pass as ssd_verify_attn.
 #include "ssd_draft_tile.cuh"
 #include "ssd_host.h"
 #include "ssd_verify_tile.cuh"
@@ -22,6 +27,9 @@ size_t draft_data_bytes(int units, int C_max, int gmax, int D);
 void draft_carve(unsigned *counters, void *data, int units, int C_max, int gmax, int D, DraftArgs &a);
 int draft_checks(const ssd_paged_kv *kv, int h_q, const void *q, const int32_t *idx, int k_max, const int32_t *cnt,
                  const float *out, const char *who);
+int launch_draft_any(int dtype, int D, const DraftArgs &a, dim3 grid, cudaStream_t st);
+bool verify_tc_supported(const ssd_paged_kv *kv, int R);
+int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st);
 
 constexpr int kUniMaxBatch = 512;
 
@@ -101,7 +109,7 @@ __global__ void __launch_bounds__(128, 2) unified_kernel(VerifyArgs va, DraftArg
 }
 
 struct UniLayout {
-  size_t v_o, v_lse, v_sp, v_sm, d_off, total;
+  size_t v_o, v_lse, v_sp, v_sm, split_off, d_off, total;
   int G, R, units, S_max, Lpad, C_max, gmax;
 };
 
@@ -115,7 +123,7 @@ static UniLayout uni_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int k_m
   l.C_max = cdiv(k_max > 0 ? k_max : 1, kDraftChunk);
   l.gmax = draft_gmax(l.G);
   Carver c(nullptr);
-  c.take<unsigned>(kCounterSlots);  // counter area (draft arrival counters)
+  c.take<unsigned>(kCounterSlots);  // counter area: verify item counters (slots 0-1), draft arrivals (2 ..)
   size_t rows = (size_t)l.units * l.S_max * l.R;
   l.v_o = c.off;
   c.take<float>(rows * kv->d);
@@ -125,6 +133,8 @@ static UniLayout uni_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int k_m
   c.take<__half>((size_t)l.units * l.R * l.Lpad);
   l.v_sm = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
+  l.split_off = c.off;
+  c.take<int>(1);
   l.d_off = c.off;
   l.total = l.d_off + draft_data_bytes(l.units, l.C_max, l.gmax, kv->d);
   return l;
@@ -225,10 +235,21 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
   da.lse = lse_draft;
   da.phase = phase;
   da.status = status;
-  draft_carve(reinterpret_cast<unsigned *>(ws), ws + lay.d_off, lay.units, lay.C_max, lay.gmax, kv->d, da);
-  const int nrt = lay.R <= 16 ? 1 : (lay.R <= 32 ? 2 : 4);
-  rc = kv->d == 128 ? uni_rows<128>(nrt, lay.gmax, va, da, phase, st) : uni_rows<64>(nrt, lay.gmax, va, da, phase, st);
-  if (rc) return rc;
+  const bool tc = verify_tc_supported(kv, lay.R);
+  // The draft counters start at slot 2 of the counter area in the three-launch form (slots 0-1 are
+  // the tcgen05 verify's item counters).
+  draft_carve(reinterpret_cast<unsigned *>(ws) + (tc ? 2 : 0), ws + lay.d_off, lay.units, lay.C_max, lay.gmax, kv->d,
+              da);
+  if (tc) {
+    va.phase = phase;
+    va.sched = reinterpret_cast<int *>(ws);
+    va.split_out = reinterpret_cast<int *>(ws + lay.split_off);
+    if ((rc = launch_verify_tc(kv, va, st))) return rc;
+  } else {
+    const int nrt = lay.R <= 16 ? 1 : (lay.R <= 32 ? 2 : 4);
+    rc = kv->d == 128 ? uni_rows<128>(nrt, lay.gmax, va, da, phase, st) : uni_rows<64>(nrt, lay.gmax, va, da, phase, st);
+    if (rc) return rc;
+  }
 
   FinalizeArgs f{};
   f.seq_lens = kv->seq_lens;
@@ -250,6 +271,9 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
   f.lse = lse_verify;
   f.scores = scores;
   f.scores_stride = scores_stride;
+  f.split_len = tc ? va.split_out : nullptr;
   const int n_tok = scores ? cdiv(kv->max_seq_len, kFinTok) : 0;
-  return launch_finalize(f, n_tok, lay.units, st);
+  if ((rc = launch_finalize(f, n_tok, lay.units, st))) return rc;
+  if (!tc) return SSD_OK;
+  return launch_draft_any(kv->dtype, kv->d, da, dim3(lay.C_max, lay.units), st);
 }

@@ -245,7 +245,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int k = 0; k < CH; ++k) {
       const int b = tid * CH + k;
       int L = 0;
-      if (b < B) {
+      if (b < B && a.phase && a.phase[b] == 0) {
+        s.len[b] = 0;  // a draft-phase request of a mixed batch: no verify items
+      } else if (b < B) {
         L = a.kv.seq_lens[b];
         if (L < a.n_c || L > a.kv.max_seq_len) {
           if (blockIdx.x == 0) atomicOr(a.status, (unsigned)SSD_FAULT_SEQLEN);

@@ -42,6 +42,7 @@ struct VerifyArgs {
   int *sched;  // [2] in the counter area: next-item counter and finished-block count (tensor-core
                // path); zero at launch, and the last block to finish returns both to zero
   int *split_out;  // tensor-core path: receives the split length it chose (read by the finalize)
+  const uint8_t *phase;  // tensor-core path: nullptr, or only requests with phase[b] == 1 get items
 };
 
 template <int D, int NRT>

@@ -45,6 +45,13 @@ def test_unified_small():
     _run_and_check(W.make_workload(spec, seed=5, device=DEV))
 
 
+def test_unified_persistent_launch_d64():
+    """d = 64 (no tcgen05 verify): one persistent launch mixes the verify and draft items."""
+    spec = W.scaled_spec(W.SPECS["qwen3_14b_unified"], name="uni64", batch=9, d=64, len_lo=600, len_hi=3000,
+                         len_median=1500.0, verify_prob=0.4)
+    _run_and_check(W.make_workload(spec, seed=6, device=DEV))
+
+
 def test_unified_full_size_sampled():
     spec = W.SPECS["qwen3_14b_unified"]
     w = W.make_workload(spec, device=DEV)
