@@ -4,11 +4,13 @@
 // SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
 // Sparse Attention") §4.1: the k drafts after a verify load and attend only the critical tokens the
 // verify selected; §4.2: sparse attention is PagedAttention with page size 1, i.e. attention over an
-// explicit token list.  A single query row per head carries too little reuse for tensor cores, so
-// the item runs on CUDA cores in fp32: the selected K and V rows are gathered into swizzled shared
-// memory with 16-byte cp.async (one K row = one contiguous 256-byte line of the page), every K/V
-// element is reused by the G heads of the group, and the chunk's partial result is merged with the
-// other chunks of the same (request, KV head) by the last chunk to finish (atomic ticket, no wait).
+// explicit token list.  The selected K and V rows are gathered into swizzled shared memory with
+// 16-byte cp.async (one K row = one contiguous 256-byte line of the page).  The two contractions
+// are small (G query rows against 64 tokens) but still dominate the instruction count, so for bf16
+// caches they run on tensor cores (mma.sync m16n8k16: S^T = K Q^T with the queries as register B
+// fragments, O^T = V^T P^T with P as bf16 high + residual parts); fp32 caches use CUDA cores.  The
+// chunk's partial result is merged with the other chunks of the same (request, KV head) by the last
+// chunk to finish (atomic ticket, no wait).
 #pragma once
 
 #include "ssd_common.cuh"
