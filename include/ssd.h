@@ -10,8 +10,11 @@
  *   2. ssd_select_topk  -- Top-K of the criticality per (request, KV head), ties to the lower index
  *                          (ssd_select_topp: the same with a per-row K from a top-p budget).
  *   3. ssd_draft_attn   -- the next k drafts: single-query attention over the selected tokens only.
- * plus the unified verify/draft launch (§4.2 "fused attention") and the block-granular variant
- * (SpecSA post, overlap-aware grouped query execution; SparDA §2 max-pooling to a block grid).
+ * plus verify and select in one call (ssd_verify_select), the unified verify/draft call over a
+ * mixed batch (§4.2 "fused attention"), the block-granular variant (SpecSA post, overlap-aware
+ * grouped query execution; SparDA §2 max-pooling to a block grid), and around the round the KV
+ * append / length rollback (SpecSA: accepted tokens' KV is kept, rejected ones' dropped) and the
+ * phase assignment of the unified batch (§4.2).
  *
  * Conventions (all calls):
  *  - Every pointer argument named as "device" is device memory of the current CUDA device; host

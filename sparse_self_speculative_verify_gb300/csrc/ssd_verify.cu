@@ -1,6 +1,7 @@
-// ssd_verify.cu -- verify attention with fused criticality, the split-KV finalize (LSE combine +
-// criticality rematerialisation + block max-pool), the block-sparse union pass and the public
-// split combine.
+// ssd_verify.cu -- verify attention with fused criticality (the host entry points and the
+// non-tcgen05 kernels; the tcgen05 kernel is in ssd_verify_tc.cu), the split-KV finalize (LSE
+// combine + criticality rematerialisation + block max-pool, and optionally the fused Top-K), the
+// block-sparse union pass and the public split combine.
 //
 // SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
 // Sparse Attention") §4.1 PillarAttn: the verify kernel dumps the attention scores while it runs,
