@@ -17,7 +17,8 @@ int draft_gmax(int G) { return G <= 4 ? 4 : (G <= 8 ? 8 : 16); }
 template <int D, typename T, int GMAX>
 static int launch_draft(const DraftArgs &a, dim3 grid, cudaStream_t st) {
   constexpr int smem = DraftCfg<D, T, GMAX>::SMEM;
-  static_assert(2 * DraftCfg<D, T, GMAX>::TILE >= (128 / (D / 2)) * GMAX * D * 4, "reduction area");
+  static_assert(DraftCfg<D, T, GMAX>::TC || 2 * DraftCfg<D, T, GMAX>::TILE >= (128 / (D / 2)) * GMAX * D * 4,
+                "reduction area");
   int rc = ensure_smem<draft_kernel<D, T, GMAX>>(smem);
   if (rc) return rc;
   draft_kernel<D, T, GMAX><<<grid, 128, smem, st>>>(a);

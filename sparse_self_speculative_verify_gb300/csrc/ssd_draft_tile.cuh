@@ -39,7 +39,12 @@ struct DraftCfg {
   static constexpr int ROWB = D * (int)sizeof(T);  // bytes of one K or V row
   static constexpr int CPR = ROWB / 16;
   static constexpr int TILE = kDraftChunk * ROWB;
-  static constexpr int SMEM = 2 * TILE + (GMAX * D + GMAX * kDraftChunk + 2 * GMAX) * 4 + kDraftChunk * 8;
+  // bf16 (tensor-core path): one row tile, K then V, so that twice as many blocks fit on an SM;
+  // fp32: a K tile and a V tile.  Then the queries (fp32; the output rows on the tensor-core path),
+  // logits, row max / sum, row offsets, and (tensor-core path) P as bf16 high + residual parts.
+  static constexpr bool TC = sizeof(T) == 2;
+  static constexpr int SMEM = (TC ? 1 : 2) * TILE + (GMAX * D + GMAX * kDraftChunk + 2 * GMAX) * 4 +
+                              kDraftChunk * 8 + (TC ? 2 * GMAX * kDraftChunk * 2 : 0);
 };
 
 __device__ __forceinline__ int draft_chunks(int n) { return n <= 0 ? 1 : cdiv(n, kDraftChunk); }
@@ -80,9 +85,10 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   if (chunk >= n_chunks) return;
   const int n = min(kDraftChunk, n_all - j0);  // may be 0 for an empty list
 
+  constexpr bool TC = C::TC;
   char *sKt = smem;
-  char *sVt = smem + C::TILE;
-  float *sQ = reinterpret_cast<float *>(smem + 2 * C::TILE);  // [GMAX][D]
+  char *sVt = TC ? smem : smem + C::TILE;  // the tensor-core path loads V into the K tile after the logits
+  float *sQ = reinterpret_cast<float *>(smem + (TC ? 1 : 2) * C::TILE);  // [GMAX][D]
   float *sS = sQ + GMAX * D;                                   // [GMAX][kDraftChunk]
   float *sM = sS + GMAX * kDraftChunk;                         // [GMAX]
   float *sL = sM + GMAX;                                       // [GMAX]
@@ -114,12 +120,11 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     const T *kr = row >= 0 ? reinterpret_cast<const T *>(a.kv.pool) + row : nullptr;
     uint32_t off = j * C::ROWB + swz_chunk(j, ch) * 16;
     cp_async16(smem_u32(sKt + off), kr ? (const void *)(kr + ch * EPC) : a.kv.pool, kr ? 16 : 0);
-    cp_async16(smem_u32(sVt + off), kr ? (const void *)(kr + v_off + ch * EPC) : a.kv.pool, kr ? 16 : 0);
+    if (!TC) cp_async16(smem_u32(sVt + off), kr ? (const void *)(kr + v_off + ch * EPC) : a.kv.pool, kr ? 16 : 0);
   }
   cp_async_commit();
   // bf16 caches: logits and P V on tensor cores (mma.sync m16n8k16, fp32 accumulate); the queries
   // stay in registers as B fragments, P goes through bf16 high + residual parts (about 16 bits).
-  constexpr bool TC = sizeof(T) == 2;
   constexpr int NT8 = (GMAX + 7) / 8;  // 8-wide head tiles
   constexpr int KS = D / 16;           // 16-wide steps over d
   const T *q = reinterpret_cast<const T *>(a.q);
@@ -204,9 +209,9 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     }
   }
   __syncthreads();
-  // P in bf16 high + residual parts [2][GMAX][kDraftChunk] for the tensor-core P V; it takes the
-  // query area, which the tensor-core path does not use.
-  uint16_t *sP = reinterpret_cast<uint16_t *>(sQ);
+  // P in bf16 high + residual parts [2][GMAX][kDraftChunk] for the tensor-core P V, after the row
+  // offsets.
+  uint16_t *sP = reinterpret_cast<uint16_t *>(sRow + kDraftChunk);
 
   // Softmax over the chunk, one warp per head.
   for (int h = warp; h < G; h += blockDim.x / 32) {
@@ -234,8 +239,21 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
 
   constexpr int NPAIR = D / 2;
   constexpr int PARTS = TC ? 1 : 128 / NPAIR;
-  float *red = reinterpret_cast<float *>(sKt);  // [PARTS][GMAX][D]: the K tile is free after the logits
+  // [PARTS][GMAX][D]: the query area on the tensor-core path (the queries live in registers), the
+  // K tile (free after the logits) on the CUDA-core path.
+  float *red = TC ? sQ : reinterpret_cast<float *>(sKt);
   if constexpr (TC) {
+    // V rows into the tile the K rows occupied (every thread is past the logits and the softmax).
+    for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
+      const int j = c / C::CPR, ch = c % C::CPR;
+      const int64_t row = sRow[j];
+      const T *kr = row >= 0 ? reinterpret_cast<const T *>(a.kv.pool) + row : nullptr;
+      cp_async16(smem_u32(sVt + j * C::ROWB + swz_chunk(j, ch) * 16), kr ? (const void *)(kr + v_off + ch * EPC)
+                                                                            : a.kv.pool, kr ? 16 : 0);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
     // O^T = V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ..; A fragments by
     // transposing ldmatrix from the swizzled V tile, B fragments (P^T) from the bf16 P parts.
     constexpr int MTW = D / 16 / 4;
