@@ -212,6 +212,18 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   // P in bf16 high + residual parts [2][GMAX][kDraftChunk] for the tensor-core P V, after the row
   // offsets.
   uint16_t *sP = reinterpret_cast<uint16_t *>(sRow + kDraftChunk);
+  if constexpr (TC) {
+    // V rows into the tile the K rows occupied (every thread is past the logits); they land while
+    // the softmax runs.
+    for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
+      const int j = c / C::CPR, ch = c % C::CPR;
+      const int64_t row = sRow[j];
+      const T *kr = row >= 0 ? reinterpret_cast<const T *>(a.kv.pool) + row : nullptr;
+      cp_async16(smem_u32(sVt + j * C::ROWB + swz_chunk(j, ch) * 16), kr ? (const void *)(kr + v_off + ch * EPC)
+                                                                            : a.kv.pool, kr ? 16 : 0);
+    }
+    cp_async_commit();
+  }
 
   // Softmax over the chunk, one warp per head.
   for (int h = warp; h < G; h += blockDim.x / 32) {
@@ -243,15 +255,6 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   // K tile (free after the logits) on the CUDA-core path.
   float *red = TC ? sQ : reinterpret_cast<float *>(sKt);
   if constexpr (TC) {
-    // V rows into the tile the K rows occupied (every thread is past the logits and the softmax).
-    for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
-      const int j = c / C::CPR, ch = c % C::CPR;
-      const int64_t row = sRow[j];
-      const T *kr = row >= 0 ? reinterpret_cast<const T *>(a.kv.pool) + row : nullptr;
-      cp_async16(smem_u32(sVt + j * C::ROWB + swz_chunk(j, ch) * 16), kr ? (const void *)(kr + v_off + ch * EPC)
-                                                                            : a.kv.pool, kr ? 16 : 0);
-    }
-    cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();
     // O^T = V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ..; A fragments by
