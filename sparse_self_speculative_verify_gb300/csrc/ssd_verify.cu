@@ -145,8 +145,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
 
   if (!tok) {
     const int D = f.D, tpr = D / 4, rpc = fin_rows_per_cta(D);
-    const int r = ((int)blockIdx.x - n_tok) * rpc + tid / tpr, q4 = tid % tpr;
-    if (r >= f.R) return;
+    const int n_comb = (int)gridDim.x - n_tok, q4 = tid % tpr;
+    for (int r = ((int)blockIdx.x - n_tok) * rpc + tid / tpr; r < f.R; r += rpc * n_comb) {
     const float ln = sLn[r];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (ln != -INFINITY) {
@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     const int64_t row = ((int64_t)b * f.n_c + i) * f.h_q + g * f.G + hl;
     reinterpret_cast<float4 *>(f.out + row * D)[q4] = acc;
     if (q4 == 0 && f.lse) f.lse[row] = ln;
+    }
     return;
   }
 
@@ -258,7 +259,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
 }
 
 int launch_finalize(const FinalizeArgs &f, int n_tok, int units, cudaStream_t st) {
-  const int n_comb = cdiv(f.R, kFinThreads / (f.D / 4));
+  // With token blocks in the grid, one combine block per unit loops over the rows (fewer blocks to
+  // schedule behind the token work); without them, a block per group of rows.
+  const int n_comb = n_tok > 0 ? 1 : cdiv(f.R, kFinThreads / (f.D / 4));
   finalize_kernel<<<dim3(n_tok + n_comb, units), kFinThreads, 0, st>>>(f, n_tok);
   return check_launch("finalize_kernel");
 }
