@@ -9,7 +9,9 @@
  *                          group and the k+1 verify positions).
  *   2. ssd_select_topk  -- Top-K of the criticality per (request, KV head), ties to the lower index
  *                          (ssd_select_topp: the same with a per-row K from a top-p budget).
- *   3. ssd_draft_attn   -- the next k drafts: single-query attention over the selected tokens only.
+ *   3. ssd_draft_attn   -- the next k drafts: single-query attention over the selected tokens only
+ *                          (ssd_draft_attn_packed: the first draft keeps the selected rows packed
+ *                          for the others).
  * plus verify and select in one call (ssd_verify_select), the unified verify/draft call over a
  * mixed batch (§4.2 "fused attention"), the block-granular variant (SpecSA post, overlap-aware
  * grouped query execution; SparDA §2 max-pooling to a block grid), and around the round the KV
@@ -195,6 +197,29 @@ size_t ssd_draft_workspace_bytes(const ssd_paged_kv *kv, int h_q, int k_max);
 int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
                    const int32_t *cnt, float scale, float *out, float *lse, void *workspace,
                    size_t workspace_bytes, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Sparse draft attention with a row pack.  The k drafts of a round all attend the set the last
+ * verify selected (SparseSpec §4.1: the pattern stays fixed until the next verify refreshes it), so
+ * the first draft can leave the selected K and V rows in a contiguous buffer and the others read
+ * them from there instead of through the index list and the page table.  Same arguments, results
+ * and workspace as ssd_draft_attn, plus:
+ *   pack        device buffer of at least ssd_draft_pack_bytes(kv, k_max) bytes, 256-byte aligned,
+ *               owned by the caller.  Its layout is private to the library.
+ *   pack_mode   SSD_PACK_NONE: exactly ssd_draft_attn (pack unused, may be NULL).
+ *               SSD_PACK_WRITE: ssd_draft_attn, and every selected row it read is stored in pack.
+ *               SSD_PACK_READ: attends the rows the last SSD_PACK_WRITE call on this pack stored;
+ *               idx is not read (may be NULL) and the page table and lengths are not consulted, so
+ *               no index or page fault is raised.  cnt and k_max must equal that call's and the
+ *               selected tokens' K / V must be unchanged since (appending new tokens is fine); a cnt
+ *               that grew reads rows the pack does not hold (wrong values, never outside pack).
+ * Entries of cnt outside [0, k_max] raise SSD_FAULT_KMAX in every mode.
+ */
+enum ssd_pack_mode { SSD_PACK_NONE = 0, SSD_PACK_WRITE = 1, SSD_PACK_READ = 2 };
+size_t ssd_draft_pack_bytes(const ssd_paged_kv *kv, int k_max);
+int ssd_draft_attn_packed(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
+                          const int32_t *cnt, float scale, float *out, float *lse, void *pack, size_t pack_bytes,
+                          int pack_mode, void *workspace, size_t workspace_bytes, ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * KV append and length advance (SpecSA post, "refresh/reuse NSA kernel fusion" and "branch

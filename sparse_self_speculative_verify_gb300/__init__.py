@@ -7,12 +7,14 @@ of one speculative round together; ``workloads`` draws the seeded synthetic inpu
 """
 
 from .binding import (KVCache, LibraryNotBuilt, SSDError, Workspace, ssd_block_sparse_attn, ssd_block_union,
-                      ssd_combine, ssd_draft_attn, ssd_draft_attn_static, ssd_kv_advance, ssd_kv_append,
+                      ssd_combine, ssd_draft_attn, ssd_draft_attn_packed, ssd_draft_attn_static,
+                      ssd_draft_pack_bytes, ssd_kv_advance, ssd_kv_append,
                       ssd_phase_assign, ssd_phase_fill, ssd_select_topk, ssd_select_topp, ssd_status, ssd_unified_attn,
                       ssd_verify_attn, ssd_verify_select, ssd_version)
 from .round import SpecRound
 
 __all__ = ["KVCache", "LibraryNotBuilt", "SSDError", "Workspace", "SpecRound", "ssd_block_sparse_attn",
-           "ssd_block_union", "ssd_combine", "ssd_draft_attn", "ssd_draft_attn_static", "ssd_kv_advance",
+           "ssd_block_union", "ssd_combine", "ssd_draft_attn", "ssd_draft_attn_packed", "ssd_draft_attn_static",
+           "ssd_draft_pack_bytes", "ssd_kv_advance",
            "ssd_kv_append", "ssd_phase_assign", "ssd_phase_fill", "ssd_select_topk", "ssd_select_topp",
            "ssd_status", "ssd_unified_attn", "ssd_verify_attn", "ssd_verify_select", "ssd_version"]

@@ -27,6 +27,7 @@ FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT, F
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
             "ssd_verify_select",
             "ssd_select_topk", "ssd_select_topp", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
+            "ssd_draft_pack_bytes", "ssd_draft_attn_packed",
             "ssd_unified_workspace_bytes", "ssd_kv_append", "ssd_kv_advance", "ssd_phase_assign", "ssd_phase_fill",
             "ssd_unified_attn", "ssd_block_union", "ssd_block_sparse_workspace_bytes", "ssd_block_sparse_attn",
             "ssd_combine"]
@@ -81,6 +82,8 @@ def load(path: Optional[str] = None):
             "ssd_draft_workspace_bytes": ([KV, I, I], S),
             "ssd_draft_attn": ([KV, P, I, P, I, P, F, P, P, P, S, P], I),
             "ssd_draft_attn_static": ([KV, P, I, P, I, P, F, P, P, P], I),
+            "ssd_draft_pack_bytes": ([KV, I], S),
+            "ssd_draft_attn_packed": ([KV, P, I, P, I, P, F, P, P, P, S, I, P, S, P], I),
             "ssd_kv_append": ([KV, P, P, I, P], I),
             "ssd_kv_advance": ([P, P, I, I, P], I),
             "ssd_phase_assign": ([P, I, I, P], I),
@@ -361,6 +364,42 @@ def ssd_draft_attn(kv: KVCache, q: torch.Tensor, idx: torch.Tensor, cnt: torch.T
     wsp, avail = _ws(dev, "draft", need, workspace)
     _check(L.ssd_draft_attn(kv.ref(), _ptr(q), h_q, _ptr(idx), k_max, _ptr(cnt), float(scale), _ptr(out), _ptr(lse),
                             wsp, avail, _stream(stream)))
+    return {"out": out, "lse": lse}
+
+
+PACK_NONE, PACK_WRITE, PACK_READ = 0, 1, 2
+
+
+def ssd_draft_pack_bytes(kv: KVCache, k_max: int) -> int:
+    return int(_lib().ssd_draft_pack_bytes(kv.ref(), int(k_max)))
+
+
+def ssd_draft_attn_packed(kv: KVCache, q: torch.Tensor, idx: Optional[torch.Tensor], cnt: torch.Tensor, scale: float,
+                          pack: torch.Tensor, pack_mode: int, *, k_max: Optional[int] = None, out=None, lse=None,
+                          want_lse: bool = True, workspace: Optional[Workspace] = None, stream=None) -> dict:
+    """ssd_draft_attn with a row pack: PACK_WRITE attends through idx and stores the selected rows in
+    ``pack`` (a uint8 device tensor of ssd_draft_pack_bytes bytes, 256-byte aligned); PACK_READ
+    attends the rows stored by the last PACK_WRITE call (idx may be None; then k_max is required)."""
+    _need(q, "q", kv.pool.dtype, kv.device)
+    dev = kv.device
+    if idx is not None:
+        _need(idx, "idx", torch.int32, dev)
+    _need(cnt, "cnt", torch.int32, dev)
+    _need(pack, "pack", torch.uint8, dev)
+    B, h_q, d = q.shape
+    if k_max is None:
+        if idx is None:
+            raise ValueError("k_max is required when idx is None")
+        k_max = idx.shape[-1]
+    if out is None:
+        out = torch.empty((B, h_q, d), dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, h_q), dtype=torch.float32, device=dev)
+    L = _lib()
+    need = L.ssd_draft_workspace_bytes(kv.ref(), h_q, k_max)
+    wsp, avail = _ws(dev, "draft", need, workspace)
+    _check(L.ssd_draft_attn_packed(kv.ref(), _ptr(q), h_q, _ptr(idx), int(k_max), _ptr(cnt), float(scale), _ptr(out),
+                                   _ptr(lse), _ptr(pack), pack.numel(), int(pack_mode), wsp, avail, _stream(stream)))
     return {"out": out, "lse": lse}
 
 

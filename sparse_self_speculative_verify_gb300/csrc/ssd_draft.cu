@@ -56,8 +56,9 @@ void draft_carve(unsigned *counters, void *data, int units, int C_max, int gmax,
 }
 
 int draft_checks(const ssd_paged_kv *kv, int h_q, const void *q, const int32_t *idx, int k_max, const int32_t *cnt,
-                 const float *out, const char *who) {
-  if (!q || !idx || !cnt || !out) return fail(SSD_ERR_INVALID_ARG, "%s: q, idx, cnt and out must be non-NULL", who);
+                 const float *out, const char *who, bool need_idx) {
+  if (!q || (need_idx && !idx) || !cnt || !out)
+    return fail(SSD_ERR_INVALID_ARG, "%s: q, idx, cnt and out must be non-NULL", who);
   if (h_q <= 0 || h_q % kv->h_kv) return fail(SSD_ERR_INVALID_ARG, "%s: h_q %d not a multiple of h_kv", who, h_q);
   if (h_q / kv->h_kv > 16) return fail(SSD_ERR_UNSUPPORTED, "%s: group size %d > 16", who, h_q / kv->h_kv);
   if (k_max < 0) return fail(SSD_ERR_INVALID_ARG, "%s: k_max < 0", who);
@@ -75,19 +76,33 @@ extern "C" size_t ssd_draft_workspace_bytes(const ssd_paged_kv *kv, int h_q, int
                                           draft_gmax(h_q / kv->h_kv), kv->d);
 }
 
-extern "C" int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
-                              const int32_t *cnt, float scale, float *out, float *lse, void *workspace,
-                              size_t workspace_bytes, ssd_stream_t stream) {
-  const char *who = "ssd_draft_attn";
+// Bytes of the row pack: a K and a V tile of kDraftChunk rows per chunk slot of every unit.
+static size_t pack_bytes_of(const ssd_paged_kv *kv, int k_max) {
+  const size_t elem = kv->dtype == SSD_DTYPE_BF16 ? 2 : 4;
+  return (size_t)kv->batch * kv->h_kv * cdiv(k_max > 0 ? k_max : 1, kDraftChunk) * 2 * kDraftChunk * kv->d * elem;
+}
+
+static int draft_call(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max, const int32_t *cnt,
+                      float scale, float *out, float *lse, void *pack, size_t pack_bytes, int pack_mode,
+                      void *workspace, size_t workspace_bytes, ssd_stream_t stream, const char *who) {
   KVView v;
   int rc = validate_kv(kv, &v, who);
   if (rc) return rc;
-  if ((rc = draft_checks(kv, h_q, q, idx, k_max, cnt, out, who))) return rc;
+  if (pack_mode != SSD_PACK_NONE && pack_mode != SSD_PACK_WRITE && pack_mode != SSD_PACK_READ)
+    return fail(SSD_ERR_INVALID_ARG, "%s: pack_mode %d unknown", who, pack_mode);
+  if ((rc = draft_checks(kv, h_q, q, idx, k_max, cnt, out, who, pack_mode != SSD_PACK_READ))) return rc;
   const size_t need = ssd_draft_workspace_bytes(kv, h_q, k_max);
   if (!workspace || workspace_bytes < need)
     return fail(SSD_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", who, workspace_bytes, need);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(SSD_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  if (pack_mode != SSD_PACK_NONE) {
+    const size_t pneed = pack_bytes_of(kv, k_max);
+    if (!pack || pack_bytes < pneed)
+      return fail(SSD_ERR_WORKSPACE, "%s: row pack %zu bytes, need %zu", who, pack ? pack_bytes : 0, pneed);
+    if (reinterpret_cast<uintptr_t>(pack) & 255u)
+      return fail(SSD_ERR_INVALID_ARG, "%s: row pack must be 256-byte aligned", who);
+  }
   if (kv->batch == 0) return SSD_OK;
   unsigned *status = device_status();
   if (!status) return SSD_ERR_CUDA;
@@ -106,7 +121,31 @@ extern "C" int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, co
   a.out = out;
   a.lse = lse;
   a.status = status;
+  a.pack = pack_mode != SSD_PACK_NONE ? static_cast<char *>(pack) : nullptr;
+  a.pack_mode = pack_mode;
   draft_carve(static_cast<unsigned *>(workspace), static_cast<char *>(workspace) + kCounterBytes, units, C_max,
               draft_gmax(a.G), kv->d, a);
   return launch_draft_any(kv->dtype, kv->d, a, dim3(C_max, units), reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
+                              const int32_t *cnt, float scale, float *out, float *lse, void *workspace,
+                              size_t workspace_bytes, ssd_stream_t stream) {
+  return draft_call(kv, q, h_q, idx, k_max, cnt, scale, out, lse, nullptr, 0, SSD_PACK_NONE, workspace,
+                    workspace_bytes, stream, "ssd_draft_attn");
+}
+
+extern "C" size_t ssd_draft_pack_bytes(const ssd_paged_kv *kv, int k_max) {
+  if (!kv || kv->h_kv <= 0 || k_max < 0 || kv->batch < 0 || (kv->d != 64 && kv->d != 128) ||
+      (kv->dtype != SSD_DTYPE_BF16 && kv->dtype != SSD_DTYPE_F32))
+    return 0;
+  return pack_bytes_of(kv, k_max);
+}
+
+extern "C" int ssd_draft_attn_packed(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
+                                     const int32_t *cnt, float scale, float *out, float *lse, void *pack,
+                                     size_t pack_bytes, int pack_mode, void *workspace, size_t workspace_bytes,
+                                     ssd_stream_t stream) {
+  return draft_call(kv, q, h_q, idx, k_max, cnt, scale, out, lse, pack, pack_bytes, pack_mode, workspace,
+                    workspace_bytes, stream, "ssd_draft_attn_packed");
 }

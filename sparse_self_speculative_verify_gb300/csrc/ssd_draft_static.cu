@@ -31,7 +31,7 @@ int draft_gmax(int G);
 size_t draft_data_bytes(int units, int C_max, int gmax, int D);
 void draft_carve(unsigned *counters, void *data, int units, int C_max, int gmax, int D, DraftArgs &a);
 int draft_checks(const ssd_paged_kv *kv, int h_q, const void *q, const int32_t *idx, int k_max, const int32_t *cnt,
-                 const float *out, const char *who);
+                 const float *out, const char *who, bool need_idx = true);
 int launch_draft_any(int dtype, int D, const DraftArgs &a, dim3 grid, cudaStream_t st);
 
 constexpr size_t kDraftStaticBytes = size_t(16) << 20;

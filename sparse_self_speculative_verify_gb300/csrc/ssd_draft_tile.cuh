@@ -11,6 +11,13 @@
 // fragments, O^T = V^T P^T with P as bf16 high + residual parts); fp32 caches use CUDA cores.  The
 // chunk's partial result is merged with the other chunks of the same (request, KV head) by the last
 // chunk to finish (atomic ticket, no wait).
+//
+// All k drafts of a round attend the same selected set (SparseSpec §4.1: the pattern is refreshed
+// only by the next verify), so the first draft can store each chunk's gathered K and V tiles, as
+// they sit in shared memory, into a contiguous "row pack"; the later drafts copy those tiles back
+// with linear loads and skip the index, length and page-table lookups and the scattered 256-byte
+// row reads.  Pack layout: [unit][chunk][K tile, V tile], each tile kDraftChunk rows of D elements
+// in the swizzled shared-memory order; rows past the chunk's count are neither stored nor read.
 #pragma once
 
 #include "ssd_common.cuh"
@@ -31,6 +38,8 @@ struct DraftArgs {
   float *out;          // [B][h_q][D]
   float *lse;          // [B][h_q] or nullptr
   const uint8_t *phase;  // unified launch: draft items only for phase == 0 (nullptr otherwise)
+  char *pack;            // row pack [units][C_max][2][TILE] (pack_mode != SSD_PACK_NONE)
+  int pack_mode;         // SSD_PACK_NONE / SSD_PACK_WRITE (gather, then store the tiles) / SSD_PACK_READ
   unsigned *status;
 };
 
@@ -71,11 +80,11 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   const int b = unit / h_kv, g = unit % h_kv, G = a.G;
   // The list length, the request length and this chunk's token indices are loaded together (none
   // depends on another), so a block waits for one memory latency before it can resolve its rows.
+  const bool from_pack = a.pack_mode == SSD_PACK_READ, to_pack = a.pack_mode == SSD_PACK_WRITE;
   const int j0 = chunk * kDraftChunk;
-  const int32_t *tok = a.idx + (int64_t)unit * a.k_max + j0;
   int t_mine = -1;
-  if (tid < kDraftChunk && j0 + tid < a.k_max) t_mine = __ldg(tok + tid);
-  const int L = effective_len(a.kv, b, 0, a.status);
+  if (!from_pack && tid < kDraftChunk && j0 + tid < a.k_max) t_mine = __ldg(a.idx + (int64_t)unit * a.k_max + j0 + tid);
+  const int L = from_pack ? 0 : effective_len(a.kv, b, 0, a.status);
   int n_all = a.cnt[unit];
   if (n_all < 0 || n_all > a.k_max) {
     atomicOr(a.status, (unsigned)SSD_FAULT_KMAX);
@@ -94,8 +103,16 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   float *sL = sM + GMAX;                                       // [GMAX]
   int64_t *sRow = reinterpret_cast<int64_t *>(sL + GMAX);       // [kDraftChunk] K row element offset, -1: none
 
+  // This chunk's K and V tiles in the row pack.
+  char *pk = a.pack ? a.pack + ((int64_t)unit * a.C_max + chunk) * (2 * C::TILE) : nullptr;
+  // Copies a landed tile's first n rows to the pack (16-byte words in shared-memory order).
+  auto store_tile = [&](char *dst, const char *src) {
+    for (int c = tid; c < n * C::CPR; c += blockDim.x)
+      reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
+  };
+
   // Each token's K row, resolved once by its own thread (index check, page-table lookup).
-  if (tid < kDraftChunk) {
+  if (!from_pack && tid < kDraftChunk) {
     int64_t row = -1;
     if (tid < n) {
       if (t_mine >= 0 && t_mine < L) {
@@ -112,8 +129,16 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   }
   __syncthreads();
 
-  // Gather the chunk's K and V rows (rows of skipped tokens are zero-filled).
+  // Gather the chunk's K and V rows (rows of skipped tokens are zero-filled), or copy the packed tiles
+  // (rows past n zero-filled).
   const int64_t v_off = (int64_t)h_kv * a.kv.page_size * D;
+  if (from_pack) {
+    for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
+      const int sz = c / C::CPR < n ? 16 : 0;
+      cp_async16(smem_u32(sKt + c * 16), pk + c * 16, sz);
+      if (!TC) cp_async16(smem_u32(sVt + c * 16), pk + C::TILE + c * 16, sz);
+    }
+  } else
   for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
     int j = c / C::CPR, ch = c % C::CPR;
     const int64_t row = sRow[j];
@@ -155,6 +180,10 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   }
   cp_async_wait<0>();
   __syncthreads();
+  if (to_pack) {
+    store_tile(pk, sKt);
+    if (!TC) store_tile(pk + C::TILE, sVt);
+  }
 
   if constexpr (TC) {
     // S^T = K Q^T: warp w takes tokens 16w .. 16w + 15; A fragments by ldmatrix from the swizzled K
@@ -213,8 +242,12 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   // offsets.
   uint16_t *sP = reinterpret_cast<uint16_t *>(sRow + kDraftChunk);
   if constexpr (TC) {
-    // V rows into the tile the K rows occupied (every thread is past the logits); they land while
-    // the softmax runs.
+    // V rows into the tile the K rows occupied (every thread is past the logits and its pack
+    // stores); they land while the softmax runs.
+    if (from_pack) {
+      for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x)
+        cp_async16(smem_u32(sVt + c * 16), pk + C::TILE + c * 16, c / C::CPR < n ? 16 : 0);
+    } else
     for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
       const int j = c / C::CPR, ch = c % C::CPR;
       const int64_t row = sRow[j];
@@ -257,6 +290,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   if constexpr (TC) {
     cp_async_wait<0>();
     __syncthreads();
+    if (to_pack) store_tile(pk + C::TILE, sVt);
     // O^T = V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ..; A fragments by
     // transposing ldmatrix from the swizzled V tile, B fragments (P^T) from the bf16 P parts.
     constexpr int MTW = D / 16 / 4;

@@ -20,7 +20,7 @@ from . import binding as B
 
 class SpecRound:
     def __init__(self, kv: B.KVCache, h_q: int, n_cand: int, k_max: int, scale: Optional[float] = None,
-                 workspace: Optional[B.Workspace] = None):
+                 workspace: Optional[B.Workspace] = None, pack_rows: bool = True):
         self.kv = kv
         self.h_q = h_q
         self.n_cand = n_cand
@@ -36,6 +36,15 @@ class SpecRound:
         self.cnt = torch.empty((Bsz * hkv,), dtype=torch.int32, device=dev)
         self.out_d = torch.empty((Bsz, h_q, d), dtype=torch.float32, device=dev)
         self.lse_d = torch.empty((Bsz, h_q), dtype=torch.float32, device=dev)
+        # Row pack: the first draft after a selection stores the selected K / V rows contiguously,
+        # the later drafts of the round read them from there.
+        self.pack = None
+        if pack_rows:
+            n = B.ssd_draft_pack_bytes(kv, k_max)
+            self.pack = torch.empty(n + 256, dtype=torch.uint8, device=dev)
+            off = (-self.pack.data_ptr()) % 256
+            self.pack = self.pack[off:off + n]
+        self._packed = False
 
     def verify(self, q_verify: torch.Tensor, stream=None):
         return B.ssd_verify_attn(self.kv, q_verify, self.n_cand, self.scale, out=self.out_v, lse=self.lse_v,
@@ -43,19 +52,29 @@ class SpecRound:
 
     def verify_select(self, q_verify: torch.Tensor, k_per_req: torch.Tensor, stream=None):
         """verify + select in one call: the selection runs inside the criticality pass."""
+        self._packed = False
         return B.ssd_verify_select(self.kv, q_verify, self.n_cand, self.scale, k_per_req, self.k_max, out=self.out_v,
                                    lse=self.lse_v, scores=self.scores, idx=self.idx, cnt=self.cnt, workspace=self.ws,
                                    stream=stream)
 
     def select(self, k_per_req: torch.Tensor, stream=None):
+        self._packed = False
         return B.ssd_select_topk(self.scores, self.kv.seq_lens, k_per_req, self.k_max, self.kv.h_kv,
                                  max_len=self.kv.max_seq_len, idx=self.idx, cnt=self.cnt, stream=stream)
 
     def draft(self, q_draft: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
-        return B.ssd_draft_attn(self.kv, q_draft, self.idx.view(self.kv.batch, self.kv.h_kv, self.k_max),
-                                self.cnt.view(self.kv.batch, self.kv.h_kv), self.scale,
-                                out=out if out is not None else self.out_d, lse=self.lse_d, workspace=self.ws,
-                                stream=stream)
+        """One draft over the current selection.  With the row pack, the first draft after a select
+        stores the selected rows and the following ones read them (same results)."""
+        idx = self.idx.view(self.kv.batch, self.kv.h_kv, self.k_max)
+        cnt = self.cnt.view(self.kv.batch, self.kv.h_kv)
+        o = out if out is not None else self.out_d
+        if self.pack is None:
+            return B.ssd_draft_attn(self.kv, q_draft, idx, cnt, self.scale, out=o, lse=self.lse_d, workspace=self.ws,
+                                    stream=stream)
+        mode = B.PACK_READ if self._packed else B.PACK_WRITE
+        self._packed = True
+        return B.ssd_draft_attn_packed(self.kv, q_draft, idx, cnt, self.scale, self.pack, mode, out=o, lse=self.lse_d,
+                                       workspace=self.ws, stream=stream)
 
     def draft_oracle_topk(self, q_draft: torch.Tensor, k_per_req: torch.Tensor, out: Optional[torch.Tensor] = None,
                           stream=None) -> dict:

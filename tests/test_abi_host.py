@@ -124,6 +124,25 @@ def test_draft_and_union_argument_errors(lib):
     assert lib.ssd_combine(None, 16, 4, 2, 128, 16, None, None) == binding.SSD_ERR_INVALID_ARG
 
 
+def test_draft_pack_sizes_and_argument_errors(lib):
+    kv = _kv()
+    need = lib.ssd_draft_pack_bytes(ctypes.byref(kv), 410)
+    assert need == 2 * 8 * 7 * 2 * 64 * 128 * 2  # units x chunks x (K, V) x 64 rows x d x bf16
+    assert lib.ssd_draft_pack_bytes(ctypes.byref(_kv(dtype=binding.SSD_DTYPE_F32)), 64) == 2 * 8 * 2 * 64 * 128 * 4
+    assert lib.ssd_draft_pack_bytes(None, 4) == 0
+    assert lib.ssd_draft_pack_bytes(ctypes.byref(_kv(d=96)), 4) == 0
+    E, W = binding.SSD_ERR_INVALID_ARG, binding.SSD_ERR_WORKSPACE
+
+    def call(idx, pack, pack_bytes, mode):
+        return lib.ssd_draft_attn_packed(ctypes.byref(kv), 16, 32, idx, 410, 16, 0.1, 16, None, pack, pack_bytes, mode,
+                                         1 << 20, 1 << 40, None)
+    assert call(16, 1 << 21, need, 3) == E            # unknown mode
+    assert call(None, 1 << 21, need, 1) == E          # writing the pack reads idx
+    assert call(16, 1 << 21, need - 1, 1) == W        # pack too small
+    assert call(None, None, need, 2) == W             # no pack to read
+    assert call(None, (1 << 21) + 16, need, 2) == E   # pack not 256-byte aligned
+
+
 def test_kv_append_and_advance_argument_errors(lib):
     kv = _kv()
     E, OK = binding.SSD_ERR_INVALID_ARG, binding.SSD_OK
