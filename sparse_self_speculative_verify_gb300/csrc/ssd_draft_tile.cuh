@@ -15,14 +15,33 @@
 // All k drafts of a round attend the same selected set (SparseSpec §4.1: the pattern is refreshed
 // only by the next verify), so the first draft can store each chunk's gathered K and V tiles, as
 // they sit in shared memory, into a contiguous "row pack"; the later drafts copy those tiles back
-// with linear loads and skip the index, length and page-table lookups and the scattered 256-byte
-// row reads.  Pack layout: [unit][chunk][K tile, V tile], each tile kDraftChunk rows of D elements
+// (bf16: one bulk copy per tile, completed on an mbarrier) and skip the index, length and
+// page-table lookups and the scattered 256-byte row reads.  Pack layout: [unit][chunk][K tile, V tile], each tile kDraftChunk rows of D elements
 // in the swizzled shared-memory order; rows past the chunk's count are neither stored nor read.
 #pragma once
 
 #include "ssd_common.cuh"
+#include "ssd_sm100.cuh"
 
 namespace ssd {
+
+// Bounded wait of every thread for a bulk tile load (about a second at the SM clock); on expiry the
+// block's outputs are flagged invalid and it carries on.
+constexpr long long kDraftWaitCycles = 2000000000ll;
+__device__ __forceinline__ bool draft_tile_wait(uint32_t bar, uint32_t parity, unsigned *status) {
+  if (sm100::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!sm100::mbar_try_wait_sleep(bar, parity, 20000u))
+    if (clock64() - t0 > kDraftWaitCycles) {
+      atomicOr(status, (unsigned)SSD_FAULT_TIMEOUT);
+      return false;
+    }
+  return true;
+}
+// Waits for the tile; after an expired wait, once more (bounded) for the copy still in flight.
+__device__ __forceinline__ void draft_tile_wait_all(uint32_t bar, uint32_t parity, unsigned *status) {
+  if (!draft_tile_wait(bar, parity, status)) draft_tile_wait(bar, parity, status);
+}
 
 struct DraftArgs {
   KVView kv;
@@ -93,8 +112,8 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   const int n_chunks = draft_chunks(n_all);
   if (chunk >= n_chunks) return;
   const int n = min(kDraftChunk, n_all - j0);  // may be 0 for an empty list
-
   constexpr bool TC = C::TC;
+
   char *sKt = smem;
   char *sVt = TC ? smem : smem + C::TILE;  // the tensor-core path loads V into the K tile after the logits
   float *sQ = reinterpret_cast<float *>(smem + (TC ? 1 : 2) * C::TILE);  // [GMAX][D]
@@ -110,6 +129,16 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     for (int c = tid; c < n * C::CPR; c += blockDim.x)
       reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
   };
+
+  // Reading the pack on the tensor-core path: each tile arrives by one bulk copy of its n rows,
+  // counted on an mbarrier in the (then unused) row table.
+  const bool bulk = TC && from_pack;
+  const uint32_t bar = smem_u32(sRow);
+  if (bulk && tid == 0) {
+    sm100::mbar_init(bar, 1);
+    sm100::mbar_init_fence();
+    sm100::fence_proxy_async_smem();
+  }
 
   // Each token's K row, resolved once by its own thread (index check, page-table lookup).
   if (!from_pack && tid < kDraftChunk) {
@@ -132,7 +161,13 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   // Gather the chunk's K and V rows (rows of skipped tokens are zero-filled), or copy the packed tiles
   // (rows past n zero-filled).
   const int64_t v_off = (int64_t)h_kv * a.kv.page_size * D;
-  if (from_pack) {
+  if (bulk) {
+    // K rows past n stay as they are: their logits are replaced by -inf.
+    if (tid == 0 && n > 0) {
+      sm100::mbar_arrive_expect_tx(bar, (uint32_t)(n * C::ROWB));
+      sm100::bulk_load(smem_u32(sKt), pk, (uint32_t)(n * C::ROWB), bar);
+    }
+  } else if (from_pack) {
     for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
       const int sz = c / C::CPR < n ? 16 : 0;
       cp_async16(smem_u32(sKt + c * 16), pk + c * 16, sz);
@@ -179,6 +214,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     }
   }
   cp_async_wait<0>();
+  if (bulk && n > 0) draft_tile_wait_all(bar, 0, a.status);
   __syncthreads();
   if (to_pack) {
     store_tile(pk, sKt);
@@ -244,7 +280,16 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   if constexpr (TC) {
     // V rows into the tile the K rows occupied (every thread is past the logits and its pack
     // stores); they land while the softmax runs.
-    if (from_pack) {
+    if (bulk) {
+      if (tid == 0 && n > 0) {
+        sm100::fence_proxy_async_smem();  // the tile's K rows were read by every thread before the barrier
+        sm100::mbar_arrive_expect_tx(bar, (uint32_t)(n * C::ROWB));
+        sm100::bulk_load(smem_u32(sVt), pk + C::TILE, (uint32_t)(n * C::ROWB), bar);
+      }
+      // V rows past n are zeroed (their P is 0, but 0 times a stale non-finite value is not).
+      for (int c = n * C::CPR + tid; c < kDraftChunk * C::CPR; c += blockDim.x)
+        reinterpret_cast<uint4 *>(sVt)[c] = make_uint4(0u, 0u, 0u, 0u);
+    } else if (from_pack) {
       for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x)
         cp_async16(smem_u32(sVt + c * 16), pk + C::TILE + c * 16, c / C::CPR < n ? 16 : 0);
     } else
@@ -289,6 +334,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   float *red = TC ? sQ : reinterpret_cast<float *>(sKt);
   if constexpr (TC) {
     cp_async_wait<0>();
+    if (bulk && n > 0) draft_tile_wait_all(bar, 1, a.status);
     __syncthreads();
     if (to_pack) store_tile(pk + C::TILE, sVt);
     // O^T = V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ..; A fragments by

@@ -1,5 +1,5 @@
 // ssd_sm100.cuh -- inline-PTX wrappers for the Blackwell (sm_100 family, built for sm_103a) features
-// the tensor-core verify kernel uses: mbarriers with bounded waits, TMA tensor loads, and the
+// the tensor-core verify kernel uses: mbarriers with bounded waits, TMA tensor and bulk loads, and the
 // tcgen05 tensor-memory MMA path (alloc, mma, commit, ld, st, fences).
 //
 // Shared-memory matrix descriptors (64-bit): start address >> 4 in bits 0-13, leading byte offset
@@ -128,6 +128,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to this
+// block's shared memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 // ---- tcgen05 --------------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
