@@ -14,6 +14,31 @@ __global__ void __launch_bounds__(128) draft_kernel(DraftArgs a) {
 
 int draft_gmax(int G) { return G <= 4 ? 4 : (G <= 8 ? 8 : 16); }
 
+// Reading the row pack of a bf16 cache: one block per (request, KV head).
+template <int D, int GMAX>
+__global__ void __launch_bounds__(128) draft_pack_kernel(DraftArgs a) {
+  extern __shared__ __align__(128) char smem[];
+  draft_pack_unit<D, GMAX>(a, blockIdx.x, smem);
+}
+
+template <int D, int GMAX>
+static int launch_draft_pack(const DraftArgs &a, int units, cudaStream_t st) {
+  constexpr int smem = DraftPackCfg<D, GMAX>::SMEM;
+  int rc = ensure_smem<draft_pack_kernel<D, GMAX>>(smem);
+  if (rc) return rc;
+  draft_pack_kernel<D, GMAX><<<units, 128, smem, st>>>(a);
+  return check_launch("draft_pack_kernel");
+}
+
+static int launch_draft_pack_any(int D, const DraftArgs &a, int units, cudaStream_t st) {
+  const int gmax = draft_gmax(a.G);
+  if (D == 128)
+    return gmax == 4 ? launch_draft_pack<128, 4>(a, units, st)
+                     : (gmax == 8 ? launch_draft_pack<128, 8>(a, units, st) : launch_draft_pack<128, 16>(a, units, st));
+  return gmax == 4 ? launch_draft_pack<64, 4>(a, units, st)
+                   : (gmax == 8 ? launch_draft_pack<64, 8>(a, units, st) : launch_draft_pack<64, 16>(a, units, st));
+}
+
 template <int D, typename T, int GMAX>
 static int launch_draft(const DraftArgs &a, dim3 grid, cudaStream_t st) {
   constexpr int smem = DraftCfg<D, T, GMAX>::SMEM;
@@ -125,6 +150,8 @@ static int draft_call(const ssd_paged_kv *kv, const void *q, int h_q, const int3
   a.pack_mode = pack_mode;
   draft_carve(static_cast<unsigned *>(workspace), static_cast<char *>(workspace) + kCounterBytes, units, C_max,
               draft_gmax(a.G), kv->d, a);
+  if (pack_mode == SSD_PACK_READ && kv->dtype == SSD_DTYPE_BF16)
+    return launch_draft_pack_any(kv->d, a, units, reinterpret_cast<cudaStream_t>(stream));
   return launch_draft_any(kv->dtype, kv->d, a, dim3(C_max, units), reinterpret_cast<cudaStream_t>(stream));
 }
 

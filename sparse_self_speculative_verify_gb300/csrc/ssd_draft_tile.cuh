@@ -502,4 +502,225 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   if (tid == 0) a.counters[unit] = 0u;
 }
 
+// ---- Reading the row pack, bf16: one block per (request, KV head) ------------------------------
+// The unit's packed chunks stream through kPackStages stages of (K tile, V tile), each tile one bulk
+// copy of the chunk's rows, while the block runs an online softmax over the chunks: a running max
+// and sum per head, the output accumulators rescaled whenever the max grows.  Nothing leaves the
+// block before the normalised output, so there are no chunk partials and no merge.
+constexpr int kPackStages = 2;
+
+template <int D, int GMAX>
+struct DraftPackCfg {
+  static constexpr int ROWB = D * 2;
+  static constexpr int CPR = ROWB / 16;
+  static constexpr int TILE = kDraftChunk * ROWB;
+  // [stages][K tile, V tile]; logits [GMAX][chunk] fp32; P as bf16 high + residual parts
+  // [2][GMAX][chunk]; running max, running sum and rescale factor [GMAX] each; an mbarrier per stage.
+  static constexpr int OFF_S = kPackStages * 2 * TILE;
+  static constexpr int OFF_P = OFF_S + GMAX * kDraftChunk * 4;
+  static constexpr int OFF_M = OFF_P + 2 * GMAX * kDraftChunk * 2;
+  static constexpr int OFF_BAR = OFF_M + 3 * GMAX * 4;
+  static constexpr int SMEM = OFF_BAR + kPackStages * 8;
+  static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+};
+
+template <int D, int GMAX>
+__device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, char *smem) {
+  using C = DraftPackCfg<D, GMAX>;
+  constexpr int NT8 = (GMAX + 7) / 8;  // 8-wide head tiles
+  constexpr int KS = D / 16;           // 16-wide steps over d
+  constexpr int MTW = D / 16 / 4;      // 16-row d tiles per warp in P V
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  const int h_kv = a.kv.h_kv, b = unit / h_kv, g = unit % h_kv, G = a.G;
+  int n_all = a.cnt[unit];
+  if (n_all < 0 || n_all > a.k_max) {
+    if (tid == 0) atomicOr(a.status, (unsigned)SSD_FAULT_KMAX);
+    n_all = n_all < 0 ? 0 : a.k_max;
+  }
+  const int nch = cdiv(n_all, kDraftChunk);  // 0 for an empty list
+  float *sS = reinterpret_cast<float *>(smem + C::OFF_S);
+  uint16_t *sP = reinterpret_cast<uint16_t *>(smem + C::OFF_P);
+  float *sM = reinterpret_cast<float *>(smem + C::OFF_M), *sL = sM + GMAX, *sA = sL + GMAX;
+  const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
+  const char *pu = a.pack + (int64_t)unit * a.C_max * (2 * C::TILE);
+
+  // Chunk c's n rows of K and of V into stage c % kPackStages (thread 0).
+  auto issue = [&](int c) {
+    const int st = c % kPackStages;
+    const uint32_t bytes = (uint32_t)(min(kDraftChunk, n_all - c * kDraftChunk) * C::ROWB);
+    const uint32_t bar = bar0 + 8 * st;
+    const char *src = pu + (int64_t)c * (2 * C::TILE);
+    const uint32_t dst = smem_u32(smem + st * (2 * C::TILE));
+    sm100::mbar_arrive_expect_tx(bar, 2 * bytes);
+    sm100::bulk_load(dst, src, bytes, bar);
+    sm100::bulk_load(dst + C::TILE, src + C::TILE, bytes, bar);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < kPackStages; ++st) sm100::mbar_init(bar0 + 8 * st, 1);
+    sm100::mbar_init_fence();
+    sm100::fence_proxy_async_smem();
+    for (int c = 0; c < min(nch, kPackStages); ++c) issue(c);
+  }
+  if (tid < GMAX) {
+    sM[tid] = -INFINITY;
+    sL[tid] = 0.f;
+  }
+
+  // B fragments of Q^T in registers: head n = 8 nt + lane / 4, dims k0, k0 + 1 and k0 + 8, k0 + 9.
+  uint32_t qb[NT8][KS][2];
+  {
+    const unsigned short *q16 = reinterpret_cast<const unsigned short *>(a.q);
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+      const int hn = nt * 8 + (lane >> 2);
+      const unsigned short *qr = q16 + ((int64_t)b * a.h_q + g * G + (hn < G ? hn : 0)) * D + (lane & 3) * 2;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t v0 = 0, v1 = 0;
+        if (hn < G) {
+          v0 = (uint32_t)__ldg(qr + ks * 16) | ((uint32_t)__ldg(qr + ks * 16 + 1) << 16);
+          v1 = (uint32_t)__ldg(qr + ks * 16 + 8) | ((uint32_t)__ldg(qr + ks * 16 + 9) << 16);
+        }
+        qb[nt][ks][0] = v0;
+        qb[nt][ks][1] = v1;
+      }
+    }
+  }
+  float o[MTW][NT8][4];
+#pragma unroll
+  for (int mi = 0; mi < MTW; ++mi)
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
+  __syncthreads();  // barriers initialised, running statistics set
+
+  for (int c = 0; c < nch; ++c) {
+    const int st = c % kPackStages;
+    const char *sKt = smem + st * (2 * C::TILE);
+    char *sVt = smem + st * (2 * C::TILE) + C::TILE;
+    const int n = min(kDraftChunk, n_all - c * kDraftChunk);
+    draft_tile_wait_all(bar0 + 8 * st, (uint32_t)((c / kPackStages) & 1), a.status);
+    // V rows past n (last chunk) are zeroed: their P is 0, but 0 times a stale non-finite value is
+    // not.  K rows past n need nothing: their logits are replaced by -inf.
+    for (int e = n * C::CPR + tid; e < kDraftChunk * C::CPR; e += blockDim.x)
+      reinterpret_cast<uint4 *>(sVt)[e] = make_uint4(0u, 0u, 0u, 0u);
+
+    // S^T = K Q^T: warp w takes tokens 16w .. 16w + 15.
+    {
+      float acc[NT8][4];
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      const int ar = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int ch = 2 * ks + (lane >> 4);
+        uint32_t af[4];
+        ldsm_x4(smem_u32(sKt + ar * C::ROWB + swz_chunk(ar, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) mma_bf16(acc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = warp * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
+          if (h < G) sS[h * kDraftChunk + j] = (j < n) ? acc[nt][e] * a.scale_log2 : -INFINITY;
+        }
+    }
+    __syncthreads();
+
+    // Online softmax, one warp per head: the new running max, this chunk's P against it (bf16 high
+    // + residual parts), the factor that rescales the earlier chunks, and the running sum.
+    for (int h = warp; h < G; h += nwarps) {
+      const float v0 = sS[h * kDraftChunk + lane], v1 = sS[h * kDraftChunk + lane + 32];
+      const float m_old = sM[h];
+      const float m_new = fmaxf(m_old, warp_max(fmaxf(v0, v1)));
+      const float base = (m_new == -INFINITY) ? 0.f : m_new;
+      const float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
+      uint32_t hi, lo;
+      split_bf16(p0, p1, hi, lo);
+      sP[h * kDraftChunk + lane] = (uint16_t)(hi & 0xffffu);
+      sP[h * kDraftChunk + lane + 32] = (uint16_t)(hi >> 16);
+      sP[(GMAX + h) * kDraftChunk + lane] = (uint16_t)(lo & 0xffffu);
+      sP[(GMAX + h) * kDraftChunk + lane + 32] = (uint16_t)(lo >> 16);
+      const float l = warp_sum(p0 + p1);
+      if (lane == 0) {
+        const float alpha = fast_exp2(m_old - base);  // 0 before the first chunk (m_old = -inf)
+        sM[h] = m_new;
+        sL[h] = sL[h] * alpha + l;
+        sA[h] = alpha;
+      }
+    }
+    __syncthreads();
+
+    // O^T = alpha O^T + V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ...
+    {
+      float al[NT8][2];
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int h = nt * 8 + (lane & 3) * 2 + k;
+          al[nt][k] = h < G ? sA[h] : 1.f;
+        }
+#pragma unroll
+      for (int mi = 0; mi < MTW; ++mi)
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mi][nt][e] *= al[nt][e & 1];
+#pragma unroll
+      for (int ks = 0; ks < kDraftChunk / 16; ++ks) {
+        uint32_t bh[NT8][2], bl[NT8][2];
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) {
+          const int hn = nt * 8 + (lane >> 2), k0 = ks * 16 + (lane & 3) * 2;
+          bh[nt][0] = bh[nt][1] = bl[nt][0] = bl[nt][1] = 0u;
+          if (hn < G) {
+            bh[nt][0] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0);
+            bh[nt][1] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0 + 8);
+            bl[nt][0] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0);
+            bl[nt][1] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0 + 8);
+          }
+        }
+        const int tr = ks * 16 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+        for (int mi = 0; mi < MTW; ++mi) {
+          const int ch = 2 * (warp * MTW + mi) + ((lane >> 3) & 1);
+          uint32_t af[4];
+          ldsm_x4_t(smem_u32(sVt + tr * C::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT8; ++nt) {
+            mma_bf16(o[mi][nt], af, bh[nt][0], bh[nt][1]);
+            mma_bf16(o[mi][nt], af, bl[nt][0], bl[nt][1]);
+          }
+        }
+      }
+    }
+    __syncthreads();  // the stage's tiles, the logits and P are free
+    if (tid == 0 && c + kPackStages < nch) {
+      sm100::fence_proxy_async_smem();  // the stage was read by every thread before the barrier
+      issue(c + kPackStages);
+    }
+  }
+
+  // Normalised output: c0, c1 at d = 16 mt + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3 at d + 8.
+#pragma unroll
+  for (int mi = 0; mi < MTW; ++mi)
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int dd = (warp * MTW + mi) * 16 + (lane >> 2) + (e >> 1) * 8;
+        const int h = nt * 8 + (lane & 3) * 2 + (e & 1);
+        if (h < G) {
+          const float l = sL[h];
+          a.out[((int64_t)b * a.h_q + g * G + h) * D + dd] = l > 0.f ? o[mi][nt][e] / l : 0.f;
+        }
+      }
+  if (a.lse && tid < G) {
+    const float l = sL[tid];
+    a.lse[(int64_t)b * a.h_q + g * G + tid] = l > 0.f ? (sM[tid] + __log2f(l)) * kLn2 : -INFINITY;
+  }
+}
+
 }  // namespace ssd

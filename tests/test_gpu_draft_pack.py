@@ -1,7 +1,8 @@
-"""Sparse draft attention through the row pack: the writing call equals the plain draft, and the
-reading calls equal plain drafts of their own queries (bit-exact: the same tiles in shared memory
-and the same arithmetic), so the plain draft's oracle parity carries over; one case is also checked
-against the oracle directly."""
+"""Sparse draft attention through the row pack.  The writing call equals the plain draft bit for bit
+(the same kernel, which also stores its tiles).  The reading calls are checked against the oracle
+and against plain drafts of their own queries: bit-exact for fp32 caches (the plain kernel reading
+the pack); within 1e-4 relative for bf16 caches, whose reader runs one block per (request, KV head) with an
+online softmax over the chunks instead of per-chunk partials merged by log-sum-exp."""
 
 import numpy as np
 import pytest
@@ -27,6 +28,18 @@ def _pack(kv, k_max, fill=None):
     if fill is not None:
         p.fill_(fill)  # NaN bytes for bf16 / fp32 (0xff): rows the reader must not use
     return p
+
+
+def _close(got, ref, what):
+    """Reader against the plain draft: the same sums in another order (online rescaling)."""
+    assert torch.allclose(got, ref, rtol=1e-4, atol=2e-5, equal_nan=False), \
+        f"{what}: max |diff| {(got - ref).abs().max().item():.3g}"
+
+
+def _lse_close(got, ref, what):
+    fin = torch.isfinite(ref)
+    assert torch.equal(fin, torch.isfinite(got)), what
+    _close(got[fin], ref[fin], what)
 
 
 def _queries(w, n):
@@ -65,9 +78,17 @@ def test_pack_write_then_reads_equal_plain_drafts(case):
     ref = [ssd_draft_attn(kv, qs[j], idx, cnt, scale) for j in range(3)]
     torch.cuda.synchronize()
     assert ssd_status() == 0
-    for j in range(3):
-        assert torch.equal(got[j]["out"], ref[j]["out"]), j
-        assert torch.equal(got[j]["lse"], ref[j]["lse"]), j
+    assert torch.equal(got[0]["out"], ref[0]["out"]) and torch.equal(got[0]["lse"], ref[0]["lse"])
+    kv_h, reqs = _gpu.host_subset(w, None)
+    for j in (1, 2):
+        if spec.dtype != "bf16":
+            assert torch.equal(got[j]["out"], ref[j]["out"]) and torch.equal(got[j]["lse"], ref[j]["lse"]), j
+        else:
+            _close(got[j]["out"], ref[j]["out"], f"read {j} out")
+            _lse_close(got[j]["lse"], ref[j]["lse"], f"read {j} lse")
+        o = oracle.draft(kv_h, qs[j].cpu()[reqs], idx.cpu()[reqs], cnt.cpu()[reqs], scale)
+        _gpu.assert_out(got[j]["out"].cpu().numpy()[reqs], o["out"], f"read {j} out vs oracle")
+        _gpu.assert_lse(got[j]["lse"].cpu().numpy()[reqs], o["lse"])
 
 
 def test_pack_read_against_oracle_after_append():
@@ -117,12 +138,12 @@ def test_pack_write_reports_index_faults_like_plain():
     c = ssd_draft_attn_packed(kv, w.q_draft[0], None, cnt, scale, pack, binding.PACK_READ, k_max=64)
     torch.cuda.synchronize()
     assert ssd_status() == 0
-    assert torch.equal(a["out"], c["out"])
+    _close(c["out"], a["out"], "read after faults")
 
 
 def test_round_with_and_without_pack_full_size():
-    """The full-size Qwen3-8B round: drafts through the row pack equal plain drafts, eagerly and when
-    the round is replayed as a CUDA graph."""
+    """The full-size Qwen3-8B round: drafts through the row pack match plain drafts (the first bit for
+    bit), and a replayed CUDA graph of the round reproduces the eager round exactly."""
     _gpu.lib()
     spec = W.SPECS["qwen3_8b"]
     w = W.make_workload(spec, device=DEV)
@@ -136,7 +157,9 @@ def test_round_with_and_without_pack_full_size():
     b.run(w.q_verify, w.q_draft, w.k_per_req, draft_outs=ob)
     torch.cuda.synchronize()
     assert ssd_status() == 0
-    assert torch.equal(oa, ob)
+    assert torch.equal(oa[0], ob[0])
+    _close(ob[1:], oa[1:], "drafts 2..k")
+    eager = ob.clone()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
@@ -149,4 +172,4 @@ def test_round_with_and_without_pack_full_size():
         g.replay()
     torch.cuda.synchronize()
     assert ssd_status() == 0
-    assert torch.equal(oa, ob)
+    assert torch.equal(eager, ob)
