@@ -31,6 +31,7 @@ static int launch_draft_pack(const DraftArgs &a, int units, cudaStream_t st) {
 }
 
 static int launch_draft_pack_any(int D, const DraftArgs &a, int units, cudaStream_t st) {
+  if (!a.pack) return fail(SSD_ERR_INVALID_ARG, "draft: reading the row pack without a pack");
   const int gmax = draft_gmax(a.G);
   if (D == 128)
     return gmax == 4 ? launch_draft_pack<128, 4>(a, units, st)
