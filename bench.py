@@ -568,8 +568,20 @@ def run_rows(args) -> list:
     idx = sel["idx"].view(spec.batch, spec.h_kv, k_max)
     cnt = sel["cnt"].view(spec.batch, spec.h_kv)
     ms = _time_calls(lambda: Bd.ssd_draft_attn(kv, w.q_draft[0], idx, cnt, scale, workspace=ws))
-    line("a5 sparse draft", spec.name, ms, M.draft_kv_bytes(kpr, lens, spec.h_kv, spec.d, spec.elem_bytes))
-    del w, kv, r, sel, idx, cnt
+    dbytes = M.draft_kv_bytes(kpr, lens, spec.h_kv, spec.d, spec.elem_bytes)
+    line("a5 sparse draft", spec.name, ms, dbytes)
+    # The same draft through the row pack: the round's first draft (gathers and stores the rows) and
+    # each later one (reads them back).
+    npk = Bd.ssd_draft_pack_bytes(kv, k_max)
+    pk = torch.empty(npk + 256, dtype=torch.uint8, device=dev)
+    pk = pk[(-pk.data_ptr()) % 256:][:npk]
+    ms = _time_calls(lambda: Bd.ssd_draft_attn_packed(kv, w.q_draft[0], idx, cnt, scale, pk, Bd.PACK_WRITE,
+                                                      workspace=ws))
+    line("a5 sparse draft, first of a round (row pack written)", spec.name, ms, dbytes)
+    ms = _time_calls(lambda: Bd.ssd_draft_attn_packed(kv, w.q_draft[1], None, cnt, scale, pk, Bd.PACK_READ,
+                                                      k_max=k_max, workspace=ws))
+    line("a5 sparse draft, later in a round (row pack read)", spec.name, ms, dbytes)
+    del w, kv, r, sel, idx, cnt, pk
     torch.cuda.empty_cache()
 
     # Qwen3-14B mixed batch: one unified launch against a verify call and a draft call on the two
