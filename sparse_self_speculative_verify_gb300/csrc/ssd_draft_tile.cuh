@@ -90,6 +90,121 @@ __device__ __forceinline__ void unpack16<float>(const uint4 &v, float *f) {
   f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
 }
 
+// ---- Tensor-core pieces of a bf16 draft chunk (mma.sync m16n8k16, fp32 accumulate) -------------
+// The queries stay in registers as B fragments; K and V come from a swizzled row tile in shared
+// memory through ldmatrix; P goes through bf16 high + residual parts (about 16 bits).
+template <int D, int GMAX>
+struct DraftMma {
+  static constexpr int NT8 = (GMAX + 7) / 8;  // 8-wide head tiles
+  static constexpr int KS = D / 16;           // 16-wide steps over d
+  static constexpr int MTW = D / 16 / 4;      // 16-row d tiles per warp (4 warps) in P V
+  static constexpr int ROWB = D * 2;
+};
+
+// B fragments of Q^T for query heads g G .. g G + G - 1 of request b: head n = 8 nt + lane / 4,
+// dims k0, k0 + 1 and k0 + 8, k0 + 9 (zero for heads past G).
+template <int D, int GMAX>
+__device__ __forceinline__ void draft_q_frags(const void *q, int64_t row0, int G, int lane,
+                                              uint32_t (&qb)[DraftMma<D, GMAX>::NT8][DraftMma<D, GMAX>::KS][2]) {
+  using M = DraftMma<D, GMAX>;
+  const unsigned short *q16 = reinterpret_cast<const unsigned short *>(q);
+#pragma unroll
+  for (int nt = 0; nt < M::NT8; ++nt) {
+    const int hn = nt * 8 + (lane >> 2);
+    const unsigned short *qr = q16 + (row0 + (hn < G ? hn : 0)) * D + (lane & 3) * 2;
+#pragma unroll
+    for (int ks = 0; ks < M::KS; ++ks) {
+      uint32_t v0 = 0, v1 = 0;
+      if (hn < G) {
+        v0 = (uint32_t)__ldg(qr + ks * 16) | ((uint32_t)__ldg(qr + ks * 16 + 1) << 16);
+        v1 = (uint32_t)__ldg(qr + ks * 16 + 8) | ((uint32_t)__ldg(qr + ks * 16 + 9) << 16);
+      }
+      qb[nt][ks][0] = v0;
+      qb[nt][ks][1] = v1;
+    }
+  }
+}
+
+// Logits S^T = K Q^T of the chunk into sS[h][j] (scaled to log2 units; -inf for j >= n): warp w
+// takes tokens 16w .. 16w + 15, its A fragments by ldmatrix from the swizzled K tile (thread t
+// addresses row (t & 7) + 8 ((t >> 3) & 1), 16-byte chunk 2 ks + (t >> 4)).
+template <int D, int GMAX>
+__device__ __forceinline__ void draft_logits_mma(const char *sKt,
+                                                 const uint32_t (&qb)[DraftMma<D, GMAX>::NT8][DraftMma<D, GMAX>::KS][2],
+                                                 float *sS, int n, float scale_log2, int G, int warp, int lane) {
+  using M = DraftMma<D, GMAX>;
+  float acc[M::NT8][4];
+#pragma unroll
+  for (int nt = 0; nt < M::NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  const int ar = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+  for (int ks = 0; ks < M::KS; ++ks) {
+    const int ch = 2 * ks + (lane >> 4);
+    uint32_t af[4];
+    ldsm_x4(smem_u32(sKt + ar * M::ROWB + swz_chunk(ar, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+    for (int nt = 0; nt < M::NT8; ++nt) mma_bf16(acc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+  }
+  // c0, c1: token 16w + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3: token + 8.
+#pragma unroll
+  for (int nt = 0; nt < M::NT8; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = warp * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
+      if (h < G) sS[h * kDraftChunk + j] = (j < n) ? acc[nt][e] * scale_log2 : -INFINITY;
+    }
+  }
+}
+
+// Writes head h's probabilities p0 (token lane) and p1 (token lane + 32) as bf16 high + residual
+// parts into sP [2][GMAX][chunk].
+template <int GMAX>
+__device__ __forceinline__ void draft_store_p(uint16_t *sP, int h, int lane, float p0, float p1) {
+  uint32_t hi, lo;
+  split_bf16(p0, p1, hi, lo);
+  sP[h * kDraftChunk + lane] = (uint16_t)(hi & 0xffffu);
+  sP[h * kDraftChunk + lane + 32] = (uint16_t)(hi >> 16);
+  sP[(GMAX + h) * kDraftChunk + lane] = (uint16_t)(lo & 0xffffu);
+  sP[(GMAX + h) * kDraftChunk + lane + 32] = (uint16_t)(lo >> 16);
+}
+
+// o += V^T P^T over the chunk: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w MTW ..; A
+// fragments by transposing ldmatrix from the swizzled V tile, B fragments (P^T) from the bf16 P
+// parts.  Accumulator element e of o[mi][nt] sits at d = 16 mt + lane / 4 (+ 8 for e >= 2), head
+// 8 nt + 2 (lane & 3) + (e & 1).
+template <int D, int GMAX>
+__device__ __forceinline__ void draft_pv_mma(const char *sVt, const uint16_t *sP, int G, int warp, int lane,
+                                             float (&o)[DraftMma<D, GMAX>::MTW][DraftMma<D, GMAX>::NT8][4]) {
+  using M = DraftMma<D, GMAX>;
+#pragma unroll
+  for (int ks = 0; ks < kDraftChunk / 16; ++ks) {
+    uint32_t bh[M::NT8][2], bl[M::NT8][2];
+#pragma unroll
+    for (int nt = 0; nt < M::NT8; ++nt) {
+      const int hn = nt * 8 + (lane >> 2), k0 = ks * 16 + (lane & 3) * 2;
+      bh[nt][0] = bh[nt][1] = bl[nt][0] = bl[nt][1] = 0u;
+      if (hn < G) {
+        bh[nt][0] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0);
+        bh[nt][1] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0 + 8);
+        bl[nt][0] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0);
+        bl[nt][1] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0 + 8);
+      }
+    }
+    const int tr = ks * 16 + (lane & 7) + ((lane >> 4) << 3);  // token row of this thread's address
+#pragma unroll
+    for (int mi = 0; mi < M::MTW; ++mi) {
+      const int ch = 2 * (warp * M::MTW + mi) + ((lane >> 3) & 1);
+      uint32_t af[4];
+      ldsm_x4_t(smem_u32(sVt + tr * M::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+      for (int nt = 0; nt < M::NT8; ++nt) {
+        mma_bf16(o[mi][nt], af, bh[nt][0], bh[nt][1]);
+        mma_bf16(o[mi][nt], af, bl[nt][0], bl[nt][1]);
+      }
+    }
+  }
+}
+
 template <int D, typename T, int GMAX>
 __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chunk, char *smem) {
   using C = DraftCfg<D, T, GMAX>;
@@ -183,30 +298,12 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     if (!TC) cp_async16(smem_u32(sVt + off), kr ? (const void *)(kr + v_off + ch * EPC) : a.kv.pool, kr ? 16 : 0);
   }
   cp_async_commit();
-  // bf16 caches: logits and P V on tensor cores (mma.sync m16n8k16, fp32 accumulate); the queries
-  // stay in registers as B fragments, P goes through bf16 high + residual parts (about 16 bits).
-  constexpr int NT8 = (GMAX + 7) / 8;  // 8-wide head tiles
-  constexpr int KS = D / 16;           // 16-wide steps over d
+  // bf16 caches: logits and P V on tensor cores (DraftMma); fp32 caches: CUDA cores.
+  using MM = DraftMma<D, GMAX>;
   const T *q = reinterpret_cast<const T *>(a.q);
-  uint32_t qb[TC ? NT8 : 1][TC ? KS : 1][2];
+  uint32_t qb[MM::NT8][MM::KS][2];
   if constexpr (TC) {
-    // B fragment of Q^T: head n = 8 nt + lane / 4, dims k0, k0 + 1 and k0 + 8, k0 + 9.
-    const unsigned short *q16 = reinterpret_cast<const unsigned short *>(a.q);
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt) {
-      const int hn = nt * 8 + (lane >> 2);
-      const unsigned short *qr = q16 + ((int64_t)b * a.h_q + g * G + (hn < G ? hn : 0)) * D + (lane & 3) * 2;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t v0 = 0, v1 = 0;
-        if (hn < G) {
-          v0 = (uint32_t)__ldg(qr + ks * 16) | ((uint32_t)__ldg(qr + ks * 16 + 1) << 16);
-          v1 = (uint32_t)__ldg(qr + ks * 16 + 8) | ((uint32_t)__ldg(qr + ks * 16 + 9) << 16);
-        }
-        qb[nt][ks][0] = v0;
-        qb[nt][ks][1] = v1;
-      }
-    }
+    draft_q_frags<D, GMAX>(a.q, (int64_t)b * a.h_q + g * G, G, lane, qb);
   } else {
     for (int e = tid; e < G * D; e += blockDim.x) {
       int hl = e / D, dd = e % D;
@@ -222,29 +319,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   }
 
   if constexpr (TC) {
-    // S^T = K Q^T: warp w takes tokens 16w .. 16w + 15; A fragments by ldmatrix from the swizzled K
-    // tile (thread t addresses row (t & 7) + 8 ((t >> 3) & 1), 16-byte chunk 2 ks + (t >> 4)).
-    float acc[NT8][4];
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const int ar = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int ch = 2 * ks + (lane >> 4);
-      uint32_t af[4];
-      ldsm_x4(smem_u32(sKt + ar * C::ROWB + swz_chunk(ar, ch) * 16), af[0], af[1], af[2], af[3]);
-#pragma unroll
-      for (int nt = 0; nt < NT8; ++nt) mma_bf16(acc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
-    }
-    // c0, c1: token 16w + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3: token + 8.
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = warp * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
-        if (h < G) sS[h * kDraftChunk + j] = (j < n) ? acc[nt][e] * a.scale_log2 : -INFINITY;
-      }
-    }
+    draft_logits_mma<D, GMAX>(sKt, qb, sS, n, a.scale_log2, G, warp, lane);
   } else {
     // Logits: thread pair (2j, 2j+1) computes token j, one half of d each.
     const int j = tid >> 1, half = tid & 1;
@@ -311,14 +386,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
     sS[h * kDraftChunk + lane] = p0;
     sS[h * kDraftChunk + lane + 32] = p1;
-    if constexpr (TC) {
-      uint32_t hi, lo;
-      split_bf16(p0, p1, hi, lo);
-      sP[h * kDraftChunk + lane] = (uint16_t)(hi & 0xffffu);
-      sP[h * kDraftChunk + lane + 32] = (uint16_t)(hi >> 16);
-      sP[(GMAX + h) * kDraftChunk + lane] = (uint16_t)(lo & 0xffffu);
-      sP[(GMAX + h) * kDraftChunk + lane + 32] = (uint16_t)(lo >> 16);
-    }
+    if constexpr (TC) draft_store_p<GMAX>(sP, h, lane, p0, p1);
     float l = warp_sum(p0 + p1);
     if (lane == 0) {
       sM[h] = m;
@@ -337,49 +405,19 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     if (bulk && n > 0) draft_tile_wait_all(bar, 1, a.status);
     __syncthreads();
     if (to_pack) store_tile(pk + C::TILE, sVt);
-    // O^T = V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ..; A fragments by
-    // transposing ldmatrix from the swizzled V tile, B fragments (P^T) from the bf16 P parts.
-    constexpr int MTW = D / 16 / 4;
-    float o[MTW][NT8][4];
+    float o[MM::MTW][MM::NT8][4];
 #pragma unroll
-    for (int mi = 0; mi < MTW; ++mi)
+    for (int mi = 0; mi < MM::MTW; ++mi)
 #pragma unroll
-      for (int nt = 0; nt < NT8; ++nt) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
+      for (int nt = 0; nt < MM::NT8; ++nt) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
+    draft_pv_mma<D, GMAX>(sVt, sP, G, warp, lane, o);
 #pragma unroll
-    for (int ks = 0; ks < kDraftChunk / 16; ++ks) {
-      uint32_t bh[NT8][2], bl[NT8][2];
+    for (int mi = 0; mi < MM::MTW; ++mi)
 #pragma unroll
-      for (int nt = 0; nt < NT8; ++nt) {
-        const int hn = nt * 8 + (lane >> 2), k0 = ks * 16 + (lane & 3) * 2;
-        bh[nt][0] = bh[nt][1] = bl[nt][0] = bl[nt][1] = 0u;
-        if (hn < G) {
-          bh[nt][0] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0);
-          bh[nt][1] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0 + 8);
-          bl[nt][0] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0);
-          bl[nt][1] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0 + 8);
-        }
-      }
-      const int tr = ks * 16 + (lane & 7) + ((lane >> 4) << 3);  // token row of this thread's address
-#pragma unroll
-      for (int mi = 0; mi < MTW; ++mi) {
-        const int ch = 2 * (warp * MTW + mi) + ((lane >> 3) & 1);
-        uint32_t af[4];
-        ldsm_x4_t(smem_u32(sVt + tr * C::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
-#pragma unroll
-        for (int nt = 0; nt < NT8; ++nt) {
-          mma_bf16(o[mi][nt], af, bh[nt][0], bh[nt][1]);
-          mma_bf16(o[mi][nt], af, bl[nt][0], bl[nt][1]);
-        }
-      }
-    }
-    // c0, c1: d = 16 mt + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3: d + 8.
-#pragma unroll
-    for (int mi = 0; mi < MTW; ++mi)
-#pragma unroll
-      for (int nt = 0; nt < NT8; ++nt)
+      for (int nt = 0; nt < MM::NT8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int dd = (warp * MTW + mi) * 16 + (lane >> 2) + (e >> 1) * 8;
+          const int dd = (warp * MM::MTW + mi) * 16 + (lane >> 2) + (e >> 1) * 8;
           const int h = nt * 8 + (lane & 3) * 2 + (e & 1);
           if (h < G) red[h * D + dd] = o[mi][nt][e];
         }
@@ -527,9 +565,8 @@ struct DraftPackCfg {
 template <int D, int GMAX>
 __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, char *smem) {
   using C = DraftPackCfg<D, GMAX>;
-  constexpr int NT8 = (GMAX + 7) / 8;  // 8-wide head tiles
-  constexpr int KS = D / 16;           // 16-wide steps over d
-  constexpr int MTW = D / 16 / 4;      // 16-row d tiles per warp in P V
+  using MM = DraftMma<D, GMAX>;
+  constexpr int NT8 = MM::NT8, MTW = MM::MTW;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int h_kv = a.kv.h_kv, b = unit / h_kv, g = unit % h_kv, G = a.G;
   int n_all = a.cnt[unit];
@@ -566,26 +603,8 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     sL[tid] = 0.f;
   }
 
-  // B fragments of Q^T in registers: head n = 8 nt + lane / 4, dims k0, k0 + 1 and k0 + 8, k0 + 9.
-  uint32_t qb[NT8][KS][2];
-  {
-    const unsigned short *q16 = reinterpret_cast<const unsigned short *>(a.q);
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt) {
-      const int hn = nt * 8 + (lane >> 2);
-      const unsigned short *qr = q16 + ((int64_t)b * a.h_q + g * G + (hn < G ? hn : 0)) * D + (lane & 3) * 2;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t v0 = 0, v1 = 0;
-        if (hn < G) {
-          v0 = (uint32_t)__ldg(qr + ks * 16) | ((uint32_t)__ldg(qr + ks * 16 + 1) << 16);
-          v1 = (uint32_t)__ldg(qr + ks * 16 + 8) | ((uint32_t)__ldg(qr + ks * 16 + 9) << 16);
-        }
-        qb[nt][ks][0] = v0;
-        qb[nt][ks][1] = v1;
-      }
-    }
-  }
+  uint32_t qb[NT8][MM::KS][2];
+  draft_q_frags<D, GMAX>(a.q, (int64_t)b * a.h_q + g * G, G, lane, qb);
   float o[MTW][NT8][4];
 #pragma unroll
   for (int mi = 0; mi < MTW; ++mi)
@@ -604,28 +623,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     for (int e = n * C::CPR + tid; e < kDraftChunk * C::CPR; e += blockDim.x)
       reinterpret_cast<uint4 *>(sVt)[e] = make_uint4(0u, 0u, 0u, 0u);
 
-    // S^T = K Q^T: warp w takes tokens 16w .. 16w + 15.
-    {
-      float acc[NT8][4];
-#pragma unroll
-      for (int nt = 0; nt < NT8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-      const int ar = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int ch = 2 * ks + (lane >> 4);
-        uint32_t af[4];
-        ldsm_x4(smem_u32(sKt + ar * C::ROWB + swz_chunk(ar, ch) * 16), af[0], af[1], af[2], af[3]);
-#pragma unroll
-        for (int nt = 0; nt < NT8; ++nt) mma_bf16(acc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = warp * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
-          if (h < G) sS[h * kDraftChunk + j] = (j < n) ? acc[nt][e] * a.scale_log2 : -INFINITY;
-        }
-    }
+    draft_logits_mma<D, GMAX>(sKt, qb, sS, n, a.scale_log2, G, warp, lane);
     __syncthreads();
 
     // Online softmax, one warp per head: the new running max, this chunk's P against it (bf16 high
@@ -636,12 +634,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
       const float m_new = fmaxf(m_old, warp_max(fmaxf(v0, v1)));
       const float base = (m_new == -INFINITY) ? 0.f : m_new;
       const float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
-      uint32_t hi, lo;
-      split_bf16(p0, p1, hi, lo);
-      sP[h * kDraftChunk + lane] = (uint16_t)(hi & 0xffffu);
-      sP[h * kDraftChunk + lane + 32] = (uint16_t)(hi >> 16);
-      sP[(GMAX + h) * kDraftChunk + lane] = (uint16_t)(lo & 0xffffu);
-      sP[(GMAX + h) * kDraftChunk + lane + 32] = (uint16_t)(lo >> 16);
+      draft_store_p<GMAX>(sP, h, lane, p0, p1);
       const float l = warp_sum(p0 + p1);
       if (lane == 0) {
         const float alpha = fast_exp2(m_old - base);  // 0 before the first chunk (m_old = -inf)
@@ -652,7 +645,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     }
     __syncthreads();
 
-    // O^T = alpha O^T + V^T P^T: warp w takes d rows 16 mt .. 16 mt + 15 for mt = w * MTW ...
+    // O^T = alpha O^T + V^T P^T (the accumulators rescaled per head, then this chunk added).
     {
       float al[NT8][2];
 #pragma unroll
@@ -668,33 +661,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
         for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) o[mi][nt][e] *= al[nt][e & 1];
-#pragma unroll
-      for (int ks = 0; ks < kDraftChunk / 16; ++ks) {
-        uint32_t bh[NT8][2], bl[NT8][2];
-#pragma unroll
-        for (int nt = 0; nt < NT8; ++nt) {
-          const int hn = nt * 8 + (lane >> 2), k0 = ks * 16 + (lane & 3) * 2;
-          bh[nt][0] = bh[nt][1] = bl[nt][0] = bl[nt][1] = 0u;
-          if (hn < G) {
-            bh[nt][0] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0);
-            bh[nt][1] = *reinterpret_cast<const uint32_t *>(sP + hn * kDraftChunk + k0 + 8);
-            bl[nt][0] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0);
-            bl[nt][1] = *reinterpret_cast<const uint32_t *>(sP + (GMAX + hn) * kDraftChunk + k0 + 8);
-          }
-        }
-        const int tr = ks * 16 + (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll
-        for (int mi = 0; mi < MTW; ++mi) {
-          const int ch = 2 * (warp * MTW + mi) + ((lane >> 3) & 1);
-          uint32_t af[4];
-          ldsm_x4_t(smem_u32(sVt + tr * C::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
-#pragma unroll
-          for (int nt = 0; nt < NT8; ++nt) {
-            mma_bf16(o[mi][nt], af, bh[nt][0], bh[nt][1]);
-            mma_bf16(o[mi][nt], af, bl[nt][0], bl[nt][1]);
-          }
-        }
-      }
+      draft_pv_mma<D, GMAX>(sVt, sP, G, warp, lane, o);
     }
     __syncthreads();  // the stage's tiles, the logits and P are free
     if (tid == 0 && c + kPackStages < nch) {
