@@ -25,6 +25,17 @@
 
 namespace ssd {
 
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from this block's
+// shared memory to global, in the thread's bulk group.  The shared source may be overwritten once
+// bulk_wait_read() has returned.
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Bounded wait of every thread for a bulk tile load (about a second at the SM clock); on expiry the
 // block's outputs are flagged invalid and it carries on.
 constexpr long long kDraftWaitCycles = 2000000000ll;
@@ -314,8 +325,18 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   if (bulk && n > 0) draft_tile_wait_all(bar, 0, a.status);
   __syncthreads();
   if (to_pack) {
-    store_tile(pk, sKt);
-    if (!TC) store_tile(pk + C::TILE, sVt);
+    if constexpr (TC) {
+      // One bulk store of the landed K rows; its reads of the tile finish before the V rows are
+      // gathered into it.
+      if (tid == 0 && n > 0) {
+        sm100::fence_proxy_async_smem();
+        bulk_store(pk, smem_u32(sKt), (uint32_t)(n * C::ROWB));
+        bulk_commit();
+      }
+    } else {
+      store_tile(pk, sKt);
+      store_tile(pk + C::TILE, sVt);
+    }
   }
 
   if constexpr (TC) {
@@ -348,6 +369,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
       if (half == 0 && h < G) sS[h * kDraftChunk + j] = (j < n) ? s * a.scale_log2 : -INFINITY;
     }
   }
+  if (TC && to_pack && tid == 0) bulk_wait_read();  // the K tile may be overwritten after the barrier
   __syncthreads();
   // P in bf16 high + residual parts [2][GMAX][kDraftChunk] for the tensor-core P V, after the row
   // offsets.
@@ -404,7 +426,11 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     cp_async_wait<0>();
     if (bulk && n > 0) draft_tile_wait_all(bar, 1, a.status);
     __syncthreads();
-    if (to_pack) store_tile(pk + C::TILE, sVt);
+    if (to_pack && tid == 0 && n > 0) {
+      sm100::fence_proxy_async_smem();
+      bulk_store(pk + C::TILE, smem_u32(sVt), (uint32_t)(n * C::ROWB));
+      bulk_commit();
+    }
     float o[MM::MTW][MM::NT8][4];
 #pragma unroll
     for (int mi = 0; mi < MM::MTW; ++mi)
@@ -422,6 +448,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
           if (h < G) red[h * D + dd] = o[mi][nt][e];
         }
     __syncthreads();
+    if (to_pack && tid == 0) bulk_wait_read();  // the V tile's bulk store has read it
   } else {
   // O = P V: thread = (pair of d columns, token part).
   constexpr int TPP = kDraftChunk / PARTS;  // tokens per part
