@@ -14,10 +14,12 @@
 //
 // All k drafts of a round attend the same selected set (SparseSpec §4.1: the pattern is refreshed
 // only by the next verify), so the first draft can store each chunk's gathered K and V tiles, as
-// they sit in shared memory, into a contiguous "row pack"; the later drafts copy those tiles back
-// (bf16: one bulk copy per tile, completed on an mbarrier) and skip the index, length and
-// page-table lookups and the scattered 256-byte row reads.  Pack layout: [unit][chunk][K tile, V tile], each tile kDraftChunk rows of D elements
-// in the swizzled shared-memory order; rows past the chunk's count are neither stored nor read.
+// they sit in shared memory, into a contiguous "row pack" (bf16: one bulk store per tile); the later
+// drafts copy those tiles back and skip the index, length and page-table lookups and the scattered
+// 256-byte row reads (bf16: draft_pack_unit below, one bulk copy per tile on an mbarrier, one block
+// per (request, KV head); fp32: this chunk kernel with linear cp.async).  Pack layout: [unit][chunk]
+// [K tile, V tile], each tile kDraftChunk rows of D elements in the swizzled shared-memory order;
+// rows past the chunk's count are neither stored nor read.
 #pragma once
 
 #include "ssd_common.cuh"
@@ -256,16 +258,6 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
       reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
   };
 
-  // Reading the pack on the tensor-core path: each tile arrives by one bulk copy of its n rows,
-  // counted on an mbarrier in the (then unused) row table.
-  const bool bulk = TC && from_pack;
-  const uint32_t bar = smem_u32(sRow);
-  if (bulk && tid == 0) {
-    sm100::mbar_init(bar, 1);
-    sm100::mbar_init_fence();
-    sm100::fence_proxy_async_smem();
-  }
-
   // Each token's K row, resolved once by its own thread (index check, page-table lookup).
   if (!from_pack && tid < kDraftChunk) {
     int64_t row = -1;
@@ -285,15 +277,9 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   __syncthreads();
 
   // Gather the chunk's K and V rows (rows of skipped tokens are zero-filled), or copy the packed tiles
-  // (rows past n zero-filled).
+  // (rows past n zero-filled).  bf16 reads of the pack normally run draft_pack_unit instead.
   const int64_t v_off = (int64_t)h_kv * a.kv.page_size * D;
-  if (bulk) {
-    // K rows past n stay as they are: their logits are replaced by -inf.
-    if (tid == 0 && n > 0) {
-      sm100::mbar_arrive_expect_tx(bar, (uint32_t)(n * C::ROWB));
-      sm100::bulk_load(smem_u32(sKt), pk, (uint32_t)(n * C::ROWB), bar);
-    }
-  } else if (from_pack) {
+  if (from_pack) {
     for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x) {
       const int sz = c / C::CPR < n ? 16 : 0;
       cp_async16(smem_u32(sKt + c * 16), pk + c * 16, sz);
@@ -322,7 +308,6 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     }
   }
   cp_async_wait<0>();
-  if (bulk && n > 0) draft_tile_wait_all(bar, 0, a.status);
   __syncthreads();
   if (to_pack) {
     if constexpr (TC) {
@@ -377,16 +362,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   if constexpr (TC) {
     // V rows into the tile the K rows occupied (every thread is past the logits and its pack
     // stores); they land while the softmax runs.
-    if (bulk) {
-      if (tid == 0 && n > 0) {
-        sm100::fence_proxy_async_smem();  // the tile's K rows were read by every thread before the barrier
-        sm100::mbar_arrive_expect_tx(bar, (uint32_t)(n * C::ROWB));
-        sm100::bulk_load(smem_u32(sVt), pk + C::TILE, (uint32_t)(n * C::ROWB), bar);
-      }
-      // V rows past n are zeroed (their P is 0, but 0 times a stale non-finite value is not).
-      for (int c = n * C::CPR + tid; c < kDraftChunk * C::CPR; c += blockDim.x)
-        reinterpret_cast<uint4 *>(sVt)[c] = make_uint4(0u, 0u, 0u, 0u);
-    } else if (from_pack) {
+    if (from_pack) {
       for (int c = tid; c < kDraftChunk * C::CPR; c += blockDim.x)
         cp_async16(smem_u32(sVt + c * 16), pk + C::TILE + c * 16, c / C::CPR < n ? 16 : 0);
     } else
@@ -424,7 +400,6 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   float *red = TC ? sQ : reinterpret_cast<float *>(sKt);
   if constexpr (TC) {
     cp_async_wait<0>();
-    if (bulk && n > 0) draft_tile_wait_all(bar, 1, a.status);
     __syncthreads();
     if (to_pack && tid == 0 && n > 0) {
       sm100::fence_proxy_async_smem();
