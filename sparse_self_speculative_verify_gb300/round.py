@@ -64,7 +64,10 @@ class SpecRound:
 
     def draft(self, q_draft: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
         """One draft over the current selection.  With the row pack, the first draft after a select
-        stores the selected rows and the following ones read them (same results)."""
+        stores the selected rows and the following ones read them (same results within the oracle
+        tolerance).  The choice is made when the call is issued, so a captured CUDA graph keeps the
+        choice of its capture: capture the drafts together with the selection (as ``run`` does), so
+        that the graph's first draft writes the pack on every replay."""
         idx = self.idx.view(self.kv.batch, self.kv.h_kv, self.k_max)
         cnt = self.cnt.view(self.kv.batch, self.kv.h_kv)
         o = out if out is not None else self.out_d
