@@ -308,13 +308,14 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     }
   }
   cp_async_wait<0>();
+  // Every thread's landed rows are made visible to the bulk store (async proxy) before the barrier.
+  if (TC && to_pack) sm100::fence_proxy_async_smem();
   __syncthreads();
   if (to_pack) {
     if constexpr (TC) {
       // One bulk store of the landed K rows; its reads of the tile finish before the V rows are
       // gathered into it.
       if (tid == 0 && n > 0) {
-        sm100::fence_proxy_async_smem();
         bulk_store(pk, smem_u32(sKt), (uint32_t)(n * C::ROWB));
         bulk_commit();
       }
@@ -400,9 +401,9 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   float *red = TC ? sQ : reinterpret_cast<float *>(sKt);
   if constexpr (TC) {
     cp_async_wait<0>();
+    if (to_pack) sm100::fence_proxy_async_smem();  // as for the K rows
     __syncthreads();
     if (to_pack && tid == 0 && n > 0) {
-      sm100::fence_proxy_async_smem();
       bulk_store(pk + C::TILE, smem_u32(sVt), (uint32_t)(n * C::ROWB));
       bulk_commit();
     }
