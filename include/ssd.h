@@ -202,8 +202,10 @@ int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t
  * Sparse draft attention with a row pack.  The k drafts of a round all attend the set the last
  * verify selected (SparseSpec §4.1: the pattern stays fixed until the next verify refreshes it), so
  * the first draft can leave the selected K and V rows in a contiguous buffer and the others read
- * them from there instead of through the index list and the page table.  Same arguments, results
- * and workspace as ssd_draft_attn, plus:
+ * them from there instead of through the index list and the page table.  Same arguments and
+ * workspace as ssd_draft_attn, and the same results up to rounding: SSD_PACK_WRITE bit for bit;
+ * SSD_PACK_READ of a bf16 cache runs one block per (request, KV head) with an online softmax over
+ * the chunks, so its sums are taken in another order.  In addition:
  *   pack        device buffer of at least ssd_draft_pack_bytes(kv, k_max) bytes, 256-byte aligned,
  *               owned by the caller.  Its layout is private to the library.
  *   pack_mode   SSD_PACK_NONE: exactly ssd_draft_attn (pack unused, may be NULL).
