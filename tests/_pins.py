@@ -256,6 +256,27 @@ def pin_draft_subset(orc):
         np.testing.assert_allclose(dr["out"][0, h], p @ V, rtol=0, atol=1e-13)
 
 
+def pin_draft_duplicates(orc):
+    """An index listed twice counts twice (the ABI's stated convention): the draft equals softmax
+    attention in which that token's weight is doubled, i.e. its logit raised by ln 2, and the
+    log-sum-exp includes both copies."""
+    rng = np.random.default_rng(37)
+    Ks, Vs, q = rand_case(rng, 1, [9], 2, 1, 4, 1)
+    kv = orc.PagedKV(*paged_from_contiguous(Ks, Vs, 4, shuffle_seed=3))
+    idx = np.full((1, 1, 4), -1, np.int32)
+    idx[0, 0, :3] = [2, 2, 7]
+    cnt = np.array([[3]], np.int32)
+    dr = orc.draft(kv, q[:, 0], idx, cnt, 0.6)
+    K = Ks[0][0, [2, 7]].astype(np.float64)
+    V = Vs[0][0, [2, 7]].astype(np.float64)
+    for h in range(2):
+        s = 0.6 * (K @ q[0, 0, h].astype(np.float64)) + np.array([math.log(2.0), 0.0])
+        m = s.max()
+        w = np.exp(s - m)
+        np.testing.assert_allclose(dr["out"][0, h], (w / w.sum()) @ V, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(dr["lse"][0, h], m + math.log(w.sum()), rtol=0, atol=1e-12)
+
+
 def pin_topk(orc):
     """Top-K special cases and a brute-force comparison with Python's sort."""
     rng = np.random.default_rng(37)
@@ -467,6 +488,7 @@ def pin_topp(orc):
 
 
 ALL_PINS = [pin_softmax_closed_form, pin_brute_force, pin_identical_keys, pin_crit_sums, pin_causality,
-            pin_paging_invariance, pin_gqa_equals_mha, pin_draft_select_all, pin_draft_subset, pin_topk,
+            pin_paging_invariance, pin_gqa_equals_mha, pin_draft_select_all, pin_draft_subset, pin_draft_duplicates,
+            pin_topk,
             pin_block_maxpool, pin_block_union, pin_block_attn, pin_kv_append_composes, pin_kv_append_skips,
             pin_kv_advance, pin_phase_assignment, pin_topp]
