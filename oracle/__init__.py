@@ -66,6 +66,8 @@ def _load(path: str):
     L.oracle_phase_assign.restype = I
     L.oracle_topp_k.argtypes = [P, I64, P, D, I, I, I, I, P]
     L.oracle_topp_k.restype = I
+    L.oracle_combine.argtypes = [P, P, I, I, I, P, P]
+    L.oracle_combine.restype = I
     L.oracle_phase_flags.restype = I
     for fn in ("oracle_verify", "oracle_draft", "oracle_topk", "oracle_block_maxpool",
                "oracle_block_union", "oracle_block_attn"):
@@ -304,3 +306,19 @@ def topp(scores, lens, p: float, k_max: int, rows_per_group: int = 1, len_div: i
                                 _ptr(kout)), "topp")
     idx, cnt = topk(s, np.repeat(lens_n, rows_per_group), kout, k_max, 1, len_div)
     return idx, cnt, kout
+
+
+def combine(o_parts, lse_parts):
+    """Split-KV combine (ssd_oracle.c, oracle_combine; SparseSpec §4.1 caches each part's LSE):
+    o_parts [n_rows, n_splits, d] normalised split outputs, lse_parts [n_rows, n_splits] their
+    natural-log LSEs (-inf = empty split), both float32.  Returns out [n_rows, d] =
+    sum_j exp(lse_j - lse) o_j and lse [n_rows] = log sum_j exp(lse_j) (float64); a row with no
+    non-empty split gives 0 and -inf."""
+    o = _np(o_parts, np.float32)
+    lp = _np(lse_parts, np.float32)
+    n_rows, n_splits, d = o.shape
+    assert lp.shape == (n_rows, n_splits)
+    out = np.zeros((n_rows, d), np.float64)
+    lse = np.zeros((n_rows,), np.float64)
+    _check(_lib().oracle_combine(_ptr(o), _ptr(lp), n_rows, n_splits, d, _ptr(out), _ptr(lse)), "combine")
+    return out, lse

@@ -609,3 +609,40 @@ int oracle_topp_k(const float *scores, int64_t stride, const int32_t *lens, doub
   }
   return 0;
 }
+
+/* ---------------------------------------------------------------------------------------------
+ * Split-KV combine ([SS] §4.1: the verify caches each part's log-sum-exp, so partial attention
+ * results over disjoint parts of the token set merge into the result over their union).
+ * For each row: o_parts [n_rows][n_splits][d] holds every split's normalised output and lse_parts
+ * [n_rows][n_splits] its natural-log log-sum-exp (-inf for an empty split).  The merged result is
+ *   lse = log sum_j exp(lse_j),   out = sum_j exp(lse_j - lse) o_j,
+ * evaluated with the largest lse_j factored out of the sum (the same value, without overflow).  A
+ * row whose splits are all empty (or that has none) gives out = 0 and lse = -inf (R7).
+ */
+int oracle_combine(const float *o_parts, const float *lse_parts, int n_rows, int n_splits, int d, double *out,
+                   double *lse) {
+  if (n_rows < 0 || n_splits < 0 || d <= 0 || !out || !lse) return ORC_EARG;
+  if (n_rows > 0 && n_splits > 0 && (!o_parts || !lse_parts)) return ORC_EARG;
+  for (int r = 0; r < n_rows; ++r) {
+    const float *lp = lse_parts ? lse_parts + (int64_t)r * n_splits : NULL;
+    double m = -INFINITY;
+    for (int j = 0; j < n_splits; ++j)
+      if ((double)lp[j] > m) m = (double)lp[j];
+    double *o = out + (int64_t)r * d;
+    for (int k = 0; k < d; ++k) o[k] = 0.0;
+    if (m == -INFINITY) {
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double z = 0.0;
+    for (int j = 0; j < n_splits; ++j) z += exp((double)lp[j] - m);
+    const double total = m + log(z);
+    for (int j = 0; j < n_splits; ++j) {
+      const double w = exp((double)lp[j] - total);
+      const float *oj = o_parts + ((int64_t)r * n_splits + j) * d;
+      for (int k = 0; k < d; ++k) o[k] += w * (double)oj[k];
+    }
+    lse[r] = total;
+  }
+  return ORC_OK;
+}

@@ -487,8 +487,49 @@ def pin_topp(orc):
     assert kc.max() <= 5 and capped.max() <= 5
 
 
+def pin_combine(orc):
+    """Split-KV combine: merging one split is the identity; two splits with equal LSEs average
+    their outputs and add ln 2 to the LSE; drafts over disjoint index subsets, merged, equal the
+    draft over their union (an empty subset, LSE -inf, changes nothing); a row of only empty
+    splits, or of none, gives 0 and -inf."""
+    rng = np.random.default_rng(83)
+    o1 = rng.standard_normal((3, 1, 8)).astype(np.float32)
+    l1 = np.array([[0.25], [-3.5], [-np.inf]], np.float32)
+    out, lse = orc.combine(o1, l1)
+    np.testing.assert_array_equal(out[:2], o1[:2, 0].astype(np.float64))
+    np.testing.assert_array_equal(lse[:2], l1[:2, 0].astype(np.float64))
+    assert lse[2] == -np.inf and not out[2].any()
+    o2 = rng.standard_normal((1, 2, 8)).astype(np.float32)
+    out, lse = orc.combine(o2, np.array([[1.5, 1.5]], np.float32))
+    np.testing.assert_allclose(out[0], o2[0].astype(np.float64).mean(axis=0), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[0], 1.5 + math.log(2.0), rtol=0, atol=1e-15)
+    out, lse = orc.combine(np.zeros((2, 0, 8), np.float32), np.zeros((2, 0), np.float32))
+    assert (lse == -np.inf).all() and not out.any()
+
+    Ks, Vs, q = rand_case(rng, 1, [40], 4, 2, 8, 1)
+    kv = orc.PagedKV(*paged_from_contiguous(Ks, Vs, 4, shuffle_seed=5))
+    sel = np.sort(rng.choice(40, 23, replace=False)).astype(np.int32)
+    parts = [sel[:7], sel[7:8], np.zeros(0, np.int32), sel[8:]]
+    k_max = 32
+
+    def draft_of(tokens):
+        idx = np.full((1, 2, k_max), -1, np.int32)
+        idx[0, :, :len(tokens)] = tokens
+        cnt = np.full((1, 2), len(tokens), np.int32)
+        return orc.draft(kv, q[:, 0], idx, cnt, 0.5)
+
+    ds = [draft_of(t) for t in parts]
+    whole = draft_of(sel)
+    o_parts = np.stack([d["out"][0] for d in ds], axis=1).astype(np.float32)   # [H_q, S, d]
+    l_parts = np.stack([d["lse"][0] for d in ds], axis=1).astype(np.float32)   # [H_q, S]
+    assert np.isneginf(l_parts[:, 2]).all()
+    out, lse = orc.combine(o_parts, l_parts)
+    np.testing.assert_allclose(out, whole["out"][0], rtol=0, atol=2e-6)
+    np.testing.assert_allclose(lse, whole["lse"][0], rtol=0, atol=2e-6)
+
+
 ALL_PINS = [pin_softmax_closed_form, pin_brute_force, pin_identical_keys, pin_crit_sums, pin_causality,
             pin_paging_invariance, pin_gqa_equals_mha, pin_draft_select_all, pin_draft_subset, pin_draft_duplicates,
             pin_topk,
             pin_block_maxpool, pin_block_union, pin_block_attn, pin_kv_append_composes, pin_kv_append_skips,
-            pin_kv_advance, pin_phase_assignment, pin_topp]
+            pin_kv_advance, pin_phase_assignment, pin_topp, pin_combine]

@@ -39,6 +39,9 @@ MUTANTS = {
     "topp_strict_reach": ("while (k < n && acc < target) acc += (double)pairs[k++].v;",
                           "while (k < n && acc <= target) acc += (double)pairs[k++].v;"),
     "topp_no_cap": ("kout[r] = k < k_max ? k : k_max;", "kout[r] = k;"),
+    "combine_weight_unnormalised": ("const double w = exp((double)lp[j] - total);",
+                                    "const double w = exp((double)lp[j] - m);"),
+    "combine_lse_is_max": ("    lse[r] = total;", "    lse[r] = m;"),
     "advance_no_range_check": ("if (v >= 0 && v <= max_seq_len) seq_lens[b] = (int32_t)v;", "seq_lens[b] = (int32_t)v;"),
 }
 
