@@ -91,15 +91,16 @@ REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw
 
 
 class ClockSampler:
-    def __init__(self, gpu_id: str):
+    def __init__(self, gpu_id: str, period_ms: int = 50):
         self.gpu_id = gpu_id
+        self.period_ms = period_ms
         self.rows = []
         self.proc = None
         self.thread = None
 
     def start(self):
         cmd = ["nvidia-smi", f"--id={self.gpu_id}", "--query-gpu=" + ",".join(CLOCK_FIELDS),
-               "--format=csv,noheader,nounits", "-lms", "200"]
+               "--format=csv,noheader,nounits", "-lms", str(self.period_ms)]
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
@@ -339,17 +340,29 @@ def run_ours(args, spec, rank, world, local):
     kv_step = sum(M.round_kv_bytes(lens, l.k_per_req.cpu().tolist(), spec.h_kv, spec.d, spec.elem_bytes, spec.k)
                   for l in layers)
 
+    wv0, wv1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        wv0.record(stream)
         for _ in range(args.warmup):
             graph.replay()
+        wv1.record(stream)
     stream.synchronize()
+    ms_warm = wv0.elapsed_time(wv1) / max(args.warmup, 1)
     barrier()
     clocks = ClockSampler(gpu_id_for(dev))
     clocks.start()
     time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Clock window: the same replays for about a second right before the timed region (untimed),
+    # so that the 50 ms clock samples see the load the timed steps run under even when the timed
+    # region itself is shorter than a sampling period; samples from the window's start to the end
+    # of the timed region are summarised.
+    n_pre = max(1, int(1.0 / max(ms_warm * 1e-3, 1e-4)))
     torch.cuda.synchronize(dev)
-    t_begin = time.time()
+    t_window = time.time()
+    with torch.cuda.stream(stream):
+        for _ in range(n_pre):
+            graph.replay()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for _ in range(args.steps):
@@ -358,7 +371,9 @@ def run_ours(args, spec, rank, world, local):
     torch.cuda.synchronize(dev)
     t_end = time.time()
     ms_total = ev0.elapsed_time(ev1)
-    clk = clocks.stop(t_begin, t_end)
+    clk = clocks.stop(t_window, t_end)
+    clk["window"] = (f"{n_pre} untimed replays of the step directly before the {args.steps} timed ones, "
+                     f"sampled every {clocks.period_ms} ms with them")
     barrier()
     ms_total = max_over_ranks(ms_total, dev)
     bytes_all = sum_over_ranks(float(kv_step * args.steps), dev)
@@ -389,6 +404,39 @@ def run_ours(args, spec, rank, world, local):
                 "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(units),
                 "peak_source": peaks["source"], "launch_ms": v_ms, "algorithmic_bytes": v_bytes,
                 "verify_tflops": M.verify_flops(lens, spec.h_q, spec.d, spec.n_cand) / (v_ms * 1e-3) / 1e12}
+
+    # Draft calls of the round, timed per launch with events on their stream, layers cycled (the
+    # other layers' drafts evict a layer's selected rows from L2 in between): the later drafts read
+    # the row pack the first one stored; the first draft gathers through the index list and stores
+    # the pack (a select before each, outside the events, makes it the first again).
+    d_bytes = M.draft_kv_bytes(layers[0].k_per_req.cpu().tolist(), lens, spec.h_kv, spec.d, spec.elem_bytes)
+    d_call_bytes = d_bytes + spec.batch * spec.h_q * (spec.d * spec.elem_bytes + (spec.d + 1) * 4)
+
+    def time_drafts(first: bool) -> float:
+        n = reps * args.layers
+        st_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        en_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                r, l, o = rounds[i % args.layers], layers[i % args.layers], outs[i % args.layers]
+                if first:
+                    r.select(l.k_per_req, stream=stream)
+                st_ev[i].record(stream)
+                r.draft(l.q_draft[1], out=o[1], stream=stream)
+                en_ev[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in zip(st_ev, en_ev))
+
+    dr_ms = time_drafts(False)
+    dw_ms = time_drafts(True)
+    assert ssd_status() == 0, "device status fault in the draft timing"
+    roofline_draft = {"bound": "hbm", "kernel": "ssd_draft_attn_packed, row pack read (draft_pack_kernel)",
+                      "achieved": d_call_bytes / (dr_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": d_call_bytes / (dr_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                      "peak_source": peaks["source"], "launch_ms": dr_ms, "algorithmic_bytes": d_call_bytes,
+                      "first_draft": {"kernel": "ssd_draft_attn_packed, row pack written (draft_kernel)",
+                                      "launch_ms": dw_ms, "achieved": d_call_bytes / (dw_ms * 1e-3) / 1e9,
+                                      "frac": d_call_bytes / (dw_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
 
     # End to end through the API with host buffers: per step, the queries of every layer (and the
     # lengths / page table) go host -> device from pinned memory, the attention outputs device ->
@@ -460,6 +508,10 @@ def run_ours(args, spec, rank, world, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = sum_over_ranks(float(kv_step * e2e_steps), dev) / (e2e_ms * 1e-3) / 1e9
 
+    cfg_records = None
+    if rank == 0 and not args.no_configs:
+        cfg_records = config_records(peaks["hbm_gbs"], dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(layers, args.cpu_budget)
@@ -478,7 +530,7 @@ def run_ours(args, spec, rank, world, local):
                        "l2": f"inputs larger than L2: {args.layers} layers x "
                              f"{M.verify_kv_bytes(lens, spec.h_kv, spec.d, spec.elem_bytes) / 1e6:.0f} MB KV, cycled",
                        "timing": "CUDA graph of one step, replayed; CUDA events on the replay stream"},
-            "roofline": roofline, "cpu_baseline": cpu,
+            "roofline": roofline, "roofline_draft": roofline_draft, "configs": cfg_records, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
                     "copies": "pinned host buffers; step s+1 uploaded and step s-1 read back on a second "
@@ -520,6 +572,118 @@ def _time_calls(fn, reps: int = 20, warm: int = 3) -> float:
         st.synchronize()
         ms.append(e0.elapsed_time(e1) / reps)
     return ms[0] - ms[1]
+
+
+def config_records(peak_gbs: float, dev) -> dict:
+    """One record per other workload of the hot path, each on one GPU: ms per round (per call for
+    the unified batch), algorithmic KV bytes per round, KV GB/s and the fraction of the measured HBM
+    peak.  Each round is captured as a CUDA graph and timed after an L2 flush (``_time_calls``).
+    A workload that fails records its error instead of stopping the benchmark."""
+    from sparse_self_speculative_verify_gb300 import binding as Bd
+    from sparse_self_speculative_verify_gb300 import KVCache, SpecRound
+
+    def rec(ms, nbytes, **extra):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        d = {"ms_per_round": ms, "kv_bytes_per_round": nbytes, "kv_GB_s": gbs, "frac_of_measured_hbm": gbs / peak_gbs,
+             "rounds_per_s": 1e3 / ms}
+        d.update(extra)
+        return d
+
+    def spec_round(name):
+        spec = W.SPECS[name]
+        w = W.make_workload(spec, seed=W.spec_seed(name), device=dev)
+        kv = KVCache.from_workload(w)
+        k_max = int(w.k_per_req.max())
+        rnd = SpecRound(kv, spec.h_q, spec.n_cand, k_max, 1.0 / math.sqrt(spec.d))
+        outs = torch.empty((spec.k, spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=dev)
+        ms = _time_calls(lambda: rnd.run(w.q_verify, w.q_draft, w.k_per_req, draft_outs=outs), reps=10)
+        lens, kpr = w.seq_lens.cpu().tolist(), w.k_per_req.cpu().tolist()
+        nbytes = M.round_kv_bytes(lens, kpr, spec.h_kv, spec.d, spec.elem_bytes, spec.k)
+        return spec, ms, nbytes
+
+    out = {}
+    for name in ("tiny", "b128_l8k", "qwen3_14b_unified", "block_131k"):
+        try:
+            if name in ("tiny", "b128_l8k"):
+                spec, ms, nbytes = spec_round(name)
+                extra = {"round": f"verify + select + {spec.k} drafts (row pack)"}
+                if name == "b128_l8k":
+                    extra["ideal_rounds_per_s_at_8TBs"] = 8e12 / nbytes
+                    extra["ideal_rounds_per_s_at_measured_peak"] = peak_gbs * 1e9 / nbytes
+                out[name] = rec(ms, nbytes, **extra)
+            elif name == "qwen3_14b_unified":
+                spec = W.SPECS[name]
+                w = W.make_workload(spec, seed=W.spec_seed(name), device=dev)
+                kv = Bd.KVCache.from_workload(w)
+                scale = 1.0 / math.sqrt(spec.d)
+                k_max = int(w.k_per_req.max())
+                uidx, ucnt = W.random_index_sets(w.seq_lens, spec.h_kv, w.k_per_req, k_max, seed=w.seed)
+                uidx, ucnt = uidx.to(dev), ucnt.to(dev)
+                phase = w.phase.cpu().numpy()
+                lens = w.seq_lens.cpu().tolist()
+                vreq = [b for b in range(spec.batch) if phase[b] == 1]
+                dreq = [b for b in range(spec.batch) if phase[b] == 0]
+                scores = torch.zeros((spec.batch, spec.h_kv, kv.max_seq_len), device=dev)
+                nbytes = (M.verify_kv_bytes([lens[b] for b in vreq], spec.h_kv, spec.d, spec.elem_bytes) +
+                          int(ucnt[dreq].sum().item()) * M.kv_bytes_per_token_head(spec.d, spec.elem_bytes))
+                wsu = Bd.Workspace()
+                ms = _time_calls(lambda: Bd.ssd_unified_attn(kv, w.phase, w.q_verify, w.q_draft[0], spec.n_cand,
+                                                             uidx, ucnt, scale, scores=scores, workspace=wsu), reps=10)
+                vi, di = torch.tensor(vreq, device=dev), torch.tensor(dreq, device=dev)
+                kv_v = Bd.KVCache(kv.pool, kv.page_table[vi].contiguous(), kv.seq_lens[vi].contiguous(),
+                                  kv.max_seq_len)
+                kv_d = Bd.KVCache(kv.pool, kv.page_table[di].contiguous(), kv.seq_lens[di].contiguous(),
+                                  kv.max_seq_len)
+                qv, qd = w.q_verify[vi].contiguous(), w.q_draft[0][di].contiguous()
+                di_idx, di_cnt = uidx[di].contiguous(), ucnt[di].contiguous()
+
+                def separate():
+                    Bd.ssd_verify_attn(kv_v, qv, spec.n_cand, scale, workspace=wsu)
+                    Bd.ssd_draft_attn(kv_d, qd, di_idx, di_cnt, scale, workspace=wsu)
+                ms_sep = _time_calls(separate, reps=10)
+                out[name] = rec(ms, nbytes, round="one ssd_unified_attn call (verify-phase requests: verify + "
+                                                  "criticality; draft-phase requests: sparse draft)",
+                                verify_requests=len(vreq), draft_requests=len(dreq), separate_calls_ms=ms_sep,
+                                unified_over_separate=ms / ms_sep)
+            else:
+                spec = W.SPECS[name]
+                w = W.make_workload(spec, seed=W.spec_seed(name), device=dev)
+                kv = Bd.KVCache.from_workload(w)
+                scale = 1.0 / math.sqrt(spec.d)
+                nb = (kv.max_seq_len + 63) // 64
+                bs = torch.zeros((spec.batch, spec.h_kv, spec.n_cand, nb), device=dev)
+                wsb = Bd.Workspace()
+                kb = spec.top_blocks
+                ks = torch.full((spec.batch,), kb, dtype=torch.int32, device=dev)
+                umax = spec.n_cand * kb
+                bi = torch.empty((spec.batch * spec.h_kv * spec.n_cand, kb), dtype=torch.int32, device=dev)
+                bc = torch.empty((spec.batch * spec.h_kv * spec.n_cand,), dtype=torch.int32, device=dev)
+                un_i = torch.empty((spec.batch * spec.h_kv, umax), dtype=torch.int32, device=dev)
+                un_m = torch.empty((spec.batch * spec.h_kv, umax), dtype=torch.int32, device=dev)
+                un_c = torch.empty((spec.batch * spec.h_kv,), dtype=torch.int32, device=dev)
+                out_b = torch.empty((spec.batch, spec.n_cand, spec.h_q, spec.d), dtype=torch.float32, device=dev)
+
+                def block_round():
+                    Bd.ssd_verify_attn(kv, w.q_verify, spec.n_cand, scale, bscores=bs, want_scores=False,
+                                       workspace=wsb)
+                    Bd.ssd_select_topk(bs, kv.seq_lens, ks, kb, spec.h_kv * spec.n_cand, len_div=64, max_len=nb,
+                                       idx=bi, cnt=bc)
+                    Bd.ssd_block_union(bi.view(-1, spec.n_cand, kb), bc.view(-1, spec.n_cand), nb, umax,
+                                       uidx=un_i, umask=un_m, ucnt=un_c)
+                    Bd.ssd_block_sparse_attn(kv, w.q_verify, spec.n_cand, un_i, un_m, un_c, scale, out=out_b,
+                                             workspace=wsb)
+                ms = _time_calls(block_round, reps=5)
+                lens = w.seq_lens.cpu().tolist()
+                ublocks = int(un_c.sum().item())
+                nbytes = (M.verify_kv_bytes(lens, spec.h_kv, spec.d, spec.elem_bytes) +
+                          ublocks * 64 * M.kv_bytes_per_token_head(spec.d, spec.elem_bytes))
+                out[name] = rec(ms, nbytes, round="verify with per-candidate block scores + block Top-16 + union "
+                                                  "+ block-sparse attention", union_blocks=ublocks)
+            assert Bd.ssd_status() == 0, "device status fault"
+        except Exception as e:  # a failing workload is reported, the benchmark goes on
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_rows(args) -> list:
@@ -661,6 +825,7 @@ def main(argv=None):
     ap.add_argument("--config", default="qwen3_8b", choices=sorted(W.SPECS))
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload records of the other configs")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--rows", action="store_true", help="time each hot-path call on its own workload (1 GPU)")

@@ -25,9 +25,8 @@
  *    returns, and takes scratch space only from the caller's workspace, sized by the matching
  *    ssd_*_workspace_bytes() query.  A workspace must be zero-filled once after allocation.  Its
  *    first 256 KiB hold only the library's counters, which every call returns to zero, so one
- *    workspace may then serve calls of any entry point and shape one after another (zero it again
- *    after a call that raised SSD_FAULT_TIMEOUT).  It must not be shared by calls that may run
- *    concurrently.
+ *    workspace may then serve calls of any entry point and shape one after another.  It must not
+ *    be shared by calls that may run concurrently.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *    Argument errors are detected on the host and returned before anything is launched; launch
  *    failures return SSD_ERR_CUDA.  Data-dependent faults found on the device (a page id outside
@@ -36,6 +35,13 @@
  *    word that ssd_status() reports.
  *  - The library never aborts, prints or traps.  ssd_last_error() returns a thread-local message
  *    for the last failing call on the calling thread.
+ *  - Per device, the library keeps state for the life of the process: the device addresses of its
+ *    status word and of ssd_draft_attn_static's built-in scratch, and its kernels' shared-memory
+ *    limits.  After cudaDeviceReset (or any other teardown of a device's primary context) it must
+ *    not be called on that device again in the same process.
+ *  - SSD_FAULT_TIMEOUT means a copy or an MMA that a kernel waited for did not complete within
+ *    about a second; the kernel stopped waiting, but the copy may still be in flight.  Treat the
+ *    CUDA context as unusable after it.
  *  - Layouts are dense and row-major unless a stride argument says otherwise.
  *  - Notation: B requests, H_q query heads, H_kv KV heads, G = H_q / H_kv, d head dim (64 or 128),
  *    n_cand = k + 1, R = G * n_cand rows per (request, KV head) (R <= 64).  Query head h reads KV
@@ -60,7 +66,7 @@ enum ssd_status_code {
   SSD_ERR_UNSUPPORTED = 2, /* dtype, head dim, page size or group shape outside what is built */
   SSD_ERR_WORKSPACE = 3,   /* workspace null or smaller than the query function says */
   SSD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-  SSD_ERR_TIMEOUT = 5      /* reserved: a bounded device wait expired */
+  SSD_ERR_TIMEOUT = 5      /* reserved, never returned: expired device waits raise SSD_FAULT_TIMEOUT */
 };
 
 enum ssd_dtype { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 };
@@ -332,7 +338,8 @@ int ssd_block_sparse_attn(const ssd_paged_kv *kv, const void *q, int h_q, int n_
  * o_parts device float [n_rows][n_splits][d] (each split's normalised output), lse_parts device
  * float [n_rows][n_splits] (natural-log LSE of each split; -inf for an empty split).  Writes
  * out [n_rows][d] = sum_j exp(lse_j - lse*) o_j and lse [n_rows] = log sum_j exp(lse_j) (NULL to
- * skip); all-empty rows give out = 0, lse = -inf.
+ * skip); all-empty rows, and every row when n_splits = 0 (o_parts and lse_parts may then be NULL),
+ * give out = 0, lse = -inf.
  */
 int ssd_combine(const float *o_parts, const float *lse_parts, int n_rows, int n_splits, int d,
                 float *out, float *lse, ssd_stream_t stream);

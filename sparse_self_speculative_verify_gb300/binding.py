@@ -474,8 +474,8 @@ def ssd_unified_attn(kv: KVCache, phase: torch.Tensor, q_verify: torch.Tensor, q
                      idx: torch.Tensor, cnt: torch.Tensor, scale: float, *, out_verify=None, lse_verify=None,
                      scores=None, out_draft=None, lse_draft=None, want_scores: bool = True,
                      workspace: Optional[Workspace] = None, stream=None) -> dict:
-    """Mixed batch: verify-phase requests (phase == 1) and draft-phase requests (phase == 0) in one
-    persistent launch, then the verify finalize."""
+    """Mixed batch: verify-phase requests (phase == 1) get verify + criticality, draft-phase requests
+    (phase == 0) the sparse draft, in one call."""
     dev = kv.device
     _need(phase, "phase", torch.uint8, dev)
     _need(q_verify, "q_verify", kv.pool.dtype, dev)
@@ -506,16 +506,23 @@ def ssd_unified_attn(kv: KVCache, phase: torch.Tensor, q_verify: torch.Tensor, q
 
 
 def ssd_block_union(blocks: torch.Tensor, bcnt: torch.Tensor, nblk_max: int, umax: Optional[int] = None, *,
-                    stream=None):
+                    uidx=None, umask=None, ucnt=None, stream=None):
     """Union of the candidates' block sets.  blocks [units, n_cand, kb], bcnt [units, n_cand]."""
     _need(blocks, "blocks", torch.int32)
     dev = blocks.device
     _need(bcnt, "bcnt", torch.int32, dev)
     U, nc, kb = blocks.shape
     um = umax or nc * kb
-    uidx = torch.empty((U, um), dtype=torch.int32, device=dev)
-    umask = torch.empty((U, um), dtype=torch.int32, device=dev)  # uint32 bit patterns
-    ucnt = torch.empty((U,), dtype=torch.int32, device=dev)
+    if uidx is None:
+        uidx = torch.empty((U, um), dtype=torch.int32, device=dev)
+    if umask is None:
+        umask = torch.empty((U, um), dtype=torch.int32, device=dev)  # uint32 bit patterns
+    if ucnt is None:
+        ucnt = torch.empty((U,), dtype=torch.int32, device=dev)
+    _need(uidx, "uidx", torch.int32, dev)
+    _need(umask, "umask", torch.int32, dev)
+    _need(ucnt, "ucnt", torch.int32, dev)
+    assert uidx.shape == (U, um) and umask.shape == (U, um) and ucnt.shape == (U,)
     _check(_lib().ssd_block_union(_ptr(blocks), _ptr(bcnt), U, nc, kb, nblk_max, _ptr(uidx), _ptr(umask), _ptr(ucnt),
                                   um, _stream(stream)))
     return uidx, umask, ucnt

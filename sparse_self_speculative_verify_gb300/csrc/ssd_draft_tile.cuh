@@ -38,8 +38,8 @@ __device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t byt
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
-// Bounded wait of every thread for a bulk tile load (about a second at the SM clock); on expiry the
-// block's outputs are flagged invalid and it carries on.
+// Bounded wait of a thread for a bulk tile load (about a second at the SM clock); on expiry the
+// status word gets SSD_FAULT_TIMEOUT and the wait reports false.
 constexpr long long kDraftWaitCycles = 2000000000ll;
 __device__ __forceinline__ bool draft_tile_wait(uint32_t bar, uint32_t parity, unsigned *status) {
   if (sm100::mbar_try_wait(bar, parity)) return true;
@@ -50,10 +50,6 @@ __device__ __forceinline__ bool draft_tile_wait(uint32_t bar, uint32_t parity, u
       return false;
     }
   return true;
-}
-// Waits for the tile; after an expired wait, once more (bounded) for the copy still in flight.
-__device__ __forceinline__ void draft_tile_wait_all(uint32_t bar, uint32_t parity, unsigned *status) {
-  if (!draft_tile_wait(bar, parity, status)) draft_tile_wait(bar, parity, status);
 }
 
 struct DraftArgs {
@@ -561,7 +557,8 @@ struct DraftPackCfg {
   static constexpr int OFF_P = OFF_S + GMAX * kDraftChunk * 4;
   static constexpr int OFF_M = OFF_P + 2 * GMAX * kDraftChunk * 2;
   static constexpr int OFF_BAR = OFF_M + 3 * GMAX * 4;
-  static constexpr int SMEM = OFF_BAR + kPackStages * 8;
+  static constexpr int OFF_ABORT = OFF_BAR + kPackStages * 8;  // set by a thread whose wait expired
+  static constexpr int SMEM = OFF_ABORT + 8;
   static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 };
 
@@ -582,6 +579,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
   uint16_t *sP = reinterpret_cast<uint16_t *>(smem + C::OFF_P);
   float *sM = reinterpret_cast<float *>(smem + C::OFF_M), *sL = sM + GMAX, *sA = sL + GMAX;
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::OFF_ABORT);
   const char *pu = a.pack + (int64_t)unit * a.C_max * (2 * C::TILE);
 
   // Chunk c's n rows of K and of V into stage c % kPackStages (thread 0).
@@ -596,6 +594,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     sm100::bulk_load(dst + C::TILE, src + C::TILE, bytes, bar);
   };
   if (tid == 0) {
+    *s_abort = 0;
     for (int st = 0; st < kPackStages; ++st) sm100::mbar_init(bar0 + 8 * st, 1);
     sm100::mbar_init_fence();
     sm100::fence_proxy_async_smem();
@@ -620,7 +619,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     const char *sKt = smem + st * (2 * C::TILE);
     char *sVt = smem + st * (2 * C::TILE) + C::TILE;
     const int n = min(kDraftChunk, n_all - c * kDraftChunk);
-    draft_tile_wait_all(bar0 + 8 * st, (uint32_t)((c / kPackStages) & 1), a.status);
+    if (!draft_tile_wait(bar0 + 8 * st, (uint32_t)((c / kPackStages) & 1), a.status)) *s_abort = 1;
     // V rows past n (last chunk) are zeroed: their P is 0, but 0 times a stale non-finite value is
     // not.  K rows past n need nothing: their logits are replaced by -inf.
     for (int e = n * C::CPR + tid; e < kDraftChunk * C::CPR; e += blockDim.x)
@@ -628,6 +627,16 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
 
     draft_logits_mma<D, GMAX>(sKt, qb, sS, n, a.scale_log2, G, warp, lane);
     __syncthreads();
+    if (*s_abort) {
+      // A tile did not land in time (SSD_FAULT_TIMEOUT is set): no more copies are issued and the
+      // unit's outputs are not written.  Thread 0 waits, bounded, for the copies still in flight
+      // into this block's shared memory before the block exits; a copy that outlives that second
+      // wait too means the device is unusable for this context.
+      if (tid == 0)
+        for (int cc = c; cc < min(c + kPackStages, nch); ++cc)
+          draft_tile_wait(bar0 + 8 * (cc % kPackStages), (uint32_t)((cc / kPackStages) & 1), a.status);
+      return;
+    }
 
     // Online softmax, one warp per head: the new running max, this chunk's P against it (bf16 high
     // + residual parts), the factor that rescales the earlier chunks, and the running sum.

@@ -1,5 +1,5 @@
-// ssd_unified.cu -- one persistent launch that runs verify work for the verify-phase requests and
-// draft work for the draft-phase requests of a mixed batch.
+// ssd_unified.cu -- one call that runs verify work for the verify-phase requests and draft work
+// for the draft-phase requests of a mixed batch.
 //
 // SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
 // Sparse Attention") §4.2: the unified batch scheduler mixes requests of both phases in every step

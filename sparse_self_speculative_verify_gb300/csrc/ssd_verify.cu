@@ -562,8 +562,9 @@ extern "C" int ssd_block_sparse_attn(const ssd_paged_kv *kv, const void *q, int 
 
 extern "C" int ssd_combine(const float *o_parts, const float *lse_parts, int n_rows, int n_splits, int d, float *out,
                            float *lse, ssd_stream_t stream) {
-  if (!o_parts || !lse_parts || !out) return fail(SSD_ERR_INVALID_ARG, "ssd_combine: NULL pointer");
   if (n_rows < 0 || n_splits < 0 || d <= 0) return fail(SSD_ERR_INVALID_ARG, "ssd_combine: bad sizes");
+  if (!out || (n_splits > 0 && (!o_parts || !lse_parts)))
+    return fail(SSD_ERR_INVALID_ARG, "ssd_combine: NULL pointer");
   if (n_rows == 0) return SSD_OK;
   if (n_rows > (1 << 30)) return fail(SSD_ERR_UNSUPPORTED, "ssd_combine: too many rows");
   combine_kernel<<<n_rows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(o_parts, lse_parts, n_splits, d, out, lse);

@@ -11,6 +11,7 @@ verify of the k+1 positions.
 from __future__ import annotations
 
 import math
+from contextlib import nullcontext as _nullcontext
 from typing import Optional
 
 import torch
@@ -61,6 +62,14 @@ class SpecRound:
         self._packed = False
         return B.ssd_select_topk(self.scores, self.kv.seq_lens, k_per_req, self.k_max, self.kv.h_kv,
                                  max_len=self.kv.max_seq_len, idx=self.idx, cnt=self.cnt, stream=stream)
+
+    def set_selection(self, idx: torch.Tensor, cnt: torch.Tensor, stream=None):
+        """Install a selection made elsewhere (idx [B, H_kv, k_max] int32, cnt [B, H_kv]) in place
+        of the last select's; the next draft stores the row pack again."""
+        self._packed = False
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            self.idx.view(self.kv.batch, self.kv.h_kv, self.k_max).copy_(idx)
+            self.cnt.view(self.kv.batch, self.kv.h_kv).copy_(cnt)
 
     def draft(self, q_draft: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
         """One draft over the current selection.  With the row pack, the first draft after a select

@@ -61,6 +61,51 @@ def test_round_qwen3_8b_full_size():
         _gpu.assert_out(g["out"].cpu().numpy()[reqs], dref["out"], f"draft {j}")
 
 
+def test_round_b128_l8k_full_size():
+    """The 128 x 8192, k = 6 workload as the benchmark's rounds run it.  On sampled requests: the
+    verify output and scores against the oracle; the GPU selection bit-exact against the oracle's
+    Top-K of the same (GPU) score tensor and a valid Top-K of the oracle's scores; then the round's
+    six drafts (the first storing the row pack, the other five reading it, K = 410 on every unit)
+    on the oracle's own selection, against the oracle drafts."""
+    spec = W.SPECS["b128_l8k"]
+    w = W.make_workload(spec, device=DEV)
+    rnd, _ = _round(w)
+    B, hkv, k_max = spec.batch, spec.h_kv, rnd.k_max
+    reqs = [0, 77, 127]
+    kv_h, reqs = _gpu.host_subset(w, reqs)
+    scale = _gpu.scale_of(spec)
+    lens = kv_h.seq_lens
+    kpr = w.k_per_req.cpu().numpy()[reqs]
+    ref = oracle.verify(kv_h, w.q_verify.cpu()[reqs], scale)
+    _gpu.assert_out(rnd.out_v.cpu().numpy()[reqs], ref["out"], "verify out")
+    _gpu.assert_lse(rnd.lse_v.cpu().numpy()[reqs], ref["lse"], "verify lse")
+    _gpu.assert_scores(rnd.scores.cpu().numpy()[reqs], ref["crit"], lens)
+    Sg = rnd.scores.cpu().numpy()[reqs]
+    gidx, gcnt = oracle.topk(Sg.reshape(-1, Sg.shape[-1]), lens, kpr, k_max, rows_per_group=hkv)
+    idx = rnd.idx.view(B, hkv, k_max).cpu().numpy()[reqs].reshape(-1, k_max)
+    cnt = rnd.cnt.view(B, hkv).cpu().numpy()[reqs].reshape(-1)
+    np.testing.assert_array_equal(idx, gidx)
+    np.testing.assert_array_equal(cnt, gcnt)
+    _gpu.assert_valid_topk(idx, cnt, ref["crit"].reshape(-1, ref["crit"].shape[-1]), kpr, lens, hkv)
+    S = ref["crit"].astype(np.float32)
+    oidx, ocnt = oracle.topk(S.reshape(-1, S.shape[-1]), lens, kpr, k_max, rows_per_group=hkv)
+    oidx = oidx.reshape(len(reqs), hkv, k_max)
+    ocnt = ocnt.reshape(len(reqs), hkv)
+    sel_idx = rnd.idx.view(B, hkv, k_max).clone()
+    sel_cnt = rnd.cnt.view(B, hkv).clone()
+    sel_idx[reqs] = torch.from_numpy(oidx).to(DEV)
+    sel_cnt[reqs] = torch.from_numpy(ocnt).to(DEV)
+    rnd.set_selection(sel_idx, sel_cnt)
+    outs = torch.empty((spec.k, B, spec.h_q, spec.d), dtype=torch.float32, device=DEV)
+    for j in range(spec.k):
+        rnd.draft(w.q_draft[j], out=outs[j])
+    torch.cuda.synchronize()
+    assert ssd_status() == 0
+    for j in range(spec.k):
+        dref = oracle.draft(kv_h, w.q_draft[j].cpu()[reqs], oidx, ocnt, scale)
+        _gpu.assert_out(outs[j].cpu().numpy()[reqs], dref["out"], f"draft {j}")
+
+
 def test_round_graph_replay_matches_eager():
     spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="graph", batch=4)
     w = W.make_workload(spec, seed=3, device=DEV, lengths=[2100, 4097, 300, 1000])

@@ -5,17 +5,22 @@ runtime that owns every device allocation and passes in only input and output bu
 serving loop that must not call cudaMalloc / cudaFree (which can synchronise the device) while other
 streams are busy.  For them the library keeps the draft scratch in one built-in device array.
 
-The GPU test calls that entry point directly through the C ABI (ctypes, no Python wrapper) and
-compares it with ssd_draft_attn, which takes a caller workspace, within the output tolerances of
-the other GPU tests.  It makes several calls in a row with different shapes: each call finds the
-array as the previous one left it.  The host test checks that a batch too big for the array is
-refused before anything runs.  The file name makes pytest collect it last.
+The GPU test calls that entry point directly through the C ABI (ctypes, no Python wrapper).  Both
+entry points run the same kernel on the same inputs and merge a unit's chunks in a fixed order, so
+the static call must reproduce ssd_draft_attn (which takes a caller workspace) bit for bit; each
+call is also checked against the CPU oracle's draft within the output tolerances of the other GPU
+tests.  It makes several calls in a row with different shapes, each finding the array as the
+previous one left it, and repeats the first call at the end, which must give the first call's
+result bit for bit.  The host test checks that a batch too big for the array is refused before
+anything runs.  The file name makes pytest collect it last.
 """
 
 import ctypes
 
 import pytest
 import torch
+
+import oracle
 
 from sparse_self_speculative_verify_gb300 import KVCache, binding, ssd_draft_attn, ssd_status
 from sparse_self_speculative_verify_gb300 import build as libbuild
@@ -68,13 +73,17 @@ def test_static_matches_workspace_entry_point_on_consecutive_calls():
         out, lse = _static_call(L, kv, q, idx, cnt, scale)
         torch.cuda.synchronize()
         assert ssd_status() == 0
-        _gpu.assert_out(out.cpu().numpy(), ref["out"].cpu().numpy(), f"call {n} out")
-        _gpu.assert_lse(lse.cpu().numpy(), ref["lse"].cpu().numpy(), f"call {n} lse")
+        assert torch.equal(out, ref["out"]), f"call {n}: out differs from ssd_draft_attn"
+        assert torch.equal(lse, ref["lse"]), f"call {n}: lse differs from ssd_draft_attn"
+        kv_h, _ = _gpu.host_subset(w)
+        oref = oracle.draft(kv_h, q.cpu(), idx.cpu(), cnt.cpu(), scale)
+        _gpu.assert_out(out.cpu().numpy(), oref["out"], f"call {n} out vs oracle")
+        _gpu.assert_lse(lse.cpu().numpy(), oref["lse"], f"call {n} lse vs oracle")
         if n == 0:
-            first = out.clone()
+            first = (out.clone(), lse.clone())
         if n == len(CALLS) - 1:
-            # Same inputs as the first call, after other shapes used the array: same result.
-            _gpu.assert_out(out.cpu().numpy(), first.cpu().numpy(), "repeat of call 0")
+            # Same inputs as the first call, after other shapes used the array: the same bits.
+            assert torch.equal(out, first[0]) and torch.equal(lse, first[1]), "repeat of call 0 differs"
 
 
 def test_static_rejects_batches_beyond_the_builtin_scratch():
