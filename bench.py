@@ -318,13 +318,16 @@ def run_ours(args, spec, rank, world, local):
 
     def step():
         for r, l in zip(rounds, layers):
-            r.verify(l.q_verify)
-            r.select(l.k_per_req)
+            if args.separate_select:
+                r.verify(l.q_verify)
+                r.select(l.k_per_req)
+            else:
+                r.verify_select(l.q_verify, l.k_per_req)
         for j in range(spec.k):
             for r, l, o in zip(rounds, layers, outs):
                 r.draft(l.q_draft[j], out=o[j])
 
-    launches_per_step = args.layers * (2 + 1 + spec.k)
+    launches_per_step = args.layers * ((3 if args.separate_select else 2) + spec.k)
     with torch.cuda.stream(stream):
         step()  # eager warm-up (also sets kernel attributes outside capture)
     stream.synchronize()
@@ -356,7 +359,7 @@ def run_ours(args, spec, rank, world, local):
     # so that the 50 ms clock samples see the load the timed steps run under even when the timed
     # region itself is shorter than a sampling period; samples from the window's start to the end
     # of the timed region are summarised.
-    n_pre = max(1, int(1.0 / max(ms_warm * 1e-3, 1e-4)))
+    n_pre = int(args.clock_window / max(ms_warm * 1e-3, 1e-4))
     torch.cuda.synchronize(dev)
     t_window = time.time()
     with torch.cuda.stream(stream):
@@ -382,55 +385,54 @@ def run_ours(args, spec, rank, world, local):
     rounds_per_s = world * args.layers / (ms_step * 1e-3)
     assert ssd_status() == 0, "device status fault in the timed region"
 
-    # Dominant call: ssd_verify_attn (verify kernel + finalize), timed per launch with events on
-    # its stream, layers cycled (cold L2).
+    # Dominant call: the round's verify call, layers cycled (cold L2): the mean time per call of a
+    # CUDA graph of consecutive calls, timed with events on its stream.  The step runs
+    # ssd_verify_select (verify kernel + criticality and Top-K pass); ssd_verify_attn (verify
+    # kernel + finalize, no selection) is timed beside it.
     reps = max(2, min(args.steps, 10))
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(reps * args.layers)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(reps * args.layers)]
-    with torch.cuda.stream(stream):
-        for i in range(reps * args.layers):
-            r, l = rounds[i % args.layers], layers[i % args.layers]
-            starts[i].record(stream)
-            r.verify(l.q_verify, stream=stream)
-            ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    v_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    va_ms = graph_mean_ms([(lambda r=r, l=l: r.verify(l.q_verify, stream=stream)) for r, l in zip(rounds, layers)],
+                          reps, stream)
+    vs_ms = graph_mean_ms([(lambda r=r, l=l: r.verify_select(l.q_verify, l.k_per_req, stream=stream))
+                           for r, l in zip(rounds, layers)], reps, stream)
     peaks = measured_peaks()
-    v_bytes = M.verify_call_bytes(lens, spec.batch, spec.h_q, spec.h_kv, spec.d, spec.elem_bytes, spec.n_cand)
+    va_bytes = M.verify_call_bytes(lens, spec.batch, spec.h_q, spec.h_kv, spec.d, spec.elem_bytes, spec.n_cand)
+    vs_bytes = va_bytes + spec.batch * spec.h_kv * (k_max + 1) * 4  # + the selected indices and counts
+    if args.separate_select:
+        v_ms, v_bytes, v_kernel = va_ms, va_bytes, "ssd_verify_attn (verify_tc_kernel + finalize_kernel)"
+    else:
+        v_ms, v_bytes, v_kernel = vs_ms, vs_bytes, "ssd_verify_select (verify_tc_kernel + crit_select_kernel)"
     achieved = v_bytes / (v_ms * 1e-3) / 1e9
     units = sum(lens) * spec.h_kv
-    roofline = {"bound": "hbm", "kernel": "ssd_verify_attn (verify_tc_kernel + finalize_kernel)",
+    roofline = {"bound": "hbm", "kernel": v_kernel,
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(units),
+                "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(units) if args.separate_select else None,
+                "verify_attn_ms": va_ms, "verify_attn_frac": va_bytes / (va_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "peak_source": peaks["source"], "launch_ms": v_ms, "algorithmic_bytes": v_bytes,
+                "timing": f"mean per call over a CUDA graph of {reps} x {args.layers} consecutive calls, layers cycled",
                 "verify_tflops": M.verify_flops(lens, spec.h_q, spec.d, spec.n_cand) / (v_ms * 1e-3) / 1e12}
 
-    # Draft calls of the round, timed per launch with events on their stream, layers cycled (the
-    # other layers' drafts evict a layer's selected rows from L2 in between): the later drafts read
-    # the row pack the first one stored; the first draft gathers through the index list and stores
-    # the pack (a select before each, outside the events, makes it the first again).
+    # Draft calls of the round, layers cycled (the other layers' drafts evict a layer's selected rows
+    # from L2 in between), as the mean time per call of a CUDA graph of consecutive calls: the later
+    # drafts of a round read the row pack the first one stored; the first gathers through the index
+    # list and stores the pack.
     d_bytes = M.draft_kv_bytes(layers[0].k_per_req.cpu().tolist(), lens, spec.h_kv, spec.d, spec.elem_bytes)
     d_call_bytes = d_bytes + spec.batch * spec.h_q * (spec.d * spec.elem_bytes + (spec.d + 1) * 4)
 
-    def time_drafts(first: bool) -> float:
-        n = reps * args.layers
-        st_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        en_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        with torch.cuda.stream(stream):
-            for i in range(n):
-                r, l, o = rounds[i % args.layers], layers[i % args.layers], outs[i % args.layers]
-                if first:
-                    r.select(l.k_per_req, stream=stream)
-                st_ev[i].record(stream)
-                r.draft(l.q_draft[1], out=o[1], stream=stream)
-                en_ev[i].record(stream)
-        torch.cuda.synchronize(dev)
-        return statistics.mean(a.elapsed_time(b) for a, b in zip(st_ev, en_ev))
+    from sparse_self_speculative_verify_gb300 import binding as Bd
 
-    dr_ms = time_drafts(False)
-    dw_ms = time_drafts(True)
+    def draft_call(r, l, o, mode):
+        idx = r.idx.view(spec.batch, spec.h_kv, r.k_max)
+        cnt = r.cnt.view(spec.batch, spec.h_kv)
+        return lambda: Bd.ssd_draft_attn_packed(r.kv, l.q_draft[1], idx, cnt, r.scale, r.pack, mode, out=o[1],
+                                                lse=r.lse_d, workspace=r.ws, stream=stream)
+
+    dw_ms = graph_mean_ms([draft_call(r, l, o, Bd.PACK_WRITE) for r, l, o in zip(rounds, layers, outs)], reps,
+                          stream)
+    dr_ms = graph_mean_ms([draft_call(r, l, o, Bd.PACK_READ) for r, l, o in zip(rounds, layers, outs)], reps, stream)
     assert ssd_status() == 0, "device status fault in the draft timing"
     roofline_draft = {"bound": "hbm", "kernel": "ssd_draft_attn_packed, row pack read (draft_pack_kernel)",
+                      "timing": f"mean per call over a CUDA graph of {reps} x {args.layers} consecutive calls, "
+                                f"layers cycled",
                       "achieved": d_call_bytes / (dr_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                       "frac": d_call_bytes / (dr_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                       "peak_source": peaks["source"], "launch_ms": dr_ms, "algorithmic_bytes": d_call_bytes,
@@ -526,7 +528,9 @@ def run_ours(args, spec, rank, world, local):
                                    f"{spec.h_q}/{spec.h_kv} heads, d={spec.d}, bf16 paged KV (page {spec.page_size}, "
                                    f"shuffled), k={spec.k}, top-K ceil(5% L)",
                        "layers": args.layers, "kv_bytes_per_step_per_gpu": kv_step,
-                       "step": "per layer: verify+criticality, select; then k drafts of every layer",
+                       "step": ("per layer: verify + criticality, then select" if args.separate_select else
+                                "per layer: verify + criticality + select (ssd_verify_select)") +
+                               "; then k drafts of every layer",
                        "l2": f"inputs larger than L2: {args.layers} layers x "
                              f"{M.verify_kv_bytes(lens, spec.h_kv, spec.d, spec.elem_bytes) / 1e6:.0f} MB KV, cycled",
                        "timing": "CUDA graph of one step, replayed; CUDA events on the replay stream"},
@@ -537,6 +541,31 @@ def run_ours(args, spec, rank, world, local):
                               "stream while step s runs"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk}
+
+
+def graph_mean_ms(calls, reps: int, stream) -> float:
+    """Mean device time per call of ``reps`` passes over ``calls`` (cycled in order), captured as
+    one CUDA graph after a warm-up pass and timed with CUDA events on ``stream`` around two
+    replays of it (the graph is replayed once before, untimed)."""
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                for c in calls:
+                    c()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        g.replay()
+        g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / (2 * reps * len(calls))
 
 
 def _time_calls(fn, reps: int = 20, warm: int = 3) -> float:
@@ -596,7 +625,8 @@ def config_records(peak_gbs: float, dev) -> dict:
         k_max = int(w.k_per_req.max())
         rnd = SpecRound(kv, spec.h_q, spec.n_cand, k_max, 1.0 / math.sqrt(spec.d))
         outs = torch.empty((spec.k, spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=dev)
-        ms = _time_calls(lambda: rnd.run(w.q_verify, w.q_draft, w.k_per_req, draft_outs=outs), reps=10)
+        ms = _time_calls(lambda: rnd.run(w.q_verify, w.q_draft, w.k_per_req, draft_outs=outs, fused_select=True),
+                         reps=10)
         lens, kpr = w.seq_lens.cpu().tolist(), w.k_per_req.cpu().tolist()
         nbytes = M.round_kv_bytes(lens, kpr, spec.h_kv, spec.d, spec.elem_bytes, spec.k)
         return spec, ms, nbytes
@@ -826,6 +856,10 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload records of the other configs")
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of untimed replays sampled for clocks before the timed steps (0: none)")
+    ap.add_argument("--separate-select", action="store_true",
+                    help="run each layer's verify and select as two calls instead of ssd_verify_select")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--rows", action="store_true", help="time each hot-path call on its own workload (1 GPU)")

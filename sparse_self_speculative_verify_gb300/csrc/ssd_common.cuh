@@ -12,6 +12,9 @@ namespace ssd {
 
 // Verify work item: a split of kSplitTokens consecutive tokens of one (request, KV head).
 constexpr int kSplitTokens = 512;
+// Split length of the fp32 (CUDA-core) verify: shorter, so that small batches still spread over
+// many blocks.
+constexpr int kSimtSplitTokens = 128;
 // Tokens staged in shared memory per pipeline step of the verify kernels.
 constexpr int kStageTokens = 64;
 // Criticality side values carry one log2-domain reference per (row, kRefGroup tokens).
@@ -71,6 +74,21 @@ __device__ __forceinline__ const T *kv_row(const KVView &kv, int b, int which, i
   int64_t row = (((int64_t)p * 2 + which) * kv.h_kv + g) * kv.page_size + (t & (kv.page_size - 1));
   return reinterpret_cast<const T *>(kv.pool) + row * D;
 }
+
+// Programmatic dependent launch.  Every kernel of the library is launched so that it may start
+// while the kernel before it on the stream is finishing: its blocks can be placed on SMs the earlier
+// grid has left and run work that reads nothing an earlier kernel wrote (shared-memory and barrier
+// set-up, tensor-memory allocation).  pdl_wait() returns once every grid this one depends on has
+// completed and its memory is visible; each kernel calls it in every block before its first access
+// to global memory that an earlier kernel may write (and before it exits), so the completion of any
+// kernel implies the completion of all kernels before it on the stream.  Without the launch
+// attribute both instructions do nothing.  pdl_trigger() lets the next kernel's launch begin once
+// every block of this grid has issued it (or exited); kernels issue it when a block's remaining
+// work is short (its last item, stage or chunk), so the next kernel's blocks arrive during this
+// one's tail rather than sitting on SMs through all of it (issued at kernel entry it measured
+// slower than no dependent launch at all).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

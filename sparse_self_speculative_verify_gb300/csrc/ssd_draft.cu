@@ -5,11 +5,19 @@
 
 namespace ssd {
 
+// One block per (chunk, unit).  With defer_wait (the unified call, launched right behind the verify
+// kernel it does not depend on): no block waits for the previous grid before its work, so the
+// draft blocks run on the SMs the verify's finishing blocks leave; block (0, 0) alone waits for it
+// before exiting, so that this grid still completes after the verify, and the finalize launched
+// behind it (which waits for this grid) sees the verify's results.
 template <int D, typename T, int GMAX>
 __global__ void __launch_bounds__(128) draft_kernel(DraftArgs a) {
   extern __shared__ __align__(128) char smem[];
-  if (a.phase && a.phase[blockIdx.y / a.kv.h_kv] != 0) return;  // a verify-phase request of a mixed batch
-  draft_item<D, T, GMAX>(a, blockIdx.y, blockIdx.x, smem);
+  const bool waiter = a.defer_wait && blockIdx.x == 0 && blockIdx.y == 0;
+  if (!a.defer_wait) pdl_wait();
+  if (!(a.phase && a.phase[blockIdx.y / a.kv.h_kv] != 0))  // not a verify-phase request of a mixed batch
+    draft_item<D, T, GMAX>(a, blockIdx.y, blockIdx.x, smem);
+  if (waiter) pdl_wait();
 }
 
 int draft_gmax(int G) { return G <= 4 ? 4 : (G <= 8 ? 8 : 16); }
@@ -26,8 +34,7 @@ static int launch_draft_pack(const DraftArgs &a, int units, cudaStream_t st) {
   constexpr int smem = DraftPackCfg<D, GMAX>::SMEM;
   int rc = ensure_smem<draft_pack_kernel<D, GMAX>>(smem);
   if (rc) return rc;
-  draft_pack_kernel<D, GMAX><<<units, 128, smem, st>>>(a);
-  return check_launch("draft_pack_kernel");
+  return launch(draft_pack_kernel<D, GMAX>, dim3(units), dim3(128), smem, st, "draft_pack_kernel", a);
 }
 
 static int launch_draft_pack_any(int D, const DraftArgs &a, int units, cudaStream_t st) {
@@ -47,8 +54,7 @@ static int launch_draft(const DraftArgs &a, dim3 grid, cudaStream_t st) {
                 "reduction area");
   int rc = ensure_smem<draft_kernel<D, T, GMAX>>(smem);
   if (rc) return rc;
-  draft_kernel<D, T, GMAX><<<grid, 128, smem, st>>>(a);
-  return check_launch("draft_kernel");
+  return launch(draft_kernel<D, T, GMAX>, grid, dim3(128), smem, st, "draft_kernel", a);
 }
 
 template <int D, typename T>

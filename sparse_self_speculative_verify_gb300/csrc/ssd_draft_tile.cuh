@@ -66,6 +66,7 @@ struct DraftArgs {
   float *out;          // [B][h_q][D]
   float *lse;          // [B][h_q] or nullptr
   const uint8_t *phase;  // unified launch: draft items only for phase == 0 (nullptr otherwise)
+  int defer_wait;        // unified launch: see draft_kernel
   char *pack;            // row pack [units][C_max][2][TILE] (pack_mode != SSD_PACK_NONE)
   int pack_mode;         // SSD_PACK_NONE / SSD_PACK_WRITE (gather, then store the tiles) / SSD_PACK_READ
   unsigned *status;
@@ -373,6 +374,7 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
     cp_async_commit();
   }
 
+  pdl_trigger();
   // Softmax over the chunk, one warp per head.
   for (int h = warp; h < G; h += blockDim.x / 32) {
     float v0 = sS[h * kDraftChunk + lane], v1 = sS[h * kDraftChunk + lane + 32];
@@ -569,6 +571,12 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
   constexpr int NT8 = MM::NT8, MTW = MM::MTW;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
   const int h_kv = a.kv.h_kv, b = unit / h_kv, g = unit % h_kv, G = a.G;
+  const char *pu = a.pack + (int64_t)unit * a.C_max * (2 * C::TILE);
+  // Before the wait for the previous kernel: the unit's first packed chunk (K and V tiles, whole)
+  // into L2, so the first bulk copies after the wait find it there.  A prefetch only warms L2, which
+  // every write also passes through, so it may overlap an earlier kernel still writing the pack.
+  if (tid == 0) sm100::prefetch_l2(pu, 2 * C::TILE);
+  pdl_wait();
   int n_all = a.cnt[unit];
   if (n_all < 0 || n_all > a.k_max) {
     if (tid == 0) atomicOr(a.status, (unsigned)SSD_FAULT_KMAX);
@@ -580,7 +588,6 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
   float *sM = reinterpret_cast<float *>(smem + C::OFF_M), *sL = sM + GMAX, *sA = sL + GMAX;
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
   volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::OFF_ABORT);
-  const char *pu = a.pack + (int64_t)unit * a.C_max * (2 * C::TILE);
 
   // Chunk c's n rows of K and of V into stage c % kPackStages (thread 0).
   auto issue = [&](int c) {
@@ -682,6 +689,7 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     }
   }
 
+  pdl_trigger();
   // Normalised output: c0, c1 at d = 16 mt + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3 at d + 8.
 #pragma unroll
   for (int mi = 0; mi < MTW; ++mi)

@@ -1,5 +1,6 @@
 // ssd_host.cu -- error reporting, the device status word and argument validation.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "ssd_host.h"
@@ -47,6 +48,14 @@ unsigned *device_status() {
     s_status_ptr[dev] = static_cast<unsigned *>(p);
   }
   return s_status_ptr[dev];
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char *v = getenv("SSD_PDL");
+    return !(v && v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
 }
 
 int sm_count() {

@@ -22,6 +22,35 @@ int sm_count();
 // Validates the cache description; fills `v`.  `need_mask` lists the accepted dtypes as bits.
 int validate_kv(const ssd_paged_kv *kv, KVView *v, const char *who);
 
+// Whether kernels are launched with programmatic stream serialization (programmatic dependent
+// launch): on unless the environment variable SSD_PDL is "0" when the library first launches.
+bool pdl_enabled();
+
+// Launches kernel<<<grid, block, smem, st>>>(args...) through cudaLaunchKernelEx, with the
+// programmatic-stream-serialization attribute when pdl_enabled() (every kernel of the library calls
+// pdl_wait() before touching data an earlier kernel may write).  Maps a launch failure to
+// SSD_ERR_CUDA with `name` in the message.
+template <typename... KArgs, typename... Args>
+int launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, const char *name,
+           Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SSD_ERR_CUDA, "%s: %s", name, cudaGetErrorString(e));
+  }
+  return check_launch(name);
+}
+
 // Raises the dynamic shared-memory limit of `Kernel` to at least `bytes` on the current device;
 // the attribute call is made only when the limit has to grow, so launches during CUDA-graph
 // capture (after an eager warm-up) make no attribute calls.

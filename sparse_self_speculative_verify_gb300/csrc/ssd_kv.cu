@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(KVView kv, ch
                                                                    unsigned *status) {
   const int b = blockIdx.x, tid = threadIdx.x;
   __shared__ int s_ok;
+  pdl_trigger();
+  pdl_wait();
   const int L = kv.seq_lens[b];
   if (tid == 0) s_ok = 1;
   __syncthreads();
@@ -62,6 +64,8 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(KVView kv, ch
 __global__ void kv_advance_kernel(int32_t *seq_lens, const int32_t *delta, int batch, int max_seq_len,
                                   unsigned *status) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if (b >= batch) return;
   const int64_t v = (int64_t)seq_lens[b] + delta[b];
   if (v >= 0 && v <= max_seq_len)
@@ -88,10 +92,9 @@ extern "C" int ssd_kv_append(const ssd_paged_kv *kv, const void *k_new, const vo
   unsigned *status = device_status();
   if (!status) return SSD_ERR_CUDA;
   const int row_bytes = kv->d * (kv->dtype == SSD_DTYPE_BF16 ? 2 : 4);
-  kv_append_kernel<<<kv->batch, kAppendThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      v, static_cast<char *>(const_cast<void *>(kv->pool)), static_cast<const char *>(k_new),
-      static_cast<const char *>(v_new), n_new, row_bytes, status);
-  return check_launch("kv_append_kernel");
+  return launch(kv_append_kernel, dim3(kv->batch), dim3(kAppendThreads), 0, reinterpret_cast<cudaStream_t>(stream),
+                "kv_append_kernel", v, static_cast<char *>(const_cast<void *>(kv->pool)),
+                static_cast<const char *>(k_new), static_cast<const char *>(v_new), n_new, row_bytes, status);
 }
 
 extern "C" int ssd_kv_advance(int32_t *seq_lens, const int32_t *delta, int batch, int max_seq_len,
@@ -102,7 +105,6 @@ extern "C" int ssd_kv_advance(int32_t *seq_lens, const int32_t *delta, int batch
   if (!seq_lens || !delta) return fail(SSD_ERR_INVALID_ARG, "%s: seq_lens and delta must be non-NULL", who);
   unsigned *status = device_status();
   if (!status) return SSD_ERR_CUDA;
-  kv_advance_kernel<<<cdiv(batch, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(seq_lens, delta, batch,
-                                                                                        max_seq_len, status);
-  return check_launch("kv_advance_kernel");
+  return launch(kv_advance_kernel, dim3(cdiv(batch, 256)), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                "kv_advance_kernel", seq_lens, delta, batch, max_seq_len, status);
 }

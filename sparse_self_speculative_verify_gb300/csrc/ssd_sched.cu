@@ -13,6 +13,8 @@ namespace ssd {
 __global__ void phase_fill_kernel(const int32_t *offsets, int batch, int n_buckets, int64_t step, uint8_t *phase,
                                   unsigned *status) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if (b >= batch) return;
   const int o = offsets[b];
   if (o < 0 || o >= n_buckets) {  // not a valid offset: treat the request as drafting, flag it
@@ -50,7 +52,6 @@ extern "C" int ssd_phase_fill(const int32_t *offsets, int batch, int n_buckets, 
   if (!offsets || !phase) return fail(SSD_ERR_INVALID_ARG, "%s: offsets and phase must be non-NULL", who);
   unsigned *status = device_status();
   if (!status) return SSD_ERR_CUDA;
-  phase_fill_kernel<<<cdiv(batch, 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(offsets, batch, n_buckets,
-                                                                                         step, phase, status);
-  return check_launch("phase_fill_kernel");
+  return launch(phase_fill_kernel, dim3(cdiv(batch, 256)), dim3(256), 0, reinterpret_cast<cudaStream_t>(stream),
+                "phase_fill_kernel", offsets, batch, n_buckets, step, phase, status);
 }

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(TopkArgs p) {
   const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
   const int grp = (int)(row / p.rows_per_group);
+  pdl_wait();
   int raw_len = p.lens[grp];
   int n = raw_len <= 0 ? 0 : cdiv(raw_len, p.len_div);
   if (raw_len < 0 || n > p.max_len) {
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(TopkArgs p) {
   }
   auto key = [&](int t) -> uint32_t { return IN_SMEM ? s_keys[t] : score_key(__ldg(src + t)); };
 
+  pdl_trigger();
   topk_row<kSelThreads>(key, n, K, out, p.k_max, sc);
   if (tid == 0) p.cnt[row] = K;
 }
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(kSelThreads) topp_k_kernel(ToppArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
   const int grp = (int)(row / a.rows_per_group);
+  pdl_trigger();
+  pdl_wait();
   const int raw_len = a.lens[grp];
   int n = raw_len <= 0 ? 0 : cdiv(raw_len, a.len_div);
   if (raw_len < 0 || n > a.max_len) {
@@ -273,7 +277,9 @@ __global__ void __launch_bounds__(kSelThreads) union_kernel(UnionArgs p) {
   __shared__ int s_total;
   const int tid = threadIdx.x;
   const int64_t u = blockIdx.x;
+  pdl_trigger();
   for (int j = tid; j < p.nblk_max; j += kSelThreads) s_mask[j] = 0u;
+  pdl_wait();
   __syncthreads();
   for (int e = tid; e < p.n_c * p.kb; e += kSelThreads) {
     int i = e / p.kb, j = e % p.kb;
@@ -341,11 +347,9 @@ extern "C" int ssd_select_topk(const float *scores, int64_t stride, const int32_
     const int smem = (max_len > 0 ? max_len : 1) * 4;
     int rc = ensure_smem<topk_kernel<true>>(smem);
     if (rc) return rc;
-    topk_kernel<true><<<(unsigned)rows, kSelThreads, smem, st>>>(p);
-  } else {
-    topk_kernel<false><<<(unsigned)rows, kSelThreads, 0, st>>>(p);
+    return launch(topk_kernel<true>, dim3((unsigned)rows), dim3(kSelThreads), smem, st, "topk_kernel", p);
   }
-  return check_launch("topk_kernel");
+  return launch(topk_kernel<false>, dim3((unsigned)rows), dim3(kSelThreads), 0, st, "topk_kernel", p);
 }
 
 extern "C" int ssd_block_union(const int32_t *blocks, const int32_t *bcnt, int n_units, int n_cand, int kb,
@@ -364,8 +368,8 @@ extern "C" int ssd_block_union(const int32_t *blocks, const int32_t *bcnt, int n
   const int smem = nblk_max * 4;
   int rc = ensure_smem<union_kernel>(smem);
   if (rc) return rc;
-  union_kernel<<<n_units, kSelThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  return check_launch("union_kernel");
+  return launch(union_kernel, dim3(n_units), dim3(kSelThreads), smem, reinterpret_cast<cudaStream_t>(stream),
+                "union_kernel", p);
 }
 
 extern "C" int ssd_select_topp(const float *scores, int64_t stride, const int32_t *lens, float p, int n_groups,
@@ -390,14 +394,11 @@ extern "C" int ssd_select_topp(const float *scores, int64_t stride, const int32_
     int rc = ensure_smem<topp_k_kernel<true>>(smem);
     if (rc) return rc;
     if ((rc = ensure_smem<topk_kernel<true>>(smem))) return rc;
-    topp_k_kernel<true><<<(unsigned)rows, kSelThreads, smem, st>>>(ta);
-    if ((rc = check_launch("topp_k_kernel"))) return rc;
-    topk_kernel<true><<<(unsigned)rows, kSelThreads, smem, st>>>(tk);
-  } else {
-    topp_k_kernel<false><<<(unsigned)rows, kSelThreads, 0, st>>>(ta);
-    int rc = check_launch("topp_k_kernel");
-    if (rc) return rc;
-    topk_kernel<false><<<(unsigned)rows, kSelThreads, 0, st>>>(tk);
+    if ((rc = launch(topp_k_kernel<true>, dim3((unsigned)rows), dim3(kSelThreads), smem, st, "topp_k_kernel", ta)))
+      return rc;
+    return launch(topk_kernel<true>, dim3((unsigned)rows), dim3(kSelThreads), smem, st, "topk_kernel", tk);
   }
-  return check_launch("topk_kernel");
+  int rc = launch(topp_k_kernel<false>, dim3((unsigned)rows), dim3(kSelThreads), 0, st, "topp_k_kernel", ta);
+  if (rc) return rc;
+  return launch(topk_kernel<false>, dim3((unsigned)rows), dim3(kSelThreads), 0, st, "topk_kernel", tk);
 }

@@ -56,8 +56,7 @@ template <int NT>
 struct TopkScratch {
   uint32_t hist[NT / 32][256];
   uint32_t tot[256];
-  int warp[NT / 32];
-  int total;
+  int wgt[NT / 32], weq[NT / 32];
   uint32_t digit;
   int rem;
 };
@@ -65,29 +64,43 @@ struct TopkScratch {
 // Writes the K (0 <= K <= n) largest of the n keys key(0..n-1) to out[0..K) in ascending index order
 // (equal keys toward the lower index) and -1 to out[K..k_max).  Every thread of the NT-thread block
 // calls it; `key` must give every thread the same value for the same index.
+//
+// Warp w owns the keys [w seg, (w + 1) seg) (seg a multiple of 32); in each round its lanes read 32
+// consecutive keys.  Four MSB-first 8-bit passes find the K-th largest key tau (per-warp shared
+// histograms; the thread that sums a bin over the warps also clears it for the next pass; warp 0
+// finds the digit), then each warp counts its keys > tau and == tau, every warp takes its prefix
+// over the warps before it, and a second pass writes the kept indices in index order: every key
+// > tau, and the keys == tau while fewer than the needed number of them lie before (ballots give
+// the ranks within a round).  Fifteen block barriers per row.
 template <int NT, typename KeyFn>
 __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, int k_max, TopkScratch<NT> &sc) {
   static_assert(NT >= 256 && NT % 32 == 0, "one thread per histogram bin");
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned lt = (1u << lane) - 1u;
   if (K == n) {
     for (int t = tid; t < n; t += NT) out[t] = t;
   } else if (K > 0) {
+    const int seg = cdiv(cdiv(n, NW), 32) * 32;
+    const int lo = min(warp * seg, n), hi = min(lo + seg, n);
+    for (int e = tid; e < NW * 256; e += NT) (&sc.hist[0][0])[e] = 0u;
+    __syncthreads();
     uint32_t prefix = 0, mask = 0;
     int rem = K;
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int e = tid; e < NW * 256; e += NT) (&sc.hist[0][0])[e] = 0u;
-      __syncthreads();
-      for (int t = tid; t < n; t += NT) {
-        uint32_t k = key(t);
+      for (int t = lo + lane; t < hi; t += 32) {
+        const uint32_t k = key(t);
         if ((k & mask) == prefix) atomicAdd(&sc.hist[warp][(k >> shift) & 255u], 1u);
       }
       __syncthreads();
       if (tid < 256) {
         uint32_t s = 0;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) s += sc.hist[w][tid];
+        for (int w = 0; w < NW; ++w) {
+          s += sc.hist[w][tid];
+          sc.hist[w][tid] = 0u;
+        }
         sc.tot[tid] = s;
       }
       __syncthreads();
@@ -125,48 +138,41 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
       prefix |= sc.digit << shift;
       mask |= 0xffu << shift;
       rem = sc.rem;
-      __syncthreads();
     }
     const uint32_t tau = prefix;
     const int need_eq = rem;
-    int base_eq = 0, base_sel = 0;
-    for (int start = 0; start < n; start += NT * kSelItems) {
-      const int t_first = start + tid * kSelItems;
-      uint32_t kk[kSelItems];
-      int c_eq = 0;
-#pragma unroll
-      for (int e = 0; e < kSelItems; ++e) {
-        int t = t_first + e;
-        kk[e] = t < n ? key(t) : 0u;
-        c_eq += (t < n && kk[e] == tau) ? 1 : 0;
+    int cgt = 0, ceq = 0;
+    for (int t0 = lo; t0 < hi; t0 += 32) {
+      const int t = t0 + lane;
+      const uint32_t k = t < hi ? key(t) : 0u;
+      cgt += __popc(__ballot_sync(0xffffffffu, t < hi && k > tau));
+      ceq += __popc(__ballot_sync(0xffffffffu, t < hi && k == tau));
+    }
+    if (lane == 0) {
+      sc.wgt[warp] = cgt;
+      sc.weq[warp] = ceq;
+    }
+    __syncthreads();
+    int pgt = 0, peq = 0;
+    for (int w = 0; w < warp; ++w) {
+      pgt += sc.wgt[w];
+      peq += sc.weq[w];
+    }
+    int run_eq = peq;                   // keys == tau before this round, whole row
+    int pos = pgt + min(peq, need_eq);  // output slot of this warp's next kept key
+    for (int t0 = lo; t0 < hi; t0 += 32) {
+      const int t = t0 + lane;
+      const uint32_t k = t < hi ? key(t) : 0u;
+      const bool gt = t < hi && k > tau, eq = t < hi && k == tau;
+      const unsigned meq = __ballot_sync(0xffffffffu, eq);
+      const bool keep = gt || (eq && run_eq + __popc(meq & lt) < need_eq);
+      const unsigned mk = __ballot_sync(0xffffffffu, keep);
+      if (keep) {
+        const int p = pos + __popc(mk & lt);
+        if (p < K) out[p] = t;
       }
-      const int ex_eq = block_excl_scan<NW>(c_eq, sc.warp, &sc.total);
-      const int tot_eq = sc.total;
-      int run = base_eq + ex_eq;
-      unsigned sel = 0;
-#pragma unroll
-      for (int e = 0; e < kSelItems; ++e) {
-        int t = t_first + e;
-        if (t < n) {
-          if (kk[e] == tau) {
-            if (run < need_eq) sel |= 1u << e;
-            ++run;
-          } else if (kk[e] > tau) {
-            sel |= 1u << e;
-          }
-        }
-      }
-      const int ex_sel = block_excl_scan<NW>(__popc(sel), sc.warp, &sc.total);
-      const int tot_sel = sc.total;
-      int pos = base_sel + ex_sel;
-#pragma unroll
-      for (int e = 0; e < kSelItems; ++e)
-        if ((sel >> e) & 1u) {
-          if (pos < K) out[pos] = t_first + e;
-          ++pos;
-        }
-      base_eq += tot_eq;
-      base_sel += tot_sel;
+      pos += __popc(mk);
+      run_eq += __popc(meq);
     }
   }
   for (int j = K + tid; j < k_max; j += NT) out[j] = -1;

@@ -6,11 +6,14 @@
 // (about 1/(k+1) of them verify), and a persistent-style fused attention kernel dispatches verify
 // and draft attention to their own tile code on chip instead of launching two kernels.
 //
-// Where the tcgen05 verify applies (bf16, d = 128, pages of 8 or more tokens), the call runs the
-// verify-phase requests through it (its blocks skip draft-phase requests), then the finalize, then
-// the draft kernel over the draft-phase requests (its blocks skip verify-phase requests): the
-// tcgen05 verify holds all of an SM's shared memory, so verify and draft work cannot share a block
-// there, and one mma.sync launch mixing both measured about twice the time of the three launches.
+// Where the tcgen05 verify applies (bf16, d = 128, pages of 8 or more tokens), the call launches the
+// verify over the verify-phase requests (its blocks skip draft-phase requests), the draft kernel
+// over the draft-phase requests (its blocks skip verify-phase requests) and then the finalize.  The
+// tcgen05 verify holds all of an SM's shared memory, so verify and draft work cannot share a block;
+// instead the draft kernel does not wait for the verify (programmatic dependent launch): its blocks
+// start once the verify has handed out its last item and run on the SMs the verify's finishing
+// blocks leave, so the draft work fills the verify's tail (one mma.sync launch mixing both measured
+// about twice the time of separate launches).
 // Otherwise one persistent launch mixes both: each block enumerates the work of the whole batch
 // itself (per-request item counts and prefix sums in shared memory: verify items first, draft items
 // after them, so the long items are started first) and then takes items c, c + grid, c + 2*grid, ...;
@@ -46,6 +49,8 @@ __global__ void __launch_bounds__(128, 2) unified_kernel(VerifyArgs va, DraftArg
   __shared__ int s_vpre[kUniMaxBatch + 1];
   __shared__ int s_dpre[kUniMaxBatch + 1];
   const int B = va.kv.batch, h_kv = va.kv.h_kv, tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   // Items per request.
   for (int b = tid; b < B; b += blockDim.x) {
     int L = va.kv.seq_lens[b];
@@ -148,8 +153,7 @@ static int launch_uni(const VerifyArgs &va, const DraftArgs &da, const uint8_t *
   int per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, unified_kernel<D, NRT, GMAX>, 128, smem);
   const int grid = sm_count() * (per_sm > 0 ? per_sm : 1);
-  unified_kernel<D, NRT, GMAX><<<grid, 128, smem, st>>>(va, da, phase);
-  return check_launch("unified_kernel");
+  return launch(unified_kernel<D, NRT, GMAX>, dim3(grid), dim3(128), smem, st, "unified_kernel", va, da, phase);
 }
 
 template <int D, int NRT>
@@ -245,6 +249,11 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
     va.sched = reinterpret_cast<int *>(ws);
     va.split_out = reinterpret_cast<int *>(ws + lay.split_off);
     if ((rc = launch_verify_tc(kv, va, st))) return rc;
+    // The draft work needs nothing the verify writes: launched right behind it, it starts as soon
+    // as the verify has handed out its last item and fills the SMs its finishing blocks leave; the
+    // finalize follows once both are done.
+    da.defer_wait = 1;
+    if ((rc = launch_draft_any(kv->dtype, kv->d, da, dim3(lay.C_max, lay.units), st))) return rc;
   } else {
     const int nrt = lay.R <= 16 ? 1 : (lay.R <= 32 ? 2 : 4);
     rc = kv->d == 128 ? uni_rows<128>(nrt, lay.gmax, va, da, phase, st) : uni_rows<64>(nrt, lay.gmax, va, da, phase, st);
@@ -272,8 +281,7 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
   f.scores = scores;
   f.scores_stride = scores_stride;
   f.split_len = tc ? va.split_out : nullptr;
+  f.balanced = tc ? 1 : 0;
   const int n_tok = scores ? cdiv(kv->max_seq_len, kFinTok) : 0;
-  if ((rc = launch_finalize(f, n_tok, lay.units, st))) return rc;
-  if (!tc) return SSD_OK;
-  return launch_draft_any(kv->dtype, kv->d, da, dim3(lay.C_max, lay.units), st);
+  return launch_finalize(f, n_tok, lay.units, st);
 }

@@ -27,6 +27,8 @@ template <int D, int NRT, bool BLOCKS>
 __global__ void __launch_bounds__(128, 2) verify_mma_kernel(VerifyArgs a) {
   extern __shared__ __align__(128) char smem[];
   const int unit = blockIdx.y, split = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if (BLOCKS) {
     int nu = min(max(a.ucnt[unit], 0), a.umax);
     if (split >= block_splits(nu)) return;
@@ -40,7 +42,10 @@ template <int D>
 __global__ void __launch_bounds__(128) verify_simt_kernel(VerifyArgs a) {
   extern __shared__ __align__(128) char smem[];
   const int unit = blockIdx.y, split = blockIdx.x;
-  if (split >= verify_splits(clamp_len(a.kv, unit / a.kv.h_kv))) return;
+  pdl_trigger();
+  pdl_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.split_out = kSimtSplitTokens;  // for the finalize
+  if (split >= verify_splits(clamp_len(a.kv, unit / a.kv.h_kv), kSimtSplitTokens)) return;
   verify_item_simt<D>(a, unit, split, smem);
 }
 
@@ -67,12 +72,84 @@ __device__ __forceinline__ void fin_fma_row(const uint4 &raw, float c, float (&a
   }
 }
 
+// LSE merge of one unit's split log-sum-exps, per row r < R: sLn[r] (natural log) and sL2[r]
+// (log2) of the row's total.  Warp w of an NW-warp block takes rows w, w + NW, ...; lane j holds
+// split j (a loop when ns > 32).  Every split value is loaded before the first reduction.
+template <int NW>
+__device__ __forceinline__ void fin_lse_merge(const FinalizeArgs &f, int64_t pbase, int ns, float *sLn, float *sL2) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int Q = (kMaxRows + NW - 1) / NW;
+  float v[Q];
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const int r = warp + NW * q;
+    v[q] = (r < f.R && lane < ns) ? f.lse_parts[pbase + (int64_t)lane * f.R + r] : -INFINITY;
+  }
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    const int r = warp + NW * q;
+    if (r >= f.R) break;
+    float M = v[q];
+    for (int j = lane + 32; j < ns; j += 32) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
+    M = warp_max(M);
+    float sum = 0.f;
+    if (M != -INFINITY) {
+      sum = lane < ns ? fast_exp2((v[q] - M) * kLog2e) : 0.f;
+      for (int j = lane + 32; j < ns; j += 32) sum += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) {
+      const float ln = (M == -INFINITY) ? -INFINITY : M + __logf(sum);
+      sLn[r] = ln;
+      sL2[r] = ln * kLog2e;
+    }
+  }
+}
+
+// Split combine of one unit (request b, KV head g): rows r = r0, r0 + rstep, ... each get
+// out = sum_j 2^((lse_j - LSE) log2 e) o_j over the splits and lse = LSE; thread q4 of the D / 4
+// threads of a row takes one float4 of d.
+__device__ __forceinline__ void fin_combine_rows(const FinalizeArgs &f, int64_t pbase, int ns, const float *sLn,
+                                                 int b, int g, int r0, int rstep, int q4) {
+  const int D = f.D;
+  for (int r = r0; r < f.R; r += rstep) {
+    const float ln = sLn[r];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ln != -INFINITY) {
+      const float *lp = f.lse_parts + pbase + r;
+      const float4 *op = reinterpret_cast<const float4 *>(f.o_parts + (pbase + r) * D) + q4;
+      const int64_t ostep = (int64_t)f.R * D / 4;
+#pragma unroll 4
+      for (int j = 0; j < ns; ++j) {
+        float w = fast_exp2((lp[(int64_t)j * f.R] - ln) * kLog2e);
+        float4 o = op[j * ostep];
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+      }
+    }
+    const int i = r / f.G, hl = r % f.G;
+    const int64_t row = ((int64_t)b * f.n_c + i) * f.h_q + g * f.G + hl;
+    reinterpret_cast<float4 *>(f.out + row * D)[q4] = acc;
+    if (q4 == 0 && f.lse) f.lse[row] = ln;
+  }
+}
+
+// Splits of unit u's request of length L, as the verify pass cut them.
+__device__ __forceinline__ int fin_splits(const FinalizeArgs &f, int u, int L) {
+  return f.ucnt       ? block_splits(min(max(f.ucnt[u], 0), f.umax))
+         : f.balanced ? tc_split_count(L, *f.split_len)
+                      : verify_splits(L, f.split_len ? *f.split_len : kSplitTokens);
+}
+
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, int n_tok) {
   __shared__ float sLn[kMaxRows];
   __shared__ float sL2[kMaxRows];
   __shared__ __align__(16) float s_coef[kMaxRows * kFinGroups];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = blockIdx.y, b = u / f.h_kv, g = u % f.h_kv;
+  pdl_wait();
   if (f.phase && f.phase[b] == 0) return;
   int L = f.seq_lens[b];
   L = L < 0 ? 0 : (L > f.max_seq_len ? f.max_seq_len : L);
@@ -83,8 +160,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     for (int j = tid; j < f.sel_kmax; j += kFinThreads) f.sel_idx[(int64_t)u * f.sel_kmax + j] = -1;
     if (tid == 0) f.sel_cnt[u] = 0;
   }
-  const int ns = f.ucnt ? block_splits(min(max(f.ucnt[u], 0), f.umax))
-                        : verify_splits(L, f.split_len ? *f.split_len : kSplitTokens);
+  const int ns = fin_splits(f, u, L);
   const int64_t pbase = (int64_t)u * f.S_max * f.R;
   const int64_t rbase = (int64_t)u * f.R;
   const int nref = f.Lpad / kRefGroup;
@@ -112,62 +188,14 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     cp_async_commit();
   }
 
-  // LSE merge: warp w takes rows w, w + kFinWarps, ...; lane j holds split j (a loop when ns > 32).
-  {
-    constexpr int kFinWarps = kFinThreads / 32;
-    float v[kMaxRows / kFinWarps];
-#pragma unroll
-    for (int q = 0; q < kMaxRows / kFinWarps; ++q) {
-      const int r = warp + kFinWarps * q;
-      v[q] = (r < f.R && lane < ns) ? f.lse_parts[pbase + (int64_t)lane * f.R + r] : -INFINITY;
-    }
-#pragma unroll
-    for (int q = 0; q < kMaxRows / kFinWarps; ++q) {
-      const int r = warp + kFinWarps * q;
-      if (r >= f.R) break;
-      float M = v[q];
-      for (int j = lane + 32; j < ns; j += 32) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
-      M = warp_max(M);
-      float sum = 0.f;
-      if (M != -INFINITY) {
-        sum = lane < ns ? fast_exp2((v[q] - M) * kLog2e) : 0.f;
-        for (int j = lane + 32; j < ns; j += 32) sum += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
-      }
-      sum = warp_sum(sum);
-      if (lane == 0) {
-        const float ln = (M == -INFINITY) ? -INFINITY : M + __logf(sum);
-        sLn[r] = ln;
-        sL2[r] = ln * kLog2e;
-      }
-    }
-  }
+  fin_lse_merge<kFinThreads / 32>(f, pbase, ns, sLn, sL2);
   __syncthreads();
+  pdl_trigger();
 
   if (!tok) {
-    const int D = f.D, tpr = D / 4, rpc = fin_rows_per_cta(D);
-    const int n_comb = (int)gridDim.x - n_tok, q4 = tid % tpr;
-    for (int r = ((int)blockIdx.x - n_tok) * rpc + tid / tpr; r < f.R; r += rpc * n_comb) {
-    const float ln = sLn[r];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ln != -INFINITY) {
-      const float *lp = f.lse_parts + pbase + r;
-      const float4 *op = reinterpret_cast<const float4 *>(f.o_parts + (pbase + r) * D) + q4;
-      const int64_t ostep = (int64_t)f.R * D / 4;
-#pragma unroll 4
-      for (int j = 0; j < ns; ++j) {
-        float w = fast_exp2((lp[(int64_t)j * f.R] - ln) * kLog2e);
-        float4 o = op[j * ostep];
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
-      }
-    }
-    const int i = r / f.G, hl = r % f.G;
-    const int64_t row = ((int64_t)b * f.n_c + i) * f.h_q + g * f.G + hl;
-    reinterpret_cast<float4 *>(f.out + row * D)[q4] = acc;
-    if (q4 == 0 && f.lse) f.lse[row] = ln;
-    }
+    const int tpr = f.D / 4, rpc = fin_rows_per_cta(f.D);
+    const int n_comb = (int)gridDim.x - n_tok;
+    fin_combine_rows(f, pbase, ns, sLn, b, g, ((int)blockIdx.x - n_tok) * rpc + tid / tpr, rpc * n_comb, tid % tpr);
     return;
   }
 
@@ -258,18 +286,106 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   }
 }
 
+// ------------------------------------------------------------------------------------------------
+// Criticality and Top-K of one unit per block, and the split combine: the pass after the verify in
+// ssd_verify_select when a row of scores fits in shared memory.  Blocks [0, units): unit
+// u = blockIdx.x merges its split LSEs, rematerialises its row of scores from the side values with
+// exactly the finalize's arithmetic (same coefficients, rows summed in the same order, so the same
+// bits), writes the row out and keeps its keys in shared memory, then selects its Top-K from there
+// (topk_row: ties to the lower index, ascending output).  Blocks [units, 2 units): the combine of
+// unit blockIdx.x - units.  One pass over the side values replaces the finalize's token blocks,
+// the separate select launch and its read of the scores.
+// ------------------------------------------------------------------------------------------------
+constexpr int kCsThreads = 512;
+constexpr int kCsSmemRow = 40960;  // longest row kept in shared memory (160 KB of keys)
+
+__global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f, int units) {
+  extern __shared__ __align__(16) uint32_t s_keys[];  // [max_seq_len] keys of the unit's scores
+  __shared__ float sLn[kMaxRows], sL2[kMaxRows];
+  __shared__ TopkScratch<kCsThreads> sc;
+  const int tid = threadIdx.x;
+  const bool comb = (int)blockIdx.x >= units;
+  const int u = comb ? (int)blockIdx.x - units : (int)blockIdx.x;
+  const int b = u / f.h_kv, g = u % f.h_kv;
+  pdl_wait();
+  int L = f.seq_lens[b];
+  L = L < 0 ? 0 : (L > f.max_seq_len ? f.max_seq_len : L);
+  const int ns = fin_splits(f, u, L);
+  const int64_t pbase = (int64_t)u * f.S_max * f.R, rbase = (int64_t)u * f.R;
+  fin_lse_merge<kCsThreads / 32>(f, pbase, ns, sLn, sL2);
+  __syncthreads();
+  if (comb) {
+    pdl_trigger();
+    const int tpr = f.D / 4;
+    fin_combine_rows(f, pbase, ns, sLn, b, g, tid / tpr, kCsThreads / tpr, tid % tpr);
+    return;
+  }
+  // crit[t] = sum_r e[r][t] * 2^(m_ref[r][t / 16] - LSE2_r), eight consecutive tokens per thread,
+  // rows in batches of kFinAhead (every load of a batch in flight together).
+  const int nref = f.Lpad / kRefGroup;
+  const __half *sp = f.side_p + rbase * f.Lpad;
+  for (int t0 = tid * 8; t0 < L; t0 += kCsThreads * 8) {
+    const int grp = t0 / kRefGroup;
+    float crit[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) crit[k] = 0.f;
+    for (int r0 = 0; r0 < f.R; r0 += kFinAhead) {
+      uint4 raw[kFinAhead];
+      float m[kFinAhead];
+#pragma unroll
+      for (int k = 0; k < kFinAhead; ++k) {
+        const int r = r0 + k;
+        raw[k] = r < f.R ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad + t0)) : make_uint4(0, 0, 0, 0);
+        m[k] = r < f.R ? __ldg(f.side_m + (rbase + r) * nref + grp) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < kFinAhead; ++k) {
+        const int r = r0 + k;
+        if (r < f.R) {
+          const float l2 = sL2[r];
+          fin_fma_row(raw[k], (l2 == -INFINITY) ? 0.f : fast_exp2(m[k] - l2), crit);
+        }
+      }
+    }
+    float *dst = f.scores + (int64_t)u * f.scores_stride + t0;
+    if (t0 + 8 <= L && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
+      reinterpret_cast<float4 *>(dst)[0] = make_float4(crit[0], crit[1], crit[2], crit[3]);
+      reinterpret_cast<float4 *>(dst)[1] = make_float4(crit[4], crit[5], crit[6], crit[7]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (t0 + k < L) dst[k] = crit[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (t0 + k < L) s_keys[t0 + k] = score_key(crit[k]);
+  }
+  pdl_trigger();
+  __syncthreads();
+  int K = f.ks[b];
+  K = K < 0 ? 0 : (K > L ? L : K);
+  if (K > f.sel_kmax) {
+    if (tid == 0) atomicOr(f.status, (unsigned)SSD_FAULT_KMAX);
+    K = f.sel_kmax;
+  }
+  topk_row<kCsThreads>([&](int t) -> uint32_t { return s_keys[t]; }, L, K, f.sel_idx + (int64_t)u * f.sel_kmax,
+                       f.sel_kmax, sc);
+  if (tid == 0) f.sel_cnt[u] = K;
+}
+
 int launch_finalize(const FinalizeArgs &f, int n_tok, int units, cudaStream_t st) {
   // With token blocks in the grid, one combine block per unit loops over the rows (fewer blocks to
   // schedule behind the token work); without them, a block per group of rows.
   const int n_comb = n_tok > 0 ? 1 : cdiv(f.R, kFinThreads / (f.D / 4));
-  finalize_kernel<<<dim3(n_tok + n_comb, units), kFinThreads, 0, st>>>(f, n_tok);
-  return check_launch("finalize_kernel");
+  return launch(finalize_kernel, dim3(n_tok + n_comb, units), dim3(kFinThreads), 0, st, "finalize_kernel", f, n_tok);
 }
 
 // Public split combine: one block per row.
 __global__ void __launch_bounds__(128) combine_kernel(const float *o_parts, const float *lse_parts, int n_splits,
                                                      int d, float *out, float *lse) {
   const int row = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
   const float *lp = lse_parts + (int64_t)row * n_splits;
   float M = -INFINITY;
   for (int j = 0; j < n_splits; ++j) M = fmaxf(M, lp[j]);
@@ -300,8 +416,7 @@ static int launch_mma(const VerifyArgs &a, dim3 grid, cudaStream_t st) {
   constexpr int smem = VerifyMmaCfg<D, NRT>::SMEM;
   int rc = ensure_smem<verify_mma_kernel<D, NRT, BLOCKS>>(smem);
   if (rc) return rc;
-  verify_mma_kernel<D, NRT, BLOCKS><<<grid, 128, smem, st>>>(a);
-  return check_launch("verify_mma_kernel");
+  return launch(verify_mma_kernel<D, NRT, BLOCKS>, grid, dim3(128), smem, st, "verify_mma_kernel", a);
 }
 
 template <bool BLOCKS>
@@ -321,8 +436,7 @@ static int launch_simt(const VerifyArgs &a, dim3 grid, cudaStream_t st) {
   constexpr int smem = VerifySimtCfg<D>::SMEM;
   int rc = ensure_smem<verify_simt_kernel<D>>(smem);
   if (rc) return rc;
-  verify_simt_kernel<D><<<grid, 128, smem, st>>>(a);
-  return check_launch("verify_simt_kernel");
+  return launch(verify_simt_kernel<D>, grid, dim3(128), smem, st, "verify_simt_kernel", a);
 }
 
 struct VerifyLayout {
@@ -355,6 +469,12 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   return l;
 }
 
+// Splits per unit the workspace holds: 512-token splits (the tensor-core verify picks longer ones),
+// 128-token splits on the fp32 path.
+static int verify_smax(const ssd_paged_kv *kv) {
+  return cdiv(kv->max_seq_len, kv->dtype == SSD_DTYPE_F32 ? kSimtSplitTokens : kSplitTokens);
+}
+
 static int verify_common_checks(const ssd_paged_kv *kv, int h_q, int n_cand, const void *q, const float *out,
                                 const char *who) {
   if (!q || !out) return fail(SSD_ERR_INVALID_ARG, "%s: q and out must be non-NULL", who);
@@ -373,7 +493,7 @@ using namespace ssd;
 
 extern "C" size_t ssd_verify_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand) {
   if (!kv || kv->h_kv <= 0 || h_q <= 0 || n_cand <= 0 || kv->batch < 0 || kv->max_seq_len < 0) return 0;
-  return verify_layout(kv, h_q, n_cand, cdiv(kv->max_seq_len, kSplitTokens)).total;
+  return verify_layout(kv, h_q, n_cand, verify_smax(kv)).total;
 }
 
 static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
@@ -391,7 +511,7 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
     if (bscores_stride < cdiv(kv->max_seq_len, kBlockTokens))
       return fail(SSD_ERR_INVALID_ARG, "%s: bscores_stride too small", who);
   }
-  const VerifyLayout lay = verify_layout(kv, h_q, n_cand, cdiv(kv->max_seq_len, kSplitTokens));
+  const VerifyLayout lay = verify_layout(kv, h_q, n_cand, verify_smax(kv));
   if (!workspace || workspace_bytes < lay.total)
     return fail(SSD_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", who, workspace_bytes, lay.total);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
@@ -427,8 +547,9 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
   a.sched = reinterpret_cast<int *>(ws + lay.ctr_off);
   dim3 grid(lay.S_max, lay.units);
   const bool tc = verify_tc_supported(kv, lay.R);
+  const bool simt = !tc && kv->dtype != SSD_DTYPE_BF16;
+  a.split_out = reinterpret_cast<int *>(ws + lay.split_off);
   if (tc) {
-    a.split_out = reinterpret_cast<int *>(ws + lay.split_off);
     rc = launch_verify_tc(kv, a, st);
   }
   else if (kv->dtype == SSD_DTYPE_BF16)
@@ -458,13 +579,20 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
   f.scores_stride = scores_stride;
   f.bscores = bscores;
   f.bstride = bscores_stride;
-  f.split_len = tc ? a.split_out : nullptr;
+  f.split_len = (tc || simt) ? a.split_out : nullptr;
+  f.balanced = tc ? 1 : 0;
   f.ks = ks;
   f.sel_idx = idx;
   f.sel_cnt = cnt;
   f.sel_kmax = k_max;
   f.sel_ctr = reinterpret_cast<unsigned *>(ws + lay.ctr_off) + 2;  // slots 0-1: the tensor-core kernel
   f.status = status;
+  if (ks && kv->max_seq_len <= kCsSmemRow) {
+    const int smem = kv->max_seq_len * 4;
+    if ((rc = ensure_smem<crit_select_kernel>(smem))) return rc;
+    return launch(crit_select_kernel, dim3(2 * lay.units), dim3(kCsThreads), smem, st, "crit_select_kernel", f,
+                  lay.units);
+  }
   const int n_tok = crit ? cdiv(kv->max_seq_len, kFinTok) : 0;
   return launch_finalize(f, n_tok, lay.units, st);
 }
@@ -567,6 +695,6 @@ extern "C" int ssd_combine(const float *o_parts, const float *lse_parts, int n_r
     return fail(SSD_ERR_INVALID_ARG, "ssd_combine: NULL pointer");
   if (n_rows == 0) return SSD_OK;
   if (n_rows > (1 << 30)) return fail(SSD_ERR_UNSUPPORTED, "ssd_combine: too many rows");
-  combine_kernel<<<n_rows, 128, 0, reinterpret_cast<cudaStream_t>(stream)>>>(o_parts, lse_parts, n_splits, d, out, lse);
-  return check_launch("combine_kernel");
+  return launch(combine_kernel, dim3(n_rows), dim3(128), 0, reinterpret_cast<cudaStream_t>(stream), "combine_kernel",
+                o_parts, lse_parts, n_splits, d, out, lse);
 }

@@ -6,8 +6,8 @@
 // logits + LSE).  Same work items, partials and criticality side values as the mma.sync tile in
 // ssd_verify_tile.cuh; the finalize pass is shared.
 //
-// One persistent block per SM works through work items (splits of 512 to 2048 tokens of one (request, KV
-// head)), tile by tile (128 tokens).  Its first item is blockIdx.x; later ones come from a global
+// One persistent block per SM works through work items (splits of about 512 to 2048 tokens of one
+// (request, KV head), whole tiles, equal within a unit: tc_split_count), tile by tile (128 tokens).  Its first item is blockIdx.x; later ones come from a global
 // counter, so the items spread over the blocks by how fast each block actually runs.
 //  * warp 8 draws the items, hands their numbers to the other warps through a small shared ring, and
 //    streams K and V tiles with TMA (one box per page and 64-column panel, 128-byte swizzle, L2
@@ -40,7 +40,7 @@
 namespace ssd {
 using namespace sm100;
 
-constexpr int kTcTile = 128;
+constexpr int kTcTile = kTcTileTokens;
 constexpr int kTcWarps = 10;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcSoftmax = 256;  // two warpgroups
@@ -52,7 +52,7 @@ constexpr int kTcItemRing = 8;  // item numbers handed from the producer to the 
 // cycles, so items are made as long as load balance allows: about kTcItemsPerBlock items per block
 // over the batch's actual tokens, a multiple of the tile, between kSplitTokens and kTcMaxSplit.
 constexpr int kTcItemsPerBlock = 6;
-constexpr int kTcMaxSplit = 2048;
+constexpr int kTcMaxSplit = kTcMaxSplitTiles * kTcTile;
 constexpr int kSlotBytes = kTcTile * 256;  // one K or V tile: 2 panels x 128 rows x 128 B
 constexpr int kPanelBytes = kTcTile * 128;
 constexpr float kLazy = 8.f;
@@ -108,8 +108,7 @@ __device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int 
   it.g = r / ns;
   it.split = r % ns;
   it.L = len[lo];
-  it.t0 = it.split * split_len;
-  it.t1 = min(it.t0 + split_len, it.L);
+  tc_split_range(it.L, split_len, it.split, it.t0, it.t1);
   it.ntiles = cdiv(it.t1 - it.t0, kTcTile);
   return it;
 }
@@ -235,6 +234,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s.len = s.pre + kTcMaxBatch + 1;
   }
 
+  // Set-up that reads nothing an earlier kernel writes runs before the wait for the previous grid:
+  // barriers, tensor memory, descriptor prefetch, zeroed query buffers.
+  if (tid == 0) {
+    *s.abort = 0;
+    for (int k = 0; k < 8; ++k) s.vote[k] = 0;
+    for (int r = 0; r < NP; ++r) s.mref[r] = r < a.R ? -INFINITY : INFINITY;  // first item's references
+    for (int k = 0; k < C::NSLOT; ++k) {
+      mbar_init(bar_addr(s.full + k), 1);
+      mbar_init(bar_addr(s.empty + k), 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar_addr(s.s_full + k), 1);
+      mbar_init(bar_addr(s.s_empty + k), kTcSoftmax);
+      mbar_init(bar_addr(s.p_full + k), kTcSoftmax);
+      mbar_init(bar_addr(s.p_empty + k), 1);
+      mbar_init(bar_addr(s.q_full + k), 1);
+      mbar_init(bar_addr(s.q_empty + k), 1);
+      mbar_init(bar_addr(s.grp + k), 128);
+    }
+    mbar_init(bar_addr(s.o_full), 1);
+    mbar_init(bar_addr(s.o_empty), kTcSoftmax);
+    mbar_init(bar_addr(s.drain), 1);
+    for (int k = 0; k < kTcItemRing; ++k) mbar_init(bar_addr(s.item_full + k), 1);
+    mbar_init_fence();
+  }
+  if (warp == kTcMmaWarp) {
+    tmem_alloc(smem_u32(s.tmem), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == kTcProducerWarp && lane == 0) {
+    tma_prefetch_desc(&kvmap);
+    tma_prefetch_desc(&qmap);
+  }
+  // Query buffers start zeroed: the TMA writes rows < R only, padded rows must read as zero.
+  for (int e = tid; e < 2 * C::Q_BYTES / 16; e += kTcThreads)
+    reinterpret_cast<uint4 *>(sm + C::OFF_Q)[e] = make_uint4(0, 0, 0, 0);
+  pdl_wait();
+
   // Per-request lengths, the split length, item counts and their prefix (chunked block scan).
   int split_len;
   {
@@ -263,40 +300,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ long long s_wtok[kTcWarps];
     __shared__ int s_wsum[kTcWarps];
     if (lane == 0) s_wtok[warp] = tok;
-    if (tid == 0) {
-      *s.abort = 0;
-      for (int k = 0; k < 8; ++k) s.vote[k] = 0;
-      for (int r = 0; r < NP; ++r) s.mref[r] = r < a.R ? -INFINITY : INFINITY;  // first item's references
-      for (int k = 0; k < C::NSLOT; ++k) {
-        mbar_init(bar_addr(s.full + k), 1);
-        mbar_init(bar_addr(s.empty + k), 1);
-      }
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(bar_addr(s.s_full + k), 1);
-        mbar_init(bar_addr(s.s_empty + k), kTcSoftmax);
-        mbar_init(bar_addr(s.p_full + k), kTcSoftmax);
-        mbar_init(bar_addr(s.p_empty + k), 1);
-        mbar_init(bar_addr(s.q_full + k), 1);
-        mbar_init(bar_addr(s.q_empty + k), 1);
-        mbar_init(bar_addr(s.grp + k), 128);
-      }
-      mbar_init(bar_addr(s.o_full), 1);
-      mbar_init(bar_addr(s.o_empty), kTcSoftmax);
-      mbar_init(bar_addr(s.drain), 1);
-      for (int k = 0; k < kTcItemRing; ++k) mbar_init(bar_addr(s.item_full + k), 1);
-      mbar_init_fence();
-    }
-    if (warp == kTcMmaWarp) {
-      tmem_alloc(smem_u32(s.tmem), C::TMEM_COLS);
-      tmem_relinquish();
-    }
-    if (warp == kTcProducerWarp && lane == 0) {
-      tma_prefetch_desc(&kvmap);
-      tma_prefetch_desc(&qmap);
-    }
-    // Query buffers start zeroed: the TMA writes rows < R only, padded rows must read as zero.
-    for (int e = tid; e < 2 * C::Q_BYTES / 16; e += kTcThreads)
-      reinterpret_cast<uint4 *>(sm + C::OFF_Q)[e] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int sum = 0;
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-      loc[k] = h_kv * verify_splits(loc[k], split_len);
+      loc[k] = h_kv * tc_split_count(loc[k], split_len);
       sum += loc[k];
     }
     int incl = sum;
@@ -372,6 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     int32_t pid_next[kPidRegs];
     load_pids(cur, pid_next);
+    const int boxes_per_tile = kTcTile / box_rows;
     for (;; ++jl) {
       // Hand the item number to the MMA and softmax roles (n_items ends their loops). The slot
       // written here last held item jl - kTcItemRing, which every role has read by now: this warp
@@ -400,7 +404,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_4d(qb + C::Q_PANEL, &qmap, 0, 1, it.g * G, it.b * n_c, qf);
       }
       __syncwarp();
-      const int boxes_per_tile = kTcTile / box_rows;
       for (int k = 0; ok && k < it.ntiles; ++k) {
         const int tb = it.t0 + k * kTcTile, tend = min(tb + kTcTile, it.t1);
         // Lane j < boxes_per_tile handles box j of this tile.
@@ -477,6 +480,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       cur = nxt;
       nxt = drew ? min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items) : n_items;
     }
+    // The block has taken its last item: the next kernel on the stream may begin launching.
+    pdl_trigger();
     // Every draw this warp issued has returned (also after an abort) before the block counts itself
     // finished below, so the counter reset cannot overtake a draw.
     const int last_draw = __shfl_sync(0xffffffffu, raw, 0);
@@ -854,8 +859,8 @@ static int launch_tc(const CUtensorMap &map, const CUtensorMap &qmap, const Veri
   constexpr int smem = TcCfg<NP>::SMEM;
   int rc = ensure_smem<verify_tc_kernel<NP>>(smem);
   if (rc) return rc;
-  verify_tc_kernel<NP><<<grid, kTcThreads, smem, st>>>(map, qmap, a, box_rows);
-  return check_launch("verify_tc_kernel");
+  return launch(verify_tc_kernel<NP>, dim3(grid), dim3(kTcThreads), smem, st, "verify_tc_kernel", map, qmap, a,
+                box_rows);
 }
 
 int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st) {

@@ -41,7 +41,7 @@ struct VerifyArgs {
   unsigned *status;
   int *sched;  // [2] in the counter area: next-item counter and finished-block count (tensor-core
                // path); zero at launch, and the last block to finish returns both to zero
-  int *split_out;  // tensor-core path: receives the split length it chose (read by the finalize)
+  int *split_out;  // tensor-core and fp32 paths: receives the split length used (read by the finalize)
   const uint8_t *phase;  // tensor-core path: nullptr, or only requests with phase[b] == 1 get items
 };
 
@@ -62,6 +62,29 @@ struct VerifyMmaCfg {
 
 // Number of work items (splits) of one unit.
 __device__ __forceinline__ int verify_splits(int L, int split = kSplitTokens) { return cdiv(L, split); }
+
+// Splits of the tensor-core verify.  A unit of L tokens is cut into whole 128-token tiles, then into
+// ns = round(L / split_len) splits (at least one, at most kTcMaxSplitTiles tiles each) whose tile
+// counts differ by at most one: no split is a short ragged tail.  A work item's pipeline latency
+// (loads, logits, softmax, P V, epilogue) is hidden behind the tiles of a long item but not of a
+// short one, so a split of one to three tiles costs about as much as one of ten.
+constexpr int kTcTileTokens = 128;
+constexpr int kTcMaxSplitTiles = 16;
+__device__ __forceinline__ int tc_split_count(int L, int split_len) {
+  const int T = cdiv(L, kTcTileTokens);
+  if (T <= 0) return 0;
+  int ns = (L + split_len / 2) / split_len;
+  ns = max(ns, cdiv(T, kTcMaxSplitTiles));
+  return min(max(ns, 1), T);
+}
+// Tokens [t0, t1) of split s of a unit of L tokens.
+__device__ __forceinline__ void tc_split_range(int L, int split_len, int s, int &t0, int &t1) {
+  const int T = cdiv(L, kTcTileTokens), ns = tc_split_count(L, split_len);
+  const int base = T / ns, extra = T % ns;
+  const int first = s * base + min(s, extra);
+  t0 = first * kTcTileTokens;
+  t1 = min((first + base + (s < extra ? 1 : 0)) * kTcTileTokens, L);
+}
 __device__ __forceinline__ int block_splits(int ucnt) { return cdiv(ucnt, kBlocksPerItem); }
 
 template <int D, int NRT, bool BLOCKS>
@@ -340,9 +363,9 @@ __device__ __forceinline__ void verify_item_mma(const VerifyArgs &a, int unit, i
 // ------------------------------------------------------------------------------------------------
 template <int D>
 struct VerifySimtCfg {
-  static constexpr int CH = 32;  // tokens staged per step
+  static constexpr int CH = 64;  // tokens staged per step
   static constexpr int KSTR = D + 1;
-  static constexpr int SMEM = (kMaxRows * D + kMaxRows * kSplitTokens + CH * KSTR + 2 * kMaxRows) * 4;
+  static constexpr int SMEM = (kMaxRows * D + kMaxRows * kSimtSplitTokens + CH * KSTR + 2 * kMaxRows) * 4;
 };
 
 template <int D>
@@ -353,12 +376,12 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
   const int b = unit / h_kv, g = unit % h_kv;
   const int G = a.G, R = a.R, n_c = a.n_c;
   const int L = effective_len(a.kv, b, n_c, a.status);
-  const int t0 = split * kSplitTokens, t1 = min(t0 + kSplitTokens, L);
+  const int t0 = split * kSimtSplitTokens, t1 = min(t0 + kSimtSplitTokens, L);
   const int n = t1 - t0;
   if (n <= 0) return;
   float *sQ = reinterpret_cast<float *>(smem);  // [R][D]
-  float *sS = sQ + kMaxRows * D;                 // [R][kSplitTokens]
-  float *sK = sS + kMaxRows * kSplitTokens;      // [CH][D+1]
+  float *sS = sQ + kMaxRows * D;                 // [R][kSimtSplitTokens]
+  float *sK = sS + kMaxRows * kSimtSplitTokens;  // [CH][D+1]
   float *sBase = sK + C::CH * C::KSTR;           // [R]
   float *sL = sBase + kMaxRows;                  // [R]
   const float *q = reinterpret_cast<const float *>(a.q);
@@ -366,34 +389,56 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
     int r = e / D, dd = e % D, i = r / G, hl = r % G;
     sQ[e] = q[(((int64_t)b * n_c + i) * a.h_q + g * G + hl) * D + dd];
   }
-  const int64_t v_off = (int64_t)h_kv * a.kv.page_size * D;
-  for (int c0 = 0; c0 < n; c0 += C::CH) {
+  // Stages CH tokens of K (which = 0) or V (which = 1) into sK: every page lookup of the step is
+  // issued before any row load, then every row load (16 bytes each) before any store, so a step
+  // costs two memory latencies whatever the number of loads per thread.
+  auto stage = [&](int c0, int which) {
+    constexpr int V4 = D / 4, PER_T = C::CH * V4 / 128;
+    static_assert(C::CH * V4 % 128 == 0, "whole 16-byte loads per thread");
     __syncthreads();
-    for (int e = tid; e < C::CH * D; e += blockDim.x) {
-      int j = e / D, dd = e % D, t = t0 + c0 + j;
-      const float *kr = (c0 + j < n) ? kv_row<D, float>(a.kv, b, 0, g, t, a.status) : nullptr;
-      sK[j * C::KSTR + dd] = kr ? kr[dd] : 0.f;
+    const float *rows[PER_T];
+#pragma unroll
+    for (int k = 0; k < PER_T; ++k) {
+      const int e = tid + k * 128, j = e / V4;
+      rows[k] = (c0 + j < n) ? kv_row<D, float>(a.kv, b, which, g, t0 + c0 + j, a.status) : nullptr;
+    }
+    float4 v[PER_T];
+#pragma unroll
+    for (int k = 0; k < PER_T; ++k)
+      v[k] = rows[k] ? __ldg(reinterpret_cast<const float4 *>(rows[k]) + (tid + k * 128) % V4)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < PER_T; ++k) {
+      const int e = tid + k * 128, j = e / V4, q4 = e % V4;
+      float *dst = sK + j * C::KSTR + 4 * q4;
+      dst[0] = v[k].x;
+      dst[1] = v[k].y;
+      dst[2] = v[k].z;
+      dst[3] = v[k].w;
     }
     __syncthreads();
+  };
+  for (int c0 = 0; c0 < n; c0 += C::CH) {
+    stage(c0, 0);
     for (int e = tid; e < R * C::CH; e += blockDim.x) {
       int r = e / C::CH, j = e % C::CH, t = t0 + c0 + j;
       float acc = 0.f;
       for (int dd = 0; dd < D; ++dd) acc = fmaf(sQ[r * D + dd], sK[j * C::KSTR + dd], acc);
       bool ok = (c0 + j < n) && (t <= L - n_c + r / G);
-      if (c0 + j < kSplitTokens) sS[r * kSplitTokens + c0 + j] = ok ? acc * a.scale_log2 : -INFINITY;
+      if (c0 + j < kSimtSplitTokens) sS[r * kSimtSplitTokens + c0 + j] = ok ? acc * a.scale_log2 : -INFINITY;
     }
   }
   __syncthreads();
   // Row maxima and sums over the split.
   for (int r = warp; r < R; r += blockDim.x / 32) {
     float m = -INFINITY;
-    for (int j = lane; j < n; j += 32) m = fmaxf(m, sS[r * kSplitTokens + j]);
+    for (int j = lane; j < n; j += 32) m = fmaxf(m, sS[r * kSimtSplitTokens + j]);
     m = warp_max(m);
     float base = (m == -INFINITY) ? 0.f : m;
     float l = 0.f;
     for (int j = lane; j < n; j += 32) {
-      float p = fast_exp2(sS[r * kSplitTokens + j] - base);
-      sS[r * kSplitTokens + j] = p;
+      float p = fast_exp2(sS[r * kSimtSplitTokens + j] - base);
+      sS[r * kSimtSplitTokens + j] = p;
       l += p;
     }
     l = warp_sum(l);
@@ -407,7 +452,7 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
     const int nref = a.Lpad / kRefGroup;
     for (int e = tid; e < R * n; e += blockDim.x) {
       int r = e / n, j = e % n;
-      a.side_p[((int64_t)unit * R + r) * a.Lpad + t0 + j] = __float2half_rn(sS[r * kSplitTokens + j]);
+      a.side_p[((int64_t)unit * R + r) * a.Lpad + t0 + j] = __float2half_rn(sS[r * kSimtSplitTokens + j]);
     }
     for (int e = tid; e < R * cdiv(n, kRefGroup); e += blockDim.x) {
       int r = e / cdiv(n, kRefGroup), j = e % cdiv(n, kRefGroup);
@@ -421,13 +466,7 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
 #pragma unroll
   for (int k = 0; k < PER; ++k) acc[k] = 0.f;
   for (int c0 = 0; c0 < n; c0 += C::CH) {
-    __syncthreads();
-    for (int e = tid; e < C::CH * D; e += blockDim.x) {
-      int j = e / D, dd = e % D, t = t0 + c0 + j;
-      const float *kr = (c0 + j < n) ? kv_row<D, float>(a.kv, b, 0, g, t, a.status) : nullptr;
-      sK[j * C::KSTR + dd] = kr ? kr[v_off + dd] : 0.f;
-    }
-    __syncthreads();
+    stage(c0, 1);
     const int jn = min(C::CH, n - c0);
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
@@ -435,7 +474,7 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
       if (e < R * D) {
         int r = e / D, dd = e % D;
         float s = acc[k];
-        for (int j = 0; j < jn; ++j) s = fmaf(sS[r * kSplitTokens + c0 + j], sK[j * C::KSTR + dd], s);
+        for (int j = 0; j < jn; ++j) s = fmaf(sS[r * kSimtSplitTokens + c0 + j], sK[j * C::KSTR + dd], s);
         acc[k] = s;
       }
     }
@@ -464,7 +503,8 @@ struct FinalizeArgs {
   const __half *side_p;   // [units][R][Lpad]
   const float *side_m;    // [units][R][Lpad / kRefGroup]
   const int32_t *ucnt;    // block-sparse pass: splits per unit from the union size
-  const int *split_len;   // tensor-core verify: the split length it chose; nullptr = kSplitTokens
+  const int *split_len;   // split length the verify wrote (tensor-core, fp32 paths); nullptr = kSplitTokens
+  int balanced;           // splits cut by tc_split_count (the tensor-core verify), else cdiv(L, split length)
   const uint8_t *phase;   // unified launch: units of draft-phase requests are skipped
   int umax;
   float *out;
