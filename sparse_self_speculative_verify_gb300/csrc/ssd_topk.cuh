@@ -62,8 +62,9 @@ struct TopkScratch {
 };
 
 // Writes the K (0 <= K <= n) largest of the n keys key(0..n-1) to out[0..K) in ascending index order
-// (equal keys toward the lower index) and -1 to out[K..k_max).  Every thread of the NT-thread block
-// calls it; `key` must give every thread the same value for the same index.
+// (equal keys toward the lower index) and -1 to out[K..k_max).  Threads 0 .. NT-1 of the block call
+// it; `key` must give every thread the same value for the same index; `sync` is a barrier over those
+// NT threads (__syncthreads when they are the whole block).
 //
 // Warp w owns the keys [w seg, (w + 1) seg) (seg a multiple of 32); in each round its lanes read 32
 // consecutive keys.  Four MSB-first 8-bit passes find the K-th largest key tau (per-warp shared
@@ -72,8 +73,9 @@ struct TopkScratch {
 // over the warps before it, and a second pass writes the kept indices in index order: every key
 // > tau, and the keys == tau while fewer than the needed number of them lie before (ballots give
 // the ranks within a round).  Fifteen block barriers per row.
-template <int NT, typename KeyFn>
-__device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, int k_max, TopkScratch<NT> &sc) {
+template <int NT, typename KeyFn, typename SyncFn>
+__device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, int k_max, TopkScratch<NT> &sc,
+                                         SyncFn sync) {
   static_assert(NT >= 256 && NT % 32 == 0, "one thread per histogram bin");
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -84,7 +86,7 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
     const int seg = cdiv(cdiv(n, NW), 32) * 32;
     const int lo = min(warp * seg, n), hi = min(lo + seg, n);
     for (int e = tid; e < NW * 256; e += NT) (&sc.hist[0][0])[e] = 0u;
-    __syncthreads();
+    sync();
     uint32_t prefix = 0, mask = 0;
     int rem = K;
     for (int pass = 0; pass < 4; ++pass) {
@@ -93,7 +95,7 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
         const uint32_t k = key(t);
         if ((k & mask) == prefix) atomicAdd(&sc.hist[warp][(k >> shift) & 255u], 1u);
       }
-      __syncthreads();
+      sync();
       if (tid < 256) {
         uint32_t s = 0;
 #pragma unroll
@@ -103,7 +105,7 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
         }
         sc.tot[tid] = s;
       }
-      __syncthreads();
+      sync();
       if (warp == 0) {
         // Lane l owns bins 255-8l .. 248-8l (descending).
         uint32_t c[8];
@@ -134,7 +136,7 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
           }
         }
       }
-      __syncthreads();
+      sync();
       prefix |= sc.digit << shift;
       mask |= 0xffu << shift;
       rem = sc.rem;
@@ -152,7 +154,7 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
       sc.wgt[warp] = cgt;
       sc.weq[warp] = ceq;
     }
-    __syncthreads();
+    sync();
     int pgt = 0, peq = 0;
     for (int w = 0; w < warp; ++w) {
       pgt += sc.wgt[w];
@@ -176,6 +178,11 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
     }
   }
   for (int j = K + tid; j < k_max; j += NT) out[j] = -1;
+}
+
+template <int NT, typename KeyFn>
+__device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, int k_max, TopkScratch<NT> &sc) {
+  topk_row<NT>(key, n, K, out, k_max, sc, [] { __syncthreads(); });
 }
 
 }  // namespace ssd

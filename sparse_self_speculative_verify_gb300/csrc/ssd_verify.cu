@@ -9,9 +9,8 @@
 // the verify positions.  SpecSA post, "overlap-aware grouped query execution": candidates whose
 // sparse layouts overlap run together so shared KV blocks are loaded once.  SparDA §2: fine scores
 // are max-pooled onto the coarser selection grid.
+#include "ssd_finalize.cuh"
 #include "ssd_host.h"
-#include "ssd_topk.cuh"
-#include "ssd_verify_tile.cuh"
 
 namespace ssd {
 
@@ -59,89 +58,6 @@ __global__ void __launch_bounds__(128) verify_simt_kernel(VerifyArgs a) {
 // covers the merge, the references and the first rows.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ int fin_rows_per_cta(int D) { return kFinThreads / (D / 4); }
-
-constexpr int kFinAhead = 5;  // side-value rows loaded per batch
-
-__device__ __forceinline__ void fin_fma_row(const uint4 &raw, float c, float (&acc)[8]) {
-  const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 pf = __half22float2(h2[k]);
-    acc[2 * k] = fmaf(pf.x, c, acc[2 * k]);
-    acc[2 * k + 1] = fmaf(pf.y, c, acc[2 * k + 1]);
-  }
-}
-
-// LSE merge of one unit's split log-sum-exps, per row r < R: sLn[r] (natural log) and sL2[r]
-// (log2) of the row's total.  Warp w of an NW-warp block takes rows w, w + NW, ...; lane j holds
-// split j (a loop when ns > 32).  Every split value is loaded before the first reduction.
-template <int NW>
-__device__ __forceinline__ void fin_lse_merge(const FinalizeArgs &f, int64_t pbase, int ns, float *sLn, float *sL2) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int Q = (kMaxRows + NW - 1) / NW;
-  float v[Q];
-#pragma unroll
-  for (int q = 0; q < Q; ++q) {
-    const int r = warp + NW * q;
-    v[q] = (r < f.R && lane < ns) ? f.lse_parts[pbase + (int64_t)lane * f.R + r] : -INFINITY;
-  }
-#pragma unroll
-  for (int q = 0; q < Q; ++q) {
-    const int r = warp + NW * q;
-    if (r >= f.R) break;
-    float M = v[q];
-    for (int j = lane + 32; j < ns; j += 32) M = fmaxf(M, f.lse_parts[pbase + (int64_t)j * f.R + r]);
-    M = warp_max(M);
-    float sum = 0.f;
-    if (M != -INFINITY) {
-      sum = lane < ns ? fast_exp2((v[q] - M) * kLog2e) : 0.f;
-      for (int j = lane + 32; j < ns; j += 32) sum += fast_exp2((f.lse_parts[pbase + (int64_t)j * f.R + r] - M) * kLog2e);
-    }
-    sum = warp_sum(sum);
-    if (lane == 0) {
-      const float ln = (M == -INFINITY) ? -INFINITY : M + __logf(sum);
-      sLn[r] = ln;
-      sL2[r] = ln * kLog2e;
-    }
-  }
-}
-
-// Split combine of one unit (request b, KV head g): rows r = r0, r0 + rstep, ... each get
-// out = sum_j 2^((lse_j - LSE) log2 e) o_j over the splits and lse = LSE; thread q4 of the D / 4
-// threads of a row takes one float4 of d.
-__device__ __forceinline__ void fin_combine_rows(const FinalizeArgs &f, int64_t pbase, int ns, const float *sLn,
-                                                 int b, int g, int r0, int rstep, int q4) {
-  const int D = f.D;
-  for (int r = r0; r < f.R; r += rstep) {
-    const float ln = sLn[r];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ln != -INFINITY) {
-      const float *lp = f.lse_parts + pbase + r;
-      const float4 *op = reinterpret_cast<const float4 *>(f.o_parts + (pbase + r) * D) + q4;
-      const int64_t ostep = (int64_t)f.R * D / 4;
-#pragma unroll 4
-      for (int j = 0; j < ns; ++j) {
-        float w = fast_exp2((lp[(int64_t)j * f.R] - ln) * kLog2e);
-        float4 o = op[j * ostep];
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
-      }
-    }
-    const int i = r / f.G, hl = r % f.G;
-    const int64_t row = ((int64_t)b * f.n_c + i) * f.h_q + g * f.G + hl;
-    reinterpret_cast<float4 *>(f.out + row * D)[q4] = acc;
-    if (q4 == 0 && f.lse) f.lse[row] = ln;
-  }
-}
-
-// Splits of unit u's request of length L, as the verify pass cut them.
-__device__ __forceinline__ int fin_splits(const FinalizeArgs &f, int u, int L) {
-  return f.ucnt       ? block_splits(min(max(f.ucnt[u], 0), f.umax))
-         : f.balanced ? tc_split_count(L, *f.split_len)
-                      : verify_splits(L, f.split_len ? *f.split_len : kSplitTokens);
-}
 
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, int n_tok) {
   __shared__ float sLn[kMaxRows];
@@ -320,46 +236,7 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
     fin_combine_rows(f, pbase, ns, sLn, b, g, tid / tpr, kCsThreads / tpr, tid % tpr);
     return;
   }
-  // crit[t] = sum_r e[r][t] * 2^(m_ref[r][t / 16] - LSE2_r), eight consecutive tokens per thread,
-  // rows in batches of kFinAhead (every load of a batch in flight together).
-  const int nref = f.Lpad / kRefGroup;
-  const __half *sp = f.side_p + rbase * f.Lpad;
-  for (int t0 = tid * 8; t0 < L; t0 += kCsThreads * 8) {
-    const int grp = t0 / kRefGroup;
-    float crit[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) crit[k] = 0.f;
-    for (int r0 = 0; r0 < f.R; r0 += kFinAhead) {
-      uint4 raw[kFinAhead];
-      float m[kFinAhead];
-#pragma unroll
-      for (int k = 0; k < kFinAhead; ++k) {
-        const int r = r0 + k;
-        raw[k] = r < f.R ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad + t0)) : make_uint4(0, 0, 0, 0);
-        m[k] = r < f.R ? __ldg(f.side_m + (rbase + r) * nref + grp) : 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < kFinAhead; ++k) {
-        const int r = r0 + k;
-        if (r < f.R) {
-          const float l2 = sL2[r];
-          fin_fma_row(raw[k], (l2 == -INFINITY) ? 0.f : fast_exp2(m[k] - l2), crit);
-        }
-      }
-    }
-    float *dst = f.scores + (int64_t)u * f.scores_stride + t0;
-    if (t0 + 8 <= L && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
-      reinterpret_cast<float4 *>(dst)[0] = make_float4(crit[0], crit[1], crit[2], crit[3]);
-      reinterpret_cast<float4 *>(dst)[1] = make_float4(crit[4], crit[5], crit[6], crit[7]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (t0 + k < L) dst[k] = crit[k];
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (t0 + k < L) s_keys[t0 + k] = score_key(crit[k]);
-  }
+  fin_unit_scores<kCsThreads>(f, u, L, sL2, s_keys, tid);
   pdl_trigger();
   __syncthreads();
   int K = f.ks[b];
@@ -549,14 +426,6 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
   const bool tc = verify_tc_supported(kv, lay.R);
   const bool simt = !tc && kv->dtype != SSD_DTYPE_BF16;
   a.split_out = reinterpret_cast<int *>(ws + lay.split_off);
-  if (tc) {
-    rc = launch_verify_tc(kv, a, st);
-  }
-  else if (kv->dtype == SSD_DTYPE_BF16)
-    rc = dispatch_mma<false>(kv->d, rows_per_tile(lay.R), a, grid, st);
-  else
-    rc = kv->d == 128 ? launch_simt<128>(a, grid, st) : launch_simt<64>(a, grid, st);
-  if (rc) return rc;
 
   FinalizeArgs f{};
   f.seq_lens = kv->seq_lens;
@@ -587,6 +456,15 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
   f.sel_kmax = k_max;
   f.sel_ctr = reinterpret_cast<unsigned *>(ws + lay.ctr_off) + 2;  // slots 0-1: the tensor-core kernel
   f.status = status;
+
+  if (tc) {
+    rc = launch_verify_tc(kv, a, st);
+  }
+  else if (kv->dtype == SSD_DTYPE_BF16)
+    rc = dispatch_mma<false>(kv->d, rows_per_tile(lay.R), a, grid, st);
+  else
+    rc = kv->d == 128 ? launch_simt<128>(a, grid, st) : launch_simt<64>(a, grid, st);
+  if (rc) return rc;
   if (ks && kv->max_seq_len <= kCsSmemRow) {
     const int smem = kv->max_seq_len * 4;
     if ((rc = ensure_smem<crit_select_kernel>(smem))) return rc;

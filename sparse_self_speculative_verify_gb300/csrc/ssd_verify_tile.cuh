@@ -22,6 +22,35 @@
 
 namespace ssd {
 
+// Arguments of the finalize pass (LSE merge of a unit's splits, output combine, criticality).
+struct FinalizeArgs {
+  const int32_t *seq_lens;
+  int max_seq_len, h_kv, h_q, n_c, G, R, D;
+  int S_max, Lpad;
+  const float *o_parts;
+  const float *lse_parts;
+  const __half *side_p;   // [units][R][Lpad]
+  const float *side_m;    // [units][R][Lpad / kRefGroup]
+  const int32_t *ucnt;    // block-sparse pass: splits per unit from the union size
+  const int *split_len;   // split length the verify wrote (tensor-core, fp32 paths); nullptr = kSplitTokens
+  int balanced;           // splits cut by tc_split_count (the tensor-core verify), else cdiv(L, split length)
+  const uint8_t *phase;   // unified launch: units of draft-phase requests are skipped
+  int umax;
+  float *out;
+  float *lse;
+  float *scores;
+  int64_t scores_stride;
+  float *bscores;
+  int64_t bstride;
+  // Fused Top-K (nullptr ks: none): row u of the scores keeps K = min(ks[b], L_b) tokens, written
+  // as the select pass writes them (sel_idx [units][sel_kmax], sel_cnt [units]).
+  const int32_t *ks;
+  int32_t *sel_idx;
+  int32_t *sel_cnt;
+  int sel_kmax;
+  unsigned *sel_ctr;  // [units] arrivals of a unit's token blocks, in the counter area
+  unsigned *status;
+};
 struct VerifyArgs {
   KVView kv;
   const void *q;  // [B][n_c][h_q][D]
@@ -493,35 +522,6 @@ __device__ __forceinline__ void verify_item_simt(const VerifyArgs &a, int unit, 
   }
 }
 
-// Arguments of the finalize pass (LSE merge of a unit's splits, output combine, criticality).
-struct FinalizeArgs {
-  const int32_t *seq_lens;
-  int max_seq_len, h_kv, h_q, n_c, G, R, D;
-  int S_max, Lpad;
-  const float *o_parts;
-  const float *lse_parts;
-  const __half *side_p;   // [units][R][Lpad]
-  const float *side_m;    // [units][R][Lpad / kRefGroup]
-  const int32_t *ucnt;    // block-sparse pass: splits per unit from the union size
-  const int *split_len;   // split length the verify wrote (tensor-core, fp32 paths); nullptr = kSplitTokens
-  int balanced;           // splits cut by tc_split_count (the tensor-core verify), else cdiv(L, split length)
-  const uint8_t *phase;   // unified launch: units of draft-phase requests are skipped
-  int umax;
-  float *out;
-  float *lse;
-  float *scores;
-  int64_t scores_stride;
-  float *bscores;
-  int64_t bstride;
-  // Fused Top-K (nullptr ks: none): row u of the scores keeps K = min(ks[b], L_b) tokens, written
-  // as the select pass writes them (sel_idx [units][sel_kmax], sel_cnt [units]).
-  const int32_t *ks;
-  int32_t *sel_idx;
-  int32_t *sel_cnt;
-  int sel_kmax;
-  unsigned *sel_ctr;  // [units] arrivals of a unit's token blocks, in the counter area
-  unsigned *status;
-};
 constexpr int kFinThreads = 256;
 constexpr int kFinTok = kFinThreads * 8;  // eight consecutive tokens per thread
 constexpr int kFinGroups = kFinTok / kRefGroup;
