@@ -32,9 +32,25 @@ int draft_checks(const ssd_paged_kv *kv, int h_q, const void *q, const int32_t *
                  const float *out, const char *who, bool need_idx = true);
 int launch_draft_any(int dtype, int D, const DraftArgs &a, dim3 grid, cudaStream_t st);
 bool verify_tc_supported(const ssd_paged_kv *kv, int R);
-int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st);
+int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st, int max_blocks = 0);
 
 constexpr int kUniMaxBatch = 512;
+
+// SMs left to the draft work while the tensor-core verify runs (ssd_unified_attn): the draft's share
+// of the SM time, estimated from the shape alone (the phases and lists are on the device).  A round
+// has n_cand - 1 draft phases per verify phase, each reading about k_max / max_seq_len of what a
+// verify reads; the draft's SM time is taken as r = 0.9 (n_cand - 1) k_max / max_seq_len of the
+// verify's, the factor fitted on the Qwen3-14B mixed batch (64 requests, k = 4, lists of 5 %): 16,
+// 24, 33, 40 and 56 draft SMs gave 279.9, 278.6, 283.0, 283.3 and 312.2 us per call, none 290.2.
+// Both kinds of work are bound by each SM's latency, not by the HBM, so the split moves SM time
+// rather than creating it: the gain is the verify's tail and the draft's launch, both filled.
+static int unified_draft_sms(const ssd_paged_kv *kv, int n_cand, int k_max) {
+  if (kv->max_seq_len <= 0) return 0;
+  const double r = 0.9 * (n_cand - 1) * (double)k_max / kv->max_seq_len;
+  const int sm = sm_count();
+  int n = (int)(sm * r / (1.0 + r) + 0.5);
+  return n < 0 ? 0 : (n > sm / 2 ? sm / 2 : n);
+}
 
 template <int D, int NRT, int GMAX>
 struct UniCfg {
@@ -248,10 +264,13 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
     va.phase = phase;
     va.sched = reinterpret_cast<int *>(ws);
     va.split_out = reinterpret_cast<int *>(ws + lay.split_off);
-    if ((rc = launch_verify_tc(kv, va, st))) return rc;
-    // The draft work needs nothing the verify writes: launched right behind it, it starts as soon
-    // as the verify has handed out its last item and fills the SMs its finishing blocks leave; the
-    // finalize follows once both are done.
+    // The draft work needs nothing the verify writes, so the two run side by side: the verify takes
+    // all SMs but unified_draft_sms() of them and lets the next kernel launch at once; the draft
+    // kernel, launched right behind it without waiting for it, runs on the SMs left free and on those
+    // the verify's finishing blocks leave.  The finalize follows once both are done.
+    const int dsm = pdl_enabled() ? unified_draft_sms(kv, n_cand, k_max) : 0;
+    va.early_trigger = dsm > 0;
+    if ((rc = launch_verify_tc(kv, va, st, sm_count() - dsm))) return rc;
     da.defer_wait = 1;
     if ((rc = launch_draft_any(kv->dtype, kv->d, da, dim3(lay.C_max, lay.units), st))) return rc;
   } else {

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *o_parts, cons
 // Host side.
 // ------------------------------------------------------------------------------------------------
 bool verify_tc_supported(const ssd_paged_kv *kv, int R);
-int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st);
+int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st, int max_blocks = 0);
 
 static int rows_per_tile(int R) { return R <= 16 ? 1 : (R <= 32 ? 2 : 4); }
 

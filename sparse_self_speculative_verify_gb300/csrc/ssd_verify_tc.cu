@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // Set-up that reads nothing an earlier kernel writes runs before the wait for the previous grid:
   // barriers, tensor memory, descriptor prefetch, zeroed query buffers.
+  if (a.early_trigger) pdl_trigger();
   if (tid == 0) {
     *s.abort = 0;
     for (int k = 0; k < 8; ++k) s.vote[k] = 0;
@@ -863,7 +864,7 @@ static int launch_tc(const CUtensorMap &map, const CUtensorMap &qmap, const Veri
                 box_rows);
 }
 
-int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st) {
+int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t st, int max_blocks) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const int box_rows = kv->page_size < kTcTile ? kv->page_size : kTcTile;
@@ -888,7 +889,8 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled (queries) failed (%d)", (int)r);
   const int64_t items_max = (int64_t)kv->batch * kv->h_kv * a.S_max;
-  const int grid = (int)(items_max < sm_count() ? items_max : sm_count());
+  int grid = (int)(items_max < sm_count() ? items_max : sm_count());
+  if (max_blocks > 0 && grid > max_blocks) grid = max_blocks;
   if (grid <= 0) return SSD_OK;
   if (!a.sched) return fail(SSD_ERR_INVALID_ARG, "verify_tc_kernel: no item counter");
   return a.R <= 32 ? launch_tc<32>(map, qmap, a, box_rows, grid, st) : launch_tc<64>(map, qmap, a, box_rows, grid, st);

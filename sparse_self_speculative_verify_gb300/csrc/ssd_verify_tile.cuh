@@ -72,6 +72,7 @@ struct VerifyArgs {
                // path); zero at launch, and the last block to finish returns both to zero
   int *split_out;  // tensor-core and fp32 paths: receives the split length used (read by the finalize)
   const uint8_t *phase;  // tensor-core path: nullptr, or only requests with phase[b] == 1 get items
+  int early_trigger;     // tensor-core path: let the next kernel launch at once (see ssd_unified.cu)
 };
 
 template <int D, int NRT>
