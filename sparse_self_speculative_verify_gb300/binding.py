@@ -58,8 +58,9 @@ def library_path() -> str:
     return _build.lib_path()
 
 
-def load(path: Optional[str] = None):
-    """Load libssd.so (no build step).  Raises LibraryNotBuilt when it is missing."""
+def load(path: Optional[str] = None, as_default: bool = False):
+    """Load libssd.so (no build step).  Raises LibraryNotBuilt when it is missing.  A library given
+    by ``path`` serves the calls of this module only with ``as_default``."""
     global _LIB
     with _LOCK:
         if _LIB is not None and path is None:
@@ -99,7 +100,7 @@ def load(path: Optional[str] = None):
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = res
-        if path is None:
+        if path is None or as_default:
             _LIB = L
         return L
 

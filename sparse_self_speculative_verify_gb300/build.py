@@ -23,12 +23,12 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibilit
               "-Xptxas", "-warn-spills"]
 
 
-def build_dir() -> str:
-    return os.path.join(PKG, "_build", platform.machine())
+def build_dir(variant: str = "") -> str:
+    return os.path.join(PKG, "_build", platform.machine() + (f"-{variant}" if variant else ""))
 
 
-def lib_path() -> str:
-    return os.path.join(build_dir(), "libssd.so")
+def lib_path(variant: str = "") -> str:
+    return os.path.join(build_dir(variant), "libssd.so")
 
 
 def _nvcc() -> str:
@@ -47,20 +47,26 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    out = lib_path()
+def up_to_date(variant: str = "") -> bool:
+    out = lib_path(variant)
     if not os.path.exists(out):
         return False
     t = os.path.getmtime(out)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libssd.so; returns its path."""
-    if not force and up_to_date():
-        return lib_path()
+# Diagnostic builds, each in a directory of its own beside the library proper (never loaded by the
+# product path): "trace" records the tensor-core verify's per-block timeline (trace_verify.py).
+VARIANT_FLAGS = {"trace": ["-DSSD_VERIFY_TRACE"]}
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, variant: str = "") -> str:
+    """Compile and link libssd.so (or a diagnostic variant of it); returns its path."""
+    if not force and up_to_date(variant):
+        return lib_path(variant)
     nvcc = _nvcc()
-    odir = os.path.join(build_dir(), "obj")
+    odir = os.path.join(build_dir(variant), "obj")
+    extra_flags = list(extra_flags or []) + VARIANT_FLAGS.get(variant, [])
     os.makedirs(odir, exist_ok=True)
     flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC] + list(extra_flags or [])
 
@@ -76,13 +82,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = lib_path() + ".tmp"
+    tmp = lib_path(variant) + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, lib_path())
-    return lib_path()
+    os.replace(tmp, lib_path(variant))
+    return lib_path(variant)
 
 
 if __name__ == "__main__":

@@ -40,6 +40,29 @@
 namespace ssd {
 using namespace sm100;
 
+// Timeline record of the diagnostic build (-DSSD_VERIFY_TRACE, trace_verify.py): per block,
+// [0] global timer at entry, [1] SM cycles to the end of the prologue, [2] global timer at exit,
+// [3] items done, then per item j < kTraceItems: [4 + 3j] cycles when the producer starts the item's
+// tiles, [5 + 3j] item number << 32 | tiles, [6 + 3j] cycles when the first softmax warp has
+// written its outputs; [127] cycles at exit.  Cycles count from the block's entry.
+#ifdef SSD_VERIFY_TRACE
+constexpr int kTraceBlocks = 256, kTraceSlots = 128, kTraceItems = 40;
+__device__ unsigned long long g_verify_trace[kTraceBlocks * kTraceSlots];
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define SSD_TRACE(stmt) \
+  do {                  \
+    stmt;               \
+  } while (0)
+#else
+#define SSD_TRACE(stmt) \
+  do {                  \
+  } while (0)
+#endif
+
 constexpr int kTcTile = kTcTileTokens;
 constexpr int kTcWarps = 10;
 constexpr int kTcThreads = kTcWarps * 32;
@@ -203,6 +226,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.kv.batch, h_kv = a.kv.h_kv;
+#ifdef SSD_VERIFY_TRACE
+  unsigned long long *TR = g_verify_trace + (blockIdx.x % kTraceBlocks) * kTraceSlots;
+  const long long clk0 = clock64();
+  if (tid == 0) {
+    TR[0] = global_ns();
+    TR[3] = 0;
+  }
+#endif
 
   TcSmem s;
   {
@@ -339,6 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const uint32_t tm = *s.tmem;
   const int n_items = s.pre[B];
+  SSD_TRACE(if (tid == 0) TR[1] = clock64() - clk0);
   const int G = a.G, R = a.R, n_c = a.n_c;
 
   if (warp == kTcProducerWarp) {
@@ -405,6 +437,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_4d(qb + C::Q_PANEL, &qmap, 0, 1, it.g * G, it.b * n_c, qf);
       }
       __syncwarp();
+      SSD_TRACE(if (lane == 0 && jl < kTraceItems) {
+        TR[4 + 3 * jl] = clock64() - clk0;
+        TR[5 + 3 * jl] = ((unsigned long long)cur << 32) | (unsigned)it.ntiles;
+      });
       for (int k = 0; ok && k < it.ntiles; ++k) {
         const int tb = it.t0 + k * kTcTile, tend = min(tb + kTcTile, it.t1);
         // Lane j < boxes_per_tile handles box j of this tile.
@@ -809,6 +845,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; j < CW; ++j)
           if (c0 + j < R) a.o_parts[(prow + c0 + j) * 128 + tw] = o[j] * inv[j];
       }
+      SSD_TRACE(if (tid == 0 && jl < kTraceItems) {
+        TR[6 + 3 * jl] = clock64() - clk0;
+        TR[3] = jl + 1;
+      });
       item = next_item;
       it = nx;
     }
@@ -817,6 +857,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  SSD_TRACE(if (tid == 0) {
+    TR[2] = global_ns();
+    TR[127] = clock64() - clk0;
+  });
   if (tid == 0 && *reinterpret_cast<volatile int *>(s.abort)) atomicOr(a.status, (unsigned)SSD_FAULT_TIMEOUT);
   if (warp == kTcMmaWarp) tmem_dealloc(tm, C::TMEM_COLS);
   // The last block to finish returns the item counter and the finished count to zero for the next
@@ -897,3 +941,12 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
 }
 
 }  // namespace ssd
+
+#ifdef SSD_VERIFY_TRACE
+// Diagnostic build only: copies the timeline record (kTraceBlocks x kTraceSlots 64-bit words) of the
+// last verify launch to host memory.
+extern "C" int ssd_verify_trace(void *dst, size_t bytes) {
+  if (!dst || bytes > sizeof(ssd::g_verify_trace)) return SSD_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(dst, ssd::g_verify_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+#endif
