@@ -543,9 +543,13 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
 
 // ---- Reading the row pack, bf16: one block per (request, KV head) ------------------------------
 // The unit's packed chunks stream through kPackStages stages of (K tile, V tile), each tile one bulk
-// copy of the chunk's rows, while the block runs an online softmax over the chunks: a running max
-// and sum per head, the output accumulators rescaled whenever the max grows.  Nothing leaves the
-// block before the normalised output, so there are no chunk partials and no merge.
+// copy of the chunk's rows.  Each warp owns 16 rows of every chunk and runs its own online softmax
+// over them: its logits stay in registers, its running max and sum per head and its P V accumulators
+// are its own, and its probabilities go from the logits' accumulator layout to the P V operand
+// layout by an 8x8 register transpose (movmatrix), so a chunk needs no exchange between warps and
+// one block barrier (the stage's release).  The four warps' states are merged once at the end (LSE
+// merge in a fixed order), and nothing leaves the block before the normalised output: no chunk
+// partials, no merge pass.
 constexpr int kPackStages = 2;
 
 template <int D, int GMAX>
@@ -553,23 +557,29 @@ struct DraftPackCfg {
   static constexpr int ROWB = D * 2;
   static constexpr int CPR = ROWB / 16;
   static constexpr int TILE = kDraftChunk * ROWB;
-  // [stages][K tile, V tile]; logits [GMAX][chunk] fp32; P as bf16 high + residual parts
-  // [2][GMAX][chunk]; running max, running sum and rescale factor [GMAX] each; an mbarrier per stage.
-  static constexpr int OFF_S = kPackStages * 2 * TILE;
-  static constexpr int OFF_P = OFF_S + GMAX * kDraftChunk * 4;
-  static constexpr int OFF_M = OFF_P + 2 * GMAX * kDraftChunk * 2;
-  static constexpr int OFF_BAR = OFF_M + 3 * GMAX * 4;
-  static constexpr int OFF_ABORT = OFF_BAR + kPackStages * 8;  // set by a thread whose wait expired
-  static constexpr int SMEM = OFF_ABORT + 8;
+  // [stages][K tile, V tile] (after the last chunk: the warps' scaled outputs [4][GMAX8][D] fp32 for
+  // the merge); the warps' running max and sum [4][GMAX8] each; an mbarrier per stage.
+  static constexpr int GMAX8 = (GMAX + 7) / 8 * 8;
+  static constexpr int OFF_M = kPackStages * 2 * TILE;
+  static constexpr int OFF_BAR = OFF_M + 2 * 4 * GMAX8 * 4;
+  static constexpr int SMEM = OFF_BAR + kPackStages * 8;
   static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+  static_assert(4 * GMAX8 * D * 4 <= kPackStages * 2 * TILE, "merge area must fit in the stages");
 };
+
+// 8x8 transpose of 16-bit elements held one 32-bit pair per thread in the mma fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t v) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
 
 template <int D, int GMAX>
 __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, char *smem) {
   using C = DraftPackCfg<D, GMAX>;
   using MM = DraftMma<D, GMAX>;
-  constexpr int NT8 = MM::NT8, MTW = MM::MTW;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  constexpr int NT8 = MM::NT8, KS = MM::KS, MT = D / 16, GMAX8 = C::GMAX8;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h_kv = a.kv.h_kv, b = unit / h_kv, g = unit % h_kv, G = a.G;
   const char *pu = a.pack + (int64_t)unit * a.C_max * (2 * C::TILE);
   // Before the wait for the previous kernel: the unit's first packed chunk (K and V tiles, whole)
@@ -583,11 +593,8 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     n_all = n_all < 0 ? 0 : a.k_max;
   }
   const int nch = cdiv(n_all, kDraftChunk);  // 0 for an empty list
-  float *sS = reinterpret_cast<float *>(smem + C::OFF_S);
-  uint16_t *sP = reinterpret_cast<uint16_t *>(smem + C::OFF_P);
-  float *sM = reinterpret_cast<float *>(smem + C::OFF_M), *sL = sM + GMAX, *sA = sL + GMAX;
+  float *sWM = reinterpret_cast<float *>(smem + C::OFF_M), *sWL = sWM + 4 * GMAX8;  // [warp][head]
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
-  volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::OFF_ABORT);
 
   // Chunk c's n rows of K and of V into stage c % kPackStages (thread 0).
   auto issue = [&](int c) {
@@ -601,112 +608,177 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     sm100::bulk_load(dst + C::TILE, src + C::TILE, bytes, bar);
   };
   if (tid == 0) {
-    *s_abort = 0;
     for (int st = 0; st < kPackStages; ++st) sm100::mbar_init(bar0 + 8 * st, 1);
     sm100::mbar_init_fence();
     sm100::fence_proxy_async_smem();
     for (int c = 0; c < min(nch, kPackStages); ++c) issue(c);
   }
-  if (tid < GMAX) {
-    sM[tid] = -INFINITY;
-    sL[tid] = 0.f;
-  }
 
-  uint32_t qb[NT8][MM::KS][2];
+  uint32_t qb[NT8][KS][2];
   draft_q_frags<D, GMAX>(a.q, (int64_t)b * a.h_q + g * G, G, lane, qb);
-  float o[MTW][NT8][4];
+  // This warp's state.  Thread (lane) holds heads 8 nt + 2 (lane & 3) + {0, 1}: their running max
+  // and sum (log2 domain), and the P V accumulators o[mi][nt][e] at d = 16 mi + lane / 4 (+ 8 for
+  // e >= 2), head 8 nt + 2 (lane & 3) + (e & 1).
+  float o[MT][NT8][4];
+  float m_run[NT8][2], l_run[NT8][2];
 #pragma unroll
-  for (int mi = 0; mi < MTW; ++mi)
+  for (int nt = 0; nt < NT8; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT8; ++nt) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
-  __syncthreads();  // barriers initialised, running statistics set
+    for (int mi = 0; mi < MT; ++mi) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
+  }
+  const int r0 = warp * 16;  // this warp's rows of every chunk
+  int c_abort = -1;          // the chunk whose tiles did not land in time
+  __syncthreads();           // barriers initialised
 
   for (int c = 0; c < nch; ++c) {
     const int st = c % kPackStages;
     const char *sKt = smem + st * (2 * C::TILE);
     char *sVt = smem + st * (2 * C::TILE) + C::TILE;
     const int n = min(kDraftChunk, n_all - c * kDraftChunk);
-    if (!draft_tile_wait(bar0 + 8 * st, (uint32_t)((c / kPackStages) & 1), a.status)) *s_abort = 1;
-    // V rows past n (last chunk) are zeroed: their P is 0, but 0 times a stale non-finite value is
-    // not.  K rows past n need nothing: their logits are replaced by -inf.
-    for (int e = n * C::CPR + tid; e < kDraftChunk * C::CPR; e += blockDim.x)
-      reinterpret_cast<uint4 *>(sVt)[e] = make_uint4(0u, 0u, 0u, 0u);
-
-    draft_logits_mma<D, GMAX>(sKt, qb, sS, n, a.scale_log2, G, warp, lane);
-    __syncthreads();
-    if (*s_abort) {
-      // A tile did not land in time (SSD_FAULT_TIMEOUT is set): no more copies are issued and the
-      // unit's outputs are not written.  Thread 0 waits, bounded, for the copies still in flight
-      // into this block's shared memory before the block exits; a copy that outlives that second
-      // wait too means the device is unusable for this context.
-      if (tid == 0)
-        for (int cc = c; cc < min(c + kPackStages, nch); ++cc)
-          draft_tile_wait(bar0 + 8 * (cc % kPackStages), (uint32_t)((cc / kPackStages) & 1), a.status);
-      return;
-    }
-
-    // Online softmax, one warp per head: the new running max, this chunk's P against it (bf16 high
-    // + residual parts), the factor that rescales the earlier chunks, and the running sum.
-    for (int h = warp; h < G; h += nwarps) {
-      const float v0 = sS[h * kDraftChunk + lane], v1 = sS[h * kDraftChunk + lane + 32];
-      const float m_old = sM[h];
-      const float m_new = fmaxf(m_old, warp_max(fmaxf(v0, v1)));
-      const float base = (m_new == -INFINITY) ? 0.f : m_new;
-      const float p0 = fast_exp2(v0 - base), p1 = fast_exp2(v1 - base);
-      draft_store_p<GMAX>(sP, h, lane, p0, p1);
-      const float l = warp_sum(p0 + p1);
-      if (lane == 0) {
-        const float alpha = fast_exp2(m_old - base);  // 0 before the first chunk (m_old = -inf)
-        sM[h] = m_new;
-        sL[h] = sL[h] * alpha + l;
-        sA[h] = alpha;
+    // A thread whose wait expires still runs the chunk (on whatever the stage holds); the block
+    // decides together at the stage barrier.
+    const bool landed = draft_tile_wait(bar0 + 8 * st, (uint32_t)((c / kPackStages) & 1), a.status);
+    // V rows past n (last chunk) of this warp's rows are zeroed: their P is 0, but 0 times a stale
+    // non-finite value is not.  K rows past n need nothing: their logits are replaced by -inf.
+    if (r0 + 16 > n)
+      for (int e = lane; e < 16 * C::CPR; e += 32)
+        if (r0 + e / C::CPR >= n)
+          reinterpret_cast<uint4 *>(sVt + (r0 + e / C::CPR) * C::ROWB)[e % C::CPR] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    // Logits of rows r0 .. r0 + 15: S^T = K Q^T (A fragments by ldmatrix from the swizzled K tile).
+    float sacc[NT8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    {
+      const int ar = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int ch = 2 * ks + (lane >> 4);
+        uint32_t af[4];
+        ldsm_x4(smem_u32(sKt + ar * MM::ROWB + swz_chunk(ar, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) mma_bf16(sacc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
       }
     }
-    __syncthreads();
-
-    // O^T = alpha O^T + V^T P^T (the accumulators rescaled per head, then this chunk added).
-    {
-      float al[NT8][2];
+    // Online softmax over the warp's 16 rows, per head: rows lane / 4 and lane / 4 + 8 are this
+    // thread's; the 8 lanes with the same lane & 3 hold the other rows of the same heads.
+    const bool in0 = r0 + (lane >> 2) < n, in1 = r0 + (lane >> 2) + 8 < n;
+    uint32_t pb_hi[NT8][2], pb_lo[NT8][2];
 #pragma unroll
-      for (int nt = 0; nt < NT8; ++nt)
+    for (int nt = 0; nt < NT8; ++nt) {
+      float p[4], alpha[2];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int h = nt * 8 + (lane & 3) * 2 + k;
-          al[nt][k] = h < G ? sA[h] : 1.f;
-        }
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const float v0 = in0 ? sacc[nt][e2] * a.scale_log2 : -INFINITY;
+        const float v1 = in1 ? sacc[nt][2 + e2] * a.scale_log2 : -INFINITY;
+        float mx = fmaxf(v0, v1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float m_new = fmaxf(m_run[nt][e2], mx);
+        const float base = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[e2] = fast_exp2(m_run[nt][e2] - base);  // 0 before the first rows (m_run = -inf)
+        p[e2] = fast_exp2(v0 - base);
+        p[2 + e2] = fast_exp2(v1 - base);
+        float ps = p[e2] + p[2 + e2];
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        l_run[nt][e2] = l_run[nt][e2] * alpha[e2] + ps;
+        m_run[nt][e2] = m_new;
+      }
 #pragma unroll
-      for (int mi = 0; mi < MTW; ++mi)
+      for (int mi = 0; mi < MT; ++mi)
 #pragma unroll
-        for (int nt = 0; nt < NT8; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[mi][nt][e] *= al[nt][e & 1];
-      draft_pv_mma<D, GMAX>(sVt, sP, G, warp, lane, o);
+        for (int e = 0; e < 4; ++e) o[mi][nt][e] *= alpha[e & 1];
+      // P as bf16 high part + residual, rows lane / 4 (pair 0) and + 8 (pair 1), heads in pairs;
+      // transposed 8x8 blocks are the P^T operand: k = row 2 (lane & 3) + {0, 1}, n = head lane / 4.
+      uint32_t h0, l0, h1, l1;
+      split_bf16(p[0], p[1], h0, l0);
+      split_bf16(p[2], p[3], h1, l1);
+      pb_hi[nt][0] = movmatrix_t(h0);
+      pb_hi[nt][1] = movmatrix_t(h1);
+      pb_lo[nt][0] = movmatrix_t(l0);
+      pb_lo[nt][1] = movmatrix_t(l1);
     }
-    __syncthreads();  // the stage's tiles, the logits and P are free
+    // O^T += V^T P^T over the warp's rows (A fragments by transposing ldmatrix from the V tile).
+    {
+      const int tr = r0 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi) {
+        const int ch = 2 * mi + ((lane >> 3) & 1);
+        uint32_t af[4];
+        ldsm_x4_t(smem_u32(sVt + tr * MM::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) {
+          mma_bf16(o[mi][nt], af, pb_hi[nt][0], pb_hi[nt][1]);
+          mma_bf16(o[mi][nt], af, pb_lo[nt][0], pb_lo[nt][1]);
+        }
+      }
+    }
+    // Every warp is done with the stage (and the block learns whether a wait expired).
+    if (__syncthreads_or(!landed)) {
+      c_abort = c;
+      break;
+    }
     if (tid == 0 && c + kPackStages < nch) {
       sm100::fence_proxy_async_smem();  // the stage was read by every thread before the barrier
       issue(c + kPackStages);
     }
   }
-
+  if (c_abort >= 0) {
+    // A tile did not land in time (SSD_FAULT_TIMEOUT is set): no more copies are issued and the
+    // unit's outputs are not written.  Thread 0 waits, bounded, for the copies still in flight into
+    // this block's shared memory before the block exits; a copy that outlives that second wait too
+    // means the device is unusable for this context.
+    if (tid == 0)
+      for (int cc = c_abort; cc < min(c_abort + kPackStages, nch); ++cc)
+        draft_tile_wait(bar0 + 8 * (cc % kPackStages), (uint32_t)((cc / kPackStages) & 1), a.status);
+    return;
+  }
+  __syncthreads();
   pdl_trigger();
-  // Normalised output: c0, c1 at d = 16 mt + lane / 4, heads 8 nt + 2 (lane & 3) + {0, 1}; c2, c3 at d + 8.
+
+  // Merge the four warps (fixed order): M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O = sum_w 2^(m_w - M) O_w.
+  float *sO = reinterpret_cast<float *>(smem);  // [4][GMAX8][D], over the stages
+  if (lane < 4) {
 #pragma unroll
-  for (int mi = 0; mi < MTW; ++mi)
+    for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        sWM[warp * GMAX8 + nt * 8 + 2 * lane + e2] = m_run[nt][e2];
+        sWL[warp * GMAX8 + nt * 8 + 2 * lane + e2] = l_run[nt][e2];
+      }
+  }
+#pragma unroll
+  for (int mi = 0; mi < MT; ++mi)
 #pragma unroll
     for (int nt = 0; nt < NT8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int dd = (warp * MTW + mi) * 16 + (lane >> 2) + (e >> 1) * 8;
-        const int h = nt * 8 + (lane & 3) * 2 + (e & 1);
-        if (h < G) {
-          const float l = sL[h];
-          a.out[((int64_t)b * a.h_q + g * G + h) * D + dd] = l > 0.f ? o[mi][nt][e] / l : 0.f;
-        }
+        const int dd = mi * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
+        sO[(warp * GMAX8 + h) * D + dd] = o[mi][nt][e];
       }
-  if (a.lse && tid < G) {
-    const float l = sL[tid];
-    a.lse[(int64_t)b * a.h_q + g * G + tid] = l > 0.f ? (sM[tid] + __log2f(l)) * kLn2 : -INFINITY;
+  __syncthreads();
+  for (int e = tid; e < G * D; e += blockDim.x) {
+    const int h = e / D, dd = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, sWM[w * GMAX8 + h]);
+    float L = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = fast_exp2(sWM[w * GMAX8 + h] - M);  // 0 for a warp that saw no rows
+        L = fmaf(f, sWL[w * GMAX8 + h], L);
+        acc = fmaf(f, sO[(w * GMAX8 + h) * D + dd], acc);
+      }
+    }
+    const int64_t row = (int64_t)b * a.h_q + g * G + h;
+    a.out[row * D + dd] = L > 0.f ? acc / L : 0.f;
+    if (dd == 0 && a.lse) a.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
   }
 }
 
