@@ -541,31 +541,12 @@ __device__ __forceinline__ void draft_item(const DraftArgs &a, int unit, int chu
   if (tid == 0) a.counters[unit] = 0u;
 }
 
-// ---- Reading the row pack, bf16: one block per (request, KV head) ------------------------------
-// The unit's packed chunks stream through kPackStages stages of (K tile, V tile), each tile one bulk
-// copy of the chunk's rows.  Each warp owns 16 rows of every chunk and runs its own online softmax
-// over them: its logits stay in registers, its running max and sum per head and its P V accumulators
-// are its own, and its probabilities go from the logits' accumulator layout to the P V operand
-// layout by an 8x8 register transpose (movmatrix), so a chunk needs no exchange between warps and
-// one block barrier (the stage's release).  The four warps' states are merged once at the end (LSE
-// merge in a fixed order), and nothing leaves the block before the normalised output: no chunk
-// partials, no merge pass.
-constexpr int kPackStages = 2;
-
-template <int D, int GMAX>
-struct DraftPackCfg {
-  static constexpr int ROWB = D * 2;
-  static constexpr int CPR = ROWB / 16;
-  static constexpr int TILE = kDraftChunk * ROWB;
-  // [stages][K tile, V tile] (after the last chunk: the warps' scaled outputs [4][GMAX8][D] fp32 for
-  // the merge); the warps' running max and sum [4][GMAX8] each; an mbarrier per stage.
-  static constexpr int GMAX8 = (GMAX + 7) / 8 * 8;
-  static constexpr int OFF_M = kPackStages * 2 * TILE;
-  static constexpr int OFF_BAR = OFF_M + 2 * 4 * GMAX8 * 4;
-  static constexpr int SMEM = OFF_BAR + kPackStages * 8;
-  static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
-  static_assert(4 * GMAX8 * D * 4 <= kPackStages * 2 * TILE, "merge area must fit in the stages");
-};
+// ---- Per-warp online softmax over a unit's chunks (bf16, tensor cores) ---------------------------
+// One block of four warps per (request, KV head).  Each warp owns 16 rows of every chunk and runs its
+// own online softmax over them: its logits stay in registers, its running max and sum per head and
+// its P V accumulators are its own, and its probabilities go from the logits' accumulator layout to
+// the P V operand layout by an 8x8 register transpose (movmatrix), so a chunk needs no exchange
+// between warps.  The four warps' states are merged once at the end (LSE merge in a fixed order).
 
 // 8x8 transpose of 16-bit elements held one 32-bit pair per thread in the mma fragment layout.
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t v) {
@@ -574,84 +555,37 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t v) {
   return r;
 }
 
+// A warp's state.  Thread (lane) holds heads 8 nt + 2 (lane & 3) + {0, 1}: their running max and sum
+// (log2 domain), and the P V accumulators o[mi][nt][e] at d = 16 mi + lane / 4 (+ 8 for e >= 2),
+// head 8 nt + 2 (lane & 3) + (e & 1); qb holds the queries as B fragments.
 template <int D, int GMAX>
-__device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, char *smem) {
-  using C = DraftPackCfg<D, GMAX>;
-  using MM = DraftMma<D, GMAX>;
-  constexpr int NT8 = MM::NT8, KS = MM::KS, MT = D / 16, GMAX8 = C::GMAX8;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h_kv = a.kv.h_kv, b = unit / h_kv, g = unit % h_kv, G = a.G;
-  const char *pu = a.pack + (int64_t)unit * a.C_max * (2 * C::TILE);
-  // Before the wait for the previous kernel: the unit's first packed chunk (K and V tiles, whole)
-  // into L2, so the first bulk copies after the wait find it there.  A prefetch only warms L2, which
-  // every write also passes through, so it may overlap an earlier kernel still writing the pack.
-  if (tid == 0) sm100::prefetch_l2(pu, 2 * C::TILE);
-  pdl_wait();
-  int n_all = a.cnt[unit];
-  if (n_all < 0 || n_all > a.k_max) {
-    if (tid == 0) atomicOr(a.status, (unsigned)SSD_FAULT_KMAX);
-    n_all = n_all < 0 ? 0 : a.k_max;
-  }
-  const int nch = cdiv(n_all, kDraftChunk);  // 0 for an empty list
-  float *sWM = reinterpret_cast<float *>(smem + C::OFF_M), *sWL = sWM + 4 * GMAX8;  // [warp][head]
-  const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
-
-  // Chunk c's n rows of K and of V into stage c % kPackStages (thread 0).
-  auto issue = [&](int c) {
-    const int st = c % kPackStages;
-    const uint32_t bytes = (uint32_t)(min(kDraftChunk, n_all - c * kDraftChunk) * C::ROWB);
-    const uint32_t bar = bar0 + 8 * st;
-    const char *src = pu + (int64_t)c * (2 * C::TILE);
-    const uint32_t dst = smem_u32(smem + st * (2 * C::TILE));
-    sm100::mbar_arrive_expect_tx(bar, 2 * bytes);
-    sm100::bulk_load(dst, src, bytes, bar);
-    sm100::bulk_load(dst + C::TILE, src + C::TILE, bytes, bar);
-  };
-  if (tid == 0) {
-    for (int st = 0; st < kPackStages; ++st) sm100::mbar_init(bar0 + 8 * st, 1);
-    sm100::mbar_init_fence();
-    sm100::fence_proxy_async_smem();
-    for (int c = 0; c < min(nch, kPackStages); ++c) issue(c);
-  }
-
+struct DraftWarp {
+  static constexpr int NT8 = DraftMma<D, GMAX>::NT8, KS = DraftMma<D, GMAX>::KS, MT = D / 16;
+  static constexpr int GMAX8 = NT8 * 8;
   uint32_t qb[NT8][KS][2];
-  draft_q_frags<D, GMAX>(a.q, (int64_t)b * a.h_q + g * G, G, lane, qb);
-  // This warp's state.  Thread (lane) holds heads 8 nt + 2 (lane & 3) + {0, 1}: their running max
-  // and sum (log2 domain), and the P V accumulators o[mi][nt][e] at d = 16 mi + lane / 4 (+ 8 for
-  // e >= 2), head 8 nt + 2 (lane & 3) + (e & 1).
   float o[MT][NT8][4];
   float m_run[NT8][2], l_run[NT8][2];
-#pragma unroll
-  for (int nt = 0; nt < NT8; ++nt) {
-    m_run[nt][0] = m_run[nt][1] = -INFINITY;
-    l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-    for (int mi = 0; mi < MT; ++mi) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
-  }
-  const int r0 = warp * 16;  // this warp's rows of every chunk
-  int c_abort = -1;          // the chunk whose tiles did not land in time
-  __syncthreads();           // barriers initialised
 
-  for (int c = 0; c < nch; ++c) {
-    const int st = c % kPackStages;
-    const char *sKt = smem + st * (2 * C::TILE);
-    char *sVt = smem + st * (2 * C::TILE) + C::TILE;
-    const int n = min(kDraftChunk, n_all - c * kDraftChunk);
-    // A thread whose wait expires still runs the chunk (on whatever the stage holds); the block
-    // decides together at the stage barrier.
-    const bool landed = draft_tile_wait(bar0 + 8 * st, (uint32_t)((c / kPackStages) & 1), a.status);
-    // V rows past n (last chunk) of this warp's rows are zeroed: their P is 0, but 0 times a stale
-    // non-finite value is not.  K rows past n need nothing: their logits are replaced by -inf.
-    if (r0 + 16 > n)
-      for (int e = lane; e < 16 * C::CPR; e += 32)
-        if (r0 + e / C::CPR >= n)
-          reinterpret_cast<uint4 *>(sVt + (r0 + e / C::CPR) * C::ROWB)[e % C::CPR] = make_uint4(0u, 0u, 0u, 0u);
-    __syncwarp();
-    // Logits of rows r0 .. r0 + 15: S^T = K Q^T (A fragments by ldmatrix from the swizzled K tile).
+  __device__ __forceinline__ void init(const DraftArgs &a, int b, int g, int lane) {
+    draft_q_frags<D, GMAX>(a.q, (int64_t)b * a.h_q + g * a.G, a.G, lane, qb);
+#pragma unroll
+    for (int nt = 0; nt < NT8; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int mi = 0; mi < MT; ++mi) o[mi][nt][0] = o[mi][nt][1] = o[mi][nt][2] = o[mi][nt][3] = 0.f;
+    }
+  }
+
+  // Rows r0 .. r0 + 15 of a chunk of n rows (swizzled K and V tiles; V rows at or past n must hold
+  // finite values, their P is 0): logits, online softmax, P V.
+  __device__ __forceinline__ void chunk(const char *sKt, const char *sVt, int n, int r0, float scale_log2, int lane) {
+    using MM = DraftMma<D, GMAX>;
     float sacc[NT8][4];
 #pragma unroll
     for (int nt = 0; nt < NT8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
     {
+      // S^T = K Q^T (A fragments by ldmatrix from the swizzled K tile).
       const int ar = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
@@ -662,8 +596,8 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
         for (int nt = 0; nt < NT8; ++nt) mma_bf16(sacc[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
       }
     }
-    // Online softmax over the warp's 16 rows, per head: rows lane / 4 and lane / 4 + 8 are this
-    // thread's; the 8 lanes with the same lane & 3 hold the other rows of the same heads.
+    // Online softmax, per head: rows lane / 4 and lane / 4 + 8 are this thread's; the 8 lanes with
+    // the same lane & 3 hold the warp's other rows of the same heads.
     const bool in0 = r0 + (lane >> 2) < n, in1 = r0 + (lane >> 2) + 8 < n;
     uint32_t pb_hi[NT8][2], pb_lo[NT8][2];
 #pragma unroll
@@ -671,8 +605,8 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
       float p[4], alpha[2];
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
-        const float v0 = in0 ? sacc[nt][e2] * a.scale_log2 : -INFINITY;
-        const float v1 = in1 ? sacc[nt][2 + e2] * a.scale_log2 : -INFINITY;
+        const float v0 = in0 ? sacc[nt][e2] * scale_log2 : -INFINITY;
+        const float v1 = in1 ? sacc[nt][2 + e2] * scale_log2 : -INFINITY;
         float mx = fmaxf(v0, v1);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -704,20 +638,146 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
       pb_lo[nt][1] = movmatrix_t(l1);
     }
     // O^T += V^T P^T over the warp's rows (A fragments by transposing ldmatrix from the V tile).
-    {
-      const int tr = r0 + (lane & 7) + ((lane >> 4) << 3);
+    const int tr = r0 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
-      for (int mi = 0; mi < MT; ++mi) {
-        const int ch = 2 * mi + ((lane >> 3) & 1);
-        uint32_t af[4];
-        ldsm_x4_t(smem_u32(sVt + tr * MM::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
+    for (int mi = 0; mi < MT; ++mi) {
+      const int ch = 2 * mi + ((lane >> 3) & 1);
+      uint32_t af[4];
+      ldsm_x4_t(smem_u32(sVt + tr * MM::ROWB + swz_chunk(tr, ch) * 16), af[0], af[1], af[2], af[3]);
 #pragma unroll
-        for (int nt = 0; nt < NT8; ++nt) {
-          mma_bf16(o[mi][nt], af, pb_hi[nt][0], pb_hi[nt][1]);
-          mma_bf16(o[mi][nt], af, pb_lo[nt][0], pb_lo[nt][1]);
-        }
+      for (int nt = 0; nt < NT8; ++nt) {
+        mma_bf16(o[mi][nt], af, pb_hi[nt][0], pb_hi[nt][1]);
+        mma_bf16(o[mi][nt], af, pb_lo[nt][0], pb_lo[nt][1]);
       }
     }
+  }
+
+  // Merges the four warps (fixed order: M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O = sum_w
+  // 2^(m_w - M) O_w) and writes the normalised output and LSE of request b's heads g G ..  Called by
+  // the whole block after its last use of the scratch areas: sO [4][GMAX8][D] fp32, sWM and sWL
+  // [4][GMAX8].
+  __device__ __forceinline__ void merge_store(const DraftArgs &a, int b, int g, float *sO, float *sWM, float *sWL) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, G = a.G;
+    if (lane < 4) {
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          sWM[warp * GMAX8 + nt * 8 + 2 * lane + e2] = m_run[nt][e2];
+          sWL[warp * GMAX8 + nt * 8 + 2 * lane + e2] = l_run[nt][e2];
+        }
+    }
+#pragma unroll
+    for (int mi = 0; mi < MT; ++mi)
+#pragma unroll
+      for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int dd = mi * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
+          sO[(warp * GMAX8 + h) * D + dd] = o[mi][nt][e];
+        }
+    __syncthreads();
+    for (int e = tid; e < G * D; e += blockDim.x) {
+      const int h = e / D, dd = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, sWM[w * GMAX8 + h]);
+      float L = 0.f, acc = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float f = fast_exp2(sWM[w * GMAX8 + h] - M);  // 0 for a warp that saw no rows
+          L = fmaf(f, sWL[w * GMAX8 + h], L);
+          acc = fmaf(f, sO[(w * GMAX8 + h) * D + dd], acc);
+        }
+      }
+      const int64_t row = (int64_t)b * a.h_q + g * G + h;
+      a.out[row * D + dd] = L > 0.f ? acc / L : 0.f;
+      if (dd == 0 && a.lse) a.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    }
+  }
+};
+
+// ---- Reading the row pack, bf16 ---------------------------------------------------------------
+// The unit's packed chunks stream through kPackStages stages of (K tile, V tile), each tile one bulk
+// copy of the chunk's rows, completed on an mbarrier; one block barrier per chunk (the stage's
+// release).  Nothing leaves the block before the normalised output: no chunk partials, no merge pass.
+constexpr int kPackStages = 2;
+
+template <int D, int GMAX>
+struct DraftPackCfg {
+  static constexpr int ROWB = D * 2;
+  static constexpr int CPR = ROWB / 16;
+  static constexpr int TILE = kDraftChunk * ROWB;
+  // [stages][K tile, V tile] (after the last chunk: the warps' outputs for the merge); the warps'
+  // running max and sum [4][GMAX8] each; an mbarrier per stage.
+  static constexpr int GMAX8 = DraftWarp<D, GMAX>::GMAX8;
+  static constexpr int OFF_M = kPackStages * 2 * TILE;
+  static constexpr int OFF_BAR = OFF_M + 2 * 4 * GMAX8 * 4;
+  static constexpr int SMEM = OFF_BAR + kPackStages * 8;
+  static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+  static_assert(4 * GMAX8 * D * 4 <= kPackStages * 2 * TILE, "merge area must fit in the stages");
+};
+
+template <int D, int GMAX>
+__device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, char *smem) {
+  using C = DraftPackCfg<D, GMAX>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h_kv = a.kv.h_kv, b = unit / h_kv, g = unit % h_kv;
+  const char *pu = a.pack + (int64_t)unit * a.C_max * (2 * C::TILE);
+  // Before the wait for the previous kernel: the unit's first packed chunk (K and V tiles, whole)
+  // into L2, so the first bulk copies after the wait find it there.  A prefetch only warms L2, which
+  // every write also passes through, so it may overlap an earlier kernel still writing the pack.
+  if (tid == 0) sm100::prefetch_l2(pu, 2 * C::TILE);
+  pdl_wait();
+  int n_all = a.cnt[unit];
+  if (n_all < 0 || n_all > a.k_max) {
+    if (tid == 0) atomicOr(a.status, (unsigned)SSD_FAULT_KMAX);
+    n_all = n_all < 0 ? 0 : a.k_max;
+  }
+  const int nch = cdiv(n_all, kDraftChunk);  // 0 for an empty list
+  float *sWM = reinterpret_cast<float *>(smem + C::OFF_M), *sWL = sWM + 4 * C::GMAX8;
+  const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
+
+  // Chunk c's n rows of K and of V into stage c % kPackStages (thread 0).
+  auto issue = [&](int c) {
+    const int st = c % kPackStages;
+    const uint32_t bytes = (uint32_t)(min(kDraftChunk, n_all - c * kDraftChunk) * C::ROWB);
+    const uint32_t bar = bar0 + 8 * st;
+    const char *src = pu + (int64_t)c * (2 * C::TILE);
+    const uint32_t dst = smem_u32(smem + st * (2 * C::TILE));
+    sm100::mbar_arrive_expect_tx(bar, 2 * bytes);
+    sm100::bulk_load(dst, src, bytes, bar);
+    sm100::bulk_load(dst + C::TILE, src + C::TILE, bytes, bar);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < kPackStages; ++st) sm100::mbar_init(bar0 + 8 * st, 1);
+    sm100::mbar_init_fence();
+    sm100::fence_proxy_async_smem();
+    for (int c = 0; c < min(nch, kPackStages); ++c) issue(c);
+  }
+  DraftWarp<D, GMAX> W;
+  W.init(a, b, g, lane);
+  const int r0 = warp * 16;  // this warp's rows of every chunk
+  int c_abort = -1;          // the chunk whose tiles did not land in time
+  __syncthreads();           // barriers initialised
+
+  for (int c = 0; c < nch; ++c) {
+    const int st = c % kPackStages;
+    const char *sKt = smem + st * (2 * C::TILE);
+    char *sVt = smem + st * (2 * C::TILE) + C::TILE;
+    const int n = min(kDraftChunk, n_all - c * kDraftChunk);
+    // A thread whose wait expires still runs the chunk (on whatever the stage holds); the block
+    // decides together at the stage barrier.
+    const bool landed = draft_tile_wait(bar0 + 8 * st, (uint32_t)((c / kPackStages) & 1), a.status);
+    // V rows past n (last chunk) of this warp's rows are zeroed: their P is 0, but 0 times a stale
+    // non-finite value is not.  K rows past n need nothing: their logits are replaced by -inf.
+    if (r0 + 16 > n)
+      for (int e = lane; e < 16 * C::CPR; e += 32)
+        if (r0 + e / C::CPR >= n)
+          reinterpret_cast<uint4 *>(sVt + (r0 + e / C::CPR) * C::ROWB)[e % C::CPR] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    W.chunk(sKt, sVt, n, r0, a.scale_log2, lane);
     // Every warp is done with the stage (and the block learns whether a wait expired).
     if (__syncthreads_or(!landed)) {
       c_abort = c;
@@ -738,48 +798,8 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
         draft_tile_wait(bar0 + 8 * (cc % kPackStages), (uint32_t)((cc / kPackStages) & 1), a.status);
     return;
   }
-  __syncthreads();
   pdl_trigger();
-
-  // Merge the four warps (fixed order): M = max_w m_w, L = sum_w 2^(m_w - M) l_w, O = sum_w 2^(m_w - M) O_w.
-  float *sO = reinterpret_cast<float *>(smem);  // [4][GMAX8][D], over the stages
-  if (lane < 4) {
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        sWM[warp * GMAX8 + nt * 8 + 2 * lane + e2] = m_run[nt][e2];
-        sWL[warp * GMAX8 + nt * 8 + 2 * lane + e2] = l_run[nt][e2];
-      }
-  }
-#pragma unroll
-  for (int mi = 0; mi < MT; ++mi)
-#pragma unroll
-    for (int nt = 0; nt < NT8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int dd = mi * 16 + (lane >> 2) + (e >> 1) * 8, h = nt * 8 + (lane & 3) * 2 + (e & 1);
-        sO[(warp * GMAX8 + h) * D + dd] = o[mi][nt][e];
-      }
-  __syncthreads();
-  for (int e = tid; e < G * D; e += blockDim.x) {
-    const int h = e / D, dd = e % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, sWM[w * GMAX8 + h]);
-    float L = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float f = fast_exp2(sWM[w * GMAX8 + h] - M);  // 0 for a warp that saw no rows
-        L = fmaf(f, sWL[w * GMAX8 + h], L);
-        acc = fmaf(f, sO[(w * GMAX8 + h) * D + dd], acc);
-      }
-    }
-    const int64_t row = (int64_t)b * a.h_q + g * G + h;
-    a.out[row * D + dd] = L > 0.f ? acc / L : 0.f;
-    if (dd == 0 && a.lse) a.lse[row] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
-  }
+  W.merge_store(a, b, g, reinterpret_cast<float *>(smem), sWM, sWL);
 }
 
 }  // namespace ssd

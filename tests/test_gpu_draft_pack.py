@@ -1,8 +1,9 @@
 """Sparse draft attention through the row pack.  The writing call equals the plain draft bit for bit
 (the same kernel, which also stores its tiles).  The reading calls are checked against the oracle
-and against plain drafts of their own queries: bit-exact for fp32 caches (the plain kernel reading
-the pack); within 1e-4 relative for bf16 caches, whose reader runs one block per (request, KV head) with an
-online softmax over the chunks instead of per-chunk partials merged by log-sum-exp."""
+and against plain drafts of their own queries: bit-exact for fp32 caches (the plain chunked kernel
+reading the pack); within 1e-4 relative for bf16 caches, whose reader runs one block per (request,
+KV head) with a per-warp online softmax over the chunks instead of per-chunk partials merged by
+log-sum-exp."""
 
 import numpy as np
 import pytest
