@@ -161,10 +161,11 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-# Sources of the dominant call (ssd_verify_attn: tensor-core verify kernel + finalize); a change to
-# any of them makes the committed DRAM-traffic capture stale.
-VERIFY_SOURCES = ("ssd_common.cuh", "ssd_host.h", "ssd_sm100.cuh", "ssd_topk.cuh", "ssd_verify.cu",
-                  "ssd_verify_tc.cu", "ssd_verify_tile.cuh")
+# Sources of the dominant calls (ssd_verify_select: tensor-core verify kernel + criticality/Top-K
+# pass; ssd_verify_attn: verify kernel + finalize); a change to any of them makes the committed
+# DRAM-traffic capture stale.
+VERIFY_SOURCES = ("ssd_common.cuh", "ssd_finalize.cuh", "ssd_host.h", "ssd_sm100.cuh", "ssd_topk.cuh",
+                  "ssd_verify.cu", "ssd_verify_tc.cu", "ssd_verify_tile.cuh")
 
 
 def kernel_source_sha() -> str:
@@ -176,16 +177,20 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(launch_units: int):
-    """DRAM bytes per verify launch from the committed ncu summary, scaled to this launch's units;
-    None when the kernels changed since the capture."""
+def profiled_traffic(launch_units: int, call: str = "ssd_verify_select"):
+    """DRAM bytes of one `call` (the sum over its kernels in the committed ncu summary), scaled from
+    the capture's units to this launch's; None when the kernels changed since the capture or the
+    capture lacks one of the call's kernels."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
         d = json.load(f)
     if d.get("kernel_src_sha") != kernel_source_sha():
         return None
-    return d["dram_bytes_per_unit"] * launch_units
+    kernels = d.get("calls", {}).get(call)
+    if not kernels or any(k not in d.get("kernel_dram_bytes", {}) for k in kernels):
+        return None
+    return sum(d["kernel_dram_bytes"][k] for k in kernels) / d["units"] * launch_units
 
 
 # --------------------------------------------------------------------------------------------
@@ -405,7 +410,8 @@ def run_ours(args, spec, rank, world, local):
     units = sum(lens) * spec.h_kv
     roofline = {"bound": "hbm", "kernel": v_kernel,
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(units) if args.separate_select else None,
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": profiled_traffic(units, "ssd_verify_attn" if args.separate_select else "ssd_verify_select"),
                 "verify_attn_ms": va_ms, "verify_attn_frac": va_bytes / (va_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "peak_source": peaks["source"], "launch_ms": v_ms, "algorithmic_bytes": v_bytes,
                 "timing": f"mean per call over a CUDA graph of {reps} x {args.layers} consecutive calls, layers cycled",
