@@ -48,6 +48,17 @@ using namespace sm100;
 #ifdef SSD_VERIFY_TRACE
 constexpr int kTraceBlocks = 256, kTraceSlots = 128, kTraceItems = 40;
 __device__ unsigned long long g_verify_trace[kTraceBlocks * kTraceSlots];
+// Per block and tile i < kTraceTiles of its sequence, cycles from the block's entry: [0] the producer
+// has a free slot for the tile's K rows, [1] the MMA issuer has issued QK, [2] the first softmax warp
+// has S, [3] it has handed P to the MMA issuer.
+constexpr int kTraceTiles = 256;
+__device__ unsigned g_verify_tile_trace[kTraceBlocks * kTraceTiles * 4];
+// Per block, its first kTraceMasked masked tiles (the first softmax warp's view), cycles from entry:
+// [0] S seen, [1] past the vote barrier, [2] past the reference update, [3] before the P-buffer wait,
+// [4] past it, [5] P handed, [6] tile index i | reference updated << 16 | causal << 17, [7] the
+// logits masked (before the vote).
+constexpr int kTraceMasked = 16;
+__device__ unsigned g_verify_masked_trace[kTraceBlocks * kTraceMasked * 8];
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -228,6 +239,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int B = a.kv.batch, h_kv = a.kv.h_kv;
 #ifdef SSD_VERIFY_TRACE
   unsigned long long *TR = g_verify_trace + (blockIdx.x % kTraceBlocks) * kTraceSlots;
+  unsigned *TT = g_verify_tile_trace + (blockIdx.x % kTraceBlocks) * kTraceTiles * 4;
+  unsigned *TM = g_verify_masked_trace + (blockIdx.x % kTraceBlocks) * kTraceMasked * 8;
+  int n_masked = 0;
+  unsigned tm_s = 0;
   const long long clk0 = clock64();
   if (tid == 0) {
     TR[0] = global_ns();
@@ -467,6 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t use = fill / C::NSLOT;
           const bool eok = lane == 0 ? mbar_wait(bar_addr(s.empty + slot), (use & 1) ^ 1, s.abort) : true;
           if (!__shfl_sync(0xffffffffu, eok, 0)) { ok = false; break; }
+          SSD_TRACE(if (lane == 0 && kv == 0 && (fill >> 1) < kTraceTiles) TT[(fill >> 1) * 4] = (unsigned)(clock64() - clk0));
           const uint32_t fb = bar_addr(s.full + slot);
           for (uint32_t gm = gmask; gm != 0; gm &= gm - 1) {
             const int j = __ffs(gm) - 1;
@@ -609,6 +625,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_bf16_ss(tm + (i & 1) * NP, ad, bd, id_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar_addr(s.s_full + (i & 1)));
+          SSD_TRACE(if (i < kTraceTiles) TT[i * 4 + 1] = (unsigned)(clock64() - clk0));
           mma_commit(bar_addr(s.empty + kslot));
           if (k == it.ntiles - 1) mma_commit(bar_addr(s.q_empty + (jl & 1)));
           if (pend && !issue_pv(pi, pfirst, plast, pj)) { ok = false; break; }
@@ -657,6 +674,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int k = 0; k < it.ntiles; ++k, ++i) {
         const int tb = it.t0 + k * kTcTile, t = tb + tw;
         if (!wwait(bar_addr(s.s_full + (i & 1)), (i >> 1) & 1, s.abort)) goto out;
+        SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * 4 + 2] = (unsigned)(clock64() - clk0));
+        SSD_TRACE(tm_s = (unsigned)(clock64() - clk0));
         tc_fence_after();
         float x[CW];
         tmem_ld_cols<CW>(tm + lane_base + (i & 1) * NP + c0, x);
@@ -679,10 +698,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // d = scale * s - m_ref (log2 domain); -inf where the row cannot see the token.
         float dl[CW];
         if (masked) {
+          // Row r sees token t iff t <= lim_base + floor(r / G), i.e. (t - lim_base) G <= r.
+          const int tg = causal ? (t - lim_base) * G : INT_MIN;
 #pragma unroll
           for (int j = 0; j < CW; ++j) {
             const int r = c0 + j;
-            const bool vis = valid && r < R && (!causal || t <= lim_base + r / G);
+            const bool vis = valid && r < R && tg <= r;
             x[j] = vis ? x[j] * a.scale_log2 : -INFINITY;
             dl[j] = vis ? x[j] - mr[j] : -INFINITY;  // never -inf - (-inf)
           }
@@ -693,10 +714,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool need = false;
 #pragma unroll
         for (int j = 0; j < CW; ++j) need |= dl[j] > kLazy;
+        SSD_TRACE(if (masked && tid == 0 && n_masked < kTraceMasked) TM[n_masked * 8 + 7] = (unsigned)(clock64() - clk0));
         if (__any_sync(0xffffffffu, need) && lane == 0) vote[i & 3] = 1;
         if (!group_sync(grp, s.abort, gph)) goto out;
         const bool any = vote[i & 3] != 0;
         if (tw == 0) vote[(i + 2) & 3] = 0;
+#ifdef SSD_VERIFY_TRACE
+        const bool trace_m = masked && tid == 0 && n_masked < kTraceMasked;
+#endif
+        SSD_TRACE(if (trace_m) {
+          TM[n_masked * 8 + 0] = tm_s;
+          TM[n_masked * 8 + 1] = (unsigned)(clock64() - clk0);
+          TM[n_masked * 8 + 6] = (unsigned)i | (any ? 1u << 16 : 0u) | (causal ? 1u << 17 : 0u);
+        });
         if (any) {
           // New reference: per-row maximum of the tile (over the group's 128 tokens).
           float v[CW];
@@ -747,6 +777,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_before();
           }
         }
+        SSD_TRACE(if (trace_m) TM[n_masked * 8 + 2] = (unsigned)(clock64() - clk0));
         // Probabilities (<= 2^kLazy; exp2(-inf) = 0), running sums, side values, P tile.
 #pragma unroll
         for (int j = 0; j < CW; ++j) {
@@ -769,7 +800,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
+        SSD_TRACE(if (trace_m) TM[n_masked * 8 + 3] = (unsigned)(clock64() - clk0));
         if (!wwait(bar_addr(s.p_empty + (i & 1)), ((i >> 1) & 1) ^ 1, s.abort)) goto out;
+        SSD_TRACE(if (trace_m) TM[n_masked * 8 + 4] = (unsigned)(clock64() - clk0));
         {
           char *prow = sm + C::OFF_P + (i & 1) * C::P_BYTES + tw * 128;
 #pragma unroll
@@ -788,6 +821,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(bar_addr(s.p_full + (i & 1)));
+        SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * 4 + 3] = (unsigned)(clock64() - clk0));
+        SSD_TRACE(if (trace_m) TM[(n_masked++) * 8 + 5] = (unsigned)(clock64() - clk0));
       }
       // The next item (published by the producer once this item's tiles were issued), decoded while
       // the last PV of this item completes.
@@ -948,5 +983,15 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
 extern "C" int ssd_verify_trace(void *dst, size_t bytes) {
   if (!dst || bytes > sizeof(ssd::g_verify_trace)) return SSD_ERR_INVALID_ARG;
   return cudaMemcpyFromSymbol(dst, ssd::g_verify_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+// Diagnostic build only: the masked-tile record (kTraceBlocks x kTraceMasked x 8 32-bit words).
+extern "C" int ssd_verify_masked_trace(void *dst, size_t bytes) {
+  if (!dst || bytes > sizeof(ssd::g_verify_masked_trace)) return SSD_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(dst, ssd::g_verify_masked_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+// Diagnostic build only: the per-tile record (kTraceBlocks x kTraceTiles x 4 32-bit words).
+extern "C" int ssd_verify_tile_trace(void *dst, size_t bytes) {
+  if (!dst || bytes > sizeof(ssd::g_verify_tile_trace)) return SSD_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(dst, ssd::g_verify_tile_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 #endif

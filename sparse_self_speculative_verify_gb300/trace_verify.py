@@ -11,8 +11,10 @@ the library proper for this process, runs ``ssd_verify_attn`` on a seeded worklo
 * per-item cost: the intercept of that fit, the time an item costs beyond its tiles;
 * tail: the spread of the blocks' exit times.
 
-Usage: ``python -m sparse_self_speculative_verify_gb300.trace_verify [workload]`` with workload
-qwen3_8b (default), b128_l8k or qwen3_14b_unified (its verify-phase requests).  Prints a JSON line.
+Usage: ``python -m sparse_self_speculative_verify_gb300.trace_verify [workload] [--dump FILE.npz]``
+with workload qwen3_8b (default), b128_l8k or qwen3_14b_unified (its verify-phase requests).  Prints
+a JSON line; ``--dump`` also saves the raw per-block, per-tile and masked-tile records and the requests'
+lengths.
 """
 
 from __future__ import annotations
@@ -30,10 +32,10 @@ from . import binding as Bd
 from . import build as libbuild
 from . import workloads as W
 
-SLOTS, BLOCKS, ITEMS = 128, 256, 40
+SLOTS, BLOCKS, ITEMS, TILES, MASKED = 128, 256, 40, 256, 16
 
 
-def run(name: str = "qwen3_8b") -> dict:
+def run(name: str = "qwen3_8b", dump: str | None = None) -> dict:
     L = Bd.load(libbuild.build(variant="trace"), as_default=True)
     L.ssd_verify_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
     L.ssd_verify_trace.restype = ctypes.c_int
@@ -58,6 +60,17 @@ def run(name: str = "qwen3_8b") -> dict:
     assert L.ssd_verify_trace(tr.ctypes.data, tr.nbytes) == 0
     nb = torch.cuda.get_device_properties(0).multi_processor_count
     tr = tr.reshape(BLOCKS, SLOTS).astype(np.int64)[:nb]
+    if dump:
+        L.ssd_verify_tile_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+        L.ssd_verify_tile_trace.restype = ctypes.c_int
+        tt = np.zeros(BLOCKS * TILES * 4, np.uint32)
+        assert L.ssd_verify_tile_trace(tt.ctypes.data, tt.nbytes) == 0
+        L.ssd_verify_masked_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+        L.ssd_verify_masked_trace.restype = ctypes.c_int
+        tm = np.zeros(BLOCKS * MASKED * 8, np.uint32)
+        assert L.ssd_verify_masked_trace(tm.ctypes.data, tm.nbytes) == 0
+        np.savez(dump, trace=tr, tiles=tt.reshape(BLOCKS, TILES, 4)[:nb], masked=tm.reshape(BLOCKS, MASKED, 8)[:nb],
+                 seq_lens=kv.seq_lens.cpu().numpy(), h_kv=spec.h_kv, n_cand=spec.n_cand)
     entry, exit_, t0 = tr[:, 0], tr[:, 2], int(tr[:, 0].min())
     span_us = (exit_.max() - t0) / 1e3
     mhz = float(np.median(tr[:, 127] / np.maximum(exit_ - entry, 1) * 1e3))  # cycles per us
@@ -94,4 +107,10 @@ def run(name: str = "qwen3_8b") -> dict:
 
 
 if __name__ == "__main__":
-    print(json.dumps(run(sys.argv[1] if len(sys.argv) > 1 else "qwen3_8b")))
+    args = sys.argv[1:]
+    out = None
+    if "--dump" in args:
+        i = args.index("--dump")
+        out = args[i + 1]
+        del args[i:i + 2]
+    print(json.dumps(run(args[0] if args else "qwen3_8b", out)))
