@@ -15,11 +15,13 @@
 //    the whole warp and each lane issues its own boxes.  Boxes that TMA cannot take whole (a
 //    request's partial last page, a skipped page) are written by the warp with plain copies and
 //    zeros.  The item's query rows arrive by one 4-D TMA box per 64-column panel.
-//  * warp 9 (one thread) issues the MMAs:  S^T[t][r] = K[t][:] . Q[r][:]    (M = 128 tokens, N = NP)
-//                                          O^T[d][n] += V[:][d] . P^T[:][n]  (M = 128 = d,   N = 2 NP)
+//  * one thread of warp 9 issues   S^T[t][r] = K[t][:] . Q[r][:]      (M = 128 tokens, N = NP)
+//    and one thread of warp 10      O^T[d][n] += V[:][d] . P^T[:][n]   (M = 128 = d,   N = 2 NP)
 //    where n < NP carries the bf16 high part of the probabilities and n >= NP the bf16 residual, so
-//    P keeps about 16 bits.  S is double-buffered in TMEM; PV of tile i is issued as soon as its
-//    probabilities are in shared memory, QK of tile i+1 as soon as its K tile has landed.
+//    P keeps about 16 bits.  S is double-buffered in TMEM.  With one issuer per product, QK of a tile
+//    goes out as soon as its K tile has landed and its S buffer is free, and PV as soon as its
+//    probabilities are in shared memory and its V tile has landed: neither waits behind the other,
+//    and V slots return to the producer sooner.
 //  * warps 0-3 and 4-7 are two softmax warpgroups: TMEM lane t is token t of the tile (for S) and
 //    head dimension d = t (for O); warpgroup w owns rows [w*NP/2, (w+1)*NP/2).  The two groups are
 //    independent (rows never mix), so each scheduler runs two softmax warps.
@@ -50,15 +52,21 @@ constexpr int kTraceBlocks = 256, kTraceSlots = 128, kTraceItems = 40;
 __device__ unsigned long long g_verify_trace[kTraceBlocks * kTraceSlots];
 // Per block and tile i < kTraceTiles of its sequence, cycles from the block's entry: [0] the producer
 // has a free slot for the tile's K rows, [1] the MMA issuer has issued QK, [2] the first softmax warp
-// has S, [3] it has handed P to the MMA issuer.
-constexpr int kTraceTiles = 256;
-__device__ unsigned g_verify_tile_trace[kTraceBlocks * kTraceTiles * 4];
+// has S, [3] it has handed P to the MMA issuer, [4] the MMA issuer has seen the K rows land, [5] the
+// V rows, [6] it has issued PV, [7] the producer has a free slot for the V rows, [8] the second
+// softmax group's first warp has S, [9] it has handed P, [10] the MMA issuer has seen all of P,
+// [11] it has seen the S buffer free for the tile's QK.
+constexpr int kTraceTiles = 256, kTT = 12;
+__device__ unsigned g_verify_tile_trace[kTraceBlocks * kTraceTiles * kTT];
 // Per block, its first kTraceMasked masked tiles (the first softmax warp's view), cycles from entry:
 // [0] S seen, [1] past the vote barrier, [2] past the reference update, [3] before the P-buffer wait,
 // [4] past it, [5] P handed, [6] tile index i | reference updated << 16 | causal << 17, [7] the
 // logits masked (before the vote).
 constexpr int kTraceMasked = 16;
 __device__ unsigned g_verify_masked_trace[kTraceBlocks * kTraceMasked * 8];
+// Per block and item j < kTraceItems, the first softmax warp's epilogue, cycles from entry: [0] start
+// (last P handed), [1] the item's O complete, [2] past the row-sum barrier, [3] outputs stored.
+__device__ unsigned g_verify_epi_trace[kTraceBlocks * kTraceItems * 4];
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -75,11 +83,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
 #endif
 
 constexpr int kTcTile = kTcTileTokens;
-constexpr int kTcWarps = 10;
+constexpr int kTcWarps = 11;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcSoftmax = 256;  // two warpgroups
 constexpr int kTcProducerWarp = 8;
-constexpr int kTcMmaWarp = 9;
+constexpr int kTcMmaWarp = 9;   // QK issuer; also allocates the tensor memory
+constexpr int kTcPvWarp = 10;   // PV issuer
 constexpr int kTcMaxBatch = 1024;
 constexpr int kTcItemRing = 8;  // item numbers handed from the producer to the other roles
 // Split length: each item ends with an epilogue and a pipeline refill that cost a few thousand
@@ -96,6 +105,12 @@ struct TcCfg {
   static_assert(NP == 32 || NP == 64, "row padding");
   static constexpr int CW = NP / 2;  // columns (rows of the GQA group) per softmax warpgroup
   static constexpr int NSLOT = NP == 32 ? 5 : 3;
+  // K tiles and V tiles stream through two rings of their own (slots [0, NK) and [NK, NSLOT)), each
+  // consumed in order by one MMA issuer, so a consumer never waits on a slot whose previous fill it
+  // has not itself consumed (the phase parity it waits for cannot alias).  A V tile stays until its
+  // PV, after the softmax, so the V ring is the deeper one.
+  static constexpr int NK = NP == 32 ? 2 : 1;
+  static constexpr int NV = NSLOT - NK;
   static constexpr int P_BYTES = kTcTile * (2 * NP) * 2;
   static constexpr int Q_PANEL = NP * 128;
   static constexpr int Q_BYTES = 2 * Q_PANEL;
@@ -239,8 +254,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int B = a.kv.batch, h_kv = a.kv.h_kv;
 #ifdef SSD_VERIFY_TRACE
   unsigned long long *TR = g_verify_trace + (blockIdx.x % kTraceBlocks) * kTraceSlots;
-  unsigned *TT = g_verify_tile_trace + (blockIdx.x % kTraceBlocks) * kTraceTiles * 4;
+  unsigned *TT = g_verify_tile_trace + (blockIdx.x % kTraceBlocks) * kTraceTiles * kTT;
   unsigned *TM = g_verify_masked_trace + (blockIdx.x % kTraceBlocks) * kTraceMasked * 8;
+  unsigned *TE = g_verify_epi_trace + (blockIdx.x % kTraceBlocks) * kTraceItems * 4;
   int n_masked = 0;
   unsigned tm_s = 0;
   const long long clk0 = clock64();
@@ -302,7 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     mbar_init(bar_addr(s.o_full), 1);
     mbar_init(bar_addr(s.o_empty), kTcSoftmax);
-    mbar_init(bar_addr(s.drain), 1);
+    mbar_init(bar_addr(s.drain), 2);  // one commit by each MMA issuer
     for (int k = 0; k < kTcItemRing; ++k) mbar_init(bar_addr(s.item_full + k), 1);
     mbar_init_fence();
   }
@@ -393,7 +409,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Control flow stays warp-uniform: lane 0 waits, the verdict is broadcast.
     const uint64_t pol = policy_evict_first();
     const int ps = a.kv.page_size, lps = a.kv.log2_ps;
-    uint32_t fill = 0;
+    uint32_t nk = 0, nv = 0;  // K and V tiles issued
     int jl = 0;
     bool ok = true;
     // Page ids of an item's boxes, read by the whole warp one item ahead of use: box j (tokens
@@ -427,8 +443,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (;; ++jl) {
       // Hand the item number to the MMA and softmax roles (n_items ends their loops). The slot
       // written here last held item jl - kTcItemRing, which every role has read by now: this warp
-      // has passed the query-buffer wait of item jl - 1, so the MMA issuer is done with item jl - 3
-      // and the softmax warps (which read the S tile two tiles back) have begun item jl - 5 at least.
+      // has passed the query-buffer wait of item jl - 1, so the QK issuer is done with item jl - 3,
+      // the softmax warps (which read the S tile two tiles back) have begun item jl - 5 at least,
+      // and the PV issuer (at most two tiles behind the softmax) has begun item jl - 7.
       if (lane == 0) {
         s.items[jl % kTcItemRing] = cur;
         mbar_arrive(bar_addr(s.item_full + jl % kTcItemRing));
@@ -477,12 +494,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool good = in_tile && nvalid == box_rows && page_ok;
         const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, good));
         const uint32_t gmask = __ballot_sync(0xffffffffu, in_tile && !good);
-        for (int kv = 0; kv < 2; ++kv, ++fill) {
-          const int slot = fill % C::NSLOT;
-          const uint32_t use = fill / C::NSLOT;
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t f = kv == 0 ? nk : nv;  // this tile's number in the block's sequence
+          const int slot = kv == 0 ? (int)(f % C::NK) : C::NK + (int)(f % C::NV);
+          const uint32_t use = kv == 0 ? f / C::NK : f / C::NV;
           const bool eok = lane == 0 ? mbar_wait(bar_addr(s.empty + slot), (use & 1) ^ 1, s.abort) : true;
           if (!__shfl_sync(0xffffffffu, eok, 0)) { ok = false; break; }
-          SSD_TRACE(if (lane == 0 && kv == 0 && (fill >> 1) < kTraceTiles) TT[(fill >> 1) * 4] = (unsigned)(clock64() - clk0));
+          SSD_TRACE(if (lane == 0 && f < kTraceTiles) TT[f * kTT + (kv ? 7 : 0)] = (unsigned)(clock64() - clk0));
           const uint32_t fb = bar_addr(s.full + slot);
           for (uint32_t gm = gmask; gm != 0; gm &= gm - 1) {
             const int j = __ffs(gm) - 1;
@@ -527,6 +545,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_3d(dst + kPanelBytes, &kvmap, 0, 1, row, fb, pol);
           }
           __syncwarp();
+          if (kv == 0) ++nk; else ++nv;
         }
       }
       const bool drew = nxt < n_items;
@@ -541,81 +560,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("" ::"r"(last_draw));
     if (!ok && lane == 0) {
       // Drain: every fill issued so far must land before the block's shared memory is released.
-      for (uint32_t f = fill > (uint32_t)C::NSLOT ? fill - C::NSLOT : 0; f < fill; ++f) {
-        volatile int never = 0;
-        mbar_wait(bar_addr(s.full + (f % C::NSLOT)), (f / C::NSLOT) & 1, &never);
-      }
+      volatile int never = 0;
+      for (uint32_t f = nk > (uint32_t)C::NK ? nk - C::NK : 0; f < nk; ++f)
+        mbar_wait(bar_addr(s.full + f % C::NK), (f / C::NK) & 1, &never);
+      for (uint32_t f = nv > (uint32_t)C::NV ? nv - C::NV : 0; f < nv; ++f)
+        mbar_wait(bar_addr(s.full + C::NK + f % C::NV), (f / C::NV) & 1, &never);
     }
     __syncwarp();
   } else if (warp == kTcMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- QK issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(128, NP, 0, 0);
-      const uint32_t id_pv = idesc_bf16_f32(128, 2 * NP, 1, 1);
-      const uint32_t o_col = tm + 2 * NP;
       uint32_t i = 0;
-      int jl = 0;
-      bool ok = true;
-      bool pend = false, pfirst = false, plast = false;
-      uint32_t pi = 0;
-      int pj = 0;
-      auto issue_pv = [&](uint32_t ti, bool first, bool last, int tj) -> bool {
-        const uint32_t vf = 2 * ti + 1;
-        const int vslot = vf % C::NSLOT;
-        if (!mbar_wait(bar_addr(s.full + vslot), (vf / C::NSLOT) & 1, s.abort)) return false;
-        if (!mbar_wait(bar_addr(s.p_full + (ti & 1)), (ti >> 1) & 1, s.abort)) return false;
-        if (first && !mbar_wait(bar_addr(s.o_empty), (tj & 1) ^ 1, s.abort)) return false;
-        tc_fence_after();
-        const uint32_t va = sbase + vslot * kSlotBytes;
-        const uint32_t pa = sbase + C::OFF_P + (ti & 1) * C::P_BYTES;
-#pragma unroll
-        for (int st = 0; st < kTcTile / 16; ++st) {
-          const uint64_t ad = smem_desc(va + st * 2048, kPanelBytes, 1024);
-          const uint64_t bd = smem_desc(pa + st * 2048, kPanelBytes, 1024);
-          mma_bf16_ss(o_col, ad, bd, id_pv, (first && st == 0) ? 0u : 1u);
-        }
-        mma_commit(bar_addr(s.empty + vslot));
-        mma_commit(bar_addr(s.p_empty + (ti & 1)));
-        if (last) mma_commit(bar_addr(s.o_full));
-        return true;
-      };
-      // The pending PV (previous tile) is issued as soon as its inputs are ready, even while the
-      // next QK still waits for its K tile (e.g. at an item boundary).
-      // While a PV is pending both conditions are polled without suspending the thread (a
-      // suspended wait may wake late); otherwise the thread sleeps in the barrier.
-      auto pv_ready = [&]() -> bool {
-        const uint32_t vf = 2 * pi + 1;
-        return mbar_test_wait(bar_addr(s.full + vf % C::NSLOT), (vf / C::NSLOT) & 1) &&
-               mbar_test_wait(bar_addr(s.p_full + (pi & 1)), (pi >> 1) & 1) &&
-               (!pfirst || mbar_test_wait(bar_addr(s.o_empty), (pj & 1) ^ 1));
-      };
-      auto wait_or_pv = [&](uint32_t bar, uint32_t parity) -> bool {
-        const long long t0 = clock64();
-        for (;;) {
-          if (pend && pv_ready()) {
-            issue_pv(pi, pfirst, plast, pj);
-            pend = false;
-          }
-          if (pend ? mbar_test_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-          if (*s.abort) return false;
-          if (clock64() - t0 > 2000000000ll) {
-            *s.abort = 1;
-            return false;
-          }
-        }
-      };
-      for (; ok; ++jl) {
-        if (!wait_or_pv(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1)) { ok = false; break; }
+      for (int jl = 0;; ++jl) {
+        if (!mbar_wait(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1, s.abort)) break;
         const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
         if (item >= n_items) break;
         const TcItem it = tc_decode(item, s.pre, s.len, B, a, split_len);
-        if (!wait_or_pv(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1, s.abort)) break;
         const uint32_t qa = sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES;
+        bool ok = true;
         for (int k = 0; k < it.ntiles; ++k, ++i) {
-          const uint32_t kf = 2 * i;
-          const int kslot = kf % C::NSLOT;
-          if (!wait_or_pv(bar_addr(s.full + kslot), (kf / C::NSLOT) & 1)) { ok = false; break; }
-          if (!wait_or_pv(bar_addr(s.s_empty + (i & 1)), ((i >> 1) & 1) ^ 1)) { ok = false; break; }
+          const int kslot = (int)(i % C::NK);
+          if (!mbar_wait(bar_addr(s.full + kslot), (i / C::NK) & 1, s.abort)) { ok = false; break; }
+          SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 4] = (unsigned)(clock64() - clk0));
+          if (!mbar_wait(bar_addr(s.s_empty + (i & 1)), ((i >> 1) & 1) ^ 1, s.abort)) { ok = false; break; }
+          SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 11] = (unsigned)(clock64() - clk0));
           tc_fence_after();
           const uint32_t ka = sbase + kslot * kSlotBytes;
 #pragma unroll
@@ -625,19 +595,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_bf16_ss(tm + (i & 1) * NP, ad, bd, id_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar_addr(s.s_full + (i & 1)));
-          SSD_TRACE(if (i < kTraceTiles) TT[i * 4 + 1] = (unsigned)(clock64() - clk0));
+          SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 1] = (unsigned)(clock64() - clk0));
           mma_commit(bar_addr(s.empty + kslot));
           if (k == it.ntiles - 1) mma_commit(bar_addr(s.q_empty + (jl & 1)));
-          if (pend && !issue_pv(pi, pfirst, plast, pj)) { ok = false; break; }
-          pend = true;
-          pi = i;
-          pfirst = (k == 0);
-          plast = (k == it.ntiles - 1);
-          pj = jl;
         }
+        if (!ok) break;
       }
-      if (ok && pend) issue_pv(pi, pfirst, plast, pj);
       // Drain every MMA this thread issued before the tensor memory is released.
+      mma_commit(bar_addr(s.drain));
+      volatile int never = 0;
+      mbar_wait(bar_addr(s.drain), 0, &never);
+    }
+    __syncwarp();
+  } else if (warp == kTcPvWarp) {
+    // ---------------------------------------------------------------- PV issuer
+    if (lane == 0) {
+      const uint32_t id_pv = idesc_bf16_f32(128, 2 * NP, 1, 1);
+      const uint32_t o_col = tm + 2 * NP;
+      uint32_t i = 0;
+      for (int jl = 0;; ++jl) {
+        if (!mbar_wait(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1, s.abort)) break;
+        const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
+        if (item >= n_items) break;
+        const TcItem it = tc_decode(item, s.pre, s.len, B, a, split_len);
+        bool ok = true;
+        for (int k = 0; k < it.ntiles; ++k, ++i) {
+          const int vslot = C::NK + (int)(i % C::NV);
+          if (!mbar_wait(bar_addr(s.full + vslot), (i / C::NV) & 1, s.abort)) { ok = false; break; }
+          SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 5] = (unsigned)(clock64() - clk0));
+          if (!mbar_wait(bar_addr(s.p_full + (i & 1)), (i >> 1) & 1, s.abort)) { ok = false; break; }
+          SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 10] = (unsigned)(clock64() - clk0));
+          if (k == 0 && !mbar_wait(bar_addr(s.o_empty), (jl & 1) ^ 1, s.abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t va = sbase + vslot * kSlotBytes;
+          const uint32_t pa = sbase + C::OFF_P + (i & 1) * C::P_BYTES;
+#pragma unroll
+          for (int st = 0; st < kTcTile / 16; ++st) {
+            const uint64_t ad = smem_desc(va + st * 2048, kPanelBytes, 1024);
+            const uint64_t bd = smem_desc(pa + st * 2048, kPanelBytes, 1024);
+            mma_bf16_ss(o_col, ad, bd, id_pv, (k == 0 && st == 0) ? 0u : 1u);
+          }
+          SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 6] = (unsigned)(clock64() - clk0));
+          mma_commit(bar_addr(s.empty + vslot));
+          mma_commit(bar_addr(s.p_empty + (i & 1)));
+          if (k == it.ntiles - 1) mma_commit(bar_addr(s.o_full));
+        }
+        if (!ok) break;
+      }
       mma_commit(bar_addr(s.drain));
       volatile int never = 0;
       mbar_wait(bar_addr(s.drain), 0, &never);
@@ -674,7 +678,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int k = 0; k < it.ntiles; ++k, ++i) {
         const int tb = it.t0 + k * kTcTile, t = tb + tw;
         if (!wwait(bar_addr(s.s_full + (i & 1)), (i >> 1) & 1, s.abort)) goto out;
-        SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * 4 + 2] = (unsigned)(clock64() - clk0));
+        SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * kTT + 2] = (unsigned)(clock64() - clk0));
+        SSD_TRACE(if (tid == 128 && i < kTraceTiles) TT[i * kTT + 8] = (unsigned)(clock64() - clk0));
         SSD_TRACE(tm_s = (unsigned)(clock64() - clk0));
         tc_fence_after();
         float x[CW];
@@ -821,7 +826,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(bar_addr(s.p_full + (i & 1)));
-        SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * 4 + 3] = (unsigned)(clock64() - clk0));
+        SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * kTT + 3] = (unsigned)(clock64() - clk0));
+        SSD_TRACE(if (tid == 128 && i < kTraceTiles) TT[i * kTT + 9] = (unsigned)(clock64() - clk0));
         SSD_TRACE(if (trace_m) TM[(n_masked++) * 8 + 5] = (unsigned)(clock64() - clk0));
       }
       // The next item (published by the producer once this item's tiles were issued), decoded while
@@ -833,7 +839,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (next_item < n_items) nx = tc_decode(next_item, s.pre, s.len, B, a, split_len);
       // Epilogue: O (high + residual columns) and the row sums -> the split's normalised partial.
       {
+        SSD_TRACE(if (tid == 0 && jl < kTraceItems) TE[jl * 4] = (unsigned)(clock64() - clk0));
         if (!wwait(bar_addr(s.o_full), jl & 1, s.abort)) goto out;
+        SSD_TRACE(if (tid == 0 && jl < kTraceItems) TE[jl * 4 + 1] = (unsigned)(clock64() - clk0));
         tc_fence_after();
         float o[CW];
         {
@@ -849,6 +857,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float ls = transpose_reduce<CW, false>(lsum);
         if (lane < CW) red[wiw * 32 + lane] = ls;
         if (!group_sync(grp, s.abort, gph)) goto out;
+        SSD_TRACE(if (tid == 0 && jl < kTraceItems) TE[jl * 4 + 2] = (unsigned)(clock64() - clk0));
         // Each thread sums the four warps' partial row sums itself (all shared reads before the global
         // stores): no second group barrier.  The next write to red comes after the next item's first
         // vote barrier.
@@ -881,6 +890,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (c0 + j < R) a.o_parts[(prow + c0 + j) * 128 + tw] = o[j] * inv[j];
       }
       SSD_TRACE(if (tid == 0 && jl < kTraceItems) {
+        TE[jl * 4 + 3] = (unsigned)(clock64() - clk0);
         TR[6 + 3 * jl] = clock64() - clk0;
         TR[3] = jl + 1;
       });
@@ -984,12 +994,17 @@ extern "C" int ssd_verify_trace(void *dst, size_t bytes) {
   if (!dst || bytes > sizeof(ssd::g_verify_trace)) return SSD_ERR_INVALID_ARG;
   return cudaMemcpyFromSymbol(dst, ssd::g_verify_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
+// Diagnostic build only: the epilogue record (kTraceBlocks x kTraceItems x 4 32-bit words).
+extern "C" int ssd_verify_epi_trace(void *dst, size_t bytes) {
+  if (!dst || bytes > sizeof(ssd::g_verify_epi_trace)) return SSD_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(dst, ssd::g_verify_epi_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
 // Diagnostic build only: the masked-tile record (kTraceBlocks x kTraceMasked x 8 32-bit words).
 extern "C" int ssd_verify_masked_trace(void *dst, size_t bytes) {
   if (!dst || bytes > sizeof(ssd::g_verify_masked_trace)) return SSD_ERR_INVALID_ARG;
   return cudaMemcpyFromSymbol(dst, ssd::g_verify_masked_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
-// Diagnostic build only: the per-tile record (kTraceBlocks x kTraceTiles x 4 32-bit words).
+// Diagnostic build only: the per-tile record (kTraceBlocks x kTraceTiles x kTT 32-bit words).
 extern "C" int ssd_verify_tile_trace(void *dst, size_t bytes) {
   if (!dst || bytes > sizeof(ssd::g_verify_tile_trace)) return SSD_ERR_INVALID_ARG;
   return cudaMemcpyFromSymbol(dst, ssd::g_verify_tile_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
