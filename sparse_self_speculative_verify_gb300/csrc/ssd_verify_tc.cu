@@ -12,9 +12,10 @@
 //  * warp 8 draws the items, hands their numbers to the other warps through a small shared ring, and
 //    streams K and V tiles with TMA (one box per page and 64-column panel, 128-byte swizzle, L2
 //    evict-first) into a ring of 32 KB slots; the next item's page ids are read one item ahead by
-//    the whole warp and each lane issues its own boxes.  Boxes that TMA cannot take whole (a
-//    request's partial last page, a skipped page) are written by the warp with plain copies and
-//    zeros.  The item's query rows arrive by one 4-D TMA box per 64-column panel.
+//    the whole warp and each lane issues its own boxes.  Every box goes through TMA: a request's
+//    partial last page whole (the softmax masks its K rows past the end and zeroes its V rows),
+//    boxes past the end or of skipped pages from a row past the pool, which TMA fills with zeros.
+//    The item's query rows arrive by one 4-D TMA box per 64-column panel.
 //  * one thread of warp 9 issues   S^T[t][r] = K[t][:] . Q[r][:]      (M = 128 tokens, N = NP)
 //    and one thread of warp 10      O^T[d][n] += V[:][d] . P^T[:][n]   (M = 128 = d,   N = 2 NP)
 //    where n < NP carries the bf16 high part of the probabilities and n >= NP the bf16 residual, so
@@ -409,6 +410,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Control flow stays warp-uniform: lane 0 waits, the verdict is broadcast.
     const uint64_t pol = policy_evict_first();
     const int ps = a.kv.page_size, lps = a.kv.log2_ps;
+    // First row past the pool (the tensor map's row count; below 2^31, checked on the host).
+    const int oob_row = (int)((int64_t)a.kv.num_pages * 2 * h_kv * ps);
     uint32_t nk = 0, nv = 0;  // K and V tiles issued
     int jl = 0;
     bool ok = true;
@@ -488,12 +491,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool page_ok = pid >= 0 && (int64_t)pid < a.kv.num_pages;
         const int nvalid = in_tile ? max(0, min(box_rows, tend - t)) : 0;  // rows of this box in [tb, tend)
         if (nvalid > 0 && !page_ok) atomicOr(a.status, (unsigned)SSD_FAULT_PAGE);
-        // Full boxes of a good page go through TMA; every other box of the tile (the request's
-        // partial last page, boxes past its end, skipped pages) is written by the warp with plain
-        // copies and zeros, in the same swizzled layout, so the MMA never reads stale or garbage rows.
-        const bool good = in_tile && nvalid == box_rows && page_ok;
-        const uint32_t nbox = __popc(__ballot_sync(0xffffffffu, good));
-        const uint32_t gmask = __ballot_sync(0xffffffffu, in_tile && !good);
+        // Every box of the tile goes through TMA.  A box with rows of the unit on a good page is
+        // loaded whole: in the request's partial last page the rows past its end hold whatever the
+        // page holds, which the softmax masks (K) and zeroes before PV reads them (V).  Boxes past
+        // the end and boxes of skipped pages start at a row past the pool's last, which TMA fills
+        // with zeros (no memory traffic).
+        const int row_kv0 = nvalid > 0 && page_ok ? (int)((((int64_t)pid * 2) * h_kv + it.g) * ps + (t & (ps - 1)))
+                                                   : -1;
         for (int kv = 0; kv < 2; ++kv) {
           const uint32_t f = kv == 0 ? nk : nv;  // this tile's number in the block's sequence
           const int slot = kv == 0 ? (int)(f % C::NK) : C::NK + (int)(f % C::NV);
@@ -502,44 +506,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!__shfl_sync(0xffffffffu, eok, 0)) { ok = false; break; }
           SSD_TRACE(if (lane == 0 && f < kTraceTiles) TT[f * kTT + (kv ? 7 : 0)] = (unsigned)(clock64() - clk0));
           const uint32_t fb = bar_addr(s.full + slot);
-          for (uint32_t gm = gmask; gm != 0; gm &= gm - 1) {
-            const int j = __ffs(gm) - 1;
-            const int nv = __shfl_sync(0xffffffffu, nvalid, j);
-            const bool okp = __shfl_sync(0xffffffffu, page_ok, j);
-            const int32_t pj = __shfl_sync(0xffffffffu, pid, j);
-            const int bt = tb + j * box_rows;
-            const __nv_bfloat16 *pool = reinterpret_cast<const __nv_bfloat16 *>(a.kv.pool);
-            // 16-byte chunks e = row * 16 + chunk; each lane loads eight before it stores any, so
-            // one memory latency covers 256 chunks (16 rows).
-            const int nchunk = box_rows * 16;
-            for (int e0 = 0; e0 < nchunk; e0 += 256) {
-              uint4 v[8];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int e = e0 + u * 32 + lane, rr = e >> 4;
-                v[u] = make_uint4(0, 0, 0, 0);
-                if (e < nchunk && rr < nv && okp) {
-                  const int64_t row = (((int64_t)pj * 2 + kv) * h_kv + it.g) * ps + ((bt + rr) & (ps - 1));
-                  v[u] = __ldg(reinterpret_cast<const uint4 *>(pool + row * 128) + (e & 15));
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int e = e0 + u * 32 + lane;
-                if (e < nchunk) {
-                  const int rr = e >> 4, ch = e & 15, panel = ch >> 3, c = ch & 7, trow = bt - tb + rr;
-                  *reinterpret_cast<uint4 *>(sm + slot * kSlotBytes + panel * kPanelBytes + trow * 128 +
-                                             ((c ^ (trow & 7)) << 4)) = v[u];
-                }
-              }
-            }
-          }
-          fence_proxy_async_smem();
+          if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(boxes_per_tile * box_rows) * 256u);
           __syncwarp();
-          if (lane == 0) mbar_arrive_expect_tx(fb, nbox * (uint32_t)box_rows * 256u);
-          __syncwarp();
-          if (good) {
-            const int row = (int)((((int64_t)pid * 2 + kv) * h_kv + it.g) * ps + (t & (ps - 1)));
+          if (in_tile) {
+            const int row = row_kv0 >= 0 ? row_kv0 + kv * h_kv * ps : oob_row;
             const uint32_t dst = sbase + slot * kSlotBytes + (t - tb) * 128;
             tma_load_3d(dst, &kvmap, 0, 0, row, fb, pol);
             tma_load_3d(dst + kPanelBytes, &kvmap, 0, 1, row, fb, pol);
@@ -578,7 +548,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (item >= n_items) break;
         const TcItem it = tc_decode(item, s.pre, s.len, B, a, split_len);
         if (!mbar_wait(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1, s.abort)) break;
-        const uint32_t qa = sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES;
+        const uint64_t qd = smem_desc(sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES, 16, 1024);
         bool ok = true;
         for (int k = 0; k < it.ntiles; ++k, ++i) {
           const int kslot = (int)(i % C::NK);
@@ -587,13 +557,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!mbar_wait(bar_addr(s.s_empty + (i & 1)), ((i >> 1) & 1) ^ 1, s.abort)) { ok = false; break; }
           SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 11] = (unsigned)(clock64() - clk0));
           tc_fence_after();
-          const uint32_t ka = sbase + kslot * kSlotBytes;
+          // Descriptors of the K step kk: the start address field (bits 0-13, address >> 4) advanced
+          // from the tile's base descriptor (addresses stay below 256 KB: no carry out of the field).
+          const uint64_t ka = smem_desc(sbase + kslot * kSlotBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = smem_desc(ka + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = smem_desc(qa + (kk >> 2) * C::Q_PANEL + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ss(tm + (i & 1) * NP, ad, bd, id_qk, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tm + (i & 1) * NP, ka + (uint64_t)(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4),
+                        qd + (uint64_t)(((kk >> 2) * C::Q_PANEL + (kk & 3) * 32) >> 4), id_qk, kk > 0 ? 1u : 0u);
           mma_commit(bar_addr(s.s_full + (i & 1)));
           SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 1] = (unsigned)(clock64() - clk0));
           mma_commit(bar_addr(s.empty + kslot));
@@ -627,14 +597,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 10] = (unsigned)(clock64() - clk0));
           if (k == 0 && !mbar_wait(bar_addr(s.o_empty), (jl & 1) ^ 1, s.abort)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t va = sbase + vslot * kSlotBytes;
-          const uint32_t pa = sbase + C::OFF_P + (i & 1) * C::P_BYTES;
+          const uint64_t vd = smem_desc(sbase + vslot * kSlotBytes, kPanelBytes, 1024);
+          const uint64_t pd = smem_desc(sbase + C::OFF_P + (i & 1) * C::P_BYTES, kPanelBytes, 1024);
 #pragma unroll
-          for (int st = 0; st < kTcTile / 16; ++st) {
-            const uint64_t ad = smem_desc(va + st * 2048, kPanelBytes, 1024);
-            const uint64_t bd = smem_desc(pa + st * 2048, kPanelBytes, 1024);
-            mma_bf16_ss(o_col, ad, bd, id_pv, (k == 0 && st == 0) ? 0u : 1u);
-          }
+          for (int st = 0; st < kTcTile / 16; ++st)  // token step st: 16 rows = 2048 bytes further
+            mma_bf16_ss(o_col, vd + (uint64_t)(st * 2048 >> 4), pd + (uint64_t)(st * 2048 >> 4), id_pv,
+                        (k == 0 && st == 0) ? 0u : 1u);
           SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 6] = (unsigned)(clock64() - clk0));
           mma_commit(bar_addr(s.empty + vslot));
           mma_commit(bar_addr(s.p_empty + (i & 1)));
@@ -687,8 +655,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(bar_addr(s.s_empty + (i & 1)));
-        // Rows past the sequence and rows of skipped pages hold zeros in the K/V slots (the producer
-        // fills them), so only t < t1 matters here.
+        // Rows of skipped pages hold zeros in the K/V slots; rows past the unit's end hold zeros or
+        // the rest of its last page, so tokens t >= t1 are masked here and their V rows zeroed below.
         const bool valid = t < it.t1;
         const bool causal = tb + kTcTile - 1 > lim_base;
         const bool masked = causal || !__all_sync(0xffffffffu, valid);
@@ -822,6 +790,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 make_uint4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<uint4 *>(prow + (nl >> 6) * kPanelBytes + ((((nl & 63) >> 3) ^ (tw & 7)) << 4)) =
                 make_uint4(l[0], l[1], l[2], l[3]);
+          }
+        }
+        if (wg == 0 && !__all_sync(0xffffffffu, valid)) {
+          // The tile ends the unit: the first group zeroes the V rows of tokens past the end once
+          // the tile has landed (their probabilities are 0, but a stale row could hold NaN bits).
+          const int vslot = C::NK + (int)(i % C::NV);
+          if (!wwait(bar_addr(s.full + vslot), (i / C::NV) & 1, s.abort)) goto out;
+          if (!valid) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              *reinterpret_cast<uint4 *>(sm + vslot * kSlotBytes + (c >> 3) * kPanelBytes + tw * 128 + (c & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
