@@ -68,6 +68,10 @@ __device__ unsigned g_verify_masked_trace[kTraceBlocks * kTraceMasked * 8];
 // Per block and item j < kTraceItems, the first softmax warp's epilogue, cycles from entry: [0] start
 // (last P handed), [1] the item's O complete, [2] past the row-sum barrier, [3] outputs stored.
 __device__ unsigned g_verify_epi_trace[kTraceBlocks * kTraceItems * 4];
+// Per block and item j < kTraceItems, the producer's item start, cycles from entry: [0] item
+// published, [1] item decoded and page ids of the next one requested, [2] query buffer free,
+// [3] the item's last tile issued.
+__device__ unsigned g_verify_prod_trace[kTraceBlocks * kTraceItems * 4];
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -119,10 +123,14 @@ struct TcCfg {
   static constexpr int OFF_P = NSLOT * kSlotBytes;
   static constexpr int OFF_Q = OFF_P + 2 * P_BYTES;
   static constexpr int OFF_MISC = OFF_Q + 2 * Q_BYTES;
-  // misc: 48 mbarriers, flags and the item ring, per-row arrays, reduction scratch, the per-request
-  // item prefix and lengths
-  static constexpr int MISC = 48 * 8 + 128 + NP * 4 * 2 + 2 * 4 * 32 * 4 + (2 * kTcMaxBatch + 1) * 4;
+  // misc: 48 mbarriers, flags and the item ring (numbers, then decoded), per-row arrays, reduction
+  // scratch, the per-request item prefix and lengths
+  static constexpr int MISC = 48 * 8 + 128 + kTcItemRing * 32 + NP * 4 * 2 + 2 * 4 * 32 * 4 + (2 * kTcMaxBatch + 1) * 4;
   static constexpr int SMEM = OFF_MISC + MISC + 1024;
+};
+
+struct TcItem {
+  int b, g, split, L, t0, t1, ntiles, pad;
 };
 
 struct TcSmem {
@@ -132,16 +140,13 @@ struct TcSmem {
   int *abort;
   int *vote;   // [2 groups][4]
   int *items;  // [kTcItemRing] item numbers in processing order; n_items ends the sequence
+  TcItem *ring;  // [kTcItemRing] the items decoded (request, head, split, token range, tiles)
   float *mref, *alpha, *red;  // red: [2 groups][4 warps][32]
   int *pre;  // [B+1] item prefix per request
   int *len;  // [B] clamped sequence lengths
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint64_t *b) { return smem_u32(b); }
-
-struct TcItem {
-  int b, g, split, L, t0, t1, ntiles;
-};
 
 // Item -> (request, head, split): items of request b are pre[b] .. pre[b+1]-1, ordered (head, split).
 __device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int *len, int B, const VerifyArgs &a,
@@ -258,6 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned *TT = g_verify_tile_trace + (blockIdx.x % kTraceBlocks) * kTraceTiles * kTT;
   unsigned *TM = g_verify_masked_trace + (blockIdx.x % kTraceBlocks) * kTraceMasked * 8;
   unsigned *TE = g_verify_epi_trace + (blockIdx.x % kTraceBlocks) * kTraceItems * 4;
+  unsigned *TP = g_verify_prod_trace + (blockIdx.x % kTraceBlocks) * kTraceItems * 4;
   int n_masked = 0;
   unsigned tm_s = 0;
   const long long clk0 = clock64();
@@ -290,6 +296,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s.vote = s.abort + 1;  // [8]
     s.items = s.vote + 8;
     m += 128;
+    s.ring = reinterpret_cast<TcItem *>(m);
+    m += kTcItemRing * sizeof(TcItem);
     s.mref = reinterpret_cast<float *>(m);
     s.alpha = s.mref + NP;
     s.red = s.alpha + NP;  // 16-byte aligned (float4 reads)
@@ -418,52 +426,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Page ids of an item's boxes, read by the whole warp one item ahead of use: box j (tokens
     // t0 + j*box_rows) lives in lane j % 32, register j / 32 (boxes hold at least 8 rows).
     constexpr int kPidRegs = kTcMaxSplit / (8 * 32);
-    auto load_pids = [&](int item_idx, int32_t(&dst)[kPidRegs]) {
+    // Page ids of item nx's boxes (none when nx is the end marker).
+    auto load_pids = [&](const TcItem &nx, bool have, int32_t(&dst)[kPidRegs]) {
 #pragma unroll
-      for (int h = 0; h < kPidRegs; ++h) dst[h] = -1;
-      if (item_idx < n_items) {
-        const TcItem nx = tc_decode(item_idx, s.pre, s.len, B, a, split_len);
-#pragma unroll
-        for (int h = 0; h < kPidRegs; ++h) {
-          const int t = nx.t0 + (h * 32 + lane) * box_rows;
-          if (t < nx.t1) dst[h] = __ldg(a.kv.page_table + (int64_t)nx.b * a.kv.max_pages + (t >> lps));
-        }
+      for (int h = 0; h < kPidRegs; ++h) {
+        const int t = nx.t0 + (h * 32 + lane) * box_rows;
+        dst[h] = have && t < nx.t1 ? __ldg(a.kv.page_table + (int64_t)nx.b * a.kv.max_pages + (t >> lps)) : -1;
       }
     };
     // Work distribution: the block's first item is blockIdx.x, every later one is drawn from a global
-    // counter (items gridDim.x, gridDim.x + 1, ...), so blocks that run ahead take more items. The
-    // draw for item j+2 is issued at the start of item j and read one item later, when item j+1's
-    // page ids are fetched, so the atomic's latency stays hidden. Lane 0 holds the raw draws.
+    // counter (items gridDim.x, gridDim.x + 1, ...), so blocks that run ahead take more items.  Item
+    // j+1 is decoded, its page ids requested and the draw for item j+2 issued right after item j's
+    // first tile, so none of it (the decode's search and divisions, the loads, the atomic) sits at an
+    // item boundary, where the ring would drain.  Lane 0 holds the raw draws.
     int cur = blockIdx.x;
     int nxt = n_items, raw = 0;
     if (cur < n_items) {
       if (lane == 0) raw = atomicAdd(a.sched, 1);
       nxt = min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items);
     }
-    int32_t pid_next[kPidRegs];
-    load_pids(cur, pid_next);
+    TcItem it_cur{};
+    if (cur < n_items) it_cur = tc_decode(cur, s.pre, s.len, B, a, split_len);
+    int32_t pid_cur[kPidRegs];
+    load_pids(it_cur, cur < n_items, pid_cur);
     const int boxes_per_tile = kTcTile / box_rows;
     for (;; ++jl) {
-      // Hand the item number to the MMA and softmax roles (n_items ends their loops). The slot
+      // Hand the item to the MMA and softmax roles (n_items ends their loops). The slot
       // written here last held item jl - kTcItemRing, which every role has read by now: this warp
       // has passed the query-buffer wait of item jl - 1, so the QK issuer is done with item jl - 3,
       // the softmax warps (which read the S tile two tiles back) have begun item jl - 5 at least,
       // and the PV issuer (at most two tiles behind the softmax) has begun item jl - 7.
       if (lane == 0) {
         s.items[jl % kTcItemRing] = cur;
+        s.ring[jl % kTcItemRing] = it_cur;
         mbar_arrive(bar_addr(s.item_full + jl % kTcItemRing));
       }
+      SSD_TRACE(if (lane == 0 && jl < kTraceItems) TP[jl * 4] = (unsigned)(clock64() - clk0));
       if (cur >= n_items || !ok) break;
-      const TcItem it = tc_decode(cur, s.pre, s.len, B, a, split_len);
-      int32_t pid_reg[kPidRegs];
-#pragma unroll
-      for (int h = 0; h < kPidRegs; ++h) pid_reg[h] = pid_next[h];
-      load_pids(nxt, pid_next);
-      if (nxt < n_items && lane == 0) raw = atomicAdd(a.sched, 1);
+      const TcItem it = it_cur;
+      TcItem it_nx{};
+      int32_t pid_nx[kPidRegs];
+      SSD_TRACE(if (lane == 0 && jl < kTraceItems) TP[jl * 4 + 1] = (unsigned)(clock64() - clk0));
       // Query rows of this item: one 4-D TMA box per 64-column panel (d x 1 x G heads x n_c
       // candidates lands as rows r = i*G + h, 128-byte swizzled); rows >= R stay zero.
       const bool qok = lane == 0 ? mbar_wait(bar_addr(s.q_empty + (jl & 1)), ((jl >> 1) & 1) ^ 1, s.abort) : true;
       if (!__shfl_sync(0xffffffffu, qok, 0)) { ok = false; break; }
+      SSD_TRACE(if (lane == 0 && jl < kTraceItems) TP[jl * 4 + 2] = (unsigned)(clock64() - clk0));
       if (lane == 0) {
         const uint32_t qf = bar_addr(s.q_full + (jl & 1));
         const uint32_t qb = sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES;
@@ -483,7 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int32_t pid = -1;
 #pragma unroll
         for (int h = 0; h < kPidRegs; ++h) {
-          const int32_t ph = __shfl_sync(0xffffffffu, pid_reg[h], jb & 31);
+          const int32_t ph = __shfl_sync(0xffffffffu, pid_cur[h], jb & 31);
           if ((jb >> 5) == h) pid = ph;
         }
         const int t = tb + lane * box_rows;
@@ -517,8 +525,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (kv == 0) ++nk; else ++nv;
         }
+        if (k == 0) {
+          // Look-ahead (see above): the next item, decoded, with its page ids and the draw after it.
+          if (nxt < n_items) it_nx = tc_decode(nxt, s.pre, s.len, B, a, split_len);
+          load_pids(it_nx, nxt < n_items, pid_nx);
+          if (nxt < n_items && lane == 0) raw = atomicAdd(a.sched, 1);
+        }
       }
+      SSD_TRACE(if (lane == 0 && jl < kTraceItems) TP[jl * 4 + 3] = (unsigned)(clock64() - clk0));
       const bool drew = nxt < n_items;
+      it_cur = it_nx;
+#pragma unroll
+      for (int h = 0; h < kPidRegs; ++h) pid_cur[h] = pid_nx[h];
       cur = nxt;
       nxt = drew ? min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items) : n_items;
     }
@@ -546,7 +564,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1, s.abort)) break;
         const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
         if (item >= n_items) break;
-        const TcItem it = tc_decode(item, s.pre, s.len, B, a, split_len);
+        const TcItem it = s.ring[jl % kTcItemRing];
         if (!mbar_wait(bar_addr(s.q_full + (jl & 1)), (jl >> 1) & 1, s.abort)) break;
         const uint64_t qd = smem_desc(sbase + C::OFF_Q + (jl & 1) * C::Q_BYTES, 16, 1024);
         bool ok = true;
@@ -587,7 +605,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(bar_addr(s.item_full + jl % kTcItemRing), (jl / kTcItemRing) & 1, s.abort)) break;
         const int item = *reinterpret_cast<volatile int *>(s.items + jl % kTcItemRing);
         if (item >= n_items) break;
-        const TcItem it = tc_decode(item, s.pre, s.len, B, a, split_len);
+        const TcItem it = s.ring[jl % kTcItemRing];
         bool ok = true;
         for (int k = 0; k < it.ntiles; ++k, ++i) {
           const int vslot = C::NK + (int)(i % C::NV);
@@ -635,7 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     TcItem it{};
     if (!wwait(bar_addr(s.item_full), 0, s.abort)) goto out;
     item = *reinterpret_cast<volatile int *>(s.items);
-    if (item < n_items) it = tc_decode(item, s.pre, s.len, B, a, split_len);
+    if (item < n_items) it = s.ring[0];
     for (;; ++jl) {
       if (item >= n_items) break;
       const int u = it.b * h_kv + it.g;
@@ -816,7 +834,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!wwait(bar_addr(s.item_full + nj % kTcItemRing), (nj / kTcItemRing) & 1, s.abort)) goto out;
       const int next_item = *reinterpret_cast<volatile int *>(s.items + nj % kTcItemRing);
       TcItem nx{};
-      if (next_item < n_items) nx = tc_decode(next_item, s.pre, s.len, B, a, split_len);
+      if (next_item < n_items) nx = s.ring[nj % kTcItemRing];
       // Epilogue: O (high + residual columns) and the row sums -> the split's normalised partial.
       {
         SSD_TRACE(if (tid == 0 && jl < kTraceItems) TE[jl * 4] = (unsigned)(clock64() - clk0));
@@ -973,6 +991,11 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
 extern "C" int ssd_verify_trace(void *dst, size_t bytes) {
   if (!dst || bytes > sizeof(ssd::g_verify_trace)) return SSD_ERR_INVALID_ARG;
   return cudaMemcpyFromSymbol(dst, ssd::g_verify_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+// Diagnostic build only: the producer's item-start record (kTraceBlocks x kTraceItems x 4 words).
+extern "C" int ssd_verify_prod_trace(void *dst, size_t bytes) {
+  if (!dst || bytes > sizeof(ssd::g_verify_prod_trace)) return SSD_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(dst, ssd::g_verify_prod_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 // Diagnostic build only: the epilogue record (kTraceBlocks x kTraceItems x 4 32-bit words).
 extern "C" int ssd_verify_epi_trace(void *dst, size_t bytes) {
