@@ -102,7 +102,11 @@ constexpr int kTcItemRing = 8;  // item numbers handed from the producer to the 
 constexpr int kTcItemsPerBlock = 6;
 constexpr int kTcMaxSplit = kTcMaxSplitTiles * kTcTile;
 constexpr int kSlotBytes = kTcTile * 256;  // one K or V tile: 2 panels x 128 rows x 128 B
-constexpr int kPanelBytes = kTcTile * 128;
+constexpr int kPanelBytes = kTcTile * 128;  // P tile: one 64-column panel of 128 rows
+// K and V tiles: token t's 128-byte row of 64-column panel p sits at (t / 8) * kGroupBytes + p * 1024
+// + (t % 8) * 128 (16-byte chunks XOR-swizzled by t % 8), so a page's rows and both panels land in
+// one TMA box; the MMA operands step through the 8-row groups with a 2048-byte stride.
+constexpr int kGroupBytes = 2048;
 constexpr float kLazy = 8.f;
 
 template <int NP>
@@ -518,9 +522,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (in_tile) {
             const int row = row_kv0 >= 0 ? row_kv0 + kv * h_kv * ps : oob_row;
-            const uint32_t dst = sbase + slot * kSlotBytes + (t - tb) * 128;
-            tma_load_3d(dst, &kvmap, 0, 0, row, fb, pol);
-            tma_load_3d(dst + kPanelBytes, &kvmap, 0, 1, row, fb, pol);
+            const uint32_t dst = sbase + slot * kSlotBytes + ((t - tb) >> 3) * kGroupBytes;
+            tma_load_4d(dst, &kvmap, 0, 0, 0, row >> 3, fb, pol);  // box_rows rows, both panels
           }
           __syncwarp();
           if (kv == 0) ++nk; else ++nv;
@@ -577,10 +580,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_after();
           // Descriptors of the K step kk: the start address field (bits 0-13, address >> 4) advanced
           // from the tile's base descriptor (addresses stay below 256 KB: no carry out of the field).
-          const uint64_t ka = smem_desc(sbase + kslot * kSlotBytes, 16, 1024);
+          const uint64_t ka = smem_desc(sbase + kslot * kSlotBytes, 16, kGroupBytes);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tm + (i & 1) * NP, ka + (uint64_t)(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4),
+            mma_bf16_ss(tm + (i & 1) * NP, ka + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4),
                         qd + (uint64_t)(((kk >> 2) * C::Q_PANEL + (kk & 3) * 32) >> 4), id_qk, kk > 0 ? 1u : 0u);
           mma_commit(bar_addr(s.s_full + (i & 1)));
           SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 1] = (unsigned)(clock64() - clk0));
@@ -615,11 +618,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 10] = (unsigned)(clock64() - clk0));
           if (k == 0 && !mbar_wait(bar_addr(s.o_empty), (jl & 1) ^ 1, s.abort)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t vd = smem_desc(sbase + vslot * kSlotBytes, kPanelBytes, 1024);
+          // V^T as an MN-major operand: 64-element d atoms (panels) 1024 bytes apart, 8-token groups
+          // kGroupBytes apart; P^T: 64-column panels kPanelBytes apart, 8-token groups 1024 apart.
+          const uint64_t vd = smem_desc(sbase + vslot * kSlotBytes, 1024, kGroupBytes);
           const uint64_t pd = smem_desc(sbase + C::OFF_P + (i & 1) * C::P_BYTES, kPanelBytes, 1024);
 #pragma unroll
-          for (int st = 0; st < kTcTile / 16; ++st)  // token step st: 16 rows = 2048 bytes further
-            mma_bf16_ss(o_col, vd + (uint64_t)(st * 2048 >> 4), pd + (uint64_t)(st * 2048 >> 4), id_pv,
+          for (int st = 0; st < kTcTile / 16; ++st)  // token step st: 16 tokens further
+            mma_bf16_ss(o_col, vd + (uint64_t)(st * 2 * kGroupBytes >> 4), pd + (uint64_t)(st * 2048 >> 4), id_pv,
                         (k == 0 && st == 0) ? 0u : 1u);
           SSD_TRACE(if (i < kTraceTiles) TT[i * kTT + 6] = (unsigned)(clock64() - clk0));
           mma_commit(bar_addr(s.empty + vslot));
@@ -818,8 +823,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!valid) {
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              *reinterpret_cast<uint4 *>(sm + vslot * kSlotBytes + (c >> 3) * kPanelBytes + tw * 128 + (c & 7) * 16) =
-                  make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4 *>(sm + vslot * kSlotBytes + (tw >> 3) * kGroupBytes + (c >> 3) * 1024 +
+                                         (tw & 7) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         fence_proxy_async_smem();
@@ -955,12 +960,14 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   const int box_rows = kv->page_size < kTcTile ? kv->page_size : kTcTile;
+  // The pool's 256-byte K / V rows as (64 columns, row in an 8-row group, 64-column panel, 8-row group):
+  // one box takes box_rows rows of both panels and lands as [group][panel][8 rows x 128 B].
   CUtensorMap map;
-  cuuint64_t dims[3] = {64, 2, (cuuint64_t)kv->num_pages * 2 * kv->h_kv * kv->page_size};
-  cuuint64_t strides[2] = {128, 256};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv->pool), dims, strides, box, es,
+  cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)kv->num_pages * 2 * kv->h_kv * kv->page_size / 8};
+  cuuint64_t strides[3] = {256, 128, 2048};
+  cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)box_rows / 8};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(kv->pool), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SSD_ERR_CUDA, "cuTensorMapEncodeTiled (KV pool) failed (%d)", (int)r);
