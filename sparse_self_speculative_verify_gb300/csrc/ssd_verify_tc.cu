@@ -72,6 +72,11 @@ __device__ unsigned g_verify_epi_trace[kTraceBlocks * kTraceItems * 4];
 // published, [1] item decoded and page ids of the next one requested, [2] query buffer free,
 // [3] the item's last tile issued.
 __device__ unsigned g_verify_prod_trace[kTraceBlocks * kTraceItems * 4];
+// Per block and tile i < kTraceStage, the first softmax warp's stages, cycles from entry: [0] S seen,
+// [1] S read and its buffer released, [2] past the vote barrier, [3] past the reference update,
+// [4] probabilities and sums done, [5] side values stored, [6] P buffer free, [7] P handed.
+constexpr int kTraceStage = 64;
+__device__ unsigned g_verify_stage_trace[kTraceBlocks * kTraceStage * 8];
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -86,6 +91,9 @@ __device__ __forceinline__ unsigned long long global_ns() {
   do {                  \
   } while (0)
 #endif
+
+// Stage k of the softmax's tile i (trace build only).
+#define SSD_STAGE(k) SSD_TRACE(if (tid == 0 && i < kTraceStage) TS[i * 8 + (k)] = (unsigned)(clock64() - clk0))
 
 constexpr int kTcTile = kTcTileTokens;
 constexpr int kTcWarps = 11;
@@ -199,6 +207,23 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N]) {
   return v[0];
 }
 
+// Transposes an 8 x 8 matrix of 32-bit words held by eight consecutive lanes (lane i = lane % 8 holds
+// row i in v[0..7]): afterwards lane i holds column i.  Three butterfly stages swap the off-diagonal
+// blocks of 4, 2 and 1 words with the partner lane i ^ s.
+__device__ __forceinline__ void transpose8x8(uint32_t (&v)[8], int i) {
+#pragma unroll
+  for (int s = 1; s < 8; s <<= 1) {
+    const bool upper = (i & s) != 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      if (p & s) continue;
+      const uint32_t send = upper ? v[p] : v[p + s];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, s);
+      if (upper) v[p] = recv; else v[p + s] = recv;
+    }
+  }
+}
+
 // Bounded arrive-and-wait over the 128 threads of one softmax warpgroup.
 __device__ __forceinline__ bool group_sync(uint64_t *bar, volatile int *abort, uint32_t &phase) {
   mbar_arrive(bar_addr(bar));
@@ -268,6 +293,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned *TM = g_verify_masked_trace + (blockIdx.x % kTraceBlocks) * kTraceMasked * 8;
   unsigned *TE = g_verify_epi_trace + (blockIdx.x % kTraceBlocks) * kTraceItems * 4;
   unsigned *TP = g_verify_prod_trace + (blockIdx.x % kTraceBlocks) * kTraceItems * 4;
+  unsigned *TS = g_verify_stage_trace + (blockIdx.x % kTraceBlocks) * kTraceStage * 8;
   int n_masked = 0;
   unsigned tm_s = 0;
   const long long clk0 = clock64();
@@ -670,6 +696,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int tb = it.t0 + k * kTcTile, t = tb + tw;
         if (!wwait(bar_addr(s.s_full + (i & 1)), (i >> 1) & 1, s.abort)) goto out;
         SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * kTT + 2] = (unsigned)(clock64() - clk0));
+        SSD_STAGE(0);
         SSD_TRACE(if (tid == 128 && i < kTraceTiles) TT[i * kTT + 8] = (unsigned)(clock64() - clk0));
         SSD_TRACE(tm_s = (unsigned)(clock64() - clk0));
         tc_fence_after();
@@ -678,6 +705,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(bar_addr(s.s_empty + (i & 1)));
+        SSD_STAGE(1);
         // Rows of skipped pages hold zeros in the K/V slots; rows past the unit's end hold zeros or
         // the rest of its last page, so tokens t >= t1 are masked here and their V rows zeroed below.
         const bool valid = t < it.t1;
@@ -715,6 +743,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!group_sync(grp, s.abort, gph)) goto out;
         const bool any = vote[i & 3] != 0;
         if (tw == 0) vote[(i + 2) & 3] = 0;
+        SSD_STAGE(2);
 #ifdef SSD_VERIFY_TRACE
         const bool trace_m = masked && tid == 0 && n_masked < kTraceMasked;
 #endif
@@ -774,18 +803,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         SSD_TRACE(if (trace_m) TM[n_masked * 8 + 2] = (unsigned)(clock64() - clk0));
+        SSD_STAGE(3);
         // Probabilities (<= 2^kLazy; exp2(-inf) = 0), running sums, side values, P tile.
 #pragma unroll
         for (int j = 0; j < CW; ++j) {
           x[j] = fast_exp2(dl[j]);
           lsum[j] += x[j];
         }
+        SSD_STAGE(4);
         if (a.side_p != nullptr) {
-          // fp16 side values, row-major per (unit, row): each warp store covers 32 consecutive tokens.
-          __half *sp = a.side_p + ((int64_t)u * R + c0) * a.Lpad + t;
+          // fp16 side values, row-major per (unit, row).  The eight lanes that hold eight consecutive
+          // tokens transpose their (row pair, token) values, so that lane j stores rows 2j and 2j + 1 of
+          // each batch of 16 rows for those eight tokens: two 16-byte stores instead of 16 two-byte ones.
+          const int j8 = lane & 7;
+          __half *sp = a.side_p + (int64_t)u * R * a.Lpad + (t - j8);
 #pragma unroll
-          for (int j = 0; j < CW; ++j)
-            if (c0 + j < R) sp[(int64_t)j * a.Lpad] = __float2half_rn(x[j]);
+          for (int hb = 0; hb < CW / 16; ++hb) {
+            uint32_t h[8];
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              const __half2 v = __floats2half2_rn(x[16 * hb + 2 * p], x[16 * hb + 2 * p + 1]);
+              h[p] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            transpose8x8(h, j8);
+            const int r = c0 + 16 * hb + 2 * j8;
+            const uint4 lo = make_uint4(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410),
+                                        __byte_perm(h[4], h[5], 0x5410), __byte_perm(h[6], h[7], 0x5410));
+            const uint4 hi = make_uint4(__byte_perm(h[0], h[1], 0x7632), __byte_perm(h[2], h[3], 0x7632),
+                                        __byte_perm(h[4], h[5], 0x7632), __byte_perm(h[6], h[7], 0x7632));
+            if (r < R) *reinterpret_cast<uint4 *>(sp + (int64_t)r * a.Lpad) = lo;
+            if (r + 1 < R) *reinterpret_cast<uint4 *>(sp + (int64_t)(r + 1) * a.Lpad) = hi;
+          }
           // References: one per (row, 16 tokens); CW rows x 8 groups entries per warpgroup.
 #pragma unroll
           for (int e = tw; e < CW * (kTcTile / kRefGroup); e += 128) {
@@ -797,7 +845,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         SSD_TRACE(if (trace_m) TM[n_masked * 8 + 3] = (unsigned)(clock64() - clk0));
+        SSD_STAGE(5);
         if (!wwait(bar_addr(s.p_empty + (i & 1)), ((i >> 1) & 1) ^ 1, s.abort)) goto out;
+        SSD_STAGE(6);
         SSD_TRACE(if (trace_m) TM[n_masked * 8 + 4] = (unsigned)(clock64() - clk0));
         {
           char *prow = sm + C::OFF_P + (i & 1) * C::P_BYTES + tw * 128;
@@ -830,6 +880,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar_addr(s.p_full + (i & 1)));
         SSD_TRACE(if (tid == 0 && i < kTraceTiles) TT[i * kTT + 3] = (unsigned)(clock64() - clk0));
+        SSD_STAGE(7);
         SSD_TRACE(if (tid == 128 && i < kTraceTiles) TT[i * kTT + 9] = (unsigned)(clock64() - clk0));
         SSD_TRACE(if (trace_m) TM[(n_masked++) * 8 + 5] = (unsigned)(clock64() - clk0));
       }
@@ -998,6 +1049,11 @@ int launch_verify_tc(const ssd_paged_kv *kv, const VerifyArgs &a, cudaStream_t s
 extern "C" int ssd_verify_trace(void *dst, size_t bytes) {
   if (!dst || bytes > sizeof(ssd::g_verify_trace)) return SSD_ERR_INVALID_ARG;
   return cudaMemcpyFromSymbol(dst, ssd::g_verify_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+// Diagnostic build only: the softmax stage record (kTraceBlocks x kTraceStage x 8 32-bit words).
+extern "C" int ssd_verify_stage_trace(void *dst, size_t bytes) {
+  if (!dst || bytes > sizeof(ssd::g_verify_stage_trace)) return SSD_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(dst, ssd::g_verify_stage_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 // Diagnostic build only: the producer's item-start record (kTraceBlocks x kTraceItems x 4 words).
 extern "C" int ssd_verify_prod_trace(void *dst, size_t bytes) {

@@ -13,7 +13,7 @@ the library proper for this process, runs ``ssd_verify_attn`` on a seeded worklo
 
 Usage: ``python -m sparse_self_speculative_verify_gb300.trace_verify [workload] [--dump FILE.npz]``
 with workload qwen3_8b (default), b128_l8k or qwen3_14b_unified (its verify-phase requests).  Prints
-a JSON line; ``--dump`` also saves the raw per-block, per-tile, masked-tile, epilogue and producer records and the requests'
+a JSON line; ``--dump`` also saves the raw per-block, per-tile, masked-tile, epilogue, producer and softmax-stage records and the requests'
 lengths.
 """
 
@@ -77,7 +77,11 @@ def run(name: str = "qwen3_8b", dump: str | None = None) -> dict:
         L.ssd_verify_prod_trace.restype = ctypes.c_int
         tp = np.zeros(BLOCKS * ITEMS * 4, np.uint32)
         assert L.ssd_verify_prod_trace(tp.ctypes.data, tp.nbytes) == 0
-        np.savez(dump, trace=tr, producer=tp.reshape(BLOCKS, ITEMS, 4)[:nb], tiles=tt.reshape(BLOCKS, TILES, 12)[:nb], masked=tm.reshape(BLOCKS, MASKED, 8)[:nb],
+        L.ssd_verify_stage_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+        L.ssd_verify_stage_trace.restype = ctypes.c_int
+        ts = np.zeros(BLOCKS * 64 * 8, np.uint32)
+        assert L.ssd_verify_stage_trace(ts.ctypes.data, ts.nbytes) == 0
+        np.savez(dump, trace=tr, producer=tp.reshape(BLOCKS, ITEMS, 4)[:nb], stage=ts.reshape(BLOCKS, 64, 8)[:nb], tiles=tt.reshape(BLOCKS, TILES, 12)[:nb], masked=tm.reshape(BLOCKS, MASKED, 8)[:nb],
                  epilogue=te.reshape(BLOCKS, ITEMS, 4)[:nb],
                  seq_lens=kv.seq_lens.cpu().numpy(), h_kv=spec.h_kv, n_cand=spec.n_cand)
     entry, exit_, t0 = tr[:, 0], tr[:, 2], int(tr[:, 0].min())
