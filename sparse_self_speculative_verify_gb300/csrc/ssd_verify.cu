@@ -239,6 +239,13 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
   fin_unit_scores<kCsThreads>(f, u, L, sL2, s_keys, tid);
   pdl_trigger();
   __syncthreads();
+  // The unit's side values have been read for the last time: drop their L2 lines unwritten (each row
+  // of the unit starts 256-byte aligned; the verify wrote whole 128-token tiles).
+  if (f.side_p) {
+    const int lines = cdiv(L, kSideAlign) * kSideAlign / 64;  // 64 fp16 per 128-byte line
+    for (int e = tid; e < f.R * lines; e += kCsThreads)
+      discard_l2_line(f.side_p + ((int64_t)u * f.R + e / lines) * f.Lpad + (e % lines) * 64);
+  }
   int K = f.ks[b];
   K = K < 0 ? 0 : (K > L ? L : K);
   if (K > f.sel_kmax) {

@@ -673,6 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float *red = s.red + wg * 4 * 32;
     const uint32_t lane_base = (uint32_t)(wiw * 32) << 16;
     const int nref = a.Lpad / kRefGroup;
+    const uint64_t side_pol = policy_l2_evict_last();
     uint32_t i = 0, gph = 0;
     int jl = 0;
     // The item sequence comes from the producer's ring.  Each item's per-row references start at
@@ -831,8 +832,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                         __byte_perm(h[4], h[5], 0x5410), __byte_perm(h[6], h[7], 0x5410));
             const uint4 hi = make_uint4(__byte_perm(h[0], h[1], 0x7632), __byte_perm(h[2], h[3], 0x7632),
                                         __byte_perm(h[4], h[5], 0x7632), __byte_perm(h[6], h[7], 0x7632));
-            if (r < R) *reinterpret_cast<uint4 *>(sp + (int64_t)r * a.Lpad) = lo;
-            if (r + 1 < R) *reinterpret_cast<uint4 *>(sp + (int64_t)(r + 1) * a.Lpad) = hi;
+            // Kept in L2 (the criticality pass reads them next and then drops them from L2 unwritten).
+            if (r < R) st_global_policy(sp + (int64_t)r * a.Lpad, lo, side_pol);
+            if (r + 1 < R) st_global_policy(sp + (int64_t)(r + 1) * a.Lpad, hi, side_pol);
           }
           // References: one per (row, 16 tokens); CW rows x 8 groups entries per warpgroup.
 #pragma unroll
