@@ -175,6 +175,14 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
         if (t0 + k < L) dst[k] = crit[k];
     }
   }
+  // This block's side values have been read for the last time: drop their L2 lines unwritten (rows
+  // start 256-byte aligned; the verify wrote whole 128-token tiles, kFinTok is a multiple of them).
+  __syncthreads();
+  {
+    const int lines = (min(tb0 + kFinTok, cdiv(L, kSideAlign) * kSideAlign) - tb0) / 64;
+    for (int e = tid; e < f.R * lines; e += kFinThreads)
+      discard_l2_line(f.side_p + (rbase + e / lines) * f.Lpad + tb0 + (e % lines) * 64);
+  }
   if (!f.ks) return;
 
   // Fused selection: the last of the unit's token blocks to finish selects the unit's row (read
