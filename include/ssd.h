@@ -216,7 +216,8 @@ int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t
  *               owned by the caller.  Its layout is private to the library.
  *   pack_mode   SSD_PACK_NONE: exactly ssd_draft_attn (pack unused, may be NULL).
  *               SSD_PACK_WRITE: ssd_draft_attn, and every selected row it read is stored in pack.
- *               SSD_PACK_READ: attends the rows the last SSD_PACK_WRITE call on this pack stored;
+ *               SSD_PACK_READ: attends the rows the last SSD_PACK_WRITE call (or the last
+ *               ssd_verify_select_packed call) on this pack stored;
  *               idx is not read (may be NULL) and the page table and lengths are not consulted, so
  *               no index or page fault is raised.  cnt and k_max must equal that call's and the
  *               selected tokens' K / V must be unchanged since (appending new tokens is fine); a cnt
@@ -228,6 +229,22 @@ size_t ssd_draft_pack_bytes(const ssd_paged_kv *kv, int k_max);
 int ssd_draft_attn_packed(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
                           const int32_t *cnt, float scale, float *out, float *lse, void *pack, size_t pack_bytes,
                           int pack_mode, void *workspace, size_t workspace_bytes, ssd_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * ssd_verify_select, and the selection's K and V rows stored in a row pack as an SSD_PACK_WRITE
+ * draft over (idx, cnt, k_max) would store them, so that every draft of the round can read the pack
+ * (SSD_PACK_READ) and none gathers through the index list (SparseSpec §4.1: the k drafts attend the
+ * set this verify selects).  The selecting blocks know their unit's indices when they finish and
+ * copy its rows then.  Same arguments and results as ssd_verify_select, plus:
+ *   pack        device buffer of at least ssd_draft_pack_bytes(kv, k_max) bytes, 256-byte aligned,
+ *               owned by the caller; its layout is private to the library.  A selected token whose
+ *               page id is out of range stores zero rows (the verify raises SSD_FAULT_PAGE).
+ *   pack_bytes  its size; smaller than needed: SSD_ERR_WORKSPACE.
+ */
+int ssd_verify_select_packed(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
+                             float *lse, float *scores, int64_t scores_stride, const int32_t *ks, int32_t *idx,
+                             int k_max, int32_t *cnt, void *pack, size_t pack_bytes, void *workspace,
+                             size_t workspace_bytes, ssd_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * KV append and length advance (SpecSA post, "refresh/reuse NSA kernel fusion" and "branch

@@ -25,7 +25,7 @@ SSD_DTYPE_F32, SSD_DTYPE_BF16 = 0, 1
 FAULT_PAGE, FAULT_SEQLEN, FAULT_INDEX, FAULT_KMAX, FAULT_UNION, FAULT_TIMEOUT, FAULT_VALUE = 1, 2, 4, 8, 16, 32, 64
 
 EXPORTED = ["ssd_last_error", "ssd_version", "ssd_status", "ssd_verify_workspace_bytes", "ssd_verify_attn",
-            "ssd_verify_select",
+            "ssd_verify_select", "ssd_verify_select_packed",
             "ssd_select_topk", "ssd_select_topp", "ssd_draft_workspace_bytes", "ssd_draft_attn", "ssd_draft_attn_static",
             "ssd_draft_pack_bytes", "ssd_draft_attn_packed",
             "ssd_unified_workspace_bytes", "ssd_kv_append", "ssd_kv_advance", "ssd_phase_assign", "ssd_phase_fill",
@@ -78,6 +78,7 @@ def load(path: Optional[str] = None, as_default: bool = False):
             "ssd_verify_workspace_bytes": ([KV, I, I], S),
             "ssd_verify_attn": ([KV, P, I, I, F, P, P, P, I64, P, I64, I, P, S, P], I),
             "ssd_verify_select": ([KV, P, I, I, F, P, P, P, I64, P, P, I, P, P, S, P], I),
+            "ssd_verify_select_packed": ([KV, P, I, I, F, P, P, P, I64, P, P, I, P, P, S, P, S, P], I),
             "ssd_select_topk": ([P, I64, P, P, I, I, I, I, P, I, P, P], I),
             "ssd_select_topp": ([P, I64, P, F, I, I, I, I, P, I, P, P, P], I),
             "ssd_draft_workspace_bytes": ([KV, I, I], S),
@@ -266,9 +267,12 @@ def ssd_verify_attn(kv: KVCache, q: torch.Tensor, n_cand: int, scale: float, *, 
 
 def ssd_verify_select(kv: KVCache, q: torch.Tensor, n_cand: int, scale: float, ks: torch.Tensor, k_max: int, *,
                       out=None, lse=None, scores=None, idx=None, cnt=None, want_lse: bool = True,
-                      workspace: Optional[Workspace] = None, stream=None) -> dict:
+                      pack: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
+                      stream=None) -> dict:
     """Verify with the Top-K selection fused into its criticality pass.  q [B, n_cand, h_q, d];
-    ks [B] int32 (K per request); idx [B * h_kv, k_max], cnt [B * h_kv]."""
+    ks [B] int32 (K per request); idx [B * h_kv, k_max], cnt [B * h_kv].  With `pack` (a uint8 buffer
+    of ssd_draft_pack_bytes(kv, k_max) bytes, 256-byte aligned), ssd_verify_select_packed: the
+    selected rows are also stored there for drafts with PACK_READ."""
     _need(q, "q", kv.pool.dtype, kv.device)
     B, nc, h_q, d = q.shape
     assert nc == n_cand and B == kv.batch and d == kv.d
@@ -291,8 +295,15 @@ def ssd_verify_select(kv: KVCache, q: torch.Tensor, n_cand: int, scale: float, k
     L = _lib()
     need = L.ssd_verify_workspace_bytes(kv.ref(), h_q, n_cand)
     wsp, avail = _ws(dev, "verify", need, workspace)
-    _check(L.ssd_verify_select(kv.ref(), _ptr(q), h_q, n_cand, float(scale), _ptr(out), _ptr(lse), _ptr(scores),
-                               scores.shape[-1], _ptr(ks), _ptr(idx), k_max, _ptr(cnt), wsp, avail, _stream(stream)))
+    if pack is None:
+        _check(L.ssd_verify_select(kv.ref(), _ptr(q), h_q, n_cand, float(scale), _ptr(out), _ptr(lse), _ptr(scores),
+                                   scores.shape[-1], _ptr(ks), _ptr(idx), k_max, _ptr(cnt), wsp, avail,
+                                   _stream(stream)))
+    else:
+        _need(pack, "pack", torch.uint8, dev)
+        _check(L.ssd_verify_select_packed(kv.ref(), _ptr(q), h_q, n_cand, float(scale), _ptr(out), _ptr(lse),
+                                          _ptr(scores), scores.shape[-1], _ptr(ks), _ptr(idx), k_max, _ptr(cnt),
+                                          _ptr(pack), pack.numel(), wsp, avail, _stream(stream)))
     return {"out": out, "lse": lse, "scores": scores, "idx": idx, "cnt": cnt}
 
 

@@ -150,4 +150,64 @@ __device__ __forceinline__ void fin_unit_scores(const FinalizeArgs &f, int u, in
   }
 }
 
+// Stores the K and V rows of unit u's n selected tokens (f.sel_idx[u][0, n)) into the row pack, as
+// the draft's pack reader takes them: the unit's chunk c holds selection slots [64 c, 64 c + 64) as a
+// K tile then a V tile of 64 rows; row j of a tile sits at j * row bytes with its 16-byte chunk ch at
+// (ch ^ (j % 8)) * 16.  Rows past n are not stored.  Threads tid < NT of the block call it, after a
+// barrier that makes the selection visible; s_rows is shared scratch of kPackBatch int64 entries.
+// First each selected token's K-row byte offset in the pool is resolved once (page lookup; -1 for a
+// page out of range, whose rows are stored as zeros: the verify has flagged SSD_FAULT_PAGE), then the
+// rows are copied 16 bytes at a time, eight copies in flight per thread.
+constexpr int kPackBatch = 1024;
+template <int NT>
+__device__ __forceinline__ void pack_unit_rows(const FinalizeArgs &f, int u, int n, int tid, int64_t *s_rows) {
+  const int b = u / f.h_kv, g = u % f.h_kv;
+  const int rowb = f.D * f.esize, cpr = rowb / 16;
+  const int64_t tile = (int64_t)kDraftChunk * rowb;
+  char *pu = f.pack + (int64_t)u * f.pack_cmax * 2 * tile;
+  const int32_t *sel = f.sel_idx + (int64_t)u * f.sel_kmax;
+  const char *pool = static_cast<const char *>(f.kv.pool);
+  const int64_t v_off = (int64_t)f.kv.h_kv * f.kv.page_size * rowb;  // a page's K rows to its V rows
+  for (int j0 = 0; j0 < n; j0 += kPackBatch) {
+    const int nb = min(kPackBatch, n - j0);
+    for (int j = tid; j < nb; j += NT) {
+      const int t = sel[j0 + j];
+      int64_t off = -1;
+      if (t >= 0) {
+        const int32_t p = __ldg(f.kv.page_table + (int64_t)b * f.kv.max_pages + (t >> f.kv.log2_ps));
+        if (p >= 0 && (int64_t)p < f.kv.num_pages)
+          off = ((((int64_t)p * 2) * f.kv.h_kv + g) * f.kv.page_size + (t & (f.kv.page_size - 1))) * rowb;
+      }
+      s_rows[j] = off;
+    }
+    __syncthreads();
+    const int total = nb * 2 * cpr;
+    constexpr int U = 8;
+    for (int e0 = tid; e0 < total; e0 += NT * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int e = e0 + k * NT;
+        v[k] = make_uint4(0, 0, 0, 0);
+        if (e < total) {
+          const int j = e / (2 * cpr), kv = (e / cpr) & 1, ch = e % cpr;
+          const int64_t off = s_rows[j];
+          if (off >= 0) v[k] = __ldg(reinterpret_cast<const uint4 *>(pool + off + kv * v_off) + ch);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int e = e0 + k * NT;
+        if (e < total) {
+          const int j = e / (2 * cpr), kv = (e / cpr) & 1, ch = e % cpr;
+          const int js = j0 + j, jr = js % kDraftChunk;
+          *reinterpret_cast<uint4 *>(pu + ((int64_t)(js / kDraftChunk) * 2 + kv) * tile + (int64_t)jr * rowb +
+                                     ((ch ^ (jr & 7)) << 4)) = v[k];
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace ssd

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   __shared__ float sLn[kMaxRows];
   __shared__ float sL2[kMaxRows];
   __shared__ __align__(16) float s_coef[kMaxRows * kFinGroups];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int u = blockIdx.y, b = u / f.h_kv, g = u % f.h_kv;
   pdl_wait();
   if (f.phase && f.phase[b] == 0) return;
@@ -204,6 +204,11 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   auto &sc = *reinterpret_cast<TopkScratch<kFinThreads> *>(s_coef);
   topk_row<kFinThreads>([&](int t) -> uint32_t { return score_key(__ldcg(row + t)); }, L, K,
                         f.sel_idx + (int64_t)u * f.sel_kmax, f.sel_kmax, sc);
+  if (f.pack) {
+    static_assert(sizeof(s_coef) >= kPackBatch * sizeof(int64_t), "row-offset scratch");
+    __syncthreads();  // the selection is read back below; the selection scratch is reused
+    pack_unit_rows<kFinThreads>(f, u, K, tid, reinterpret_cast<int64_t *>(s_coef));
+  }
   if (tid == 0) {
     f.sel_cnt[u] = K;
     f.sel_ctr[u] = 0u;
@@ -223,6 +228,26 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
 constexpr int kCsThreads = 512;
 constexpr int kCsSmemRow = 40960;  // longest row kept in shared memory (160 KB of keys)
 
+#ifdef SSD_VERIFY_TRACE
+// Diagnostic build: per unit-block of the criticality pass, global-timer stamps [0] entry, [1] past the
+// wait for the verify, [2] LSE merge done, [3] scores done, [4] Top-K done, [5] row pack done.
+constexpr int kCsTraceUnits = 4096;
+__device__ unsigned long long g_cs_trace[kCsTraceUnits * 8];
+__device__ __forceinline__ unsigned long long cs_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define CS_STAMP(k) \
+  do {              \
+    if (tid == 0 && u < kCsTraceUnits) g_cs_trace[u * 8 + (k)] = cs_ns(); \
+  } while (0)
+#else
+#define CS_STAMP(k) \
+  do {              \
+  } while (0)
+#endif
+
 __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f, int units) {
   extern __shared__ __align__(16) uint32_t s_keys[];  // [max_seq_len] keys of the unit's scores
   __shared__ float sLn[kMaxRows], sL2[kMaxRows];
@@ -231,13 +256,16 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
   const bool comb = (int)blockIdx.x >= units;
   const int u = comb ? (int)blockIdx.x - units : (int)blockIdx.x;
   const int b = u / f.h_kv, g = u % f.h_kv;
+  if (!comb) CS_STAMP(0);
   pdl_wait();
+  if (!comb) CS_STAMP(1);
   int L = f.seq_lens[b];
   L = L < 0 ? 0 : (L > f.max_seq_len ? f.max_seq_len : L);
   const int ns = fin_splits(f, u, L);
-  const int64_t pbase = (int64_t)u * f.S_max * f.R, rbase = (int64_t)u * f.R;
+  const int64_t pbase = (int64_t)u * f.S_max * f.R;
   fin_lse_merge<kCsThreads / 32>(f, pbase, ns, sLn, sL2);
   __syncthreads();
+  if (!comb) CS_STAMP(2);
   if (comb) {
     pdl_trigger();
     const int tpr = f.D / 4;
@@ -247,6 +275,7 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
   fin_unit_scores<kCsThreads>(f, u, L, sL2, s_keys, tid);
   pdl_trigger();
   __syncthreads();
+  CS_STAMP(3);
   // The unit's side values have been read for the last time: drop their L2 lines unwritten (each row
   // of the unit starts 256-byte aligned; the verify wrote whole 128-token tiles).
   if (f.side_p) {
@@ -263,7 +292,22 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
   topk_row<kCsThreads>([&](int t) -> uint32_t { return s_keys[t]; }, L, K, f.sel_idx + (int64_t)u * f.sel_kmax,
                        f.sel_kmax, sc);
   if (tid == 0) f.sel_cnt[u] = K;
+  CS_STAMP(4);
+  if (f.pack) {
+    static_assert(sizeof(sc) >= kPackBatch * sizeof(int64_t), "row-offset scratch");
+    __syncthreads();  // the selection, written by the whole block, is read back below
+    pack_unit_rows<kCsThreads>(f, u, K, tid, reinterpret_cast<int64_t *>(&sc));
+  }
+  CS_STAMP(5);
 }
+
+#ifdef SSD_VERIFY_TRACE
+// Diagnostic build only: the criticality-pass record (kCsTraceUnits x 8 64-bit words).
+extern "C" int ssd_crit_select_trace(void *dst, size_t bytes) {
+  if (!dst || bytes > sizeof(g_cs_trace)) return SSD_ERR_INVALID_ARG;
+  return cudaMemcpyFromSymbol(dst, g_cs_trace, bytes) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+#endif
 
 int launch_finalize(const FinalizeArgs &f, int n_tok, int units, cudaStream_t st) {
   // With token blocks in the grid, one combine block per unit loops over the rows (fewer blocks to
@@ -390,8 +434,9 @@ extern "C" size_t ssd_verify_workspace_bytes(const ssd_paged_kv *kv, int h_q, in
 
 static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
                        float *lse, float *scores, int64_t scores_stride, float *bscores, int64_t bscores_stride,
-                       int block_size, const int32_t *ks, int32_t *idx, int k_max, int32_t *cnt, void *workspace,
-                       size_t workspace_bytes, ssd_stream_t stream, const char *who) {
+                       int block_size, const int32_t *ks, int32_t *idx, int k_max, int32_t *cnt, void *pack,
+                       size_t pack_bytes, void *workspace, size_t workspace_bytes, ssd_stream_t stream,
+                       const char *who) {
   KVView v;
   int rc = validate_kv(kv, &v, who);
   if (rc) return rc;
@@ -413,6 +458,13 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
     if (!cnt || (!idx && k_max > 0) || k_max < 0) return fail(SSD_ERR_INVALID_ARG, "%s: idx / cnt / k_max", who);
     if ((int64_t)kv->batch * kv->h_kv > kCounterSlots - 2)
       return fail(SSD_ERR_UNSUPPORTED, "%s: batch*h_kv above %d", who, kCounterSlots - 2);
+  }
+  if (pack) {
+    const size_t pneed = ssd_draft_pack_bytes(kv, k_max);
+    if (!ks || pneed == 0 || pack_bytes < pneed)
+      return fail(SSD_ERR_WORKSPACE, "%s: row pack %zu bytes, need %zu", who, pack_bytes, pneed);
+    if (reinterpret_cast<uintptr_t>(pack) & 255u)
+      return fail(SSD_ERR_INVALID_ARG, "%s: row pack must be 256-byte aligned", who);
   }
   if (kv->batch == 0 || kv->max_seq_len == 0) return SSD_OK;
   unsigned *status = device_status();
@@ -470,6 +522,10 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
   f.sel_cnt = cnt;
   f.sel_kmax = k_max;
   f.sel_ctr = reinterpret_cast<unsigned *>(ws + lay.ctr_off) + 2;  // slots 0-1: the tensor-core kernel
+  f.pack = static_cast<char *>(pack);
+  f.pack_cmax = cdiv(k_max > 0 ? k_max : 1, kDraftChunk);
+  f.esize = kv->dtype == SSD_DTYPE_BF16 ? 2 : 4;
+  f.kv = v;
   f.status = status;
 
   if (tc) {
@@ -495,7 +551,7 @@ extern "C" int ssd_verify_attn(const ssd_paged_kv *kv, const void *q, int h_q, i
                                int64_t bscores_stride, int block_size, void *workspace, size_t workspace_bytes,
                                ssd_stream_t stream) {
   return verify_call(kv, q, h_q, n_cand, scale, out, lse, scores, scores_stride, bscores, bscores_stride, block_size,
-                     nullptr, nullptr, 0, nullptr, workspace, workspace_bytes, stream, "ssd_verify_attn");
+                     nullptr, nullptr, 0, nullptr, nullptr, 0, workspace, workspace_bytes, stream, "ssd_verify_attn");
 }
 
 extern "C" int ssd_verify_select(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale, float *out,
@@ -505,7 +561,19 @@ extern "C" int ssd_verify_select(const ssd_paged_kv *kv, const void *q, int h_q,
   const char *who = "ssd_verify_select";
   if (!ks) return fail(SSD_ERR_INVALID_ARG, "%s: ks must be non-NULL", who);
   return verify_call(kv, q, h_q, n_cand, scale, out, lse, scores, scores_stride, nullptr, 0, kBlockTokens, ks, idx,
-                     k_max, cnt, workspace, workspace_bytes, stream, who);
+                     k_max, cnt, nullptr, 0, workspace, workspace_bytes, stream, who);
+}
+
+extern "C" int ssd_verify_select_packed(const ssd_paged_kv *kv, const void *q, int h_q, int n_cand, float scale,
+                                        float *out, float *lse, float *scores, int64_t scores_stride,
+                                        const int32_t *ks, int32_t *idx, int k_max, int32_t *cnt, void *pack,
+                                        size_t pack_bytes, void *workspace, size_t workspace_bytes,
+                                        ssd_stream_t stream) {
+  const char *who = "ssd_verify_select_packed";
+  if (!ks) return fail(SSD_ERR_INVALID_ARG, "%s: ks must be non-NULL", who);
+  if (!pack) return fail(SSD_ERR_INVALID_ARG, "%s: pack must be non-NULL", who);
+  return verify_call(kv, q, h_q, n_cand, scale, out, lse, scores, scores_stride, nullptr, 0, kBlockTokens, ks, idx,
+                     k_max, cnt, pack, pack_bytes, workspace, workspace_bytes, stream, who);
 }
 
 extern "C" size_t ssd_block_sparse_workspace_bytes(const ssd_paged_kv *kv, int h_q, int n_cand, int umax) {

@@ -49,6 +49,12 @@ struct FinalizeArgs {
   int32_t *sel_cnt;
   int sel_kmax;
   unsigned *sel_ctr;  // [units] arrivals of a unit's token blocks, in the counter area
+  // Row pack (nullptr: none): the selected tokens' K and V rows, stored where the draft's pack reader
+  // takes them ([unit][chunk of 64][K tile, V tile], rows in the draft's swizzled order).
+  char *pack;
+  int pack_cmax;  // chunks per unit
+  int esize;      // bytes per cache element
+  KVView kv;
   unsigned *status;
 };
 struct VerifyArgs {

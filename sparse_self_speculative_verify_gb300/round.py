@@ -21,7 +21,7 @@ from . import binding as B
 
 class SpecRound:
     def __init__(self, kv: B.KVCache, h_q: int, n_cand: int, k_max: int, scale: Optional[float] = None,
-                 workspace: Optional[B.Workspace] = None, pack_rows: bool = True):
+                 workspace: Optional[B.Workspace] = None, pack_rows: bool = True, pack_in_select: bool = False):
         self.kv = kv
         self.h_q = h_q
         self.n_cand = n_cand
@@ -37,8 +37,11 @@ class SpecRound:
         self.cnt = torch.empty((Bsz * hkv,), dtype=torch.int32, device=dev)
         self.out_d = torch.empty((Bsz, h_q, d), dtype=torch.float32, device=dev)
         self.lse_d = torch.empty((Bsz, h_q), dtype=torch.float32, device=dev)
-        # Row pack: the first draft after a selection stores the selected K / V rows contiguously,
-        # the later drafts of the round read them from there.
+        # Row pack: the selected K / V rows stored contiguously, by the first draft after a selection
+        # or (pack_in_select) by the fused verify-select itself; the other drafts of the round read
+        # them from there.  On the Qwen3-8B round the first draft's gather is the cheaper of the two
+        # (the criticality pass's copy lengthens the verify call by more than it saves the draft).
+        self.pack_in_select = pack_in_select
         self.pack = None
         if pack_rows:
             n = B.ssd_draft_pack_bytes(kv, k_max)
@@ -52,11 +55,14 @@ class SpecRound:
                                  scores=self.scores, workspace=self.ws, stream=stream)
 
     def verify_select(self, q_verify: torch.Tensor, k_per_req: torch.Tensor, stream=None):
-        """verify + select in one call: the selection runs inside the criticality pass."""
-        self._packed = False
-        return B.ssd_verify_select(self.kv, q_verify, self.n_cand, self.scale, k_per_req, self.k_max, out=self.out_v,
-                                   lse=self.lse_v, scores=self.scores, idx=self.idx, cnt=self.cnt, workspace=self.ws,
-                                   stream=stream)
+        """verify + select in one call: the selection runs inside the criticality pass, which also
+        stores the selected rows in the row pack (pack_in_select), so every draft reads it."""
+        pack = self.pack if self.pack_in_select else None
+        r = B.ssd_verify_select(self.kv, q_verify, self.n_cand, self.scale, k_per_req, self.k_max, out=self.out_v,
+                                lse=self.lse_v, scores=self.scores, idx=self.idx, cnt=self.cnt, pack=pack,
+                                workspace=self.ws, stream=stream)
+        self._packed = pack is not None
+        return r
 
     def select(self, k_per_req: torch.Tensor, stream=None):
         self._packed = False

@@ -11,10 +11,11 @@ the library proper for this process, runs ``ssd_verify_attn`` on a seeded worklo
 * per-item cost: the intercept of that fit, the time an item costs beyond its tiles;
 * tail: the spread of the blocks' exit times.
 
-Usage: ``python -m sparse_self_speculative_verify_gb300.trace_verify [workload] [--dump FILE.npz]``
+Usage: ``python -m sparse_self_speculative_verify_gb300.trace_verify [workload] [--dump FILE.npz] [--select]``
 with workload qwen3_8b (default), b128_l8k or qwen3_14b_unified (its verify-phase requests).  Prints
-a JSON line; ``--dump`` also saves the raw per-block, per-tile, masked-tile, epilogue, producer and softmax-stage records and the requests'
-lengths.
+a JSON line.  ``--select`` traces ``ssd_verify_select`` instead, as the benchmark's round calls it
+(its criticality pass's phases go into the dump).  ``--dump`` also saves the raw per-block, per-tile, masked-tile,
+epilogue, producer and softmax-stage records and the requests' lengths.
 """
 
 from __future__ import annotations
@@ -35,7 +36,7 @@ from . import workloads as W
 SLOTS, BLOCKS, ITEMS, TILES, MASKED = 128, 256, 40, 256, 16
 
 
-def run(name: str = "qwen3_8b", dump: str | None = None) -> dict:
+def run(name: str = "qwen3_8b", dump: str | None = None, select: bool = False) -> dict:
     L = Bd.load(libbuild.build(variant="trace"), as_default=True)
     L.ssd_verify_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
     L.ssd_verify_trace.restype = ctypes.c_int
@@ -51,9 +52,13 @@ def run(name: str = "qwen3_8b", dump: str | None = None) -> dict:
     scale = 1.0 / math.sqrt(spec.d)
     ws = Bd.Workspace()
     flush = W.flush_buffer(dev)
+    ks, k_max = w.k_per_req, int(w.k_per_req.max())
     for _ in range(4):
         flush.fill_(1.0)
-        Bd.ssd_verify_attn(kv, q, spec.n_cand, scale, workspace=ws)
+        if select:
+            Bd.ssd_verify_select(kv, q, spec.n_cand, scale, ks, k_max, workspace=ws)
+        else:
+            Bd.ssd_verify_attn(kv, q, spec.n_cand, scale, workspace=ws)
     torch.cuda.synchronize()
     assert Bd.ssd_status() == 0
     tr = np.zeros(BLOCKS * SLOTS, np.uint64)
@@ -81,7 +86,13 @@ def run(name: str = "qwen3_8b", dump: str | None = None) -> dict:
         L.ssd_verify_stage_trace.restype = ctypes.c_int
         ts = np.zeros(BLOCKS * 64 * 8, np.uint32)
         assert L.ssd_verify_stage_trace(ts.ctypes.data, ts.nbytes) == 0
-        np.savez(dump, trace=tr, producer=tp.reshape(BLOCKS, ITEMS, 4)[:nb], stage=ts.reshape(BLOCKS, 64, 8)[:nb], tiles=tt.reshape(BLOCKS, TILES, 12)[:nb], masked=tm.reshape(BLOCKS, MASKED, 8)[:nb],
+        cs = np.zeros(4096 * 8, np.uint64)
+        if select:
+            L.ssd_crit_select_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+            L.ssd_crit_select_trace.restype = ctypes.c_int
+            assert L.ssd_crit_select_trace(cs.ctypes.data, cs.nbytes) == 0
+        np.savez(dump, trace=tr, producer=tp.reshape(BLOCKS, ITEMS, 4)[:nb], stage=ts.reshape(BLOCKS, 64, 8)[:nb],
+                 crit_select=cs.reshape(4096, 8)[:kv.batch * kv.h_kv], tiles=tt.reshape(BLOCKS, TILES, 12)[:nb], masked=tm.reshape(BLOCKS, MASKED, 8)[:nb],
                  epilogue=te.reshape(BLOCKS, ITEMS, 4)[:nb],
                  seq_lens=kv.seq_lens.cpu().numpy(), h_kv=spec.h_kv, n_cand=spec.n_cand)
     entry, exit_, t0 = tr[:, 0], tr[:, 2], int(tr[:, 0].min())
@@ -122,8 +133,11 @@ def run(name: str = "qwen3_8b", dump: str | None = None) -> dict:
 if __name__ == "__main__":
     args = sys.argv[1:]
     out = None
+    sel = "--select" in args
+    if sel:
+        args.remove("--select")
     if "--dump" in args:
         i = args.index("--dump")
         out = args[i + 1]
         del args[i:i + 2]
-    print(json.dumps(run(args[0] if args else "qwen3_8b", out)))
+    print(json.dumps(run(args[0] if args else "qwen3_8b", out, sel)))

@@ -1,6 +1,7 @@
 """SpecRound's call sequence on the host (no GPU): with the row pack, the first draft after each
-selection writes the pack and the later drafts read it; without it, every draft is the plain call.
-The binding's calls are replaced by recorders, so only the sequencing is under test."""
+selection writes it (or, with pack_in_select, the fused verify-select does) and the other drafts
+read it; without it, every draft is the plain call.  The binding's calls are replaced
+by recorders, so only the sequencing is under test."""
 
 import torch
 
@@ -19,7 +20,10 @@ def _record(monkeypatch):
     calls = []
     monkeypatch.setattr(B, "ssd_draft_pack_bytes", lambda kv, k_max: 4096)
     monkeypatch.setattr(B, "ssd_verify_attn", lambda *a, **k: calls.append("verify"))
-    monkeypatch.setattr(B, "ssd_verify_select", lambda *a, **k: calls.append("verify_select"))
+    def verify_select(*a, pack=None, **k):
+        assert pack is None or (pack.data_ptr() % 256 == 0 and pack.numel() == 4096)
+        calls.append("verify_select" if pack is None else "verify_select+pack")
+    monkeypatch.setattr(B, "ssd_verify_select", verify_select)
     monkeypatch.setattr(B, "ssd_select_topk", lambda *a, **k: calls.append("select"))
     monkeypatch.setattr(B, "ssd_draft_attn", lambda *a, **k: calls.append("draft"))
 
@@ -51,6 +55,17 @@ def test_pack_written_once_per_selection(monkeypatch):
     r.select(ks)
     r.draft(qd[0])  # a new selection is written first
     assert calls == ["read", "select", "write"]
+
+
+def test_pack_written_by_the_select_when_asked(monkeypatch):
+    calls = _record(monkeypatch)
+    r = SpecRound(_KV(), h_q=4, n_cand=3, k_max=70, workspace=B.Workspace(), pack_in_select=True)
+    qv, qd, ks = _inputs()
+    r.run(qv, qd, ks, fused_select=True)
+    assert calls == ["verify_select+pack", "read", "read", "read"]
+    calls.clear()
+    r.run(qv, qd, ks)  # a separate select: the first draft writes the pack
+    assert calls == ["verify", "select", "write", "read", "read"]
 
 
 def test_without_pack_every_draft_is_plain(monkeypatch):
