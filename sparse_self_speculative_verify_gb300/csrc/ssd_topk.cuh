@@ -91,7 +91,18 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
     int rem = K;
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int t = lo + lane; t < hi; t += 32) {
+      // Four keys per lane are loaded before their atomics, so the loads of a lane overlap (the
+      // compiler cannot move them across the shared atomics itself).
+      int t = lo + lane;
+      for (; t + 96 < hi; t += 128) {
+        uint32_t k[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) k[j] = key(t + 32 * j);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((k[j] & mask) == prefix) atomicAdd(&sc.hist[warp][(k[j] >> shift) & 255u], 1u);
+      }
+      for (; t < hi; t += 32) {
         const uint32_t k = key(t);
         if ((k & mask) == prefix) atomicAdd(&sc.hist[warp][(k >> shift) & 255u], 1u);
       }
