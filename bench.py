@@ -330,7 +330,7 @@ def run_ours(args, spec, rank, world, local):
                 r.verify_select(l.q_verify, l.k_per_req)
         for j in range(spec.k):
             for r, l, o in zip(rounds, layers, outs):
-                r.draft(l.q_draft[j], out=o[j])
+                r.draft(l.q_draft[j], out=o[j], last=j == spec.k - 1)
 
     launches_per_step = args.layers * ((3 if args.separate_select else 2) + spec.k)
     with torch.cuda.stream(stream):

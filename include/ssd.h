@@ -222,9 +222,12 @@ int ssd_draft_attn(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t
  *               no index or page fault is raised.  cnt and k_max must equal that call's and the
  *               selected tokens' K / V must be unchanged since (appending new tokens is fine); a cnt
  *               that grew reads rows the pack does not hold (wrong values, never outside pack).
+ *               SSD_PACK_READ_DISCARD: SSD_PACK_READ, after which the pack's contents are undefined
+ *               (for the last draft of a round: a bf16 pack's lines are dropped from the L2 cache
+ *               without being written back to memory).  Write the pack again before the next read.
  * Entries of cnt outside [0, k_max] raise SSD_FAULT_KMAX in every mode.
  */
-enum ssd_pack_mode { SSD_PACK_NONE = 0, SSD_PACK_WRITE = 1, SSD_PACK_READ = 2 };
+enum ssd_pack_mode { SSD_PACK_NONE = 0, SSD_PACK_WRITE = 1, SSD_PACK_READ = 2, SSD_PACK_READ_DISCARD = 3 };
 size_t ssd_draft_pack_bytes(const ssd_paged_kv *kv, int k_max);
 int ssd_draft_attn_packed(const ssd_paged_kv *kv, const void *q, int h_q, const int32_t *idx, int k_max,
                           const int32_t *cnt, float scale, float *out, float *lse, void *pack, size_t pack_bytes,

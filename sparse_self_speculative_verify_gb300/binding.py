@@ -379,7 +379,7 @@ def ssd_draft_attn(kv: KVCache, q: torch.Tensor, idx: torch.Tensor, cnt: torch.T
     return {"out": out, "lse": lse}
 
 
-PACK_NONE, PACK_WRITE, PACK_READ = 0, 1, 2
+PACK_NONE, PACK_WRITE, PACK_READ, PACK_READ_DISCARD = 0, 1, 2, 3
 
 
 def ssd_draft_pack_bytes(kv: KVCache, k_max: int) -> int:
@@ -391,7 +391,9 @@ def ssd_draft_attn_packed(kv: KVCache, q: torch.Tensor, idx: Optional[torch.Tens
                           want_lse: bool = True, workspace: Optional[Workspace] = None, stream=None) -> dict:
     """ssd_draft_attn with a row pack: PACK_WRITE attends through idx and stores the selected rows in
     ``pack`` (a uint8 device tensor of ssd_draft_pack_bytes bytes, 256-byte aligned); PACK_READ
-    attends the rows stored by the last PACK_WRITE call (idx may be None; then k_max is required)."""
+    attends the rows stored by the last PACK_WRITE call (idx may be None; then k_max is required);
+    PACK_READ_DISCARD reads likewise and leaves the pack undefined (the round's last draft: its lines
+    leave L2 without being written back)."""
     _need(q, "q", kv.pool.dtype, kv.device)
     dev = kv.device
     if idx is not None:

@@ -120,8 +120,11 @@ static int draft_call(const ssd_paged_kv *kv, const void *q, int h_q, const int3
   KVView v;
   int rc = validate_kv(kv, &v, who);
   if (rc) return rc;
-  if (pack_mode != SSD_PACK_NONE && pack_mode != SSD_PACK_WRITE && pack_mode != SSD_PACK_READ)
+  if (pack_mode != SSD_PACK_NONE && pack_mode != SSD_PACK_WRITE && pack_mode != SSD_PACK_READ &&
+      pack_mode != SSD_PACK_READ_DISCARD)
     return fail(SSD_ERR_INVALID_ARG, "%s: pack_mode %d unknown", who, pack_mode);
+  const bool discard = pack_mode == SSD_PACK_READ_DISCARD;
+  if (discard) pack_mode = SSD_PACK_READ;  // a read, then the pack's lines are dropped
   if ((rc = draft_checks(kv, h_q, q, idx, k_max, cnt, out, who, pack_mode != SSD_PACK_READ))) return rc;
   const size_t need = ssd_draft_workspace_bytes(kv, h_q, k_max);
   if (!workspace || workspace_bytes < need)
@@ -155,6 +158,7 @@ static int draft_call(const ssd_paged_kv *kv, const void *q, int h_q, const int3
   a.status = status;
   a.pack = pack_mode != SSD_PACK_NONE ? static_cast<char *>(pack) : nullptr;
   a.pack_mode = pack_mode;
+  a.pack_discard = discard && kv->dtype == SSD_DTYPE_BF16 ? 1 : 0;  // the fp32 read keeps its lines
   draft_carve(static_cast<unsigned *>(workspace), static_cast<char *>(workspace) + kCounterBytes, units, C_max,
               draft_gmax(a.G), kv->d, a);
   if (pack_mode == SSD_PACK_READ && kv->dtype == SSD_DTYPE_BF16)

@@ -69,6 +69,7 @@ struct DraftArgs {
   int defer_wait;        // unified launch: see draft_kernel
   char *pack;            // row pack [units][C_max][2][TILE] (pack_mode != SSD_PACK_NONE)
   int pack_mode;         // SSD_PACK_NONE / SSD_PACK_WRITE (gather, then store the tiles) / SSD_PACK_READ
+  int pack_discard;      // SSD_PACK_READ_DISCARD: the pack reader drops the unit's pack lines from L2
   unsigned *status;
 };
 
@@ -799,6 +800,15 @@ __device__ __forceinline__ void draft_pack_unit(const DraftArgs &a, int unit, ch
     return;
   }
   pdl_trigger();
+  if (a.pack_discard) {
+    // The round's last read of the pack: its rows are in shared memory by now, so the unit's lines
+    // (the stored rows of every chunk, K and V tiles) leave L2 without being written back.
+    for (int c = 0; c < nch; ++c) {
+      const int lines = min(kDraftChunk, n_all - c * kDraftChunk) * C::ROWB / 128;
+      for (int e = tid; e < 2 * lines; e += blockDim.x)
+        discard_l2_line(pu + (int64_t)c * (2 * C::TILE) + (e >= lines ? C::TILE : 0) + (int64_t)(e % lines) * 128);
+    }
+  }
   W.merge_store(a, b, g, reinterpret_cast<float *>(smem), sWM, sWL);
 }
 

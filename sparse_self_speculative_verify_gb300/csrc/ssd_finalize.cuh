@@ -91,6 +91,15 @@ __device__ __forceinline__ void fin_combine_rows(const FinalizeArgs &f, int64_t 
   }
 }
 
+// Drops unit u's split partials (ns splits x R rows of D floats from row pbase, read for the last time
+// by this block's combine) from L2 without writing them back.  Threads tid < nt of the block, after a
+// barrier that follows the block's last read of them; every row starts 128-byte aligned.
+__device__ __forceinline__ void fin_discard_parts(const FinalizeArgs &f, int64_t pbase, int ns, int tid, int nt) {
+  const char *base = reinterpret_cast<const char *>(f.o_parts + pbase * f.D);
+  const int lines = ns * f.R * f.D * 4 / 128;
+  for (int e = tid; e < lines; e += nt) discard_l2_line(base + (int64_t)e * 128);
+}
+
 // Splits of unit u's request of length L, as the verify pass cut them.
 __device__ __forceinline__ int fin_splits(const FinalizeArgs &f, int u, int L) {
   return f.ucnt       ? block_splits(min(max(f.ucnt[u], 0), f.umax))

@@ -112,6 +112,10 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     const int tpr = f.D / 4, rpc = fin_rows_per_cta(f.D);
     const int n_comb = (int)gridDim.x - n_tok;
     fin_combine_rows(f, pbase, ns, sLn, b, g, ((int)blockIdx.x - n_tok) * rpc + tid / tpr, rpc * n_comb, tid % tpr);
+    if (n_comb == 1) {  // this block read every partial of the unit
+      __syncthreads();
+      fin_discard_parts(f, pbase, ns, tid, kFinThreads);
+    }
     return;
   }
 
@@ -270,6 +274,8 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
     pdl_trigger();
     const int tpr = f.D / 4;
     fin_combine_rows(f, pbase, ns, sLn, b, g, tid / tpr, kCsThreads / tpr, tid % tpr);
+    __syncthreads();
+    fin_discard_parts(f, pbase, ns, tid, kCsThreads);
     return;
   }
   fin_unit_scores<kCsThreads>(f, u, L, sL2, s_keys, tid);

@@ -77,20 +77,25 @@ class SpecRound:
             self.idx.view(self.kv.batch, self.kv.h_kv, self.k_max).copy_(idx)
             self.cnt.view(self.kv.batch, self.kv.h_kv).copy_(cnt)
 
-    def draft(self, q_draft: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None):
+    def draft(self, q_draft: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None, last: bool = False):
         """One draft over the current selection.  With the row pack, the first draft after a select
         stores the selected rows and the following ones read them (same results within the oracle
         tolerance).  The choice is made when the call is issued, so a captured CUDA graph keeps the
         choice of its capture: capture the drafts together with the selection (as ``run`` does), so
-        that the graph's first draft writes the pack on every replay."""
+        that the graph's first draft writes the pack on every replay.  ``last`` marks the round's last
+        draft: it reads the pack and then drops it from L2 unwritten, so the next draft writes it
+        again."""
         idx = self.idx.view(self.kv.batch, self.kv.h_kv, self.k_max)
         cnt = self.cnt.view(self.kv.batch, self.kv.h_kv)
         o = out if out is not None else self.out_d
         if self.pack is None:
             return B.ssd_draft_attn(self.kv, q_draft, idx, cnt, self.scale, out=o, lse=self.lse_d, workspace=self.ws,
                                     stream=stream)
-        mode = B.PACK_READ if self._packed else B.PACK_WRITE
-        self._packed = True
+        if not self._packed:
+            mode = B.PACK_WRITE
+        else:
+            mode = B.PACK_READ_DISCARD if last else B.PACK_READ
+        self._packed = not (self._packed and last)
         return B.ssd_draft_attn_packed(self.kv, q_draft, idx, cnt, self.scale, self.pack, mode, out=o, lse=self.lse_d,
                                        workspace=self.ws, stream=stream)
 
@@ -134,5 +139,7 @@ class SpecRound:
         else:
             self.verify(q_verify, stream)
             self.select(k_per_req, stream)
-        for j in range(q_drafts.shape[0]):
-            self.draft(q_drafts[j], out=None if draft_outs is None else draft_outs[j], stream=stream)
+        k = q_drafts.shape[0]
+        for j in range(k):
+            self.draft(q_drafts[j], out=None if draft_outs is None else draft_outs[j], stream=stream,
+                       last=j == k - 1)

@@ -136,7 +136,7 @@ def test_draft_pack_sizes_and_argument_errors(lib):
     def call(idx, pack, pack_bytes, mode):
         return lib.ssd_draft_attn_packed(ctypes.byref(kv), 16, 32, idx, 410, 16, 0.1, 16, None, pack, pack_bytes, mode,
                                          1 << 20, 1 << 40, None)
-    assert call(16, 1 << 21, need, 3) == E            # unknown mode
+    assert call(16, 1 << 21, need, 4) == E            # unknown mode (3 is SSD_PACK_READ_DISCARD)
     assert call(None, 1 << 21, need, 1) == E          # writing the pack reads idx
     assert call(16, 1 << 21, need - 1, 1) == W        # pack too small
     assert call(None, None, need, 2) == W             # no pack to read

@@ -76,9 +76,12 @@ def test_pack_write_then_reads_equal_plain_drafts(case):
     got = [ssd_draft_attn_packed(kv, qs[0], idx, cnt, scale, pack, binding.PACK_WRITE)]
     for j in (1, 2):
         got.append(ssd_draft_attn_packed(kv, qs[j], None, cnt, scale, pack, binding.PACK_READ, k_max=k_max))
+    # The round's last read drops the pack from L2 afterwards: same results as a plain read.
+    last = ssd_draft_attn_packed(kv, qs[2], None, cnt, scale, pack, binding.PACK_READ_DISCARD, k_max=k_max)
     ref = [ssd_draft_attn(kv, qs[j], idx, cnt, scale) for j in range(3)]
     torch.cuda.synchronize()
     assert ssd_status() == 0
+    assert torch.equal(last["out"], got[2]["out"]) and torch.equal(last["lse"], got[2]["lse"])
     assert torch.equal(got[0]["out"], ref[0]["out"]) and torch.equal(got[0]["lse"], ref[0]["lse"])
     kv_h, reqs = _gpu.host_subset(w, None)
     for j in (1, 2):

@@ -1,6 +1,6 @@
 """SpecRound's call sequence on the host (no GPU): with the row pack, the first draft after each
-selection writes it (or, with pack_in_select, the fused verify-select does) and the other drafts
-read it; without it, every draft is the plain call.  The binding's calls are replaced
+selection writes it (or, with pack_in_select, the fused verify-select does), the other drafts read
+it and the round's last draft drops it; without it, every draft is the plain call.  The binding's calls are replaced
 by recorders, so only the sequencing is under test."""
 
 import torch
@@ -29,7 +29,7 @@ def _record(monkeypatch):
 
     def packed(kv, q, idx, cnt, scale, pack, mode, **k):
         assert pack.data_ptr() % 256 == 0 and pack.numel() == 4096
-        calls.append("write" if mode == B.PACK_WRITE else "read" if mode == B.PACK_READ else "?")
+        calls.append({B.PACK_WRITE: "write", B.PACK_READ: "read", B.PACK_READ_DISCARD: "read+drop"}.get(mode, "?"))
     monkeypatch.setattr(B, "ssd_draft_attn_packed", packed)
     return calls
 
@@ -46,15 +46,16 @@ def test_pack_written_once_per_selection(monkeypatch):
     r = SpecRound(_KV(), h_q=4, n_cand=3, k_max=70, workspace=B.Workspace())
     qv, qd, ks = _inputs()
     r.run(qv, qd, ks)
-    assert calls == ["verify", "select", "write", "read", "read"]
+    assert calls == ["verify", "select", "write", "read", "read+drop"]  # the round's last draft drops it
     calls.clear()
     r.run(qv, qd, ks, fused_select=True)
-    assert calls == ["verify_select", "write", "read", "read"]
+    assert calls == ["verify_select", "write", "read", "read+drop"]
     calls.clear()
-    r.draft(qd[0])  # another draft on the same selection reads the pack
+    r.draft(qd[0])  # another draft after the round: the pack was dropped, so it is written again
+    r.draft(qd[0])  # and read by the next one
     r.select(ks)
     r.draft(qd[0])  # a new selection is written first
-    assert calls == ["read", "select", "write"]
+    assert calls == ["write", "read", "select", "write"]
 
 
 def test_pack_written_by_the_select_when_asked(monkeypatch):
@@ -62,10 +63,10 @@ def test_pack_written_by_the_select_when_asked(monkeypatch):
     r = SpecRound(_KV(), h_q=4, n_cand=3, k_max=70, workspace=B.Workspace(), pack_in_select=True)
     qv, qd, ks = _inputs()
     r.run(qv, qd, ks, fused_select=True)
-    assert calls == ["verify_select+pack", "read", "read", "read"]
+    assert calls == ["verify_select+pack", "read", "read", "read+drop"]
     calls.clear()
     r.run(qv, qd, ks)  # a separate select: the first draft writes the pack
-    assert calls == ["verify", "select", "write", "read", "read"]
+    assert calls == ["verify", "select", "write", "read", "read+drop"]
 
 
 def test_without_pack_every_draft_is_plain(monkeypatch):
