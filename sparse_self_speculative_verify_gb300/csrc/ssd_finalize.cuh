@@ -103,7 +103,7 @@ __device__ __forceinline__ void fin_discard_parts(const FinalizeArgs &f, int64_t
 // Splits of unit u's request of length L, as the verify pass cut them.
 __device__ __forceinline__ int fin_splits(const FinalizeArgs &f, int u, int L) {
   return f.ucnt       ? block_splits(min(max(f.ucnt[u], 0), f.umax))
-         : f.balanced ? tc_split_count(L, *f.split_len)
+         : f.balanced ? tc_split_count(L, tc_tail_split(f.split_len[0], u / f.h_kv, f.split_len[1]))
                       : verify_splits(L, f.split_len ? *f.split_len : kSplitTokens);
 }
 

@@ -155,7 +155,7 @@ static UniLayout uni_layout(const ssd_paged_kv *kv, int h_q, int n_cand, int k_m
   l.v_sm = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
   l.split_off = c.off;
-  c.take<int>(1);
+  c.take<int>(2);  // split length, first request of the half-length tail
   l.d_off = c.off;
   l.total = l.d_off + draft_data_bytes(l.units, l.C_max, l.gmax, kv->d);
   return l;

@@ -406,7 +406,7 @@ static VerifyLayout verify_layout(const ssd_paged_kv *kv, int h_q, int n_cand, i
   l.sm_off = c.off;
   c.take<float>((size_t)l.units * l.R * (l.Lpad / kRefGroup));
   l.split_off = c.off;
-  c.take<int>(1);
+  c.take<int>(2);  // split length, first request of the half-length tail
   l.total = c.off;
   return l;
 }

@@ -162,7 +162,7 @@ __device__ __forceinline__ uint32_t bar_addr(uint64_t *b) { return smem_u32(b); 
 
 // Item -> (request, head, split): items of request b are pre[b] .. pre[b+1]-1, ordered (head, split).
 __device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int *len, int B, const VerifyArgs &a,
-                                           int split_len) {
+                                           int split_len, int tail_from) {
   int lo = 0, hi = B;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
@@ -175,7 +175,7 @@ __device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int 
   it.g = r / ns;
   it.split = r % ns;
   it.L = len[lo];
-  tc_split_range(it.L, split_len, it.split, it.t0, it.t1);
+  tc_split_range(it.L, tc_tail_split(split_len, lo, tail_from), it.split, it.t0, it.t1);
   it.ntiles = cdiv(it.t1 - it.t0, kTcTile);
   return it;
 }
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_wait();
 
   // Per-request lengths, the split length, item counts and their prefix (chunked block scan).
-  int split_len;
+  int split_len, tail_from;  // the batch's split length; requests from tail_from on get half-length splits
   {
     constexpr int CH = cdiv(kTcMaxBatch + 1, kTcThreads);
     int loc[CH];
@@ -412,29 +412,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       long long per = total * h_kv / ((long long)gridDim.x * kTcItemsPerBlock) / kTcTile * kTcTile;
       split_len = (int)min(max(per, (long long)kSplitTokens), (long long)kTcMaxSplit);
     }
-    if (blockIdx.x == 0 && tid == 0) *a.split_out = split_len;
-    int sum = 0;
+    // Item counts and their prefix, in two passes: the first with the batch's split length for every
+    // request finds the tail (the shortest suffix of requests whose items fit in one wave of blocks),
+    // the second cuts the tail's requests into half-length splits (tc_tail_split).
+    int lens[CH];
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      loc[k] = h_kv * tc_split_count(loc[k], split_len);
-      sum += loc[k];
+    for (int k = 0; k < CH; ++k) lens[k] = loc[k];
+    __shared__ int s_tail;
+    tail_from = B;
+    for (int pass = 0; pass < 2; ++pass) {
+      int sum = 0;
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        loc[k] = h_kv * tc_split_count(lens[k], tc_tail_split(split_len, tid * CH + k, tail_from));
+        sum += loc[k];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) s_wsum[warp] = incl;
+      __syncthreads();
+      int off = 0;
+      for (int w = 0; w < warp; ++w) off += s_wsum[w];
+      off += incl - sum;
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        const int b = tid * CH + k;
+        if (b <= B) s.pre[b] = off;
+        off += loc[k];
+      }
+      __syncthreads();
+      if (pass == 1) break;
+      // The first b whose suffix of items is at most one per block (b = B qualifies: exactly one does).
+      const int total_items = s.pre[B];
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        const int b = tid * CH + k;
+        if (b <= B && total_items - s.pre[b] <= (int)gridDim.x && (b == 0 || total_items - s.pre[b - 1] > (int)gridDim.x))
+          s_tail = b;
+      }
+      __syncthreads();
+      tail_from = s_tail;
+      __syncthreads();  // every thread has read s.pre before the second pass rewrites it
     }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    __syncthreads();
-    int off = 0;
-    for (int w = 0; w < warp; ++w) off += s_wsum[w];
-    off += incl - sum;
-#pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      const int b = tid * CH + k;
-      if (b <= B) s.pre[b] = off;
-      off += loc[k];
+    if (blockIdx.x == 0 && tid == 0) {
+      a.split_out[0] = split_len;
+      a.split_out[1] = tail_from;
     }
     __syncthreads();
   }
@@ -476,7 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       nxt = min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items);
     }
     TcItem it_cur{};
-    if (cur < n_items) it_cur = tc_decode(cur, s.pre, s.len, B, a, split_len);
+    if (cur < n_items) it_cur = tc_decode(cur, s.pre, s.len, B, a, split_len, tail_from);
     int32_t pid_cur[kPidRegs];
     load_pids(it_cur, cur < n_items, pid_cur);
     const int boxes_per_tile = kTcTile / box_rows;
@@ -556,7 +582,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (k == 0) {
           // Look-ahead (see above): the next item, decoded, with its page ids and the draw after it.
-          if (nxt < n_items) it_nx = tc_decode(nxt, s.pre, s.len, B, a, split_len);
+          if (nxt < n_items) it_nx = tc_decode(nxt, s.pre, s.len, B, a, split_len, tail_from);
           load_pids(it_nx, nxt < n_items, pid_nx);
           if (nxt < n_items && lane == 0) raw = atomicAdd(a.sched, 1);
         }

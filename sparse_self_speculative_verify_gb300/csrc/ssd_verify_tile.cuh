@@ -32,7 +32,8 @@ struct FinalizeArgs {
   const __half *side_p;   // [units][R][Lpad]
   const float *side_m;    // [units][R][Lpad / kRefGroup]
   const int32_t *ucnt;    // block-sparse pass: splits per unit from the union size
-  const int *split_len;   // split length the verify wrote (tensor-core, fp32 paths); nullptr = kSplitTokens
+  const int *split_len;   // split length the verify wrote (tensor-core, fp32 paths); nullptr = kSplitTokens;
+                          // tensor-core path: [1] holds the first request of the half-length tail
   int balanced;           // splits cut by tc_split_count (the tensor-core verify), else cdiv(L, split length)
   const uint8_t *phase;   // unified launch: units of draft-phase requests are skipped
   int umax;
@@ -76,7 +77,8 @@ struct VerifyArgs {
   unsigned *status;
   int *sched;  // [2] in the counter area: next-item counter and finished-block count (tensor-core
                // path); zero at launch, and the last block to finish returns both to zero
-  int *split_out;  // tensor-core and fp32 paths: receives the split length used (read by the finalize)
+  int *split_out;  // tensor-core and fp32 paths: receives the split length used (read by the finalize);
+                   // tensor-core path: [1] the first request cut into half-length splits
   const uint8_t *phase;  // tensor-core path: nullptr, or only requests with phase[b] == 1 get items
   int early_trigger;     // tensor-core path: let the next kernel launch at once (see ssd_unified.cu)
 };
@@ -106,6 +108,13 @@ __device__ __forceinline__ int verify_splits(int L, int split = kSplitTokens) { 
 // short one, so a split of one to three tiles costs about as much as one of ten.
 constexpr int kTcTileTokens = 128;
 constexpr int kTcMaxSplitTiles = 16;
+// Split length of request b: the requests whose items are handed out last (b >= tail_from: the shortest
+// suffix of the batch whose items fit in one wave of blocks) get splits of half the length (whole tiles,
+// at least kSplitTokens), so the last items of a launch are short and the blocks run out of work
+// closer together.
+__device__ __forceinline__ int tc_tail_split(int split_len, int b, int tail_from) {
+  return b < tail_from ? split_len : max(kSplitTokens, split_len / 2 / kTcTileTokens * kTcTileTokens);
+}
 __device__ __forceinline__ int tc_split_count(int L, int split_len) {
   const int T = cdiv(L, kTcTileTokens);
   if (T <= 0) return 0;
