@@ -7,8 +7,9 @@
 // and the hierarchical layout representation: the candidates' block sets are merged into one
 // ordered union with a per-block candidate mask.
 //
-// One block selects one row with topk_row (ssd_topk.cuh: exact radix select, ties to the lower
-// index, output sorted).
+// One block selects one row with topk_row_smem (a row staged in shared memory) or topk_row (a longer
+// row read from global memory); ssd_topk.cuh: exact radix select, ties to the lower index, output
+// sorted.
 #include "ssd_host.h"
 #include "ssd_topk.cuh"
 
@@ -36,6 +37,7 @@ template <bool IN_SMEM>
 __global__ void __launch_bounds__(kSelThreads) topk_kernel(TopkArgs p) {
   extern __shared__ uint32_t s_keys[];
   __shared__ TopkScratch<kSelThreads> sc;
+  __shared__ uint32_t s_cand[kTopkCand];
   const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
   const int grp = (int)(row / p.rows_per_group);
@@ -55,13 +57,23 @@ __global__ void __launch_bounds__(kSelThreads) topk_kernel(TopkArgs p) {
   const float *src = p.scores + row * p.stride;
   int32_t *out = p.idx + row * p.k_max;
   if (IN_SMEM) {
-    for (int t = tid; t < n; t += kSelThreads) s_keys[t] = score_key(src[t]);
+    // The keys, and the histogram of their top 12 bits that the selection starts from.
+    for (int e = tid; e < kSelWarps * 256; e += kSelThreads) (&sc.hist[0][0])[e] = 0u;
+    __syncthreads();
+    for (int t = tid; t < n; t += kSelThreads) {
+      const uint32_t k = score_key(src[t]);
+      s_keys[t] = k;
+      topk_h12_add(&sc.hist[0][0], k);
+    }
     __syncthreads();
   }
   auto key = [&](int t) -> uint32_t { return IN_SMEM ? s_keys[t] : score_key(__ldg(src + t)); };
 
   pdl_trigger();
-  topk_row<kSelThreads>(key, n, K, out, p.k_max, sc);
+  if (IN_SMEM)
+    topk_row_smem<kSelThreads>(s_keys, n, K, out, p.k_max, sc, s_cand, true);
+  else
+    topk_row<kSelThreads>(key, n, K, out, p.k_max, sc);
   if (tid == 0) p.cnt[row] = K;
 }
 

@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     K = f.sel_kmax;
   }
   const float *row = f.scores + (int64_t)u * f.scores_stride;
+  static_assert(sizeof(s_coef) >= sizeof(TopkScratch<kFinThreads>), "selection scratch");
   auto &sc = *reinterpret_cast<TopkScratch<kFinThreads> *>(s_coef);
   topk_row<kFinThreads>([&](int t) -> uint32_t { return score_key(__ldcg(row + t)); }, L, K,
                         f.sel_idx + (int64_t)u * f.sel_kmax, f.sel_kmax, sc);
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
 // u = blockIdx.x merges its split LSEs, rematerialises its row of scores from the side values with
 // exactly the finalize's arithmetic (same coefficients, rows summed in the same order, so the same
 // bits), writes the row out and keeps its keys in shared memory, then selects its Top-K from there
-// (topk_row: ties to the lower index, ascending output).  Blocks [units, 2 units): the combine of
+// (topk_row_smem: ties to the lower index, ascending output).  Blocks [units, 2 units): the combine of
 // unit blockIdx.x - units.  One pass over the side values replaces the finalize's token blocks,
 // the separate select launch and its read of the scores.
 // ------------------------------------------------------------------------------------------------
@@ -234,9 +235,12 @@ constexpr int kCsSmemRow = 40960;  // longest row kept in shared memory (160 KB 
 
 #ifdef SSD_VERIFY_TRACE
 // Diagnostic build: per unit-block of the criticality pass, global-timer stamps [0] entry, [1] past the
-// wait for the verify, [2] LSE merge done, [3] scores done, [4] Top-K done, [5] row pack done.
+// wait for the verify, [2] LSE merge done, [3] scores done, [4] Top-K done, [5] row pack done, [6] side
+// values dropped from L2; and the Top-K's phases: [8] histogram of the keys' top 12 bits, [9] threshold
+// bin found, [10] tau found, [11] indices written.
 constexpr int kCsTraceUnits = 4096;
-__device__ unsigned long long g_cs_trace[kCsTraceUnits * 8];
+constexpr int kCsTraceSlots = 16;
+__device__ unsigned long long g_cs_trace[kCsTraceUnits * kCsTraceSlots];
 __device__ __forceinline__ unsigned long long cs_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -244,7 +248,7 @@ __device__ __forceinline__ unsigned long long cs_ns() {
 }
 #define CS_STAMP(k) \
   do {              \
-    if (tid == 0 && u < kCsTraceUnits) g_cs_trace[u * 8 + (k)] = cs_ns(); \
+    if (tid == 0 && u < kCsTraceUnits) g_cs_trace[u * kCsTraceSlots + (k)] = cs_ns(); \
   } while (0)
 #else
 #define CS_STAMP(k) \
@@ -252,10 +256,11 @@ __device__ __forceinline__ unsigned long long cs_ns() {
   } while (0)
 #endif
 
-__global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f, int units) {
+__global__ void __launch_bounds__(kCsThreads, 2) crit_select_kernel(FinalizeArgs f, int units) {
   extern __shared__ __align__(16) uint32_t s_keys[];  // [max_seq_len] keys of the unit's scores
   __shared__ float sLn[kMaxRows], sL2[kMaxRows];
   __shared__ TopkScratch<kCsThreads> sc;
+  __shared__ uint32_t s_cand[kTopkCand];
   const int tid = threadIdx.x;
   const bool comb = (int)blockIdx.x >= units;
   const int u = comb ? (int)blockIdx.x - units : (int)blockIdx.x;
@@ -282,21 +287,14 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
   pdl_trigger();
   __syncthreads();
   CS_STAMP(3);
-  // The unit's side values have been read for the last time: drop their L2 lines unwritten (each row
-  // of the unit starts 256-byte aligned; the verify wrote whole 128-token tiles).
-  if (f.side_p) {
-    const int lines = cdiv(L, kSideAlign) * kSideAlign / 64;  // 64 fp16 per 128-byte line
-    for (int e = tid; e < f.R * lines; e += kCsThreads)
-      discard_l2_line(f.side_p + ((int64_t)u * f.R + e / lines) * f.Lpad + (e % lines) * 64);
-  }
   int K = f.ks[b];
   K = K < 0 ? 0 : (K > L ? L : K);
   if (K > f.sel_kmax) {
     if (tid == 0) atomicOr(f.status, (unsigned)SSD_FAULT_KMAX);
     K = f.sel_kmax;
   }
-  topk_row<kCsThreads>([&](int t) -> uint32_t { return s_keys[t]; }, L, K, f.sel_idx + (int64_t)u * f.sel_kmax,
-                       f.sel_kmax, sc);
+  topk_row_smem<kCsThreads>(s_keys, L, K, f.sel_idx + (int64_t)u * f.sel_kmax, f.sel_kmax, sc, s_cand, false,
+                            [&](int k) { CS_STAMP(8 + k); });
   if (tid == 0) f.sel_cnt[u] = K;
   CS_STAMP(4);
   if (f.pack) {
@@ -305,6 +303,15 @@ __global__ void __launch_bounds__(kCsThreads) crit_select_kernel(FinalizeArgs f,
     pack_unit_rows<kCsThreads>(f, u, K, tid, reinterpret_cast<int64_t *>(&sc));
   }
   CS_STAMP(5);
+  // The unit's side values were read for the last time before the Top-K: drop their L2 lines unwritten
+  // (each row of the unit starts 256-byte aligned; the verify wrote whole 128-token tiles).  Issued
+  // last, so that no barrier of the block waits for them.
+  if (f.side_p) {
+    const int lines = cdiv(L, kSideAlign) * kSideAlign / 64;  // 64 fp16 per 128-byte line
+    for (int e = tid; e < f.R * lines; e += kCsThreads)
+      discard_l2_line(f.side_p + ((int64_t)u * f.R + e / lines) * f.Lpad + (e % lines) * 64);
+  }
+  CS_STAMP(6);
 }
 
 #ifdef SSD_VERIFY_TRACE

@@ -136,8 +136,8 @@ struct TcCfg {
   static constexpr int OFF_Q = OFF_P + 2 * P_BYTES;
   static constexpr int OFF_MISC = OFF_Q + 2 * Q_BYTES;
   // misc: 48 mbarriers, flags and the item ring (numbers, then decoded), per-row arrays, reduction
-  // scratch, the per-request item prefix and lengths
-  static constexpr int MISC = 48 * 8 + 128 + kTcItemRing * 32 + NP * 4 * 2 + 2 * 4 * 32 * 4 + (2 * kTcMaxBatch + 1) * 4;
+  // scratch, the per-request item prefix, lengths and split shapes
+  static constexpr int MISC = 48 * 8 + 128 + kTcItemRing * 32 + NP * 4 * 2 + 2 * 4 * 32 * 4 + (3 * kTcMaxBatch + 1) * 4;
   static constexpr int SMEM = OFF_MISC + MISC + 1024;
 };
 
@@ -156,26 +156,36 @@ struct TcSmem {
   float *mref, *alpha, *red;  // red: [2 groups][4 warps][32]
   int *pre;  // [B+1] item prefix per request
   int *len;  // [B] clamped sequence lengths
+  int *nsx;  // [B] splits per unit | tiles per split (before the remainder) << 16
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint64_t *b) { return smem_u32(b); }
 
-// Item -> (request, head, split): items of request b are pre[b] .. pre[b+1]-1, ordered (head, split).
-__device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int *len, int B, const VerifyArgs &a,
-                                           int split_len, int tail_from) {
-  int lo = 0, hi = B;
+// Item -> (request, head, split): items of request b are pre[b] .. pre[b+1]-1, ordered (head, split);
+// nsx[b] holds request b's splits per unit (low 16 bits) and tiles per split before the remainder
+// (high bits), as tc_split_range cuts them.  Called by a whole warp (warp-uniform item): a 32-ary
+// search over pre (one shared load and one ballot per round), then one division.
+__device__ __forceinline__ TcItem tc_decode(int item, const int *pre, const int *len, const int *nsx, int B) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = B;  // request b in [lo, hi) with pre[b] <= item < pre[b + 1]
   while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (pre[mid] <= item) lo = mid; else hi = mid;
+    const int step = cdiv(hi - lo, 32);
+    const int idx = lo + (lane + 1) * step;
+    const bool le = idx < hi && pre[idx] <= item;
+    lo += __popc(__ballot_sync(0xffffffffu, le)) * step;
+    hi = min(lo + step, hi);
   }
   TcItem it;
   it.b = lo;
   const int r = item - pre[lo];
-  const int ns = (pre[lo + 1] - pre[lo]) / a.kv.h_kv;
+  const int x = nsx[lo], ns = x & 0xffff, base = x >> 16;
   it.g = r / ns;
-  it.split = r % ns;
+  it.split = r - it.g * ns;
   it.L = len[lo];
-  tc_split_range(it.L, tc_tail_split(split_len, lo, tail_from), it.split, it.t0, it.t1);
+  const int T = cdiv(it.L, kTcTile), extra = T - base * ns;
+  const int first = it.split * base + min(it.split, extra);
+  it.t0 = first * kTcTile;
+  it.t1 = min((first + base + (it.split < extra ? 1 : 0)) * kTcTile, it.L);
   it.ntiles = cdiv(it.t1 - it.t0, kTcTile);
   return it;
 }
@@ -333,6 +343,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s.red = s.alpha + NP;  // 16-byte aligned (float4 reads)
     s.pre = reinterpret_cast<int *>(s.red + 2 * 4 * 32);
     s.len = s.pre + kTcMaxBatch + 1;
+    s.nsx = s.len + kTcMaxBatch;
   }
 
   // Set-up that reads nothing an earlier kernel writes runs before the wait for the previous grid:
@@ -424,8 +435,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int sum = 0;
 #pragma unroll
       for (int k = 0; k < CH; ++k) {
-        loc[k] = h_kv * tc_split_count(lens[k], tc_tail_split(split_len, tid * CH + k, tail_from));
+        const int b = tid * CH + k, sl = tc_tail_split(split_len, b, tail_from);
+        const int ns = tc_split_count(lens[k], sl);
+        loc[k] = h_kv * ns;
         sum += loc[k];
+        if (pass == 1 && b < B && ns > 0) s.nsx[b] = ns | (cdiv(lens[k], kTcTile) / ns) << 16;
       }
       int incl = sum;
 #pragma unroll
@@ -491,18 +505,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     };
     // Work distribution: the block's first item is blockIdx.x, every later one is drawn from a global
-    // counter (items gridDim.x, gridDim.x + 1, ...), so blocks that run ahead take more items.  Item
-    // j+1 is decoded, its page ids requested and the draw for item j+2 issued right after item j's
-    // first tile, so none of it (the decode's search and divisions, the loads, the atomic) sits at an
-    // item boundary, where the ring would drain.  Lane 0 holds the raw draws.
+    // counter (items gridDim.x, gridDim.x + 1, ...), so blocks that run ahead take more items.  The
+    // draw for item j+1 is issued after the loads of item j's fourth tile from the end, and item j+1
+    // is decoded (tc_decode: a few hundred cycles) and its page ids requested after the loads of its
+    // second tile from the end: none of it sits at an item boundary, where the ring would drain, the
+    // atomic has two tiles to return, and a block holds a drawn item only for the last tiles of the
+    // current one, so the blocks run out of work close together.  Lane 0 holds the raw draw.
     int cur = blockIdx.x;
-    int nxt = n_items, raw = 0;
-    if (cur < n_items) {
-      if (lane == 0) raw = atomicAdd(a.sched, 1);
-      nxt = min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items);
-    }
+    int raw = 0;
     TcItem it_cur{};
-    if (cur < n_items) it_cur = tc_decode(cur, s.pre, s.len, B, a, split_len, tail_from);
+    if (cur < n_items) it_cur = tc_decode(cur, s.pre, s.len, s.nsx, B);
     int32_t pid_cur[kPidRegs];
     load_pids(it_cur, cur < n_items, pid_cur);
     const int boxes_per_tile = kTcTile / box_rows;
@@ -522,6 +534,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const TcItem it = it_cur;
       TcItem it_nx{};
       int32_t pid_nx[kPidRegs];
+      int nxt = n_items;
+      const int k_draw = max(0, it.ntiles - 4), k_next = min(it.ntiles - 1, max(k_draw + 2, it.ntiles - 2));
       SSD_TRACE(if (lane == 0 && jl < kTraceItems) TP[jl * 4 + 1] = (unsigned)(clock64() - clk0));
       // Query rows of this item: one 4-D TMA box per 64-column panel (d x 1 x G heads x n_c
       // candidates lands as rows r = i*G + h, 128-byte swizzled); rows >= R stay zero.
@@ -580,20 +594,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (kv == 0) ++nk; else ++nv;
         }
-        if (k == 0) {
-          // Look-ahead (see above): the next item, decoded, with its page ids and the draw after it.
-          if (nxt < n_items) it_nx = tc_decode(nxt, s.pre, s.len, B, a, split_len, tail_from);
+        // Look-ahead (see above): the draw, then the drawn item decoded with its page ids.
+        if (k == k_draw && lane == 0) raw = atomicAdd(a.sched, 1);
+        if (k == k_next) {
+          nxt = min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items);
+          if (nxt < n_items) it_nx = tc_decode(nxt, s.pre, s.len, s.nsx, B);
           load_pids(it_nx, nxt < n_items, pid_nx);
-          if (nxt < n_items && lane == 0) raw = atomicAdd(a.sched, 1);
         }
       }
       SSD_TRACE(if (lane == 0 && jl < kTraceItems) TP[jl * 4 + 3] = (unsigned)(clock64() - clk0));
-      const bool drew = nxt < n_items;
       it_cur = it_nx;
 #pragma unroll
       for (int h = 0; h < kPidRegs; ++h) pid_cur[h] = pid_nx[h];
       cur = nxt;
-      nxt = drew ? min((int)gridDim.x + __shfl_sync(0xffffffffu, raw, 0), n_items) : n_items;
     }
     // The block has taken its last item: the next kernel on the stream may begin launching.
     pdl_trigger();
@@ -1021,8 +1034,9 @@ static EncodeTiledFn encode_fn() {
 }
 
 bool verify_tc_supported(const ssd_paged_kv *kv, int R) {
+  // max_seq_len below 2^24 keeps a unit's split count within the 16 bits the item decode stores it in.
   return kv->dtype == SSD_DTYPE_BF16 && kv->d == 128 && kv->page_size >= 8 && R <= 64 && kv->batch <= kTcMaxBatch &&
-         (int64_t)kv->num_pages * 2 * kv->h_kv * kv->page_size < (1ll << 31);
+         kv->max_seq_len < (1 << 24) && (int64_t)kv->num_pages * 2 * kv->h_kv * kv->page_size < (1ll << 31);
 }
 
 template <int NP>

@@ -86,13 +86,13 @@ def run(name: str = "qwen3_8b", dump: str | None = None, select: bool = False) -
         L.ssd_verify_stage_trace.restype = ctypes.c_int
         ts = np.zeros(BLOCKS * 64 * 8, np.uint32)
         assert L.ssd_verify_stage_trace(ts.ctypes.data, ts.nbytes) == 0
-        cs = np.zeros(4096 * 8, np.uint64)
+        cs = np.zeros(4096 * 16, np.uint64)
         if select:
             L.ssd_crit_select_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
             L.ssd_crit_select_trace.restype = ctypes.c_int
             assert L.ssd_crit_select_trace(cs.ctypes.data, cs.nbytes) == 0
         np.savez(dump, trace=tr, producer=tp.reshape(BLOCKS, ITEMS, 4)[:nb], stage=ts.reshape(BLOCKS, 64, 8)[:nb],
-                 crit_select=cs.reshape(4096, 8)[:kv.batch * kv.h_kv], tiles=tt.reshape(BLOCKS, TILES, 12)[:nb], masked=tm.reshape(BLOCKS, MASKED, 8)[:nb],
+                 crit_select=cs.reshape(4096, 16)[:kv.batch * kv.h_kv], tiles=tt.reshape(BLOCKS, TILES, 12)[:nb], masked=tm.reshape(BLOCKS, MASKED, 8)[:nb],
                  epilogue=te.reshape(BLOCKS, ITEMS, 4)[:nb],
                  seq_lens=kv.seq_lens.cpu().numpy(), h_kv=spec.h_kv, n_cand=spec.n_cand)
     entry, exit_, t0 = tr[:, 0], tr[:, 2], int(tr[:, 0].min())

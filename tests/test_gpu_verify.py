@@ -113,3 +113,15 @@ def test_verify_full_size_sampled(name):
     r = _run(w)
     B = spec.batch
     _compare(w, r, reqs=[0, B // 3, B - 1])
+
+
+def test_verify_many_short_requests():
+    """300 ragged requests of 5 to 700 tokens (some a single tile, some one split of several): the
+    verify's item decode searches the per-request item prefix in more than one round.  Every request
+    against the oracle."""
+    rng = np.random.default_rng(17)
+    lens = [int(x) for x in rng.integers(5, 701, 300)]
+    lens[:4] = [5, 128, 129, 700]
+    spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="many", batch=len(lens))
+    w = W.make_workload(spec, seed=23, device=DEV, lengths=lens)
+    _compare(w, _run(w))
