@@ -107,7 +107,7 @@ constexpr int kTcItemRing = 8;  // item numbers handed from the producer to the 
 // Split length: each item ends with an epilogue and a pipeline refill that cost a few thousand
 // cycles, so items are made as long as load balance allows: about kTcItemsPerBlock items per block
 // over the batch's actual tokens, a multiple of the tile, between kSplitTokens and kTcMaxSplit.
-constexpr int kTcItemsPerBlock = 6;
+constexpr int kTcItemsPerBlock = 4;
 constexpr int kTcMaxSplit = kTcMaxSplitTiles * kTcTile;
 constexpr int kSlotBytes = kTcTile * 256;  // one K or V tile: 2 panels x 128 rows x 128 B
 constexpr int kPanelBytes = kTcTile * 128;  // P tile: one 64-column panel of 128 rows
