@@ -248,9 +248,10 @@ __device__ __forceinline__ void topk_row(KeyFn key, int n, int K, int32_t *out, 
 //   2. The keys of that bin are gathered into cand (any order).
 //   3. Warp 0 narrows them to tau: one 8-bit pass (bits 19-12); the few keys left (at most 32)
 //      rank themselves against each other across the lanes; else two more 8-bit passes.
-//   4. Each thread counts its keys > tau and == tau; a scan over the threads gives its first output
-//      slot and the keys == tau before it, and it writes its kept indices: every key > tau and the
-//      keys == tau while fewer than need_eq lie before (ties to the lower index, ascending output).
+//   4. Each thread counts its keys > tau and == tau (the keys above the bin, counted in step 2, and its
+//      own gathered keys); a scan over the threads gives its first output slot and the keys == tau
+//      before it, and it writes its kept indices: every key > tau and the keys == tau while fewer
+//      than need_eq lie before (ties to the lower index, ascending output).
 // A bin of more than kTopkCandCap keys (long runs of equal scores) takes three 8-bit block passes over
 // the row instead of steps 2-3.  `stamp(k)` marks the end of phase k (0: histogram, 1: threshold bin,
 // 2: tau, 3: indices written) for a diagnostic timeline; every thread calls it.
@@ -361,17 +362,26 @@ __device__ __forceinline__ void topk_row_smem(const uint32_t *s_keys, int n, int
     const int nb = sc.cbin;
     uint32_t tau;
     int need_eq;
+    int gt_pre = -1, cand_mine = 0, cand_cnt = 0;  // gathered path: keys above the bin, own gathered keys
     if (nb <= kTopkCandCap) {
-      int cin = 0;
-      topk_visit(s_keys, t0, t1, [&](int, uint32_t k) { cin += (k & mask) == prefix ? 1 : 0; });
+      int cin = 0, above = 0;
+      topk_visit(s_keys, t0, t1, [&](int, uint32_t k) {
+        const uint32_t top = k & mask;
+        cin += top == prefix ? 1 : 0;
+        above += top > prefix ? 1 : 0;
+      });
       const int incl = warp_incl_scan(cin);
       int base = 0;
       if (lane == 31 && incl > 0) base = atomicAdd(&sc.ncand, incl);
       base = __shfl_sync(0xffffffffu, base, 31) + incl - cin;
+      const int mine = base;  // this thread's gathered keys are cand[mine, mine + cin)
       if (cin > 0)
         topk_visit(s_keys, t0, t1, [&](int, uint32_t k) {
           if ((k & mask) == prefix) cand[base++] = k;
         });
+      gt_pre = above;
+      cand_mine = mine;
+      cand_cnt = cin;
       sync();
       if (warp == 0) {
         uint32_t *hw = sc.tot;
@@ -406,10 +416,9 @@ __device__ __forceinline__ void topk_row_smem(const uint32_t *s_keys, int n, int
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const uint32_t vj = __shfl_sync(0xffffffffu, v, j);
-            if (j < m) {
-              gt += vj > v ? 1 : 0;
-              ge += vj >= v ? 1 : 0;
-            }
+            const int in = j < m ? 1 : 0;
+            gt += (vj > v ? 1 : 0) & in;
+            ge += (vj >= v ? 1 : 0) & in;
           }
           const int f = __ffs(__ballot_sync(0xffffffffu, have && gt < rem && rem <= ge)) - 1;
           tau = __shfl_sync(0xffffffffu, v, f);
@@ -457,10 +466,20 @@ __device__ __forceinline__ void topk_row_smem(const uint32_t *s_keys, int n, int
     }
     stamp(2);
     int gt = 0, eq = 0;
-    topk_visit(s_keys, t0, t1, [&](int, uint32_t k) {
-      gt += k > tau ? 1 : 0;
-      eq += k == tau ? 1 : 0;
-    });
+    if (gt_pre >= 0) {
+      // Keys above the threshold bin are all > tau; of the bin's keys only this thread's own decide.
+      gt = gt_pre;
+      for (int i = 0; i < cand_cnt; ++i) {
+        const uint32_t k = cand[cand_mine + i];
+        gt += k > tau ? 1 : 0;
+        eq += k == tau ? 1 : 0;
+      }
+    } else {
+      topk_visit(s_keys, t0, t1, [&](int, uint32_t k) {
+        gt += k > tau ? 1 : 0;
+        eq += k == tau ? 1 : 0;
+      });
+    }
     // Both counts in one scan (each total is at most n < 2^16).
     const int pk = block_excl_scan1<NW>(gt | eq << 16, sc.weq);
     const int pgt = pk & 0xffff, peq = pk >> 16;
