@@ -100,3 +100,25 @@ def test_block_union_matches_oracle():
     np.testing.assert_array_equal(gc.cpu().numpy(), oc)
     np.testing.assert_array_equal(gi.cpu().numpy(), oi)
     np.testing.assert_array_equal(gm.cpu().numpy().view(np.uint32), om)
+
+
+def test_topk_threshold_bin_paths():
+    """Rows built for each way the shared-memory selection narrows its threshold bin (the bin of the
+    keys' top 12 bits that holds the K-th largest): more than 1024 keys in the bin (three passes over
+    the row); more than 32 keys left after the bin's next 8 bits (two more passes over the gathered
+    keys); and a few left (their ranks across a warp)."""
+    n = 5000
+    rng = np.random.default_rng(31)
+    rows = np.zeros((3, n), np.float32)
+    # 3000 distinct values in [1, 1.1) (one 12-bit bin: sign, exponent and 3 mantissa bits), 2000 in [2, 4).
+    rows[0, :3000] = 1.0 + rng.permutation(3000).astype(np.float32) * np.float32(2.0 ** -15)
+    rows[0, 3000:] = rng.uniform(2.0, 4.0, 2000).astype(np.float32)
+    # 400 values in the bin: 120 of them share their top 20 bits (differ in the low 12 only).
+    rows[1, :280] = 1.0 + (4096 + rng.permutation(280)).astype(np.float32) * np.float32(2.0 ** -19)
+    rows[1, 280:400] = 1.0 + rng.permutation(120).astype(np.float32) * np.float32(2.0 ** -23)
+    rows[1, 400:] = rng.uniform(0.0, 0.5, n - 400).astype(np.float32)
+    rows[2] = rng.uniform(0.0, 1.0, n).astype(np.float32)
+    for r in range(3):
+        rng.shuffle(rows[r])
+    # Row 0: K inside the 3000-key bin; row 1: inside the 120 shared keys (280 lie above them); row 2: 5 %.
+    _both(torch.from_numpy(rows), [n] * 3, [2500, 340, 250], 2500)
