@@ -19,6 +19,11 @@ constexpr int kSimtSplitTokens = 128;
 constexpr int kStageTokens = 64;
 // Criticality side values carry one log2-domain reference per (row, kRefGroup tokens).
 constexpr int kRefGroup = 16;
+constexpr int kRefShift = 4;    // log2(kRefGroup): one reference per 16 tokens (the mma.sync and SIMT verify)
+constexpr int kTcRefShift = 7;  // the tensor-core verify: one reference per 128-token tile
+// Row stride of the per-row references with one reference per (1 << ref_shift) tokens: a multiple of
+// four floats, so that every row starts 16-byte aligned (Lpad / 16 already is one).
+__host__ __device__ constexpr int ref_stride(int Lpad, int ref_shift) { return ((Lpad >> ref_shift) + 3) / 4 * 4; }
 // Row length of the criticality side buffer is a multiple of this (the largest tile that writes it).
 constexpr int kSideAlign = 128;
 // Draft work item: up to kDraftChunk selected tokens of one (request, KV head).

@@ -5,8 +5,9 @@
 //
 // SparseSpec ("Accelerating Large-Scale Reasoning Model Inference: Self-Speculative Decoding with
 // Sparse Attention") §4.1: the verify caches logits and the log-sum-exp so that the attention scores
-// can be rematerialised; crit[t] = sum over the rows r of the unit of e[r][t] * 2^(m_ref[r][t / 16] -
-// LSE2_r), with e the cached fp16 values and m_ref their log2 reference per 16 tokens.
+// can be rematerialised; crit[t] = sum over the rows r of the unit of e[r][t] *
+// 2^(m_ref[r][t >> ref_shift] - LSE2_r), with e the cached fp16 values and m_ref their log2 reference
+// per 2^ref_shift tokens (16, or 128 from the tensor-core verify).
 #pragma once
 
 #include "ssd_topk.cuh"
@@ -117,10 +118,10 @@ template <int NT>
 __device__ __forceinline__ void fin_unit_scores(const FinalizeArgs &f, int u, int L, const float *sL2, uint32_t *s_keys,
                                                 int tid) {
   const int64_t rbase = (int64_t)u * f.R;
-  const int nref = f.Lpad / kRefGroup;
+  const int nref = ref_stride(f.Lpad, f.ref_shift);
   const __half *sp = f.side_p + rbase * f.Lpad;
   for (int t0 = tid * 8; t0 < L; t0 += NT * 8) {
-    const int grp = t0 / kRefGroup;
+    const int grp = t0 >> f.ref_shift;
     float crit[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) crit[k] = 0.f;

@@ -301,6 +301,7 @@ extern "C" int ssd_unified_attn(const ssd_paged_kv *kv, const uint8_t *phase, co
   f.scores_stride = scores_stride;
   f.split_len = tc ? va.split_out : nullptr;
   f.balanced = tc ? 1 : 0;
+  f.ref_shift = tc ? kTcRefShift : kRefShift;
   const int n_tok = scores ? cdiv(kv->max_seq_len, kFinTok) : 0;
   return launch_finalize(f, n_tok, lay.units, st);
 }

@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
   const int ns = fin_splits(f, u, L);
   const int64_t pbase = (int64_t)u * f.S_max * f.R;
   const int64_t rbase = (int64_t)u * f.R;
-  const int nref = f.Lpad / kRefGroup;
+  const int nref = ref_stride(f.Lpad, f.ref_shift);
+  const int ng = kFinTok >> f.ref_shift;  // reference groups per token block (128 or 16)
 
   // Early loads of a token block: its first rows of side values and its reference values.
   const int t0 = tb0 + tid * 8;
@@ -96,10 +97,10 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     // References straight into the coefficient table (16 bytes = 4 groups per copy; a row's
     // references start 16-byte aligned since Lpad is a multiple of 128 tokens).  Groups at or past
     // L are not fetched: no stored score reads their coefficient.
-    for (int e = tid; e < f.R * (kFinGroups / 4); e += kFinThreads) {
-      const int r = e / (kFinGroups / 4), j4 = (e % (kFinGroups / 4)) * 4;
-      if (tb0 + j4 * kRefGroup < L)
-        cp_async16(smem_u32(s_coef + r * kFinGroups + j4), f.side_m + (rbase + r) * nref + tb0 / kRefGroup + j4, 16);
+    for (int e = tid; e < f.R * (ng / 4); e += kFinThreads) {
+      const int r = e / (ng / 4), j4 = (e % (ng / 4)) * 4;
+      if (tb0 + (j4 << f.ref_shift) < L)
+        cp_async16(smem_u32(s_coef + r * ng + j4), f.side_m + (rbase + r) * nref + (tb0 >> f.ref_shift) + j4, 16);
     }
     cp_async_commit();
   }
@@ -119,23 +120,23 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
     return;
   }
 
-  // Criticality: coef[r][j] = 2^(m_ref[r][group j] - LSE2_r) for the kFinGroups 16-token groups of
-  // this block, then crit[t] = sum_r e[r][t] * coef[r][t/16], eight consecutive tokens per thread.
+  // Criticality: coef[r][j] = 2^(m_ref[r][group j] - LSE2_r) for the ng reference groups of this
+  // block, then crit[t] = sum_r e[r][t] * coef[r][group of t], eight consecutive tokens per thread.
   cp_async_wait<0>();
   __syncthreads();
-  for (int e = tid; e < f.R * kFinGroups; e += kFinThreads) {
-    const float l2 = sL2[e / kFinGroups];
+  for (int e = tid; e < f.R * ng; e += kFinThreads) {
+    const float l2 = sL2[e / ng];
     s_coef[e] = (l2 == -INFINITY) ? 0.f : fast_exp2(s_coef[e] - l2);
   }
   __syncthreads();
-  const int grp = tid >> 1;  // 8 tokens = half a 16-token group
+  const int grp = (tid * 8) >> f.ref_shift;  // this thread's 8 tokens lie in one reference group
   float crit[8], cc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) crit[k] = cc[k] = 0.f;
   if (fast) {
 #pragma unroll
     for (int k = 0; k < kFinAhead; ++k)
-      if (k < f.R) fin_fma_row(raw[k], s_coef[k * kFinGroups + grp], crit);
+      if (k < f.R) fin_fma_row(raw[k], s_coef[k * ng + grp], crit);
     for (int r0 = kFinAhead; r0 < f.R; r0 += kFinAhead) {
 #pragma unroll
       for (int k = 0; k < kFinAhead; ++k)
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
                                          : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int k = 0; k < kFinAhead; ++k)
-        if (r0 + k < f.R) fin_fma_row(raw[k], s_coef[(r0 + k) * kFinGroups + grp], crit);
+        if (r0 + k < f.R) fin_fma_row(raw[k], s_coef[(r0 + k) * ng + grp], crit);
     }
   } else {
     for (int i = 0; i < f.n_c; ++i) {
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(FinalizeArgs f, i
       for (int hl = 0; hl < f.G; ++hl) {
         const int r = i * f.G + hl;
         const uint4 rw = valid ? __ldg(reinterpret_cast<const uint4 *>(sp + (int64_t)r * f.Lpad)) : make_uint4(0, 0, 0, 0);
-        fin_fma_row(rw, s_coef[r * kFinGroups + grp], cc);
+        fin_fma_row(rw, s_coef[r * ng + grp], cc);
       }
       // Candidate i's block maximum: 64 tokens = 8 lanes x 8 tokens.
       float m = cc[0];
@@ -530,6 +531,7 @@ static int verify_call(const ssd_paged_kv *kv, const void *q, int h_q, int n_can
   f.bstride = bscores_stride;
   f.split_len = (tc || simt) ? a.split_out : nullptr;
   f.balanced = tc ? 1 : 0;
+  f.ref_shift = tc ? kTcRefShift : kRefShift;
   f.ks = ks;
   f.sel_idx = idx;
   f.sel_cnt = cnt;

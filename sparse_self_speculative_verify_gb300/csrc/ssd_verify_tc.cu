@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int *vote = s.vote + wg * 4;
     float *red = s.red + wg * 4 * 32;
     const uint32_t lane_base = (uint32_t)(wiw * 32) << 16;
-    const int nref = a.Lpad / kRefGroup;
+    const int nref = ref_stride(a.Lpad, kTcRefShift);
     const uint64_t side_pol = policy_l2_evict_last();
     uint32_t i = 0, gph = 0;
     int jl = 0;
@@ -875,14 +875,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (r < R) st_global_policy(sp + (int64_t)r * a.Lpad, lo, side_pol);
             if (r + 1 < R) st_global_policy(sp + (int64_t)(r + 1) * a.Lpad, hi, side_pol);
           }
-          // References: one per (row, 16 tokens); CW rows x 8 groups entries per warpgroup.
-#pragma unroll
-          for (int e = tw; e < CW * (kTcTile / kRefGroup); e += 128) {
-            const int r = c0 + e / (kTcTile / kRefGroup), gi = e % (kTcTile / kRefGroup);
-            if (r < R) {
-              const float m = s.mref[r];
-              a.side_m[((int64_t)u * R + r) * nref + tb / kRefGroup + gi] = (m == -INFINITY) ? 0.f : m;
-            }
+          // References: one per (row, tile), since every value of the tile was taken against the
+          // same reference.
+          if (tw < CW && c0 + tw < R) {
+            const float m = s.mref[c0 + tw];
+            a.side_m[((int64_t)u * R + c0 + tw) * nref + (tb >> kTcRefShift)] = (m == -INFINITY) ? 0.f : m;
           }
         }
         SSD_TRACE(if (trace_m) TM[n_masked * 8 + 3] = (unsigned)(clock64() - clk0));

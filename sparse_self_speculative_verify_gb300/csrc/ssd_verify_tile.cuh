@@ -30,11 +30,12 @@ struct FinalizeArgs {
   const float *o_parts;
   const float *lse_parts;
   const __half *side_p;   // [units][R][Lpad]
-  const float *side_m;    // [units][R][Lpad / kRefGroup]
+  const float *side_m;    // [units][R][ref_stride(Lpad, ref_shift)]
   const int32_t *ucnt;    // block-sparse pass: splits per unit from the union size
   const int *split_len;   // split length the verify wrote (tensor-core, fp32 paths); nullptr = kSplitTokens;
                           // tensor-core path: [1] holds the first request of the half-length tail
   int balanced;           // splits cut by tc_split_count (the tensor-core verify), else cdiv(L, split length)
+  int ref_shift = kRefShift;  // one reference per (1 << ref_shift) tokens: kTcRefShift from the tensor-core verify
   const uint8_t *phase;   // unified launch: units of draft-phase requests are skipped
   int umax;
   float *out;
@@ -68,7 +69,7 @@ struct VerifyArgs {
   float *o_parts;    // [units][S_max][R][D], normalised by the split's own sum
   float *lse_parts;  // [units][S_max][R], natural log; -inf for an empty split
   __half *side_p;    // [units][R][Lpad], or nullptr (no criticality)
-  float *side_m;     // [units][R][Lpad / kRefGroup]
+  float *side_m;     // [units][R][Lpad / kRefGroup] (the tensor-core verify: [units][R][ref_stride(Lpad, kTcRefShift)])
   // Block-sparse token source (union of candidate block sets); nullptr for contiguous splits.
   const int32_t *uidx;
   const uint32_t *umask;
