@@ -450,7 +450,8 @@ def run_ours(args, spec, rank, world, local):
     # lengths / page table) go host -> device from pinned memory, the attention outputs device ->
     # host.  As a serving loop would run it, the copies are pipelined on a second stream: step s+1's
     # inputs are uploaded and step s-1's outputs read back while step s computes, through two sets of
-    # device staging buffers (device-to-device copies into and out of the graph's own buffers).
+    # device staging buffers (device-to-device copies into and out of the step's own buffers, captured
+    # with the step in one graph per staging set).
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)  # noqa: E731
     h_in = [(pin(l.q_verify), pin(l.q_draft)) for l in layers]
     h_meta = (pin(layers[0].seq_lens), pin(layers[0].page_table))
@@ -462,6 +463,25 @@ def run_ours(args, spec, rank, world, local):
     st_in = [[(torch.empty_like(l.q_verify), torch.empty_like(l.q_draft)) for l in layers] for _ in range(2)]
     st_meta = [(torch.empty_like(layers[0].seq_lens), torch.empty_like(layers[0].page_table)) for _ in range(2)]
     st_out = [[(torch.empty_like(r.out_v), torch.empty_like(o)) for r, o in zip(rounds, outs)] for _ in range(2)]
+    # One graph per staging set: the staged inputs copied into the step's buffers, the step, and the
+    # step's outputs copied out to the staging set, all captured together (no host launch between the
+    # copies and the step).
+    g_io = []
+    for b in range(2):
+        g_b = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g_b, stream=stream):
+                for (dv, dd), l in zip(st_in[b], layers):
+                    l.q_verify.copy_(dv, non_blocking=True)
+                    l.q_draft.copy_(dd, non_blocking=True)
+                layers[0].seq_lens.copy_(st_meta[b][0], non_blocking=True)
+                layers[0].page_table.copy_(st_meta[b][1], non_blocking=True)
+                step()
+                for (ov, od), r, o in zip(st_out[b], rounds, outs):
+                    ov.copy_(r.out_v, non_blocking=True)
+                    od.copy_(o, non_blocking=True)
+        g_io.append(g_b)
+    stream.synchronize()
     ev = lambda: torch.cuda.Event()  # noqa: E731
     in_ready, in_free = [ev(), ev()], [ev(), ev()]
     out_ready, out_free = [ev(), ev()], [ev(), ev()]
@@ -489,18 +509,10 @@ def run_ours(args, spec, rank, world, local):
         b = s % 2
         with torch.cuda.stream(stream):
             stream.wait_event(in_ready[b])
-            for (dv, dd), l in zip(st_in[b], layers):
-                l.q_verify.copy_(dv, non_blocking=True)
-                l.q_draft.copy_(dd, non_blocking=True)
-            layers[0].seq_lens.copy_(st_meta[b][0], non_blocking=True)
-            layers[0].page_table.copy_(st_meta[b][1], non_blocking=True)
-            in_free[b].record(stream)
-            graph.replay()
             if s >= 2:
                 stream.wait_event(out_free[b])
-            for (ov, od), r, o in zip(st_out[b], rounds, outs):
-                ov.copy_(r.out_v, non_blocking=True)
-                od.copy_(o, non_blocking=True)
+            g_io[b].replay()
+            in_free[b].record(stream)
             out_ready[b].record(stream)
         with torch.cuda.stream(cstream):
             if s + 1 < e2e_steps:
@@ -544,7 +556,8 @@ def run_ours(args, spec, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
                     "copies": "pinned host buffers; step s+1 uploaded and step s-1 read back on a second "
-                              "stream while step s runs"},
+                              "stream while step s runs; the device staging copies into and out of the step's "
+                              "buffers captured with the step (one graph per staging set)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk}
 
