@@ -319,6 +319,27 @@ def run_ours(args, spec, rank, world, local):
     k_max = max(int(l.k_per_req.max()) for l in layers)
     rounds = [SpecRound(KVCache.from_workload(l), spec.h_q, spec.n_cand, k_max, scale) for l in layers]
     outs = [torch.empty((spec.k, spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=dev) for _ in layers]
+    # The step's inputs (the queries of every layer) and outputs (the verify and draft outputs of every
+    # layer) each live in one buffer, so that a step's host copies are one per direction.
+    q_arena = torch.empty(sum(l.q_verify.numel() + l.q_draft.numel() for l in layers), dtype=layers[0].q_verify.dtype,
+                          device=dev)
+    off = 0
+    for l in layers:
+        for name in ("q_verify", "q_draft"):
+            t = getattr(l, name)
+            v = q_arena[off:off + t.numel()].view(t.shape)
+            v.copy_(t)
+            setattr(l, name, v)
+            off += t.numel()
+    o_arena = torch.empty(sum(r.out_v.numel() + o.numel() for r, o in zip(rounds, outs)), dtype=torch.float32,
+                          device=dev)
+    off, arena_outs = 0, []
+    for r, o in zip(rounds, outs):
+        r.out_v = o_arena[off:off + r.out_v.numel()].view(r.out_v.shape)
+        off += r.out_v.numel()
+        arena_outs.append(o_arena[off:off + o.numel()].view(o.shape))
+        off += o.numel()
+    outs = arena_outs
     stream = torch.cuda.Stream(device=dev)
 
     def step():
@@ -453,16 +474,14 @@ def run_ours(args, spec, rank, world, local):
     # device staging buffers (device-to-device copies into and out of the step's own buffers, captured
     # with the step in one graph per staging set).
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)  # noqa: E731
-    h_in = [(pin(l.q_verify), pin(l.q_draft)) for l in layers]
+    h_in = pin(q_arena)
     h_meta = (pin(layers[0].seq_lens), pin(layers[0].page_table))
-    h_out = [(torch.empty(r.out_v.shape, pin_memory=True), torch.empty(o.shape, pin_memory=True))
-             for r, o in zip(rounds, outs)]
-    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_in) + \
-        sum(t.numel() * t.element_size() for t in h_meta)
-    d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_out)
-    st_in = [[(torch.empty_like(l.q_verify), torch.empty_like(l.q_draft)) for l in layers] for _ in range(2)]
+    h_out = torch.empty(o_arena.shape, dtype=o_arena.dtype, pin_memory=True)
+    h2d = h_in.numel() * h_in.element_size() + sum(t.numel() * t.element_size() for t in h_meta)
+    d2h = h_out.numel() * h_out.element_size()
+    st_in = [torch.empty_like(q_arena) for _ in range(2)]
     st_meta = [(torch.empty_like(layers[0].seq_lens), torch.empty_like(layers[0].page_table)) for _ in range(2)]
-    st_out = [[(torch.empty_like(r.out_v), torch.empty_like(o)) for r, o in zip(rounds, outs)] for _ in range(2)]
+    st_out = [torch.empty_like(o_arena) for _ in range(2)]
     # One graph per staging set: the staged inputs copied into the step's buffers, the step, and the
     # step's outputs copied out to the staging set, all captured together (no host launch between the
     # copies and the step).
@@ -471,15 +490,11 @@ def run_ours(args, spec, rank, world, local):
         g_b = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g_b, stream=stream):
-                for (dv, dd), l in zip(st_in[b], layers):
-                    l.q_verify.copy_(dv, non_blocking=True)
-                    l.q_draft.copy_(dd, non_blocking=True)
+                q_arena.copy_(st_in[b], non_blocking=True)
                 layers[0].seq_lens.copy_(st_meta[b][0], non_blocking=True)
                 layers[0].page_table.copy_(st_meta[b][1], non_blocking=True)
                 step()
-                for (ov, od), r, o in zip(st_out[b], rounds, outs):
-                    ov.copy_(r.out_v, non_blocking=True)
-                    od.copy_(o, non_blocking=True)
+                st_out[b].copy_(o_arena, non_blocking=True)
         g_io.append(g_b)
     stream.synchronize()
     ev = lambda: torch.cuda.Event()  # noqa: E731
@@ -492,9 +507,7 @@ def run_ours(args, spec, rank, world, local):
         b = s % 2
         if s >= 2:
             cstream.wait_event(in_free[b])
-        for (qv, qd), (dv, dd) in zip(h_in, st_in[b]):
-            dv.copy_(qv, non_blocking=True)
-            dd.copy_(qd, non_blocking=True)
+        st_in[b].copy_(h_in, non_blocking=True)
         st_meta[b][0].copy_(h_meta[0], non_blocking=True)
         st_meta[b][1].copy_(h_meta[1], non_blocking=True)
         in_ready[b].record(cstream)
@@ -518,9 +531,7 @@ def run_ours(args, spec, rank, world, local):
             if s + 1 < e2e_steps:
                 upload(s + 1)
             cstream.wait_event(out_ready[b])
-            for (hv, hd), (ov, od) in zip(h_out, st_out[b]):
-                hv.copy_(ov, non_blocking=True)
-                hd.copy_(od, non_blocking=True)
+            h_out.copy_(st_out[b], non_blocking=True)
             out_free[b].record(cstream)
     with torch.cuda.stream(cstream):
         e1.record(cstream)
@@ -556,8 +567,9 @@ def run_ours(args, spec, rank, world, local):
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
                     "copies": "pinned host buffers; step s+1 uploaded and step s-1 read back on a second "
-                              "stream while step s runs; the device staging copies into and out of the step's "
-                              "buffers captured with the step (one graph per staging set)"},
+                              "stream while step s runs (one copy per direction: every layer's queries in one "
+                              "buffer, every output in another); the device staging copies into and out of the "
+                              "step's buffers captured with the step (one graph per staging set)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk}
 
