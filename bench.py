@@ -317,7 +317,8 @@ def run_ours(args, spec, rank, world, local):
     layers = make_layers(spec, args.layers, seed, dev)
     scale = 1.0 / math.sqrt(spec.d)
     k_max = max(int(l.k_per_req.max()) for l in layers)
-    rounds = [SpecRound(KVCache.from_workload(l), spec.h_q, spec.n_cand, k_max, scale) for l in layers]
+    rounds = [SpecRound(KVCache.from_workload(l), spec.h_q, spec.n_cand, k_max, scale, pack_rows=not args.no_pack)
+              for l in layers]
     outs = [torch.empty((spec.k, spec.batch, spec.h_q, spec.d), dtype=torch.float32, device=dev) for _ in layers]
     # The step's inputs (the queries of every layer) and outputs (the verify and draft outputs of every
     # layer) each live in one buffer, so that a step's host copies are one per direction.
@@ -453,19 +454,37 @@ def run_ours(args, spec, rank, world, local):
         return lambda: Bd.ssd_draft_attn_packed(r.kv, l.q_draft[1], idx, cnt, r.scale, r.pack, mode, out=o[1],
                                                 lse=r.lse_d, workspace=r.ws, stream=stream)
 
-    dw_ms = graph_mean_ms([draft_call(r, l, o, Bd.PACK_WRITE) for r, l, o in zip(rounds, layers, outs)], reps,
-                          stream)
-    dr_ms = graph_mean_ms([draft_call(r, l, o, Bd.PACK_READ) for r, l, o in zip(rounds, layers, outs)], reps, stream)
+    def plain_call(r, l, o):
+        idx = r.idx.view(spec.batch, spec.h_kv, r.k_max)
+        cnt = r.cnt.view(spec.batch, spec.h_kv)
+        return lambda: Bd.ssd_draft_attn(r.kv, l.q_draft[1], idx, cnt, r.scale, out=o[1], lse=r.lse_d,
+                                         workspace=r.ws, stream=stream)
+
+    if args.no_pack:
+        dw_ms = dr_ms = None
+    else:
+        dw_ms = graph_mean_ms([draft_call(r, l, o, Bd.PACK_WRITE) for r, l, o in zip(rounds, layers, outs)], reps,
+                              stream)
+        dr_ms = graph_mean_ms([draft_call(r, l, o, Bd.PACK_READ) for r, l, o in zip(rounds, layers, outs)], reps,
+                              stream)
+    dp_ms = graph_mean_ms([plain_call(r, l, o) for r, l, o in zip(rounds, layers, outs)], reps, stream)
     assert ssd_status() == 0, "device status fault in the draft timing"
-    roofline_draft = {"bound": "hbm", "kernel": "ssd_draft_attn_packed, row pack read (draft_pack_kernel)",
+    def draft_rec(ms, kernel):
+        return {"kernel": kernel, "launch_ms": ms, "achieved": d_call_bytes / (ms * 1e-3) / 1e9,
+                "frac": d_call_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+
+    plain_kernel = "ssd_draft_attn (rows gathered through the index list, draft_kernel)"
+    main_ms = dp_ms if args.no_pack else dr_ms
+    roofline_draft = {"bound": "hbm",
+                      "kernel": plain_kernel if args.no_pack else "ssd_draft_attn_packed, row pack read (draft_pack_kernel)",
                       "timing": f"mean per call over a CUDA graph of {reps} x {args.layers} consecutive calls, "
                                 f"layers cycled",
-                      "achieved": d_call_bytes / (dr_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                      "frac": d_call_bytes / (dr_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
-                      "peak_source": peaks["source"], "launch_ms": dr_ms, "algorithmic_bytes": d_call_bytes,
-                      "first_draft": {"kernel": "ssd_draft_attn_packed, row pack written (draft_kernel)",
-                                      "launch_ms": dw_ms, "achieved": d_call_bytes / (dw_ms * 1e-3) / 1e9,
-                                      "frac": d_call_bytes / (dw_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+                      "achieved": d_call_bytes / (main_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": d_call_bytes / (main_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                      "peak_source": peaks["source"], "launch_ms": main_ms, "algorithmic_bytes": d_call_bytes,
+                      "plain": draft_rec(dp_ms, plain_kernel)}
+    if not args.no_pack:
+        roofline_draft["first_draft"] = draft_rec(dw_ms, "ssd_draft_attn_packed, row pack written (draft_kernel)")
 
     # End to end through the API with host buffers: per step, the queries of every layer (and the
     # lengths / page table) go host -> device from pinned memory, the attention outputs device ->
@@ -894,6 +913,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-requests", type=int, default=2)
     ap.add_argument("--rows", action="store_true", help="time each hot-path call on its own workload (1 GPU)")
+    ap.add_argument("--no-pack", action="store_true",
+                    help="every draft of the round gathers its rows (no row pack written by the first draft)")
     args = ap.parse_args(argv)
     if args.rows:
         for d in run_rows(args):

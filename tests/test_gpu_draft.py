@@ -52,6 +52,38 @@ def test_draft_random_sets(case):
     _check(w, _draft(w, idx, cnt), idx, cnt)
 
 
+# Lists of exactly four 64-row chunks (256), one row more (257), seventeen chunks (1025), fewer rows
+# than one warp's 16 (15), G = 1 / 5 / 16, and pages of 8, 32 and 64 tokens (rows are gathered one
+# token at a time, anywhere in a page).
+GATHER_CASES = [
+    (dict(batch=4, page_size=8), [4000, 3000, 2000, 600], [256, 257, 1025, 15], 1025),
+    (dict(batch=2, page_size=64, h_q=8), [5000, 3000], [640, 63], 640),
+    (dict(batch=2, page_size=32, h_q=40), [9000, 2500], [700, 128], 700),
+    (dict(batch=2, h_q=128), [3000, 900], [513, 191], 513),
+]
+
+
+@pytest.mark.parametrize("case", GATHER_CASES, ids=lambda c: f"ps{c[0]['page_size'] if 'page_size' in c[0] else 16}-"
+                         f"hq{c[0].get('h_q', 32)}-k{c[3]}")
+def test_draft_gather_boundaries(case):
+    over, lens, ks, k_max = case
+    spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="dgb", **over)
+    w = W.make_workload(spec, seed=61 + k_max, device=DEV, lengths=lens)
+    idx, cnt = W.random_index_sets(w.seq_lens, spec.h_kv, torch.tensor(ks, dtype=torch.int32), k_max, seed=k_max + 5)
+    _check(w, _draft(w, idx, cnt), idx, cnt)
+
+
+def test_draft_many_short_lists():
+    """A batch of 1040 (request, KV head) lists of 5 to 44 rows: one chunk each, every unit's output
+    written by its single chunk."""
+    lens = [int(x) for x in np.random.default_rng(3).integers(100, 900, size=130)]
+    spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="dmany", batch=130)
+    w = W.make_workload(spec, seed=17, device=DEV, lengths=lens)
+    ks = [max(1, L // 20) for L in lens]
+    idx, cnt = W.random_index_sets(w.seq_lens, spec.h_kv, torch.tensor(ks, dtype=torch.int32), max(ks), seed=4)
+    _check(w, _draft(w, idx, cnt), idx, cnt)
+
+
 def test_draft_repeat_calls_identical():
     """Consecutive calls reuse the workspace counters: results are bit-identical."""
     spec = W.scaled_spec(W.SPECS["qwen3_8b"], name="rep", batch=2)
