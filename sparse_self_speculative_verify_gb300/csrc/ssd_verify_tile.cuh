@@ -96,8 +96,13 @@ struct VerifyMmaCfg {
   static constexpr int QBYTES = ROWS * D * 2;
   static constexpr int MERGE = NTG * ROWS * (D + 2) * 4;  // O, m, l of every token group
   static_assert(MERGE <= RING, "merge area must fit in the stage ring");
-  static constexpr int SMEM = RING + QBYTES;
+  // The pool row of every token of the item, resolved once at the item's start (after Q): kept where
+  // it leaves room for two blocks per SM (all shapes but d = 128 with four row tiles).
+  static constexpr int ROWTAB_BYTES = kSplitTokens * 4 + 2 * kBlocksPerItem * 4;  // + stage bases, masks
+  static constexpr bool ROWTAB = RING + QBYTES + ROWTAB_BYTES <= 113 * 1024;
+  static constexpr int SMEM = RING + QBYTES + (ROWTAB ? ROWTAB_BYTES : 0);
 };
+static_assert(kSplitTokens == kBlocksPerItem * kStageTokens, "an item is at most kSplitTokens tokens either way");
 
 // Number of work items (splits) of one unit.
 __device__ __forceinline__ int verify_splits(int L, int split = kSplitTokens) { return cdiv(L, split); }
@@ -174,20 +179,59 @@ __device__ __forceinline__ void verify_item_mma(const VerifyArgs &a, int unit, i
     return BLOCKS ? a.umask[(int64_t)unit * a.umax + blk_first + s] : 0xffffffffu;
   };
 
+  const int lim = BLOCKS ? L : t_end;
+  // Pool row of every token of the item (0xffffffff: zero-filled), resolved once before the first
+  // copies: the union block ids (block-sparse items), then the page ids, two loads deep for the
+  // whole item instead of per stage, where the threads that issue a stage's copies would otherwise
+  // wait for them right before computing the stage before it.
+  uint32_t *s_rows = reinterpret_cast<uint32_t *>(smem + C::RING + C::QBYTES);
+  if constexpr (C::ROWTAB) {
+    constexpr int PER = kSplitTokens / 128;
+    int tk[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int j = tid + 128 * k;
+      tk[k] = j < n_stages * kStageTokens ? stage_base(j / kStageTokens) + j % kStageTokens : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int j = tid + 128 * k, t = tk[k];
+      uint32_t row = 0xffffffffu;
+      if (j < n_stages * kStageTokens && t >= 0 && t < lim) {
+        const int32_t p = __ldg(a.kv.page_table + (int64_t)b * a.kv.max_pages + (t >> a.kv.log2_ps));
+        const int64_t r = (((int64_t)p * 2) * h_kv + g) * a.kv.page_size + (t & (a.kv.page_size - 1));
+        if (p < 0 || (int64_t)p >= a.kv.num_pages || r >= 0xffffffffll)
+          atomicOr(a.status, (unsigned)SSD_FAULT_PAGE);
+        else
+          row = (uint32_t)r;
+      }
+      if (j < kSplitTokens) s_rows[j] = row;
+    }
+    if (BLOCKS && tid < n_stages) {  // the stages' first tokens and candidate masks, for the compute
+      s_rows[kSplitTokens + tid] = (uint32_t)stage_base(tid);
+      s_rows[kSplitTokens + kBlocksPerItem + tid] = a.umask[(int64_t)unit * a.umax + blk_first + tid];
+    }
+    __syncthreads();
+  }
+
   // Issue the cp.async copies of stage s into ring buffer `buf`.  Rows past L (and rows whose page
   // id is out of range) are zero-filled.
   auto load_stage = [&](int s, int buf) {
-    const int base = stage_base(s);
-    const int lim = BLOCKS ? L : t_end;
+    const int base = C::ROWTAB ? 0 : stage_base(s);
     char *kt = ring + buf * 2 * C::TILE;
     char *vt = kt + C::TILE;
 #pragma unroll
     for (int it = 0; it < kStageTokens * CPR / 128; ++it) {
       int c = it * 128 + tid;
       int row = c / CPR, ch = c % CPR;
-      int t = base + row;
       const __nv_bfloat16 *kr = nullptr;
-      if (t >= 0 && t < lim) kr = kv_row<D, __nv_bfloat16>(a.kv, b, 0, g, t, a.status);
+      if constexpr (C::ROWTAB) {
+        const uint32_t rw = s_rows[s * kStageTokens + row];
+        if (rw != 0xffffffffu) kr = pool + (int64_t)rw * D;
+      } else {
+        const int t = base + row;
+        if (t >= 0 && t < lim) kr = kv_row<D, __nv_bfloat16>(a.kv, b, 0, g, t, a.status);
+      }
       uint32_t off = row * (D * 2) + swz_chunk(row, ch) * 16;
       cp_async16(smem_u32(kt + off), kr ? (const void *)(kr + ch * 8) : (const void *)pool, kr ? 16 : 0);
       cp_async16(smem_u32(vt + off), kr ? (const void *)(kr + v_off + ch * 8) : (const void *)pool, kr ? 16 : 0);
@@ -246,8 +290,8 @@ __device__ __forceinline__ void verify_item_mma(const VerifyArgs &a, int unit, i
     }
     const char *kt = ring + (s % C::NSTAGE) * 2 * C::TILE;
     const char *vt = kt + C::TILE;
-    const int base = stage_base(s);
-    const uint32_t bits = stage_bits(s);
+    const int base = BLOCKS && C::ROWTAB ? (int)s_rows[kSplitTokens + s] : stage_base(s);
+    const uint32_t bits = BLOCKS && C::ROWTAB ? s_rows[kSplitTokens + kBlocksPerItem + s] : stage_bits(s);
 
     // S = Q K^T for this warp's 16 rows x TW tokens.
     float sacc[TW / 8][4];
