@@ -81,3 +81,16 @@ def test_block_path_small():
 def test_block_path_full_size_sampled():
     w = W.make_workload(W.SPECS["block_131k"], device=DEV)
     _check_block_path(w, reqs=[0, 7])
+
+
+# Pages of 8 and 32 tokens (a union block's rows in 8 or 2 runs of the pool), R = 40 (four row tiles:
+# the block-sparse kernel without its shared row table), and d = 64.
+@pytest.mark.parametrize("over,lens", [
+    (dict(batch=2, page_size=8), [5000, 2100]),
+    (dict(batch=2, page_size=32), [6000, 777]),
+    (dict(batch=2, h_q=64), [4100, 2500]),
+    (dict(batch=2, d=64), [3000, 1500]),
+], ids=["ps8", "ps32", "R40", "d64"])
+def test_block_path_shapes(over, lens):
+    spec = W.scaled_spec(W.SPECS["block_131k"], name="blks", **over)
+    _check_block_path(W.make_workload(spec, seed=21, device=DEV, lengths=lens))
